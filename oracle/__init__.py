@@ -1,0 +1,225 @@
+"""fp64 CPU oracle for paged decode attention -- TEST INFRASTRUCTURE ONLY.
+
+Only the test-suite, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The product library never does, and this
+package imports nothing from the product.  The arithmetic lives in ``pa_oracle.c``
+(plain C, IEEE double); this module only marshals numpy arrays through ctypes.
+
+Every array argument is a numpy array; 16-bit floating-point tensors (q, caches,
+new rows) are passed as their raw ``uint16`` bit patterns, so both fp16 and bf16
+take the same route and the oracle decodes them itself from the format
+definitions.
+
+Layouts (row-major):
+  q            [num_seqs, q_len, num_q_heads, head_dim]
+  k/v cache    [num_blocks, num_kv_heads, block_size, head_dim]
+  k/v new      [n_tokens, num_kv_heads, head_dim]
+  block_tables [num_seqs, max_blocks_per_seq] int32
+  context_lens [num_seqs] int32 (they already count this step's new tokens)
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from concurrent.futures import ThreadPoolExecutor
+
+import numpy as np
+
+from . import build as _build
+
+DTYPES = {"fp16": 0, "bf16": 1}
+
+_c_i64p = ctypes.POINTER(ctypes.c_int64)
+_c_i32p = ctypes.POINTER(ctypes.c_int32)
+_c_u16p = ctypes.POINTER(ctypes.c_uint16)
+_c_f64p = ctypes.POINTER(ctypes.c_double)
+
+
+def _ptr(a: np.ndarray, ctype):
+    return a.ctypes.data_as(ctype)
+
+
+def _u16(a: np.ndarray) -> np.ndarray:
+    a = np.ascontiguousarray(a)
+    if a.dtype == np.uint16:
+        return a
+    if a.dtype in (np.int16, np.float16):
+        return a.view(np.uint16)
+    raise TypeError(f"expected 16-bit pattern array, got {a.dtype}")
+
+
+def _dtype_code(dtype) -> int:
+    if isinstance(dtype, int):
+        return dtype
+    return DTYPES[dtype]
+
+
+class Oracle:
+    """ctypes wrapper around one compiled copy of ``pa_oracle.c``."""
+
+    def __init__(self, path: str = _build.LIBRARY):
+        self.path = path
+        lib = ctypes.CDLL(path)
+        lib.orc_fp16_to_double.restype = ctypes.c_double
+        lib.orc_fp16_to_double.argtypes = [ctypes.c_uint16]
+        lib.orc_bf16_to_double.restype = ctypes.c_double
+        lib.orc_bf16_to_double.argtypes = [ctypes.c_uint16]
+        lib.orc_decode_bits.restype = None
+        lib.orc_decode_bits.argtypes = [_c_f64p, _c_u16p, ctypes.c_int64, ctypes.c_int]
+        lib.orc_slot_mapping.restype = ctypes.c_int
+        lib.orc_slot_mapping.argtypes = [_c_i64p, _c_i32p, _c_i32p, ctypes.c_int, ctypes.c_int,
+                                         ctypes.c_int, ctypes.c_int]
+        lib.orc_append_kv.restype = None
+        lib.orc_append_kv.argtypes = [_c_u16p, _c_u16p, _c_u16p, _c_u16p, _c_i64p, ctypes.c_int,
+                                      ctypes.c_int, ctypes.c_int, ctypes.c_int]
+        lib.orc_decode.restype = ctypes.c_int
+        lib.orc_decode.argtypes = [_c_f64p, _c_i64p, ctypes.c_int64, _c_u16p, _c_u16p, _c_u16p,
+                                   _c_i32p, _c_i32p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                   ctypes.c_int, ctypes.c_int, ctypes.c_float, ctypes.c_int,
+                                   ctypes.c_int, ctypes.c_int]
+        lib.orc_decode_partitions.restype = ctypes.c_int
+        lib.orc_decode_partitions.argtypes = [_c_f64p, _c_f64p, _c_f64p, _c_u16p, _c_u16p,
+                                              _c_u16p, _c_i32p, _c_i32p, ctypes.c_int,
+                                              ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                              ctypes.c_int, ctypes.c_float, ctypes.c_int,
+                                              ctypes.c_int, ctypes.c_int, ctypes.c_int]
+        lib.orc_combine.restype = None
+        lib.orc_combine.argtypes = [_c_f64p, _c_f64p, _c_f64p, _c_f64p, ctypes.c_int,
+                                    ctypes.c_int, ctypes.c_int64, ctypes.c_int]
+        self.lib = lib
+
+    # -- element decoding -------------------------------------------------------
+    def decode_bits(self, bits: np.ndarray, dtype) -> np.ndarray:
+        b = _u16(bits)
+        out = np.empty(b.shape, dtype=np.float64)
+        self.lib.orc_decode_bits(_ptr(out, _c_f64p), _ptr(b, _c_u16p), b.size, _dtype_code(dtype))
+        return out
+
+    # -- slot mapping -----------------------------------------------------------
+    def slot_mapping(self, block_tables: np.ndarray, context_lens: np.ndarray,
+                     block_size: int, q_len: int = 1) -> np.ndarray:
+        bt = np.ascontiguousarray(block_tables, dtype=np.int32)
+        cl = np.ascontiguousarray(context_lens, dtype=np.int32)
+        n = cl.shape[0]
+        out = np.empty(n * q_len, dtype=np.int64)
+        rc = self.lib.orc_slot_mapping(_ptr(out, _c_i64p), _ptr(bt, _c_i32p), _ptr(cl, _c_i32p),
+                                       n, bt.shape[1], block_size, q_len)
+        if rc != 0:
+            raise ValueError("a new token's position lies beyond the block table")
+        return out
+
+    # -- append (in place) ------------------------------------------------------
+    def append_kv(self, k_cache: np.ndarray, v_cache: np.ndarray, k_new: np.ndarray,
+                  v_new: np.ndarray, slot_mapping: np.ndarray) -> None:
+        for a in (k_cache, v_cache):
+            if not (a.flags.c_contiguous and a.dtype in (np.uint16, np.int16, np.float16)):
+                raise TypeError("caches must be contiguous 16-bit arrays (modified in place)")
+        kc, vc = k_cache.view(np.uint16), v_cache.view(np.uint16)
+        kn, vn = _u16(k_new), _u16(v_new)
+        sm = np.ascontiguousarray(slot_mapping, dtype=np.int64)
+        _, h_kv, block_size, head_dim = kc.shape
+        self.lib.orc_append_kv(_ptr(kc, _c_u16p), _ptr(vc, _c_u16p), _ptr(kn, _c_u16p),
+                               _ptr(vn, _c_u16p), _ptr(sm, _c_i64p), sm.shape[0], h_kv,
+                               head_dim, block_size)
+
+    # -- attention --------------------------------------------------------------
+    def decode(self, q, k_cache, v_cache, block_tables, context_lens, scale: float,
+               dtype, q_len: int = 1, rows=None, threads: int = 1) -> np.ndarray:
+        """fp64 attention output.
+
+        ``q`` is [num_seqs, q_len, num_q_heads, head_dim] (or [num_seqs, num_q_heads,
+        head_dim] when q_len == 1).  Without ``rows`` the result has q's shape; with
+        ``rows`` (flat output-row indices r = (seq*q_len + u)*num_q_heads + head) it
+        is [len(rows), head_dim].
+        """
+        qb = _u16(q)
+        kc, vc = _u16(k_cache), _u16(v_cache)
+        bt = np.ascontiguousarray(block_tables, dtype=np.int32)
+        cl = np.ascontiguousarray(context_lens, dtype=np.int32)
+        num_seqs = cl.shape[0]
+        _, h_kv, block_size, head_dim = kc.shape
+        h_q = qb.size // (num_seqs * q_len * head_dim)
+        if rows is None:
+            rows_arr = np.arange(num_seqs * q_len * h_q, dtype=np.int64)
+        else:
+            rows_arr = np.ascontiguousarray(rows, dtype=np.int64)
+        out = np.empty((rows_arr.shape[0], head_dim), dtype=np.float64)
+
+        def run(lo: int, hi: int) -> int:
+            sub = rows_arr[lo:hi]
+            o = out[lo:hi]
+            return self.lib.orc_decode(_ptr(o, _c_f64p), _ptr(sub, _c_i64p), hi - lo,
+                                       _ptr(qb, _c_u16p), _ptr(kc, _c_u16p), _ptr(vc, _c_u16p),
+                                       _ptr(bt, _c_i32p), _ptr(cl, _c_i32p), num_seqs, h_q, h_kv,
+                                       head_dim, block_size, float(scale), bt.shape[1], q_len,
+                                       _dtype_code(dtype))
+
+        n = rows_arr.shape[0]
+        if threads <= 1 or n < 2:
+            rcs = [run(0, n)]
+        else:
+            bounds = np.linspace(0, n, min(n, threads * 4) + 1).astype(int)
+            with ThreadPoolExecutor(max_workers=threads) as ex:
+                rcs = list(ex.map(lambda ab: run(*ab), zip(bounds[:-1], bounds[1:])))
+        if any(rc != 0 for rc in rcs):
+            raise ValueError(f"oracle decode failed: {rcs}")
+        if rows is None:
+            return out.reshape(qb.shape)
+        return out
+
+    def decode_partitions(self, q, k_cache, v_cache, block_tables, context_lens, scale: float,
+                          dtype, num_splits: int, q_len: int = 1):
+        """Per-partition (m, l, acc), natural-log domain, fp64.
+
+        m, l: [num_seqs, num_splits, q_len*num_q_heads]; acc: same + [head_dim].
+        """
+        qb = _u16(q)
+        kc, vc = _u16(k_cache), _u16(v_cache)
+        bt = np.ascontiguousarray(block_tables, dtype=np.int32)
+        cl = np.ascontiguousarray(context_lens, dtype=np.int32)
+        num_seqs = cl.shape[0]
+        _, h_kv, block_size, head_dim = kc.shape
+        h_q = qb.size // (num_seqs * q_len * head_dim)
+        rps = q_len * h_q
+        m = np.empty((num_seqs, num_splits, rps), dtype=np.float64)
+        l = np.empty_like(m)
+        acc = np.empty((num_seqs, num_splits, rps, head_dim), dtype=np.float64)
+        rc = self.lib.orc_decode_partitions(_ptr(m, _c_f64p), _ptr(l, _c_f64p), _ptr(acc, _c_f64p),
+                                            _ptr(qb, _c_u16p), _ptr(kc, _c_u16p), _ptr(vc, _c_u16p),
+                                            _ptr(bt, _c_i32p), _ptr(cl, _c_i32p), num_seqs, h_q,
+                                            h_kv, head_dim, block_size, float(scale), bt.shape[1],
+                                            q_len, _dtype_code(dtype), num_splits)
+        if rc != 0:
+            raise ValueError(f"oracle partitions failed: {rc}")
+        return m, l, acc
+
+    def combine(self, m: np.ndarray, l: np.ndarray, acc: np.ndarray) -> np.ndarray:
+        m = np.ascontiguousarray(m, dtype=np.float64)
+        l = np.ascontiguousarray(l, dtype=np.float64)
+        acc = np.ascontiguousarray(acc, dtype=np.float64)
+        num_seqs, num_splits, rps, head_dim = acc.shape
+        out = np.empty((num_seqs, rps, head_dim), dtype=np.float64)
+        self.lib.orc_combine(_ptr(out, _c_f64p), _ptr(m, _c_f64p), _ptr(l, _c_f64p),
+                             _ptr(acc, _c_f64p), num_seqs, num_splits, rps, head_dim)
+        return out
+
+
+_lock = threading.Lock()
+_default: Oracle | None = None
+
+
+def get() -> Oracle:
+    """The oracle built from this directory's source (compiled on first use)."""
+    global _default
+    with _lock:
+        if _default is None:
+            if _build.needs_build():
+                _build.build()
+            _default = Oracle()
+        return _default
+
+
+def load(path: str) -> Oracle:
+    """Load another compiled copy (e.g. a deliberately altered one in a test)."""
+    return Oracle(os.path.abspath(path))

@@ -1,0 +1,94 @@
+"""Plausible mistakes planted in copies of the oracle must each fail a pin.
+
+Every mutant is a textual edit of ``oracle/pa_oracle.c`` compiled into a
+temporary directory and checked in a child process (a wrong index could read out
+of bounds; a crash then fails only that child).  The real oracle is never
+modified.  CPU only.
+"""
+import os
+import subprocess
+import sys
+import tempfile
+from concurrent.futures import ThreadPoolExecutor
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+from oracle import build as oracle_build  # noqa: E402
+
+MUTANTS = [
+    # (name, original text, mistaken text)
+    ("gqa_interleaved_heads", "*kvh = *h / group;", "*kvh = *h % c->num_kv_heads;"),
+    ("no_tail_mask",
+     "*T = (int64_t)c->context_lens[*i] - c->q_len + *u + 1;",
+     "*T = ((int64_t)c->context_lens[*i] + c->block_size - 1) / c->block_size * c->block_size - c->q_len + *u + 1;"),
+    ("no_causal_offset",
+     "*T = (int64_t)c->context_lens[*i] - c->q_len + *u + 1;",
+     "*T = (int64_t)c->context_lens[*i];"),
+    ("scale_dropped", "return c->scale * dot;", "return dot;"),
+    ("max_subtracted_backwards", "s[t] = exp(s[t] - mx);", "s[t] = exp(mx - s[t]);"),
+    ("nhd_read_layout",
+     "return (size_t)(((physical_block * c->num_kv_heads + h) * c->block_size + block_offset) * c->head_dim);",
+     "return (size_t)(((physical_block * c->block_size + block_offset) * c->num_kv_heads + h) * c->head_dim);"),
+    ("table_lookup_skipped", "out = physical_block * block_size + block_offset;",
+     "out = logical_block * block_size + block_offset;"),
+    ("combine_unweighted_denominator", "den += exp(m[w] - M) * l[w];", "den += l[w];"),
+    ("partition_off_by_one", "int64_t t1 = t0 + C * block_size;",
+     "int64_t t1 = t0 + C * block_size - 1;"),
+    ("dot_drops_first_term",
+     "    for (int d = 0; d < c->head_dim; d++)\n        dot +=",
+     "    for (int d = 1; d < c->head_dim; d++)\n        dot +="),
+    ("keys_used_as_values", "o[d] += p * elt(c->v_cache, vrow + d, c->dtype);",
+     "o[d] += p * elt(c->k_cache, vrow + d, c->dtype);"),
+    ("append_writes_key_into_value", "v_cache[dst] = v_new[src];", "v_cache[dst] = k_new[src];"),
+    ("fp16_exponent_bias", "v = ldexp((double)(1024 + f), e - 25);",
+     "v = ldexp((double)(1024 + f), e - 24);"),
+    ("bf16_subnormal_scale", "v = ldexp((double)f, -133);", "v = ldexp((double)f, -126);"),
+    ("softmax_not_normalised", "double p = s[t] / den;", "double p = s[t];"),
+]
+
+
+def _source() -> str:
+    with open(oracle_build.SOURCE) as f:
+        return f.read()
+
+
+def _check(lib: str) -> subprocess.CompletedProcess:
+    return subprocess.run([sys.executable, "-m", "tests.oracle_pins", lib], cwd=ROOT,
+                          capture_output=True, text=True, timeout=600)
+
+
+@pytest.fixture(scope="module")
+def mutant_results():
+    src = _source()
+    tmp = tempfile.mkdtemp(prefix="oracle_mutants_")
+    jobs = []
+    for name, old, new in MUTANTS:
+        assert src.count(old) == 1, f"mutant {name}: pattern not found exactly once"
+        path = os.path.join(tmp, f"{name}.c")
+        with open(path, "w") as f:
+            f.write(src.replace(old, new))
+        jobs.append((name, path, os.path.join(tmp, f"lib_{name}.so")))
+
+    def run(job):
+        name, path, lib = job
+        oracle_build.build(source=path, output=lib, werror=False)
+        return name, _check(lib)
+
+    with ThreadPoolExecutor(max_workers=min(8, os.cpu_count() or 1)) as ex:
+        return dict(ex.map(run, jobs))
+
+
+def test_real_oracle_passes_every_pin():
+    lib = os.path.join(tempfile.mkdtemp(prefix="oracle_real_"), "lib.so")
+    oracle_build.build(output=lib)
+    res = _check(lib)
+    assert res.returncode == 0, res.stdout + res.stderr
+
+
+@pytest.mark.parametrize("name", [m[0] for m in MUTANTS])
+def test_mutant_is_caught(mutant_results, name):
+    res = mutant_results[name]
+    assert res.returncode != 0, f"mutant {name} passed every pin:\n{res.stdout}{res.stderr}"
