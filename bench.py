@@ -1,0 +1,491 @@
+"""Benchmark: paged decode attention (append + attend) on GB300.
+
+One step = one pass of the whole hot path over one batch: pa_slot_mapping ->
+pa_append_kv -> pa_decode (or pa_decode_partial + pa_decode_combine for a
+split-KV workload), on one stream, with every input resident in HBM.
+
+Metric: KV tokens/s = sum of context lengths / step time (a token is counted once
+per sequence, whatever the number of heads or query rows), with the achieved HBM
+bandwidth of the attention kernel as a fraction of the measured peak.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl ours|reference]
+
+Default workload: llama7b_mha (32 seqs, 32/32 heads, head_dim 128, fp16, context
+lengths uniform in [512, 4096]).  The other workloads are measured the same way
+and reported under "other_configs" (skip with --only).  Under torchrun each rank
+runs its own independent batch (different seed) on its own GPU: weak scaling,
+no collective on the data path; the barrier and the max-over-ranks reduction are
+timing only.
+
+--impl reference times the fp64 CPU oracle (the checker, plain C) on the host
+cores on a bounded sample of the same workload, as the reference arm.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "paged decode attention: KV tokens/s and achieved HBM GB/s (% of GB300 peak)"
+UNIT = "KV tokens/s"
+DEFAULT_CONFIG = "llama7b_mha"
+OTHER_CONFIGS = ["gqa", "long_split", "prefix_verify"]
+FLUSH_BYTES = 512 << 20          # > 2x the 129 MB L2: written between timed steps
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+ELT = 2                           # bytes per fp16 / bf16 element
+
+
+# --------------------------------------------------------------------------- helpers
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def init_dist(world: int):
+    if world > 1 and not torch.distributed.is_initialized():
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        torch.distributed.init_process_group(backend=backend)
+
+
+def barrier(world: int):
+    if world > 1:
+        torch.distributed.barrier()
+
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    if world == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(x: float, world: int, device) -> float:
+    if world == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.SUM)
+    return float(t.item())
+
+
+def measured_peaks() -> dict:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return json.load(f)
+    return {}
+
+
+def algorithmic_bytes(w: workloads.Workload) -> dict:
+    """Bytes the step must move at minimum (unique KV once, q, out, tables, lens, append)."""
+    c = w.cfg
+    per_token = 2 * c.num_kv_heads * c.head_dim * ELT          # K and V of one token, one layer
+    lens = w.context_lens.numpy().astype(np.int64)
+    nb = (lens + c.block_size - 1) // c.block_size
+    kv = w.info["unique_tokens"] * per_token
+    q = c.num_seqs * c.q_len * c.num_q_heads * c.head_dim * ELT
+    out = q
+    tables = int(nb.sum()) * 4 + c.num_seqs * 4
+    n_new = c.num_seqs * c.q_len
+    append = 2 * n_new * c.num_kv_heads * c.head_dim * ELT * 2   # read new rows + write slots
+    ws = 0
+    if c.num_splits > 1:   # partial writes, combine reads, per row: D + 2 floats
+        rows = c.num_seqs * c.num_splits * c.q_len * c.num_q_heads
+        ws = 2 * rows * (c.head_dim + 2) * 4
+    # the attention launch: reads unique KV, q, tables; writes out (or the workspace)
+    decode = kv + q + tables + (ws // 2 if c.num_splits > 1 else out)
+    return {"per_token": per_token, "kv": kv, "decode_launch": decode,
+            "step": kv + q + out + tables + append + ws + n_new * 8}
+
+
+def traffic_record(kernel_name: str, config: str):
+    """dram bytes per launch from the committed ncu summary, if the kernel source is
+    unchanged since the counters were taken (else None)."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    want_sha = kernel_source_sha()
+    for line in open(path):
+        line = line.strip()
+        if not line or line.startswith("#"):
+            continue
+        kv = dict(x.split("=", 1) for x in line.split())
+        if kv.get("config") == config and kv.get("kernel") == kernel_name and \
+                kv.get("src_sha") == want_sha:
+            return float(kv["dram_bytes_per_launch"])
+    return None
+
+
+def kernel_source_sha() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "paged_kv_cache_20_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.f, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return None
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
+            except ValueError:
+                continue
+        if not rows:
+            return None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, r in rows for i, v in enumerate(r) if v == "Active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows),
+                "sm_max_mhz": max(r[1] for r in rows), "reasons": reasons,
+                "samples": len(rows)}
+
+
+# --------------------------------------------------------------------------- our arm
+class Runner:
+    """Device buffers and launch sequence for one workload."""
+
+    def __init__(self, pa, w: workloads.Workload, device):
+        self.pa, self.w, self.dev = pa, w, device
+        c = w.cfg
+        self.d = {k: getattr(w, k).to(device) for k in
+                  ("q", "k_new", "v_new", "k_cache", "v_cache", "block_tables", "context_lens")}
+        self.out = torch.empty_like(self.d["q"])
+        self.slots = torch.empty(c.num_seqs * c.q_len, dtype=torch.int64, device=device)
+        self.ws = None
+        if c.num_splits > 1:
+            nbytes = pa.pa_decode_workspace_size(c.num_seqs, c.num_q_heads, c.q_len, c.head_dim,
+                                                 c.num_splits)
+            self.ws = torch.empty(nbytes, dtype=torch.uint8, device=device)
+        self.launches_per_step = 3 + (1 if c.num_splits > 1 else 0)
+
+    def step(self, ev_pair=None):
+        pa, d, c = self.pa, self.d, self.w.cfg
+        pa.pa_slot_mapping(d["block_tables"], d["context_lens"], c.block_size, c.q_len,
+                           out=self.slots)
+        pa.pa_append_kv(d["k_cache"], d["v_cache"], d["k_new"], d["v_new"], self.slots)
+        if ev_pair is not None:
+            ev_pair[0].record()
+        if c.num_splits > 1:
+            pa.pa_decode_partial(self.ws, d["q"], d["k_cache"], d["v_cache"], d["block_tables"],
+                                 d["context_lens"], self.w.scale, c.num_splits, c.q_len)
+            if ev_pair is not None:
+                ev_pair[1].record()
+            pa.pa_decode_combine(self.out, self.ws, c.num_splits)
+        else:
+            pa.pa_decode(self.out, d["q"], d["k_cache"], d["v_cache"], d["block_tables"],
+                         d["context_lens"], self.w.scale, c.q_len)
+            if ev_pair is not None:
+                ev_pair[1].record()
+
+
+def time_device(runner: Runner, steps: int, warmup: int, flush: torch.Tensor, world: int):
+    for _ in range(warmup):
+        runner.step()
+    torch.cuda.synchronize()
+    E = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    evs = [(E(), E(), E(), E()) for _ in range(steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for s0, s1, k0, k1 in evs:
+        flush.zero_()                     # evict L2 between steps (untimed)
+        s0.record()
+        runner.step((k0, k1))
+        s1.record()
+    torch.cuda.synchronize()
+    barrier(world)
+    wall = time.perf_counter() - t0
+    step_ms = [a.elapsed_time(b) for a, b, _, _ in evs]
+    kern_ms = [a.elapsed_time(b) for _, _, a, b in evs]
+    return step_ms, kern_ms, wall
+
+
+def time_e2e(runner: Runner, steps: int, warmup: int, flush: torch.Tensor):
+    """Same step through the public API with the inputs in pinned host memory:
+    H2D of q, new K/V rows, block tables and context lengths, then the step, then
+    D2H of the output, all inside the timed region."""
+    w = runner.w
+    names = ("q", "k_new", "v_new", "block_tables", "context_lens")
+    host = {k: getattr(w, k).pin_memory() for k in names}
+    out_host = torch.empty(runner.out.shape, dtype=runner.out.dtype).pin_memory()
+    h2d = sum(host[k].numel() * host[k].element_size() for k in names)
+    d2h = out_host.numel() * out_host.element_size()
+
+    def one():
+        for k in names:
+            runner.d[k].copy_(host[k], non_blocking=True)
+        runner.step()
+        out_host.copy_(runner.out, non_blocking=True)
+
+    for _ in range(warmup):
+        one()
+    torch.cuda.synchronize()
+    E = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    evs = [(E(), E()) for _ in range(steps)]
+    for a, b in evs:
+        flush.zero_()
+        a.record()
+        one()
+        b.record()
+    torch.cuda.synchronize()
+    ms = [a.elapsed_time(b) for a, b in evs]
+    return ms, h2d, d2h
+
+
+def cpu_baseline(w: workloads.Workload, budget_s: float = 5.0) -> dict:
+    """The oracle as it stands, on the host cores, over the same workload: slot
+    mapping, append and attention sequence by sequence, repeated until the time
+    budget is spent.  Value in KV tokens/s."""
+    import oracle
+    orc = oracle.get()
+    threads = os.cpu_count() or 1
+    c = w.cfg
+    kc, vc = w.bits("k_cache"), w.bits("v_cache")        # append is idempotent: in place
+    bt, cl = w.block_tables.numpy(), w.context_lens.numpy()
+    slots = orc.slot_mapping(bt, cl, c.block_size, c.q_len)
+    qb = w.bits("q")
+    rows_per_seq = c.q_len * c.num_q_heads
+    done_tokens, done_seqs, passes = 0, 0, 0
+    t0 = time.perf_counter()
+    while time.perf_counter() - t0 < budget_s and passes < 100:
+        for i in range(c.num_seqs):
+            sl = slice(i * c.q_len, (i + 1) * c.q_len)
+            orc.append_kv(kc, vc, w.bits("k_new")[sl], w.bits("v_new")[sl], slots[sl])
+            rows = np.arange(i * rows_per_seq, (i + 1) * rows_per_seq)
+            orc.decode(qb, kc, vc, bt, cl, w.scale, c.dtype, q_len=c.q_len, rows=rows,
+                       threads=threads)
+            done_tokens += int(cl[i])
+            done_seqs += 1
+            if time.perf_counter() - t0 > budget_s:
+                break
+        passes += 1
+    dt = time.perf_counter() - t0
+    return {"value": done_tokens / dt, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"{c.name}: {done_seqs} sequence-steps ({passes} pass(es) over the "
+                      f"{c.num_seqs} sequences, {done_tokens} KV tokens), fp64 C oracle, "
+                      f"{threads} threads, {dt:.1f} s wall"}
+
+
+def measure_config(pa, name, seed, device, steps, warmup, flush, world, peaks, e2e=False):
+    w = workloads.make(name, seed=seed, poison=False)
+    runner = Runner(pa, w, device)
+    step_ms, kern_ms, wall = time_device(runner, steps, warmup, flush, world)
+    assert pa.pa_device_error() == 0, "device error during the timed run"
+    ab = algorithmic_bytes(w)
+    total_ms = max_over_ranks(sum(step_ms), world, device)
+    tokens = sum_over_ranks(float(w.total_tokens), world, device)
+    ms_per_step = total_ms / steps
+    kern_avg = statistics.mean(kern_ms)
+    kern_name = "paged_decode_kernel" + ("(partial)" if w.cfg.num_splits > 1 else "")
+    achieved = ab["decode_launch"] / (kern_avg * 1e-3) / 1e9
+    peak = peaks.get("hbm_gbs")
+    peak_src = "measured" if peak else "fallback"
+    peak = peak or FALLBACK_HBM_GBS
+    res = {
+        "w": w, "runner": runner, "ms_per_step": ms_per_step, "value": tokens / (ms_per_step * 1e-3),
+        "wall_s": wall,
+        "step_ms_p10_p50_p90": [float(np.percentile(step_ms, p)) for p in (10, 50, 90)],
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_source": peak_src,
+                     "frac_of_8tbs": achieved / NOMINAL_HBM_GBS,
+                     "traffic": traffic_record(kern_name, name), "kernel": kern_name,
+                     "kernel_us": kern_avg * 1e3,
+                     "bytes_per_launch": ab["decode_launch"],
+                     "bytes_per_kv_token": ab["per_token"]},
+        "step_gbs": ab["step"] / (ms_per_step * 1e-3) / 1e9,
+    }
+    if e2e:
+        ms, h2d, d2h = time_e2e(runner, steps, max(3, warmup), flush)
+        e_ms = max_over_ranks(sum(ms), world, device) / steps
+        res["e2e"] = {"value": tokens / (e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                      "d2h_bytes_per_step": d2h, "ms_per_step": e_ms}
+    return res
+
+
+def config_obj(w: workloads.Workload, path: str) -> dict:
+    c = w.cfg
+    return {"workload": c.name, "num_seqs": c.num_seqs, "num_q_heads": c.num_q_heads,
+            "num_kv_heads": c.num_kv_heads, "head_dim": c.head_dim, "block_size": c.block_size,
+            "kv_dtype": c.dtype, "q_len": c.q_len, "num_splits": c.num_splits,
+            "context_tokens": w.total_tokens, "unique_kv_tokens": w.info["unique_tokens"],
+            "pool_blocks": w.num_blocks, "path": path,
+            "l2": "flushed between steps (512 MiB write, untimed)"}
+
+
+def run_ours(args):
+    world, rank, local = dist_env()
+    init_dist(world)
+    import paged_kv_cache_20_gb300 as pa
+    assert torch.cuda.is_available(), "bench needs a GPU"
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    pa.load()
+    peaks = measured_peaks()
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device)
+    main = args.config
+    with ClockSampler(local) as clk:
+        r = measure_config(pa, main, rank, device, args.steps, args.warmup, flush, world, peaks,
+                           e2e=True)
+    clocks = clk.summary()
+    others = {}
+    if not args.only:
+        for name in OTHER_CONFIGS:
+            if name == main:
+                continue
+            o = measure_config(pa, name, rank, device, args.steps, args.warmup, flush, world,
+                               peaks)
+            others[name] = {"value": o["value"], "unit": UNIT, "ms_per_step": o["ms_per_step"],
+                            "roofline_frac": o["roofline"]["frac"],
+                            "achieved_gbs": o["roofline"]["achieved"],
+                            "kernel_us": o["roofline"]["kernel_us"],
+                            "frac_of_8tbs": o["roofline"]["frac_of_8tbs"],
+                            "config": config_obj(o["w"], _path(o["w"]))}
+            del o
+    cpu = cpu_baseline(r["w"]) if (rank == 0 and not args.no_cpu) else None
+    if rank != 0:
+        return
+    w = r["w"]
+    line = {
+        "metric": METRIC, "value": r["value"], "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": r["ms_per_step"],
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": f"{w.cfg.dtype} in, fp32 accumulate", "data": "synthetic",
+        "config": config_obj(w, _path(w)),
+        "roofline": r["roofline"], "cpu_baseline": cpu, "e2e": r["e2e"],
+        "gpu_launches": args.steps * r["runner"].launches_per_step,
+        "clocks": clocks, "step_p10_p50_p90_ms": r["step_ms_p10_p50_p90"],
+        "step_algorithmic_gbs": r["step_gbs"], "other_configs": others,
+        "kernel_src_sha": kernel_source_sha(),
+    }
+    print(json.dumps(line))
+
+
+def _path(w):
+    return ("pa_slot_mapping+pa_append_kv+pa_decode_partial+pa_decode_combine"
+            if w.cfg.num_splits > 1 else "pa_slot_mapping+pa_append_kv+pa_decode")
+
+
+# --------------------------------------------------------------------------- reference arm
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    orc = oracle.get()
+    threads = os.cpu_count() or 1
+    name = args.config
+    w = workloads.make(name, seed=0, poison=False)
+    c = w.cfg
+    n_seq = max(1, min(c.num_seqs, args.ref_seqs))       # bounded sample per step
+    kc, vc = w.bits("k_cache"), w.bits("v_cache")
+    bt, cl = w.block_tables.numpy(), w.context_lens.numpy()
+    qb = w.bits("q")
+    rows = np.arange(n_seq * c.q_len * c.num_q_heads)
+    tokens = int(cl[:n_seq].sum())
+
+    def step():
+        slots = orc.slot_mapping(bt[:n_seq], cl[:n_seq], c.block_size, c.q_len)
+        orc.append_kv(kc, vc, w.bits("k_new")[:n_seq * c.q_len], w.bits("v_new")[:n_seq * c.q_len],
+                      slots)
+        orc.decode(qb, kc, vc, bt, cl, w.scale, c.dtype, q_len=c.q_len, rows=rows,
+                   threads=threads)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = (time.perf_counter() - t0) / args.steps
+    value = tokens / dt
+    sample = (f"{name}: first {n_seq} of {c.num_seqs} sequences per step ({tokens} KV tokens), "
+              f"fp64 C oracle, {threads} threads")
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic", "config": config_obj(w, "fp64 CPU oracle"),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }))
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", default=DEFAULT_CONFIG, choices=sorted(workloads.CONFIGS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--only", action="store_true", help="skip the other workloads")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
+    ap.add_argument("--ref-seqs", type=int, default=2,
+                    help="sequences per step in the reference arm's bounded sample")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,187 @@
+/*
+ * pagedattn.h -- C ABI of the GB300 (sm_103a) paged decode-attention library
+ * (libpagedattn.so).
+ *
+ * Sources (web pages on LLM inference, cited by short tag):
+ *   [QA]    "LLM推理与服务：面试问题与推荐回答" (LLM inference & serving interview Q&A)
+ *   [SB11]  "Scaling Book 入门第 11 章：推理优化 — KV Cache / Continuous Batching / 量化"
+ *   [H100]  "09-inference-optimization.md" (LLM-Code-Hot-100, "⚡ 推理优化")
+ *   [ANIM]  "推理机制动态图解（进阶）：并行、投机解码、PD、FlashAttention、调度"
+ *   [PANO]  "LLM 推理优化全景实战：从 PagedAttention 到投机解码"
+ *
+ * The KV cache of one attention layer is a pool of fixed-size physical blocks
+ * ([QA] Q2; [PANO] §2.2-2.3).  Each sequence owns a block table mapping its
+ * logical blocks to physical ones, like an operating-system page table.
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ *  - Pointers are DEVICE pointers on the current CUDA device; `stream` is a
+ *    cudaStream_t passed as void* (NULL = legacy default stream).  Every call is
+ *    asynchronous on `stream` and returns after the launch.
+ *  - The caller owns every buffer.  The library allocates no device memory and
+ *    keeps no per-call state; its only device-resident state is one 32-bit error
+ *    word per device (see pa_device_error).
+ *  - 16-bit floating point (fp16 or bf16, chosen by `dtype`) for q, K, V and the
+ *    output; fp32 arithmetic inside.
+ *  - Layouts (dense, row-major):
+ *      k_cache, v_cache  [num_blocks][num_kv_heads][block_size][head_dim]
+ *                        (per page and head, block_size consecutive token rows:
+ *                        the [H100] PagedKVCache page shape
+ *                        [layers, heads, page_size, head_dim] for one layer)
+ *      q, out            [num_seqs][q_len][num_q_heads][head_dim]
+ *      k_new, v_new      [n_tokens][num_kv_heads][head_dim]
+ *      block_tables      int32 [num_seqs][max_blocks_per_seq]
+ *      context_lens      int32 [num_seqs]
+ *      slot_mapping      int64 [n_tokens]
+ *  - Token position pos of sequence i lives in slot
+ *      block_tables[i][pos / block_size] * block_size + pos % block_size
+ *    ([PANO] §2.3 write_kv), i.e. block slot / block_size, row slot % block_size.
+ *  - context_lens count this step's new tokens: append runs first, then
+ *    attention, and a new token attends to itself ([H100] "KV Cache":
+ *    AttentionWithKVCache.forward updates the cache before computing scores).
+ *  - GQA: query head h reads KV head h / (num_q_heads / num_kv_heads)
+ *    (contiguous groups; [QA] Q7, [ANIM] §1 figure).
+ *  - Supported now: block_size 16; head_dim 64 or 128; q_len 1..16.
+ *  - Alignment: every pointer 16-byte aligned.
+ *
+ * Errors: argument checks run on the host before any launch and return
+ * PA_ERR_INVALID_ARG (null pointer, non-positive size, num_q_heads not a
+ * multiple of num_kv_heads, misaligned pointer, workspace too small, sizes whose
+ * indices overflow 32 bits) or PA_ERR_UNSUPPORTED (head_dim, block_size, q_len or
+ * dtype outside the supported set).  A failed launch returns PA_ERR_CUDA.
+ * Kernels never trap or assert: a block id outside [0, num_blocks) or a slot
+ * outside the pool is skipped (attention reads zeros in its place) and sets
+ * PA_ERR_DEVICE_CHECK in the device error word; a device-side wait that exceeds
+ * about two seconds gives up and sets PA_ERR_DEVICE_TIMEOUT.
+ */
+#ifndef PAGEDATTN_H
+#define PAGEDATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define PA_API __attribute__((visibility("default")))
+#else
+#define PA_API
+#endif
+
+typedef enum {
+    PA_OK = 0,
+    PA_ERR_INVALID_ARG = -1,
+    PA_ERR_UNSUPPORTED = -2,
+    PA_ERR_CUDA = -3,
+    PA_ERR_DEVICE_CHECK = -4,
+    PA_ERR_DEVICE_TIMEOUT = -5
+} pa_status;
+
+typedef enum { PA_FP16 = 0, PA_BF16 = 1 } pa_dtype;
+
+/* Human-readable name of a status code (static string, never NULL). */
+PA_API const char *pa_status_string(pa_status status);
+
+/* Library ABI version (major * 100 + minor). */
+PA_API int pa_version(void);
+
+/*
+ * pa_slot_mapping -- slots of this step's new tokens ([PANO] §2.3 write_kv:
+ * logical_block = pos // block_size, block_offset = pos % block_size).
+ * For sequence i the new tokens are its last q_len positions
+ * pos = context_lens[i] - q_len + u (u = 0..q_len-1), written to
+ * slot_mapping[i*q_len + u]; a position < 0 gives -1 (skipped by pa_append_kv).
+ * A position whose logical block is >= max_blocks_per_seq gives -1 and sets
+ * PA_ERR_DEVICE_CHECK.  slot_mapping: int64 [num_seqs*q_len], written.
+ */
+PA_API pa_status pa_slot_mapping(int64_t *slot_mapping, const int32_t *block_tables,
+                                 const int32_t *context_lens, int num_seqs,
+                                 int max_blocks_per_seq, int block_size, int q_len,
+                                 void *stream);
+
+/*
+ * pa_append_kv -- scatter this step's new K/V rows into the pool
+ * ([PANO] §2.3 write_kv; [H100] PagedKVCache.append_token).
+ * Row t of k_new/v_new (all heads) is copied bit for bit to slot
+ * slot_mapping[t]: block slot / block_size, row slot % block_size.  Slots < 0
+ * are skipped; slots >= num_blocks*block_size are skipped and set
+ * PA_ERR_DEVICE_CHECK.  Two tokens with the same slot: undefined which wins.
+ * k_cache, v_cache: read-write.  n_tokens == 0 is a no-op.
+ */
+PA_API pa_status pa_append_kv(void *k_cache, void *v_cache, const void *k_new,
+                              const void *v_new, const int64_t *slot_mapping, int n_tokens,
+                              int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                              pa_dtype dtype, void *stream);
+
+/*
+ * pa_decode -- attention of every query row over its sequence's paged K/V, in
+ * one pass with online softmax ([ANIM] §5: running max m, running sum l,
+ * unnormalised output rescaled by exp(m_old - m_new), output O / l at the end;
+ * [PANO] §2.4 for what is computed: softmax(q K^T * scale) V over the gathered
+ * blocks).  Only positions t < context_lens[i] are used ([H100]
+ * PagedKVCache.get_kv keeps used_slots rows of the last page).  With q_len > 1,
+ * query u of sequence i sees positions t <= context_lens[i] - q_len + u (the
+ * [H100] causal mask triu(diagonal = Lk - Lq + 1)).  A row that sees no
+ * position (context length 0) is written as zeros.
+ * out: [num_seqs][q_len][num_q_heads][head_dim], written (round to nearest even).
+ * The query heads of one GQA group share every K/V read.
+ */
+PA_API pa_status pa_decode(void *out, const void *q, const void *k_cache, const void *v_cache,
+                           const int32_t *block_tables, const int32_t *context_lens,
+                           int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                           int block_size, float scale, void *stream,
+                           int max_blocks_per_seq, int num_blocks, int q_len, pa_dtype dtype);
+
+/*
+ * Split-KV (flash-decoding, [SB11] §11.8): one sequence's blocks are cut into
+ * num_splits partitions processed by different thread blocks, then merged.
+ *
+ * Workspace layout (fp32, caller-allocated, pa_decode_workspace_size bytes),
+ * with R = q_len * num_q_heads rows per sequence (row u*num_q_heads + h):
+ *   acc [num_seqs][num_splits][R][head_dim]   unnormalised sum_t 2^(s_t - m) V_t
+ *   m   [num_seqs][num_splits][R]             max_t s_t  (-inf if empty)
+ *   l   [num_seqs][num_splits][R]             sum_t 2^(s_t - m)  (0 if empty)
+ * where s_t = scale * log2(e) * q.k_t (base-2 units).  Section m starts at
+ * byte offset align256(sizeof acc), section l at align256 after m.
+ * Partition p of sequence i covers blocks [p*C, (p+1)*C) with
+ * C = ceil(ceil(context_lens[i] / block_size) / num_splits); partitions past
+ * the end are empty.
+ */
+PA_API size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int q_len, int head_dim,
+                                       int num_splits);
+
+/* Partial pass: writes every (sequence, partition, row) entry of the workspace. */
+PA_API pa_status pa_decode_partial(void *workspace, size_t workspace_bytes, const void *q,
+                                   const void *k_cache, const void *v_cache,
+                                   const int32_t *block_tables, const int32_t *context_lens,
+                                   int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                                   int block_size, float scale, int num_splits,
+                                   int max_blocks_per_seq, int num_blocks, int q_len,
+                                   pa_dtype dtype, void *stream);
+
+/*
+ * Combine pass (the online-softmax rescale of [ANIM] §5 applied across
+ * partitions): M = max_p m_p; out = sum_p 2^(m_p - M) acc_p / sum_p 2^(m_p - M) l_p
+ * over non-empty partitions; zeros if all are empty.  Reads the workspace,
+ * writes out [num_seqs][q_len][num_q_heads][head_dim].
+ */
+PA_API pa_status pa_decode_combine(void *out, const void *workspace, size_t workspace_bytes,
+                                   int num_seqs, int num_q_heads, int head_dim, int q_len,
+                                   int num_splits, pa_dtype dtype, void *stream);
+
+/*
+ * pa_device_error -- synchronise `stream`, then return PA_OK or the first error
+ * recorded by a kernel on the current device since the last clear
+ * (PA_ERR_DEVICE_TIMEOUT takes precedence over PA_ERR_DEVICE_CHECK).  With
+ * clear != 0 the word is reset to zero.  Returns PA_ERR_CUDA if the
+ * synchronisation itself fails.
+ */
+PA_API pa_status pa_device_error(void *stream, int clear);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGEDATTN_H */

@@ -1,0 +1,372 @@
+// pa_api.cu -- the C ABI of libpagedattn.so: argument validation, TMA tensor-map
+// encoding, launch dispatch, the per-device error word, and the two small
+// scatter kernels (slot mapping and KV append).
+//
+// Slot arithmetic and append follow "LLM 推理优化全景实战：从 PagedAttention 到投机解码"
+// §2.3 (write_kv: logical_block = pos // block_size, block_offset = pos % block_size,
+// physical block from the request's page table) and "09-inference-optimization.md"
+// (LLM-Code-Hot-100), PagedKVCache.append_token (write the new token's K/V into
+// its slot of the last page).
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "../../include/pagedattn.h"
+#include "pa_decode.cuh"
+#include "pa_launch.h"
+
+namespace {
+
+constexpr int kBlockSize = 16;
+constexpr int kMaxDevices = 64;
+constexpr int kMaxQLen = 16;
+
+__device__ unsigned int g_error_word;  // one per device (module global)
+
+// ---- scatter kernels ---------------------------------------------------------------
+
+__global__ void slot_mapping_kernel(int64_t *out, const int32_t *block_tables,
+                                    const int32_t *context_lens, int num_seqs,
+                                    int max_blocks_per_seq, int block_size, int q_len,
+                                    unsigned *err) {
+  const int idx = blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= num_seqs * q_len) return;
+  const int i = idx / q_len, u = idx % q_len;
+  const int64_t pos = (int64_t)context_lens[i] - q_len + u;
+  int64_t slot = -1;
+  if (pos >= 0) {
+    const int64_t logical_block = pos / block_size;
+    if (logical_block < max_blocks_per_seq) {
+      const int64_t physical_block = block_tables[(int64_t)i * max_blocks_per_seq + logical_block];
+      slot = physical_block * block_size + pos % block_size;
+    } else {
+      pa::record_error(err, pa::kErrCheck);
+    }
+  }
+  out[idx] = slot;
+}
+
+// One thread per 16-byte chunk of one (token, head) row; K and V together.
+template <int D>
+__global__ void append_kv_kernel(uint16_t *k_cache, uint16_t *v_cache, const uint16_t *k_new,
+                                 const uint16_t *v_new, const int64_t *slot_mapping, int n_tokens,
+                                 int num_kv_heads, int64_t num_slots, unsigned *err) {
+  constexpr int kChunks = D / 8;
+  const int64_t total = (int64_t)n_tokens * num_kv_heads * kChunks;
+  for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
+       idx += (int64_t)gridDim.x * blockDim.x) {
+    const int c = (int)(idx % kChunks);
+    const int64_t th = idx / kChunks;
+    const int h = (int)(th % num_kv_heads);
+    const int64_t t = th / num_kv_heads;
+    const int64_t slot = slot_mapping[t];
+    if (slot < 0) continue;
+    if (slot >= num_slots) {
+      if (c == 0 && h == 0) pa::record_error(err, pa::kErrCheck);
+      continue;
+    }
+    const int64_t block = slot / kBlockSize, offset = slot % kBlockSize;
+    const int64_t dst = ((block * num_kv_heads + h) * kBlockSize + offset) * D + c * 8;
+    const int64_t src = (t * num_kv_heads + h) * D + c * 8;
+    const uint4 kv = __ldg(reinterpret_cast<const uint4 *>(k_new + src));
+    const uint4 vv = __ldg(reinterpret_cast<const uint4 *>(v_new + src));
+    *reinterpret_cast<uint4 *>(k_cache + dst) = kv;
+    *reinterpret_cast<uint4 *>(v_cache + dst) = vv;
+  }
+}
+
+// ---- host helpers --------------------------------------------------------------------
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+void load_encode() {
+  void *fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                       &q) == cudaSuccess &&
+      q == cudaDriverEntryPointSuccess)
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+}
+
+std::mutex g_err_mutex;
+unsigned *g_err_ptr[kMaxDevices] = {};
+
+// Device address of this device's error word (looked up once per device).
+unsigned *error_word() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(g_err_mutex);
+  if (g_err_ptr[dev] == nullptr) {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_error_word) != cudaSuccess) return nullptr;
+    g_err_ptr[dev] = static_cast<unsigned *>(p);
+  }
+  return g_err_ptr[dev];
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool supported_dtype(pa_dtype d) { return d == PA_FP16 || d == PA_BF16; }
+
+// Tensor map over one cache: [num_blocks * num_kv_heads tiles][16 rows][head_dim],
+// box = 16 rows x 64 columns, 128-byte swizzle, zero fill outside.
+pa_status make_map(CUtensorMap *map, const void *cache, pa_dtype dtype, int head_dim,
+                   int num_blocks, int num_kv_heads) {
+  std::call_once(g_encode_once, load_encode);
+  if (g_encode == nullptr) return PA_ERR_CUDA;
+  cuuint64_t dims[3] = {(cuuint64_t)head_dim, (cuuint64_t)kBlockSize,
+                        (cuuint64_t)num_blocks * (cuuint64_t)num_kv_heads};
+  cuuint64_t strides[2] = {(cuuint64_t)head_dim * 2, (cuuint64_t)kBlockSize * head_dim * 2};
+  cuuint32_t box[3] = {64, (cuuint32_t)kBlockSize, 1};
+  cuuint32_t elem_strides[3] = {1, 1, 1};
+  CUresult r = g_encode(map,
+                        dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                         : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                        3, const_cast<void *>(cache), dims, strides, box, elem_strides,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? PA_OK : PA_ERR_CUDA;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+struct WsLayout {
+  size_t acc_off, m_off, l_off, total;
+};
+
+WsLayout ws_layout(int num_seqs, int num_q_heads, int q_len, int head_dim, int num_splits) {
+  const size_t rows = (size_t)num_seqs * num_splits * q_len * num_q_heads;
+  WsLayout w;
+  w.acc_off = 0;
+  w.m_off = align256(rows * head_dim * sizeof(float));
+  w.l_off = w.m_off + align256(rows * sizeof(float));
+  w.total = w.l_off + align256(rows * sizeof(float));
+  return w;
+}
+
+// Checks shared by pa_decode and pa_decode_partial.
+pa_status check_decode(const void *q, const void *k_cache, const void *v_cache,
+                       const int32_t *block_tables, const int32_t *context_lens, int num_seqs,
+                       int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                       float scale, int max_blocks_per_seq, int num_blocks, int q_len,
+                       pa_dtype dtype) {
+  if (!q || !k_cache || !v_cache || !block_tables || !context_lens) return PA_ERR_INVALID_ARG;
+  if (num_seqs <= 0 || num_q_heads <= 0 || num_kv_heads <= 0 || max_blocks_per_seq <= 0 ||
+      num_blocks <= 0 || q_len <= 0 || head_dim <= 0 || block_size <= 0)
+    return PA_ERR_INVALID_ARG;
+  if (num_q_heads % num_kv_heads != 0) return PA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return PA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache)) return PA_ERR_INVALID_ARG;
+  if (!supported_dtype(dtype)) return PA_ERR_UNSUPPORTED;
+  if (head_dim != 64 && head_dim != 128) return PA_ERR_UNSUPPORTED;
+  if (block_size != kBlockSize) return PA_ERR_UNSUPPORTED;
+  if (q_len > kMaxQLen) return PA_ERR_UNSUPPORTED;
+  // 32-bit index limits used by the kernels
+  if ((int64_t)num_blocks * num_kv_heads >= (int64_t)1 << 31) return PA_ERR_INVALID_ARG;
+  if ((int64_t)num_seqs * max_blocks_per_seq >= (int64_t)1 << 31) return PA_ERR_INVALID_ARG;
+  if ((int64_t)num_seqs * q_len * num_q_heads >= (int64_t)1 << 31) return PA_ERR_INVALID_ARG;
+  return PA_OK;
+}
+
+pa_status decode_common(void *out, float *ws, const WsLayout *lay, const void *q,
+                        const void *k_cache, const void *v_cache, const int32_t *block_tables,
+                        const int32_t *context_lens, int num_seqs, int num_q_heads,
+                        int num_kv_heads, int head_dim, float scale, int num_splits,
+                        int max_blocks_per_seq, int num_blocks, int q_len, pa_dtype dtype,
+                        void *stream) {
+  const int64_t units = (int64_t)num_seqs * num_kv_heads * num_splits;
+  if (units >= (int64_t)1 << 31) return PA_ERR_INVALID_ARG;
+  CUtensorMap kmap, vmap;
+  pa_status st = make_map(&kmap, k_cache, dtype, head_dim, num_blocks, num_kv_heads);
+  if (st != PA_OK) return st;
+  st = make_map(&vmap, v_cache, dtype, head_dim, num_blocks, num_kv_heads);
+  if (st != PA_OK) return st;
+  pa::DecodeArgs a;
+  a.q = q;
+  a.out = out;
+  a.ws_acc = ws ? reinterpret_cast<float *>(reinterpret_cast<char *>(ws) + lay->acc_off) : nullptr;
+  a.ws_m = ws ? reinterpret_cast<float *>(reinterpret_cast<char *>(ws) + lay->m_off) : nullptr;
+  a.ws_l = ws ? reinterpret_cast<float *>(reinterpret_cast<char *>(ws) + lay->l_off) : nullptr;
+  a.block_tables = block_tables;
+  a.context_lens = context_lens;
+  a.err = error_word();
+  if (a.err == nullptr) return PA_ERR_CUDA;
+  a.num_seqs = num_seqs;
+  a.num_q_heads = num_q_heads;
+  a.num_kv_heads = num_kv_heads;
+  a.q_len = q_len;
+  a.group = num_q_heads / num_kv_heads;
+  a.rows = a.group * q_len;
+  a.max_blocks_per_seq = max_blocks_per_seq;
+  a.num_blocks = num_blocks;
+  a.num_splits = num_splits;
+  a.scale_log2 = scale * 1.4426950408889634f;  // log2(e)
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const bool partial = ws != nullptr;
+  cudaError_t e = dtype == PA_FP16
+                      ? pa::launch_decode_fp16(kmap, vmap, a, head_dim, partial, (int)units, s)
+                      : pa::launch_decode_bf16(kmap, vmap, a, head_dim, partial, (int)units, s);
+  return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+PA_API const char *pa_status_string(pa_status status) {
+  switch (status) {
+    case PA_OK: return "PA_OK";
+    case PA_ERR_INVALID_ARG: return "PA_ERR_INVALID_ARG";
+    case PA_ERR_UNSUPPORTED: return "PA_ERR_UNSUPPORTED";
+    case PA_ERR_CUDA: return "PA_ERR_CUDA";
+    case PA_ERR_DEVICE_CHECK: return "PA_ERR_DEVICE_CHECK";
+    case PA_ERR_DEVICE_TIMEOUT: return "PA_ERR_DEVICE_TIMEOUT";
+  }
+  return "PA_UNKNOWN_STATUS";
+}
+
+PA_API int pa_version(void) { return 100; }
+
+PA_API pa_status pa_slot_mapping(int64_t *slot_mapping, const int32_t *block_tables,
+                                 const int32_t *context_lens, int num_seqs,
+                                 int max_blocks_per_seq, int block_size, int q_len,
+                                 void *stream) {
+  if (!slot_mapping || !block_tables || !context_lens) return PA_ERR_INVALID_ARG;
+  if (num_seqs <= 0 || max_blocks_per_seq <= 0 || block_size <= 0 || q_len <= 0)
+    return PA_ERR_INVALID_ARG;
+  if (block_size != kBlockSize) return PA_ERR_UNSUPPORTED;
+  if ((int64_t)num_seqs * q_len >= (int64_t)1 << 31 ||
+      (int64_t)num_seqs * max_blocks_per_seq >= (int64_t)1 << 31)
+    return PA_ERR_INVALID_ARG;
+  unsigned *err = error_word();
+  if (err == nullptr) return PA_ERR_CUDA;
+  const int n = num_seqs * q_len;
+  slot_mapping_kernel<<<(n + 255) / 256, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+      slot_mapping, block_tables, context_lens, num_seqs, max_blocks_per_seq, block_size, q_len,
+      err);
+  return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+PA_API pa_status pa_append_kv(void *k_cache, void *v_cache, const void *k_new, const void *v_new,
+                              const int64_t *slot_mapping, int n_tokens, int num_kv_heads,
+                              int head_dim, int block_size, int num_blocks, pa_dtype dtype,
+                              void *stream) {
+  if (!k_cache || !v_cache || !k_new || !v_new || !slot_mapping) return PA_ERR_INVALID_ARG;
+  if (n_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 || num_blocks <= 0)
+    return PA_ERR_INVALID_ARG;
+  if (!aligned16(k_cache) || !aligned16(v_cache) || !aligned16(k_new) || !aligned16(v_new))
+    return PA_ERR_INVALID_ARG;
+  if (!supported_dtype(dtype)) return PA_ERR_UNSUPPORTED;
+  if (head_dim != 64 && head_dim != 128) return PA_ERR_UNSUPPORTED;
+  if (block_size != kBlockSize) return PA_ERR_UNSUPPORTED;
+  if (n_tokens == 0) return PA_OK;
+  unsigned *err = error_word();
+  if (err == nullptr) return PA_ERR_CUDA;
+  const int64_t total = (int64_t)n_tokens * num_kv_heads * (head_dim / 8);
+  const int threads = 256;
+  const int blocks = (int)std::min<int64_t>((total + threads - 1) / threads, 1 << 20);
+  const int64_t num_slots = (int64_t)num_blocks * kBlockSize;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  auto kc = static_cast<uint16_t *>(k_cache);
+  auto vc = static_cast<uint16_t *>(v_cache);
+  auto kn = static_cast<const uint16_t *>(k_new);
+  auto vn = static_cast<const uint16_t *>(v_new);
+  if (head_dim == 128)
+    append_kv_kernel<128><<<blocks, threads, 0, s>>>(kc, vc, kn, vn, slot_mapping, n_tokens,
+                                                     num_kv_heads, num_slots, err);
+  else
+    append_kv_kernel<64><<<blocks, threads, 0, s>>>(kc, vc, kn, vn, slot_mapping, n_tokens,
+                                                    num_kv_heads, num_slots, err);
+  return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+PA_API pa_status pa_decode(void *out, const void *q, const void *k_cache, const void *v_cache,
+                           const int32_t *block_tables, const int32_t *context_lens,
+                           int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                           int block_size, float scale, void *stream, int max_blocks_per_seq,
+                           int num_blocks, int q_len, pa_dtype dtype) {
+  if (!out || !aligned16(out)) return PA_ERR_INVALID_ARG;
+  pa_status st = check_decode(q, k_cache, v_cache, block_tables, context_lens, num_seqs,
+                              num_q_heads, num_kv_heads, head_dim, block_size, scale,
+                              max_blocks_per_seq, num_blocks, q_len, dtype);
+  if (st != PA_OK) return st;
+  return decode_common(out, nullptr, nullptr, q, k_cache, v_cache, block_tables, context_lens,
+                       num_seqs, num_q_heads, num_kv_heads, head_dim, scale, 1,
+                       max_blocks_per_seq, num_blocks, q_len, dtype, stream);
+}
+
+PA_API size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int q_len, int head_dim,
+                                       int num_splits) {
+  if (num_seqs <= 0 || num_q_heads <= 0 || q_len <= 0 || head_dim <= 0 || num_splits <= 0)
+    return 0;
+  return ws_layout(num_seqs, num_q_heads, q_len, head_dim, num_splits).total;
+}
+
+PA_API pa_status pa_decode_partial(void *workspace, size_t workspace_bytes, const void *q,
+                                   const void *k_cache, const void *v_cache,
+                                   const int32_t *block_tables, const int32_t *context_lens,
+                                   int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                                   int block_size, float scale, int num_splits,
+                                   int max_blocks_per_seq, int num_blocks, int q_len,
+                                   pa_dtype dtype, void *stream) {
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return PA_ERR_INVALID_ARG;
+  if (num_splits <= 0) return PA_ERR_INVALID_ARG;
+  pa_status st = check_decode(q, k_cache, v_cache, block_tables, context_lens, num_seqs,
+                              num_q_heads, num_kv_heads, head_dim, block_size, scale,
+                              max_blocks_per_seq, num_blocks, q_len, dtype);
+  if (st != PA_OK) return st;
+  const WsLayout lay = ws_layout(num_seqs, num_q_heads, q_len, head_dim, num_splits);
+  if (workspace_bytes < lay.total) return PA_ERR_INVALID_ARG;
+  return decode_common(nullptr, static_cast<float *>(workspace), &lay, q, k_cache, v_cache,
+                       block_tables, context_lens, num_seqs, num_q_heads, num_kv_heads, head_dim,
+                       scale, num_splits, max_blocks_per_seq, num_blocks, q_len, dtype, stream);
+}
+
+PA_API pa_status pa_decode_combine(void *out, const void *workspace, size_t workspace_bytes,
+                                   int num_seqs, int num_q_heads, int head_dim, int q_len,
+                                   int num_splits, pa_dtype dtype, void *stream) {
+  if (!out || !workspace || !aligned16(out) || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return PA_ERR_INVALID_ARG;
+  if (num_seqs <= 0 || num_q_heads <= 0 || head_dim <= 0 || q_len <= 0 || num_splits <= 0)
+    return PA_ERR_INVALID_ARG;
+  if (!supported_dtype(dtype)) return PA_ERR_UNSUPPORTED;
+  if (head_dim != 64 && head_dim != 128) return PA_ERR_UNSUPPORTED;
+  if (q_len > kMaxQLen) return PA_ERR_UNSUPPORTED;
+  if ((int64_t)num_seqs * q_len * num_q_heads >= (int64_t)1 << 31) return PA_ERR_INVALID_ARG;
+  const WsLayout lay = ws_layout(num_seqs, num_q_heads, q_len, head_dim, num_splits);
+  if (workspace_bytes < lay.total) return PA_ERR_INVALID_ARG;
+  const char *base = static_cast<const char *>(workspace);
+  pa::CombineArgs a;
+  a.out = out;
+  a.ws_acc = reinterpret_cast<const float *>(base + lay.acc_off);
+  a.ws_m = reinterpret_cast<const float *>(base + lay.m_off);
+  a.ws_l = reinterpret_cast<const float *>(base + lay.l_off);
+  a.num_seqs = num_seqs;
+  a.rows_per_seq = q_len * num_q_heads;
+  a.num_splits = num_splits;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = dtype == PA_FP16 ? pa::launch_combine_fp16(a, head_dim, s)
+                                   : pa::launch_combine_bf16(a, head_dim, s);
+  return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+PA_API pa_status pa_device_error(void *stream, int clear) {
+  unsigned *err = error_word();
+  if (err == nullptr) return PA_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  unsigned host = 0;
+  if (cudaMemcpyAsync(&host, err, sizeof(host), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return PA_ERR_CUDA;
+  if (clear && cudaMemsetAsync(err, 0, sizeof(unsigned), s) != cudaSuccess) return PA_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return PA_ERR_CUDA;
+  if (host & pa::kErrTimeout) return PA_ERR_DEVICE_TIMEOUT;
+  if (host & pa::kErrCheck) return PA_ERR_DEVICE_CHECK;
+  return PA_OK;
+}
+
+}  // extern "C"

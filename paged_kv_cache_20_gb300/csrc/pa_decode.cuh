@@ -1,0 +1,630 @@
+// pa_decode.cuh -- paged decode attention kernels for sm_103a.
+//
+// What is computed (pages cited by title):
+//   "LLM 推理优化全景实战：从 PagedAttention 到投机解码" §2.4: attention of a query
+//   over the K/V rows gathered from the sequence's physical blocks,
+//   softmax(q K^T * scale) V;
+//   "09-inference-optimization.md" (LLM-Code-Hot-100), PagedKVCache.get_kv: only
+//   the used slots of the last page take part; AttentionWithKVCache.forward: the
+//   causal offset triu(diagonal = Lk - Lq + 1) when several queries are new;
+//   "推理机制动态图解（进阶）" §5: online softmax -- running max m, running sum l,
+//   unnormalised output rescaled by 2^(m_old - m_new) when the max grows, O / l at
+//   the end, so the score row is never written out;
+//   "Scaling Book 入门第 11 章" §11.8 (FlashDecoding): a sequence's KV split over
+//   several thread blocks, merged afterwards.
+//
+// Design (GB300-first, not a port of any earlier kernel):
+//   * One CTA = one work unit (sequence, KV head, split partition, row group).
+//     All query rows of a GQA group (times the q_len new positions) are served
+//     by every K/V tile the CTA reads, so each KV byte leaves HBM once.
+//   * Each of the NW warps owns an NSTAGE-deep ring of shared-memory stages.
+//     Lane 0 of the warp looks up the physical block id and issues TMA tiled
+//     loads (cp.async.bulk.tensor, 128-byte swizzle) of the whole 16-token K and
+//     V tiles of its next block into a stage; completion arrives on the stage's
+//     mbarrier.  Warps take the unit's blocks round-robin and keep independent
+//     online-softmax states, merged once at the end (warp shuffles, then shared
+//     memory).  No CTA-wide synchronisation inside the block loop.
+//   * A tensor map covers the cache as [num_blocks*num_kv_heads][16][head_dim],
+//     so a bad block id turns into an out-of-range TMA coordinate (zero fill),
+//     never an out-of-bounds address; the id is also reported in the error word.
+//   * Rows per unit 1..2: CUDA-core FMA path.  The K lanes sharing a token each
+//     hold head_dim/K dimensions of q in registers; partial dot products are
+//     summed with a K-lane butterfly.  Lanes that hold different tokens keep
+//     separate softmax states, so no warp-wide reduction is needed per block.
+//   * Rows per unit 3..16: warp-level tensor cores (mma.sync m16n8k16, fp32
+//     accumulate).  S = Q K^T with Q (16 rows, padded) as the A operand from
+//     registers and K^T from ldmatrix; P = 2^(S - m) re-packed in registers as the
+//     A operand of O += P V, V^T fragments from ldmatrix.trans.
+//   * Slots past the context (and NaN-poisoned padding) never reach the
+//     arithmetic: scores are replaced by -inf with a select and V rows past the
+//     context are zeroed in shared memory before P.V (0 * NaN would be NaN).
+#pragma once
+
+#include "pa_device.cuh"
+
+namespace pa {
+
+constexpr int kTileTokens = 16;  // block_size: tokens per physical block / TMA tile
+
+struct DecodeArgs {
+  const void *q;                 // [num_seqs][q_len][num_q_heads][D]
+  void *out;                     // [num_seqs][q_len][num_q_heads][D]   (single pass)
+  float *ws_acc;                 // split-KV workspace sections (partial pass)
+  float *ws_m;
+  float *ws_l;
+  const int32_t *block_tables;   // [num_seqs][max_blocks_per_seq]
+  const int32_t *context_lens;   // [num_seqs]
+  unsigned *err;                 // device error word
+  int num_seqs, num_q_heads, num_kv_heads, q_len, group, rows;  // rows = group * q_len
+  int max_blocks_per_seq, num_blocks, num_splits;
+  float scale_log2;              // scale * log2(e): scores in base-2 units
+};
+
+// ---------------------------------------------------------------------------------
+// Row bookkeeping shared by both paths.  Unit row rho (0 <= rho < rows) is query
+// position u = rho / group of query head kvh * group + rho % group.
+struct RowInfo {
+  int u, h, valid;
+};
+
+__device__ __forceinline__ RowInfo row_info(const DecodeArgs &a, int kvh, int rho) {
+  RowInfo ri;
+  ri.valid = rho < a.rows;
+  const int r = ri.valid ? rho : 0;
+  ri.u = r / a.group;
+  ri.h = kvh * a.group + r % a.group;
+  return ri;
+}
+
+// ---------------------------------------------------------------------------------
+// CUDA-core path: R rows, K lanes per token.
+template <typename T, int D, int K, int R>
+struct FmaPath {
+  static constexpr int RPC = R;                    // rows per CTA
+  static constexpr int TPP = 32 / K;               // tokens per pass
+  static constexpr int PASSES = kTileTokens / TPP;  // passes per tile
+  static constexpr int CH = D / 8 / K;             // 16-byte chunks per lane per token
+  // Under the 128-byte swizzle, head_dim 128 with 4 or 8 lanes per token puts
+  // two lanes of an 8-lane shared-memory phase on one bank group unless each lane
+  // starts its chunk loop at a lane-dependent rotation; the rotation below makes
+  // every phase hit 8 distinct groups (checked exhaustively for these shapes).
+  static constexpr bool kRotate = (D == 128 && (K == 4 || K == 8));
+  static constexpr int kRotShift = (K == 8) ? 2 : 0;
+  static_assert(PASSES * TPP == kTileTokens && CH >= 1, "bad lane layout");
+
+  float q[R][CH * 8];
+  float acc[R][CH * 8];
+  float m[R], l[R];
+  int lim[R];
+  int part, tip, rot;
+
+  __device__ __forceinline__ int chunk(int jj) const {
+    return part * CH + (kRotate ? ((jj + rot) % CH) : jj);
+  }
+
+  __device__ __forceinline__ void init(const DecodeArgs &a, int seq, int kvh, int row0, int L) {
+    const int lane = threadIdx.x & 31;
+    part = lane % K;
+    tip = lane / K;
+    rot = (lane >> kRotShift) % CH;
+    const T *qb = static_cast<const T *>(a.q);
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      const RowInfo ri = row_info(a, kvh, row0 + r);
+      lim[r] = ri.valid ? (L - a.q_len + ri.u + 1) : 0;
+      m[r] = -INFINITY;
+      l[r] = 0.f;
+      const T *qrow = qb + ((size_t)(seq * a.q_len + ri.u) * a.num_q_heads + ri.h) * D;
+#pragma unroll
+      for (int jj = 0; jj < CH; ++jj) {
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (ri.valid) v = __ldg(reinterpret_cast<const uint4 *>(qrow + chunk(jj) * 8));
+        const float2 f0 = Elt<T>::to_f2(v.x), f1 = Elt<T>::to_f2(v.y);
+        const float2 f2 = Elt<T>::to_f2(v.z), f3 = Elt<T>::to_f2(v.w);
+        const float f[8] = {f0.x, f0.y, f1.x, f1.y, f2.x, f2.y, f3.x, f3.y};
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          q[r][jj * 8 + e] = f[e] * a.scale_log2;
+          acc[r][jj * 8 + e] = 0.f;
+        }
+      }
+    }
+  }
+
+  template <bool MASKED>
+  __device__ __forceinline__ void tile(uint32_t kt, uint32_t vt, int tile_idx, float) {
+    float s[PASSES][R];
+#pragma unroll
+    for (int p = 0; p < PASSES; ++p) {
+      const int t = p * TPP + tip;
+#pragma unroll
+      for (int r = 0; r < R; ++r) s[p][r] = 0.f;
+#pragma unroll
+      for (int jj = 0; jj < CH; ++jj) {
+        const uint4 kv = lds128(kt + sw128_offset<kTileTokens>(t, chunk(jj)));
+        const float2 f0 = Elt<T>::to_f2(kv.x), f1 = Elt<T>::to_f2(kv.y);
+        const float2 f2 = Elt<T>::to_f2(kv.z), f3 = Elt<T>::to_f2(kv.w);
+        const float f[8] = {f0.x, f0.y, f1.x, f1.y, f2.x, f2.y, f3.x, f3.y};
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+#pragma unroll
+          for (int e = 0; e < 8; ++e) s[p][r] = fmaf(q[r][jj * 8 + e], f[e], s[p][r]);
+      }
+    }
+    // sum the K partial dot products of each token (bitwise identical on all K lanes)
+#pragma unroll
+    for (int p = 0; p < PASSES; ++p)
+#pragma unroll
+      for (int r = 0; r < R; ++r)
+#pragma unroll
+        for (int o = 1; o < K; o <<= 1) s[p][r] += __shfl_xor_sync(0xffffffffu, s[p][r], o);
+    if (MASKED) {
+#pragma unroll
+      for (int p = 0; p < PASSES; ++p) {
+        const int tg = tile_idx * kTileTokens + p * TPP + tip;
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+          if (tg >= lim[r]) s[p][r] = -INFINITY;
+      }
+    }
+    // online softmax, per lane group (tokens p*TPP + tip)
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      float mx = s[0][r];
+#pragma unroll
+      for (int p = 1; p < PASSES; ++p) mx = fmaxf(mx, s[p][r]);
+      if (mx > m[r]) {
+        const float c = fast_exp2(m[r] - mx);  // m = -inf -> 0
+        l[r] *= c;
+#pragma unroll
+        for (int e = 0; e < CH * 8; ++e) acc[r][e] *= c;
+        m[r] = mx;
+      }
+#pragma unroll
+      for (int p = 0; p < PASSES; ++p) {
+        float pv;
+        if (MASKED)
+          pv = (s[p][r] == -INFINITY) ? 0.f : fast_exp2(s[p][r] - m[r]);
+        else
+          pv = fast_exp2(s[p][r] - m[r]);
+        s[p][r] = pv;
+        l[r] += pv;
+      }
+    }
+    // P.V
+#pragma unroll
+    for (int p = 0; p < PASSES; ++p) {
+      const int t = p * TPP + tip;
+#pragma unroll
+      for (int jj = 0; jj < CH; ++jj) {
+        const uint4 vv = lds128(vt + sw128_offset<kTileTokens>(t, chunk(jj)));
+        const float2 f0 = Elt<T>::to_f2(vv.x), f1 = Elt<T>::to_f2(vv.y);
+        const float2 f2 = Elt<T>::to_f2(vv.z), f3 = Elt<T>::to_f2(vv.w);
+        const float f[8] = {f0.x, f0.y, f1.x, f1.y, f2.x, f2.y, f3.x, f3.y};
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+#pragma unroll
+          for (int e = 0; e < 8; ++e) acc[r][jj * 8 + e] = fmaf(s[p][r], f[e], acc[r][jj * 8 + e]);
+      }
+    }
+  }
+
+  // Merge the lane groups of this warp, then publish the warp's state:
+  // mrg_m/mrg_l [RPC], mrg_acc [RPC][D] for this warp.
+  __device__ __forceinline__ void publish(float *mrg_m, float *mrg_l, float *mrg_acc) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int o = K; o < 32; o <<= 1) {
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        const float mo = __shfl_xor_sync(0xffffffffu, m[r], o);
+        const float lo = __shfl_xor_sync(0xffffffffu, l[r], o);
+        const float mn = fmaxf(m[r], mo);
+        const float cs = (m[r] == -INFINITY) ? 0.f : fast_exp2(m[r] - mn);
+        const float co = (mo == -INFINITY) ? 0.f : fast_exp2(mo - mn);
+        l[r] = l[r] * cs + lo * co;
+#pragma unroll
+        for (int e = 0; e < CH * 8; ++e) {
+          const float ao = __shfl_xor_sync(0xffffffffu, acc[r][e], o);
+          acc[r][e] = acc[r][e] * cs + ao * co;
+        }
+        m[r] = mn;
+      }
+    }
+    if (lane < K) {
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        if (lane == 0) {
+          mrg_m[r] = m[r];
+          mrg_l[r] = l[r];
+        }
+#pragma unroll
+        for (int jj = 0; jj < CH; ++jj) {
+          float4 *dst = reinterpret_cast<float4 *>(mrg_acc + r * D + chunk(jj) * 8);
+          dst[0] = make_float4(acc[r][jj * 8 + 0], acc[r][jj * 8 + 1], acc[r][jj * 8 + 2],
+                               acc[r][jj * 8 + 3]);
+          dst[1] = make_float4(acc[r][jj * 8 + 4], acc[r][jj * 8 + 5], acc[r][jj * 8 + 6],
+                               acc[r][jj * 8 + 7]);
+        }
+      }
+    }
+  }
+};
+
+// ---------------------------------------------------------------------------------
+// Tensor-core path: up to 16 rows (padded), warp-level mma.sync m16n8k16.
+template <typename T, int D>
+struct MmaPath {
+  static constexpr int RPC = 16;
+  static constexpr int KS = D / 16;  // k-steps of S = Q K^T
+  static constexpr int NT = D / 8;   // n-tiles (8 dims) of O
+
+  uint32_t qa[KS][4];  // A fragments of Q
+  float o[NT][4];      // O: rows (lane/4, lane/4 + 8), dims nt*8 + (lane%4)*2 + {0,1}
+  float m[2], l[2];
+  int lim[2];
+
+  __device__ __forceinline__ void init(const DecodeArgs &a, int seq, int kvh, int row0, int L) {
+    const int lane = threadIdx.x & 31;
+    const int g = lane >> 2, c2 = (lane & 3) * 2;
+    const T *qb = static_cast<const T *>(a.q);
+    const T *qrow[2];
+#pragma unroll
+    for (int hr = 0; hr < 2; ++hr) {
+      const RowInfo ri = row_info(a, kvh, row0 + g + 8 * hr);
+      lim[hr] = ri.valid ? (L - a.q_len + ri.u + 1) : 0;
+      qrow[hr] = ri.valid ? qb + ((size_t)(seq * a.q_len + ri.u) * a.num_q_heads + ri.h) * D
+                          : nullptr;
+      m[hr] = -INFINITY;
+      l[hr] = 0.f;
+    }
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int hr = i & 1, col = ks * 16 + c2 + (i >> 1) * 8;
+        qa[ks][i] = qrow[hr] ? __ldg(reinterpret_cast<const uint32_t *>(qrow[hr] + col)) : 0u;
+      }
+    }
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) o[nt][e] = 0.f;
+  }
+
+  template <bool MASKED>
+  __device__ __forceinline__ void tile(uint32_t kt, uint32_t vt, int tile_idx, float scale_log2) {
+    const int lane = threadIdx.x & 31;
+    const int mi = lane >> 3, ri = lane & 7;
+    float sc[2][4];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) sc[nt][e] = 0.f;
+    // S = Q K^T: B fragments (K rows = tokens, 8 dims each) by ldmatrix
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+      uint32_t b00, b01, b10, b11;
+      const int tok = ri + ((mi >> 1) << 3), ch = 2 * ks + (mi & 1);
+      ldmatrix_x4(kt + sw128_offset<kTileTokens>(tok, ch), b00, b01, b10, b11);
+      Elt<T>::mma16816(sc[0], qa[ks], b00, b01);
+      Elt<T>::mma16816(sc[1], qa[ks], b10, b11);
+    }
+    // scale to base-2 units, mask, row max over the 16 tokens (4 lanes per row)
+    float mx[2];
+#pragma unroll
+    for (int hr = 0; hr < 2; ++hr) {
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          float v = sc[nt][2 * hr + e] * scale_log2;
+          if (MASKED) {
+            const int tg = tile_idx * kTileTokens + nt * 8 + (lane & 3) * 2 + e;
+            if (tg >= lim[hr]) v = -INFINITY;
+          }
+          sc[nt][2 * hr + e] = v;
+        }
+      mx[hr] = fmaxf(fmaxf(sc[0][2 * hr], sc[0][2 * hr + 1]), fmaxf(sc[1][2 * hr], sc[1][2 * hr + 1]));
+      mx[hr] = fmaxf(mx[hr], __shfl_xor_sync(0xffffffffu, mx[hr], 1));
+      mx[hr] = fmaxf(mx[hr], __shfl_xor_sync(0xffffffffu, mx[hr], 2));
+      if (mx[hr] > m[hr]) {
+        const float c = fast_exp2(m[hr] - mx[hr]);
+        l[hr] *= c;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          o[nt][2 * hr] *= c;
+          o[nt][2 * hr + 1] *= c;
+        }
+        m[hr] = mx[hr];
+      }
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const float v = sc[nt][2 * hr + e];
+          float p;
+          if (MASKED)
+            p = (v == -INFINITY) ? 0.f : fast_exp2(v - m[hr]);
+          else
+            p = fast_exp2(v - m[hr]);
+          sc[nt][2 * hr + e] = p;
+          l[hr] += p;
+        }
+    }
+    // P as the A operand (rows x 16 tokens), straight from the S fragments.  P has
+    // to be rounded to the 16-bit operand type.  fp16 keeps 11 significant bits
+    // (output error <= 2^-12 max|v|); bf16 keeps 8, too coarse for peaked rows, so
+    // bf16 P is split into hi + lo bf16 parts and both are multiplied by V
+    // (residual relative error ~2^-17).
+    constexpr bool kSplitP = Elt<T>::kMantBits < 10;
+    uint32_t pa[4], pl[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float p0 = sc[i >> 1][2 * (i & 1)], p1 = sc[i >> 1][2 * (i & 1) + 1];
+      pa[i] = Elt<T>::from_f2(p0, p1);
+      if (kSplitP) {
+        const float2 hi = Elt<T>::to_f2(pa[i]);
+        pl[i] = Elt<T>::from_f2(p0 - hi.x, p1 - hi.y);
+      }
+    }
+    // O += P V: B fragments (V^T) by ldmatrix.trans, two 8-dim n-tiles per load
+#pragma unroll
+    for (int dp = 0; dp < NT / 2; ++dp) {
+      uint32_t v0, v1, v2, v3;
+      const int tok = ri + ((mi & 1) << 3), ch = 2 * dp + (mi >> 1);
+      ldmatrix_x4_trans(vt + sw128_offset<kTileTokens>(tok, ch), v0, v1, v2, v3);
+      Elt<T>::mma16816(o[2 * dp], pa, v0, v1);
+      Elt<T>::mma16816(o[2 * dp + 1], pa, v2, v3);
+      if (kSplitP) {
+        Elt<T>::mma16816(o[2 * dp], pl, v0, v1);
+        Elt<T>::mma16816(o[2 * dp + 1], pl, v2, v3);
+      }
+    }
+  }
+
+  __device__ __forceinline__ void publish(float *mrg_m, float *mrg_l, float *mrg_acc) {
+    const int lane = threadIdx.x & 31;
+    const int g = lane >> 2, c2 = (lane & 3) * 2;
+#pragma unroll
+    for (int hr = 0; hr < 2; ++hr) {
+      l[hr] += __shfl_xor_sync(0xffffffffu, l[hr], 1);
+      l[hr] += __shfl_xor_sync(0xffffffffu, l[hr], 2);
+      if ((lane & 3) == 0) {
+        mrg_m[g + 8 * hr] = m[hr];
+        mrg_l[g + 8 * hr] = l[hr];
+      }
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+        *reinterpret_cast<float2 *>(mrg_acc + (g + 8 * hr) * D + nt * 8 + c2) =
+            make_float2(o[nt][2 * hr], o[nt][2 * hr + 1]);
+    }
+  }
+};
+
+// ---------------------------------------------------------------------------------
+// The kernel: work unit = (sequence, KV head, split) x row group.
+template <typename T, int D, int NW, int NSTAGE, class Path, bool PARTIAL>
+__global__ void __launch_bounds__(NW * 32)
+    paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
+                        const __grid_constant__ CUtensorMap vmap, const DecodeArgs a) {
+  constexpr int kTileBytes = kTileTokens * D * 2;  // one head of one block: 4 KiB at D = 128
+  constexpr int kStageBytes = 2 * kTileBytes;      // K tile + V tile
+  constexpr int RPC = Path::RPC;
+  static_assert(NW * RPC * (D + 2) * 4 <= NW * NSTAGE * kStageBytes, "merge area");
+
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t bars[NW * NSTAGE];
+  __shared__ int s_failed;
+
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  const uint32_t smem_base = (smem_u32(smem_raw) + 1023u) & ~1023u;  // 128B-swizzle tiles: 1 KiB
+  uint8_t *smem_gen = smem_raw + (smem_base - smem_u32(smem_raw));
+
+  const int unit = blockIdx.x;
+  const int kvh = unit % a.num_kv_heads;
+  const int rest = unit / a.num_kv_heads;
+  const int split = rest % a.num_splits;
+  const int seq = rest / a.num_splits;
+  const int row0 = blockIdx.y * RPC;
+
+  const int L = max(0, __ldg(a.context_lens + seq));
+  int nb = (L + kTileTokens - 1) / kTileTokens;
+  if (nb > a.max_blocks_per_seq) {  // context longer than its block table
+    if (threadIdx.x == 0 && split == 0 && kvh == 0 && blockIdx.y == 0) record_error(a.err, kErrCheck);
+    nb = a.max_blocks_per_seq;
+  }
+  const int per = (nb + a.num_splits - 1) / a.num_splits;
+  const int tb = min(nb, split * per);
+  const int te = min(nb, tb + per);
+  const int first_masked = (L - a.q_len + 1) / kTileTokens;  // tiles >= this need masking
+
+  if (threadIdx.x == 0) {
+    s_failed = 0;
+    prefetch_tensormap(&kmap);
+    prefetch_tensormap(&vmap);
+  }
+  if (lane == 0) {
+#pragma unroll
+    for (int s = 0; s < NSTAGE; ++s) mbar_init(smem_u32(&bars[warp * NSTAGE + s]), 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+
+  Path path;
+  path.init(a, seq, kvh, row0, L);
+
+  // this warp's tiles: j = tb + warp + NW * n, n = 0 .. n_my-1
+  const int n_my = (te - tb - warp > 0) ? (te - tb - warp + NW - 1) / NW : 0;
+  const int32_t *table = a.block_tables + (size_t)seq * a.max_blocks_per_seq;
+  const uint32_t my_stages = smem_base + warp * NSTAGE * kStageBytes;
+  int tbl = 0;  // lane i holds the block id of tile n = window + i
+
+  auto issue = [&](int n) {
+    if ((n & 31) == 0) {
+      const int j = tb + warp + NW * (n + lane);
+      tbl = (j < te) ? __ldg(table + j) : 0;
+    }
+    const int phys = __shfl_sync(0xffffffffu, tbl, n & 31);
+    if (lane == 0) {
+      const int s = n % NSTAGE;
+      const uint32_t bar = smem_u32(&bars[warp * NSTAGE + s]);
+      const uint32_t kdst = my_stages + s * kStageBytes;
+      int z;
+      if (phys >= 0 && phys < a.num_blocks) {
+        z = phys * a.num_kv_heads + kvh;
+      } else {
+        record_error(a.err, kErrCheck);
+        z = -1;  // entirely outside the tensor map: TMA fills the tile with zeros
+      }
+      mbar_arrive_expect_tx(bar, kStageBytes);
+#pragma unroll
+      for (int hh = 0; hh < D / 64; ++hh) {
+        tma_load_3d(kdst + hh * (kTileTokens * 128), &kmap, hh * 64, 0, z, bar);
+        tma_load_3d(kdst + kTileBytes + hh * (kTileTokens * 128), &vmap, hh * 64, 0, z, bar);
+      }
+    }
+  };
+
+  const int prologue = min(NSTAGE, n_my);
+  for (int n = 0; n < prologue; ++n) issue(n);
+
+  bool failed = false;
+  int n = 0;
+  for (; n < n_my; ++n) {
+    const int s = n % NSTAGE;
+    const uint32_t bar = smem_u32(&bars[warp * NSTAGE + s]);
+    const bool ok = mbar_wait_bounded(bar, (n / NSTAGE) & 1);
+    if (!__all_sync(0xffffffffu, ok)) {
+      failed = true;
+      break;
+    }
+    const int j = tb + warp + NW * n;
+    const uint32_t kt = my_stages + s * kStageBytes;
+    const uint32_t vt = kt + kTileBytes;
+    if (j >= first_masked) {
+      const int nvalid = L - j * kTileTokens;  // rows >= nvalid are past the context
+      if (nvalid < kTileTokens) {
+        for (int idx = lane; idx < (kTileTokens - nvalid) * (D / 8); idx += 32) {
+          const int row = nvalid + idx / (D / 8), ch = idx % (D / 8);
+          sts128_zero(vt + sw128_offset<kTileTokens>(row, ch));
+        }
+        __syncwarp();
+      }
+      path.template tile<true>(kt, vt, j, a.scale_log2);
+    } else {
+      path.template tile<false>(kt, vt, j, a.scale_log2);
+    }
+    __syncwarp();
+    if (n + NSTAGE < n_my) issue(n + NSTAGE);
+  }
+  if (failed) {
+    // drain the loads this warp still has in flight (bounded), then report
+    for (int k = n; k < min(n_my, n + NSTAGE); ++k)
+      (void)mbar_wait_bounded(smem_u32(&bars[warp * NSTAGE + (k % NSTAGE)]), (k / NSTAGE) & 1);
+    if (lane == 0) {
+      record_error(a.err, kErrTimeout);
+      s_failed = 1;
+    }
+  }
+  __syncthreads();  // every stage consumed: the stage memory becomes the merge area
+  if (s_failed) return;
+
+  float *mrg_m = reinterpret_cast<float *>(smem_gen);
+  float *mrg_l = mrg_m + NW * RPC;
+  float *mrg_acc = mrg_l + NW * RPC;  // [NW][RPC][D], 16-byte aligned (NW*RPC*8 bytes before)
+  path.publish(mrg_m + warp * RPC, mrg_l + warp * RPC, mrg_acc + warp * RPC * D);
+  __syncthreads();
+
+  // merge the warps and write: (row, 8 dims) per item
+  for (int item = threadIdx.x; item < RPC * (D / 8); item += NW * 32) {
+    const int r = item / (D / 8), d8 = item % (D / 8);
+    const RowInfo ri = row_info(a, kvh, row0 + r);
+    if (!ri.valid) continue;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) M = fmaxf(M, mrg_m[w * RPC + r]);
+    float den = 0.f, num[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int w = 0; w < NW; ++w) {
+      const float mw = mrg_m[w * RPC + r];
+      const float wt = (mw == -INFINITY) ? 0.f : fast_exp2(mw - M);
+      den += wt * mrg_l[w * RPC + r];
+      const float4 *src = reinterpret_cast<const float4 *>(mrg_acc + (w * RPC + r) * D + d8 * 8);
+      const float4 x0 = src[0], x1 = src[1];
+      num[0] += wt * x0.x; num[1] += wt * x0.y; num[2] += wt * x0.z; num[3] += wt * x0.w;
+      num[4] += wt * x1.x; num[5] += wt * x1.y; num[6] += wt * x1.z; num[7] += wt * x1.w;
+    }
+    const size_t orow = (size_t)(seq * a.q_len + ri.u) * a.num_q_heads + ri.h;  // row of out
+    if constexpr (PARTIAL) {
+      const size_t wrow = ((size_t)seq * a.num_splits + split) * (a.q_len * a.num_q_heads) +
+                          (size_t)ri.u * a.num_q_heads + ri.h;
+      float4 *dst = reinterpret_cast<float4 *>(a.ws_acc + wrow * D + d8 * 8);
+      dst[0] = make_float4(num[0], num[1], num[2], num[3]);
+      dst[1] = make_float4(num[4], num[5], num[6], num[7]);
+      if (d8 == 0) {
+        a.ws_m[wrow] = M;
+        a.ws_l[wrow] = den;
+      }
+      (void)orow;
+    } else {
+      const float inv = den > 0.f ? 1.f / den : 0.f;
+      uint4 packed;
+      packed.x = Elt<T>::from_f2(num[0] * inv, num[1] * inv);
+      packed.y = Elt<T>::from_f2(num[2] * inv, num[3] * inv);
+      packed.z = Elt<T>::from_f2(num[4] * inv, num[5] * inv);
+      packed.w = Elt<T>::from_f2(num[6] * inv, num[7] * inv);
+      *reinterpret_cast<uint4 *>(static_cast<T *>(a.out) + orow * D + d8 * 8) = packed;
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------------
+// Split-KV combine: one warp per (sequence, row); lanes cover head_dim.
+struct CombineArgs {
+  void *out;
+  const float *ws_acc, *ws_m, *ws_l;
+  int num_seqs, rows_per_seq, num_splits;
+};
+
+template <typename T, int D>
+__global__ void __launch_bounds__(128) split_combine_kernel(const CombineArgs a) {
+  constexpr int PER = D / 32;  // dims per lane
+  const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (gw >= a.num_seqs * a.rows_per_seq) return;
+  const int seq = gw / a.rows_per_seq, r = gw % a.rows_per_seq;
+  const size_t base = (size_t)seq * a.num_splits * a.rows_per_seq + r;
+  float M = -INFINITY;
+  for (int p = 0; p < a.num_splits; ++p) {
+    const size_t w = base + (size_t)p * a.rows_per_seq;
+    if (a.ws_l[w] > 0.f) M = fmaxf(M, a.ws_m[w]);
+  }
+  float den = 0.f, num[PER];
+#pragma unroll
+  for (int k = 0; k < PER; ++k) num[k] = 0.f;
+  if (M != -INFINITY) {
+    for (int p = 0; p < a.num_splits; ++p) {
+      const size_t w = base + (size_t)p * a.rows_per_seq;
+      const float lw = a.ws_l[w];
+      if (!(lw > 0.f)) continue;
+      const float wt = fast_exp2(a.ws_m[w] - M);
+      den += wt * lw;
+      const float *acc = a.ws_acc + w * D + lane * PER;
+#pragma unroll
+      for (int k = 0; k < PER; k += 2) {
+        const float2 x = *reinterpret_cast<const float2 *>(acc + k);
+        num[k] += wt * x.x;
+        num[k + 1] += wt * x.y;
+      }
+    }
+  }
+  const float inv = den > 0.f ? 1.f / den : 0.f;
+  T *o = static_cast<T *>(a.out) + ((size_t)seq * a.rows_per_seq + r) * D + lane * PER;
+#pragma unroll
+  for (int k = 0; k < PER; k += 2)
+    *reinterpret_cast<uint32_t *>(o + k) = Elt<T>::from_f2(num[k] * inv, num[k + 1] * inv);
+}
+
+}  // namespace pa

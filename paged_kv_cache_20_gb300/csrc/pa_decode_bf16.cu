@@ -1,0 +1,13 @@
+// pa_decode_bf16.cu -- bf16 instantiations of the decode and combine kernels.
+#include "pa_decode_inst.cuh"
+
+namespace pa {
+cudaError_t launch_decode_bf16(const CUtensorMap &kmap, const CUtensorMap &vmap,
+                               const DecodeArgs &args, int head_dim, bool partial, int units,
+                               cudaStream_t stream) {
+  return launch_decode_t<__nv_bfloat16>(kmap, vmap, args, head_dim, partial, units, stream);
+}
+cudaError_t launch_combine_bf16(const CombineArgs &args, int head_dim, cudaStream_t stream) {
+  return launch_combine_t<__nv_bfloat16>(args, head_dim, stream);
+}
+}  // namespace pa

@@ -1,0 +1,285 @@
+"""CUDA library vs the fp64 oracle, through the C ABI (needs a GPU).
+
+Append and slot mapping are compared bit for bit; attention within the tolerance
+of tests/_tol.py.  Small cases compare every output element; the full-size
+workloads (run in the launch configuration bench.py times) compare sampled rows
+the oracle computes one by one, plus properties that hold at any size.
+"""
+import numpy as np
+import pytest
+import torch
+
+import workloads
+from tests import _tol
+from tests.oracle_pins import Paged, _bits
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def pa():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import paged_kv_cache_20_gb300 as pa
+    pa.load()
+    assert pa.pa_device_error() == 0
+    return pa
+
+
+DEV = "cuda:0"
+
+
+def _dev(w):
+    return {k: getattr(w, k).to(DEV) for k in
+            ("q", "k_new", "v_new", "k_cache", "v_cache", "block_tables", "context_lens")}
+
+
+def _u16(t: torch.Tensor) -> np.ndarray:
+    return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def _f64(t: torch.Tensor) -> np.ndarray:
+    return t.detach().cpu().to(torch.float64).numpy()
+
+
+def gpu_step(pa, w, num_splits=None):
+    d = _dev(w)
+    s = w.cfg.num_splits if num_splits is None else num_splits
+    out = pa.paged_decode_step(d["q"], d["k_new"], d["v_new"], d["k_cache"], d["v_cache"],
+                               d["block_tables"], d["context_lens"], w.scale, q_len=w.cfg.q_len,
+                               num_splits=s)
+    torch.cuda.synchronize()
+    assert pa.pa_device_error() == 0
+    return out, d
+
+
+def oracle_step(orc, w, rows=None, threads=8):
+    kc, vc = w.bits("k_cache").copy(), w.bits("v_cache").copy()
+    slots = orc.slot_mapping(w.block_tables.numpy(), w.context_lens.numpy(), w.cfg.block_size,
+                             w.cfg.q_len)
+    orc.append_kv(kc, vc, w.bits("k_new"), w.bits("v_new"), slots)
+    out = orc.decode(w.bits("q"), kc, vc, w.block_tables.numpy(), w.context_lens.numpy(),
+                     w.scale, w.cfg.dtype, q_len=w.cfg.q_len, rows=rows, threads=threads)
+    return out, kc, vc, slots
+
+
+SMALL = [
+    ("tiny", {}),
+    ("llama7b_mha", {"num_seqs": 3}),
+    ("gqa", {"num_seqs": 5}),
+    ("long_split", {"num_seqs": 1, "lens": ("fixed", (4100,))}),
+    ("prefix_verify", {"num_seqs": 4}),
+]
+
+
+@pytest.mark.parametrize("name,over", SMALL, ids=[s[0] for s in SMALL])
+def test_small_configs_every_element(pa, orc, name, over):
+    w = workloads.make(name, **over)
+    out, d = gpu_step(pa, w)
+    ref, kc, vc, slots = oracle_step(orc, w)
+    # append is bit-exact over the whole pool (NaN-poisoned slots included)
+    assert np.array_equal(_u16(d["k_cache"]), kc)
+    assert np.array_equal(_u16(d["v_cache"]), vc)
+    _tol.check(_f64(out), ref, w.cfg.dtype, name)
+
+
+FULL = ["llama7b_mha", "gqa", "long_split", "prefix_verify"]
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_sampled_rows(pa, orc, name):
+    w = workloads.make(name)
+    out, d = gpu_step(pa, w)
+    n_rows = w.cfg.num_seqs * w.cfg.q_len * w.cfg.num_q_heads
+    rng = np.random.default_rng(1)
+    rows = np.sort(rng.choice(n_rows, size=min(n_rows, 48), replace=False))
+    ref, kc, vc, slots = oracle_step(orc, w, rows=rows)
+    got = _f64(out).reshape(n_rows, -1)[rows]
+    _tol.check(got, ref, w.cfg.dtype, name)
+    # slot mapping and the appended rows, bit for bit
+    gslots = pa.pa_slot_mapping(d["block_tables"], d["context_lens"], 16, w.cfg.q_len)
+    assert np.array_equal(gslots.cpu().numpy(), slots)
+    assert np.array_equal(_u16(d["k_cache"]), kc)
+    assert np.array_equal(_u16(d["v_cache"]), vc)
+
+
+def _logical_case(seed, lens, h_q, h_kv, d, dtype, q_len=1, qscale=1.0):
+    rng = np.random.default_rng(seed)
+    K = [_bits(rng.standard_normal((L, h_kv, d)), dtype) for L in lens]
+    V = [_bits(rng.standard_normal((L, h_kv, d)), dtype) for L in lens]
+    q = _bits(qscale * rng.standard_normal((len(lens), q_len, h_q, d)), dtype)
+    return q, K, V
+
+
+def _to_dev(arr, dtype):
+    t = torch.from_numpy(np.ascontiguousarray(arr).view(np.int16))
+    return t.view(torch.float16 if dtype == "fp16" else torch.bfloat16).to(DEV)
+
+
+def _gpu_decode(pa, pc, q, scale, q_len, num_splits=1, lens=None):
+    qd = _to_dev(q, pc.dtype)
+    kd, vd = _to_dev(pc.k, pc.dtype), _to_dev(pc.v, pc.dtype)
+    bt = torch.from_numpy(pc.tables).to(DEV)
+    cl = torch.from_numpy(pc.lens if lens is None else np.asarray(lens, np.int32)).to(DEV)
+    out = torch.empty_like(qd)
+    if num_splits == 1:
+        pa.pa_decode(out, qd, kd, vd, bt, cl, scale, q_len)
+    else:
+        nbytes = pa.pa_decode_workspace_size(q.shape[0], q.shape[2], q_len, q.shape[3], num_splits)
+        ws = torch.empty(nbytes, dtype=torch.uint8, device=DEV)
+        pa.pa_decode_partial(ws, qd, kd, vd, bt, cl, scale, num_splits, q_len)
+        pa.pa_decode_combine(out, ws, num_splits)
+    torch.cuda.synchronize()
+    assert pa.pa_device_error() == 0
+    return _f64(out)
+
+
+EDGE_LENS = [0, 1, 2, 15, 16, 17, 31, 32, 33, 100, 257]
+
+
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("h_q,h_kv,q_len", [(4, 4, 1), (8, 4, 1), (12, 4, 1), (16, 4, 1),
+                                            (8, 8, 2), (8, 2, 4), (32, 4, 4), (6, 2, 3)])
+def test_edge_lengths_groups_and_query_counts(pa, orc, dtype, d, h_q, h_kv, q_len):
+    lens = EDGE_LENS
+    q, K, V = _logical_case(3, lens, h_q, h_kv, d, dtype, q_len=q_len, qscale=2.0)
+    pc = Paged(orc, K, V, 16, dtype, perm_seed=5)
+    scale = float(np.float32(1.0) / np.sqrt(np.float32(d)))
+    ref = pc.decode(orc, q, scale, q_len=q_len)
+    got = _gpu_decode(pa, pc, q, scale, q_len)
+    _tol.check(got, ref, dtype, f"{dtype} d{d} {h_q}/{h_kv} q_len{q_len}")
+    for S in (2, 3, 16, 40):
+        got_s = _gpu_decode(pa, pc, q, scale, q_len, num_splits=S)
+        _tol.check(got_s, ref, dtype, f"split {S}")
+
+
+def test_context_one_returns_v_exactly(pa, orc):
+    for dtype in ("fp16", "bf16"):
+        q, K, V = _logical_case(4, [1, 1, 1], 8, 2, 128, dtype, qscale=5.0)
+        pc = Paged(orc, K, V, 16, dtype, perm_seed=1)
+        got = _gpu_decode(pa, pc, q, 0.1, 1)
+        for i in range(3):
+            want = np.repeat(orc.decode_bits(V[i][0], dtype), 4, axis=0)
+            assert np.array_equal(got[i, 0], want)
+
+
+def test_identical_value_rows(pa, orc):
+    rng = np.random.default_rng(6)
+    L = 300
+    row = _bits(rng.standard_normal((1, 2, 128)), "bf16")
+    V = [np.repeat(row, L, axis=0)]
+    K = [_bits(rng.standard_normal((L, 2, 128)), "bf16")]
+    q = _bits(2 * rng.standard_normal((1, 1, 8, 128)), "bf16")
+    pc = Paged(orc, K, V, 16, "bf16", perm_seed=2)
+    got = _gpu_decode(pa, pc, q, 0.09, 1)
+    want = np.repeat(orc.decode_bits(row[0], "bf16"), 4, axis=0)
+    assert np.abs(got[0, 0] - want).max() <= 2e-3
+
+
+def test_paging_permutation_is_bit_invariant(pa, orc):
+    lens = [70, 511, 1000, 33]
+    for h_q, h_kv in ((8, 8), (32, 8)):
+        q, K, V = _logical_case(7, lens, h_q, h_kv, 128, "fp16")
+        outs = []
+        for seed in (None, 11, 12):
+            pc = Paged(orc, K, V, 16, "fp16", perm_seed=seed)
+            outs.append(_gpu_decode(pa, pc, q, 0.0884, 1))
+        assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[0], outs[2])
+
+
+def test_stress_rescale_peaked_scores(pa, orc):
+    # large q makes each row's softmax nearly one-hot and the running max move often
+    lens = [40, 333, 900]
+    q, K, V = _logical_case(8, lens, 8, 2, 128, "fp16", qscale=8.0)
+    pc = Paged(orc, K, V, 16, "fp16", perm_seed=3)
+    ref = pc.decode(orc, q, 0.0884)
+    _tol.check(_gpu_decode(pa, pc, q, 0.0884, 1), ref, "fp16", "peaked")
+    # increasing scores along the sequence: every block raises the max
+    L = 400
+    rng = np.random.default_rng(9)
+    k = rng.standard_normal((L, 1, 128)) * 0.1
+    k[:, 0, 0] = np.linspace(-4, 4, L)
+    qv = np.zeros((1, 1, 1, 128))
+    qv[..., 0] = 3.0
+    qb = _bits(qv, "fp16")
+    pc2 = Paged(orc, [_bits(k, "fp16")], [_bits(rng.standard_normal((L, 1, 128)), "fp16")], 16,
+                "fp16", perm_seed=4)
+    _tol.check(_gpu_decode(pa, pc2, qb, 1.0, 1), pc2.decode(orc, qb, 1.0), "fp16", "rising")
+
+
+def test_partial_statistics_match_oracle_partitions(pa, orc):
+    lens = [1, 40, 700, 0]
+    q_len, S = 2, 5
+    q, K, V = _logical_case(10, lens, 8, 2, 128, "bf16", q_len=q_len)
+    pc = Paged(orc, K, V, 16, "bf16", perm_seed=6)
+    m, l, acc = orc.decode_partitions(q, pc.k, pc.v, pc.tables, pc.lens, 0.0884, "bf16", S,
+                                      q_len=q_len)
+    qd = _to_dev(q, "bf16")
+    nbytes = pa.pa_decode_workspace_size(4, 8, q_len, 128, S)
+    ws = torch.full((nbytes,), 0x7F, dtype=torch.uint8, device=DEV)   # garbage-filled
+    pa.pa_decode_partial(ws, qd, _to_dev(pc.k, "bf16"), _to_dev(pc.v, "bf16"),
+                         torch.from_numpy(pc.tables).to(DEV), torch.from_numpy(pc.lens).to(DEV),
+                         0.0884, S, q_len)
+    g_acc, g_m, g_l = (t.double().cpu().numpy() for t in pa.workspace_views(ws, 4, 8, q_len, 128, S))
+    empty = l == 0
+    assert np.array_equal(g_l == 0, empty)
+    assert np.all(np.isneginf(g_m[empty])) and np.all(g_acc[empty] == 0)
+    ok = ~empty
+    # normalised partition output and log-sum-exp (natural units) per partition
+    norm_g = g_acc[ok] / g_l[ok][:, None]
+    norm_o = acc[ok] / l[ok][:, None]
+    _tol.check(norm_g, norm_o, "bf16", "partition output")
+    lse_g = g_m[ok] * np.log(2.0) + np.log(g_l[ok])
+    lse_o = m[ok] + np.log(l[ok])
+    assert np.abs(lse_g - lse_o).max() < 1e-4
+
+
+def test_combine_alone_on_oracle_partials(pa, orc):
+    lens = [3, 64, 500, 0, 17]
+    S, q_len = 7, 1
+    q, K, V = _logical_case(12, lens, 4, 4, 64, "fp16", q_len=q_len, qscale=2.0)
+    pc = Paged(orc, K, V, 16, "fp16", perm_seed=8)
+    m, l, acc = orc.decode_partitions(q, pc.k, pc.v, pc.tables, pc.lens, 0.125, "fp16", S)
+    want = orc.combine(m, l, acc).reshape(5, 1, 4, 64)
+    nbytes = pa.pa_decode_workspace_size(5, 4, 1, 64, S)
+    ws = torch.zeros(nbytes, dtype=torch.uint8, device=DEV)
+    g_acc, g_m, g_l = pa.workspace_views(ws, 5, 4, 1, 64, S)
+    g_acc.copy_(torch.from_numpy(acc).float())
+    g_m.copy_(torch.from_numpy(m / np.log(2.0)).float())   # base-2 units
+    g_l.copy_(torch.from_numpy(l).float())
+    out = torch.empty((5, 1, 4, 64), dtype=torch.float16, device=DEV)
+    pa.pa_decode_combine(out, ws, S)
+    torch.cuda.synchronize()
+    _tol.check(_f64(out), want, "fp16", "combine")
+
+
+def test_bad_block_id_is_reported_not_faulted(pa, orc):
+    q, K, V = _logical_case(13, [40, 40], 4, 4, 128, "fp16")
+    pc = Paged(orc, K, V, 16, "fp16", perm_seed=9)
+    pc.tables[1, 1] = pc.k.shape[0] + 5          # beyond the pool
+    qd = _to_dev(q, "fp16")
+    out = torch.empty_like(qd)
+    pa.pa_decode(out, qd, _to_dev(pc.k, "fp16"), _to_dev(pc.v, "fp16"),
+                 torch.from_numpy(pc.tables).to(DEV), torch.from_numpy(pc.lens).to(DEV), 0.1, 1)
+    assert pa.pa_device_error() == pa.PA_ERR_DEVICE_CHECK
+    assert pa.pa_device_error() == 0                         # cleared
+    got = _f64(out)
+    assert np.isfinite(got).all()
+    ref = pc.decode(orc, q, 0.1)
+    _tol.check(got[0], ref[0], "fp16", "unaffected sequence")
+
+
+def test_append_skips_negative_and_reports_out_of_pool_slots(pa):
+    P, H, D = 6, 2, 128
+    kc = torch.zeros((P, H, 16, D), dtype=torch.float16, device=DEV)
+    vc = torch.zeros_like(kc)
+    kn = torch.randn((3, H, D), dtype=torch.float16, device=DEV)
+    vn = torch.randn((3, H, D), dtype=torch.float16, device=DEV)
+    slots = torch.tensor([5, -1, P * 16 + 3], dtype=torch.int64, device=DEV)
+    pa.pa_append_kv(kc, vc, kn, vn, slots)
+    assert pa.pa_device_error() == pa.PA_ERR_DEVICE_CHECK
+    assert torch.equal(kc[0, :, 5], kn[0]) and torch.equal(vc[0, :, 5], vn[0])
+    kc[0, :, 5] = 0
+    vc[0, :, 5] = 0
+    assert int(kc.abs().sum()) == 0 and int(vc.abs().sum()) == 0
