@@ -19,8 +19,9 @@
  *    cudaStream_t passed as void* (NULL = legacy default stream).  Every call is
  *    asynchronous on `stream` and returns after the launch.
  *  - The caller owns every buffer.  The library allocates no device memory and
- *    keeps no per-call state; its only device-resident state is one 32-bit error
- *    word per device (see pa_device_error).
+ *    keeps no per-call state; its device-resident state is one 32-bit error
+ *    word per device (see pa_device_error) and the fixed workspace array of
+ *    pa_decode_split_noalloc.
  *  - 16-bit floating point (fp16 or bf16, chosen by `dtype`) for q, K, V and the
  *    output; fp32 arithmetic inside.
  *  - Layouts (dense, row-major):
@@ -179,6 +180,34 @@ PA_API pa_status pa_decode_combine(void *out, const void *workspace, size_t work
  * synchronisation itself fails.
  */
 PA_API pa_status pa_device_error(void *stream, int clear);
+
+/*
+ * pa_decode_split_noalloc -- the split-KV pair (pa_decode_partial, then
+ * pa_decode_combine) with its workspace in a fixed device array that the library
+ * owns, for callers that cannot allocate device memory where they run attention:
+ * a plug-in whose host runtime owns every device allocation, or a serving loop
+ * that must not allocate (nor risk the implicit device synchronisation of
+ * cudaMalloc/cudaFree) once it is running.  The pages have no counterpart; this
+ * is an allocation-free convenience of this library, not a step of the method.
+ *
+ * Arguments are those of pa_decode_partial without the workspace; out is written
+ * as by pa_decode_combine.  The array holds PA_NOALLOC_SCRATCH_BYTES on every
+ * device that loads the library, until the process exits.  If
+ * pa_decode_workspace_size(num_seqs, num_q_heads, q_len, head_dim, num_splits)
+ * exceeds it, the call returns PA_ERR_INVALID_ARG and launches nothing.  No
+ * device memory is allocated or freed.  All calls on a device share the array:
+ * calls that can overlap on the GPU (unordered streams) race.  The first call on
+ * a device looks up the array's device address with that device current; make
+ * it before any stream capture.
+ */
+#define PA_NOALLOC_SCRATCH_BYTES ((size_t)8 << 20)
+PA_API pa_status pa_decode_split_noalloc(void *out, const void *q, const void *k_cache,
+                                         const void *v_cache, const int32_t *block_tables,
+                                         const int32_t *context_lens, int num_seqs,
+                                         int num_q_heads, int num_kv_heads, int head_dim,
+                                         int block_size, float scale, int num_splits,
+                                         int max_blocks_per_seq, int num_blocks, int q_len,
+                                         pa_dtype dtype, void *stream);
 
 #ifdef __cplusplus
 }

@@ -54,7 +54,12 @@ _SIGNATURES = {
     "pa_decode_combine": (_c_int, [_c_vp, _c_vp, _c_size, _c_int, _c_int, _c_int, _c_int,
                                    _c_int, _c_int, _c_vp]),
     "pa_device_error": (_c_int, [_c_vp, _c_int]),
+    "pa_decode_split_noalloc": (_c_int, [_c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_int, _c_int,
+                                         _c_int, _c_int, _c_int, _c_float, _c_int, _c_int,
+                                         _c_int, _c_int, _c_int, _c_vp]),
 }
+
+NOALLOC_SCRATCH_BYTES = 8 << 20   # PA_NOALLOC_SCRATCH_BYTES
 
 _lock = threading.Lock()
 _lib = None
@@ -265,3 +270,27 @@ def paged_decode_step(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
     pa_decode_partial(workspace, q, k_cache, v_cache, block_tables, context_lens, scale,
                       num_splits, q_len, stream=stream)
     return pa_decode_combine(out, workspace, num_splits, stream=stream)
+
+
+def pa_decode_split_noalloc(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor,
+                            v_cache: torch.Tensor, block_tables: torch.Tensor,
+                            context_lens: torch.Tensor, scale: float, num_splits: int,
+                            q_len: int = 1, stream=None) -> torch.Tensor:
+    """Split-KV attention whose workspace is the library's fixed device array.
+
+    For callers that may not allocate device memory at this point; no tensor is
+    allocated here either.  Raises PagedAttnError (PA_ERR_INVALID_ARG) when the
+    workspace this call needs exceeds NOALLOC_SCRATCH_BYTES.  Calls that can run
+    concurrently on one GPU share the array and must be ordered by the caller.
+    """
+    num_blocks, h_kv, block_size, head_dim, num_seqs, h_q, maxb = _decode_dims(
+        q, k_cache, block_tables, context_lens, q_len)
+    if out.shape != q.shape or out.dtype != q.dtype or q.dtype != k_cache.dtype:
+        raise ValueError("out must match q; q must have the cache dtype")
+    _check("pa_decode_split_noalloc", load().pa_decode_split_noalloc(
+        _cuda(out, "out"), _cuda(q, "q"), _cuda(k_cache, "k_cache"), _cuda(v_cache, "v_cache"),
+        _cuda(block_tables, "block_tables", torch.int32),
+        _cuda(context_lens, "context_lens", torch.int32), num_seqs, h_q, h_kv, head_dim,
+        block_size, float(scale), num_splits, maxb, num_blocks, q_len, _elt(k_cache, "k_cache"),
+        _stream(stream)))
+    return out
