@@ -323,8 +323,10 @@ def cpu_baseline(w: workloads.Workload, budget_s: float = 5.0) -> dict:
                       f"{threads} threads, {dt:.1f} s wall"}
 
 
-def measure_config(pa, name, seed, device, steps, warmup, flush, world, peaks, e2e=False):
-    w = workloads.make(name, seed=seed, poison=False)
+def measure_config(pa, name, seed, device, steps, warmup, flush, world, peaks, e2e=False,
+                   num_seqs=None):
+    over = {"num_seqs": num_seqs} if num_seqs else {}
+    w = workloads.make(name, seed=seed, poison=False, **over)
     runner = Runner(pa, w, device)
     step_ms, kern_ms, wall = time_device(runner, steps, warmup, flush, world)
     assert pa.pa_device_error() == 0, "device error during the timed run"
@@ -382,7 +384,7 @@ def run_ours(args):
     main = args.config
     with ClockSampler(local) as clk:
         r = measure_config(pa, main, rank, device, args.steps, args.warmup, flush, world, peaks,
-                           e2e=True)
+                           e2e=not args.no_e2e, num_seqs=args.num_seqs)
     clocks = clk.summary()
     others = {}
     if not args.only:
@@ -408,7 +410,7 @@ def run_ours(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": f"{w.cfg.dtype} in, fp32 accumulate", "data": "synthetic",
         "config": config_obj(w, _path(w)),
-        "roofline": r["roofline"], "cpu_baseline": cpu, "e2e": r["e2e"],
+        "roofline": r["roofline"], "cpu_baseline": cpu, "e2e": r.get("e2e"),
         "gpu_launches": args.steps * r["runner"].launches_per_step,
         "clocks": clocks, "step_p10_p50_p90_ms": r["step_ms_p10_p50_p90"],
         "step_algorithmic_gbs": r["step_gbs"], "other_configs": others,
@@ -476,6 +478,9 @@ def main(argv=None):
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--only", action="store_true", help="skip the other workloads")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end timing")
+    ap.add_argument("--num-seqs", type=int, default=None,
+                    help="scale the main workload down to this many sequences (profiling)")
     ap.add_argument("--ref-seqs", type=int, default=2,
                     help="sequences per step in the reference arm's bounded sample")
     args = ap.parse_args(argv)
