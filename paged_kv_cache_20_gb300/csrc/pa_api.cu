@@ -205,6 +205,7 @@ pa_status decode_common(void *out, float *ws, const WsLayout *lay, const void *q
   a.max_blocks_per_seq = max_blocks_per_seq;
   a.num_blocks = num_blocks;
   a.num_splits = num_splits;
+  a.lpt = num_seqs <= pa::kLptMaxSeqs ? 1 : 0;
   a.scale_log2 = scale * 1.4426950408889634f;  // log2(e)
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const bool partial = ws != nullptr;

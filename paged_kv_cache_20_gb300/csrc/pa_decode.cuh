@@ -57,8 +57,38 @@ struct DecodeArgs {
   unsigned *err;                 // device error word
   int num_seqs, num_q_heads, num_kv_heads, q_len, group, rows;  // rows = group * q_len
   int max_blocks_per_seq, num_blocks, num_splits;
+  int lpt;                       // 1: take sequences longest first (num_seqs <= kLptMaxSeqs)
   float scale_log2;              // scale * log2(e): scores in base-2 units
 };
+
+constexpr int kLptMaxSeqs = 256;
+
+// Longest-processing-time order: the sequence of rank `rank` when sequences are
+// sorted by context length, longest first (ties by index).  Every CTA computes
+// the same order from context_lens, so consecutive CTAs start on the longest
+// sequences and short ones fill the tail.  All threads of the CTA must call it.
+__device__ __forceinline__ int lpt_sequence(const int32_t *lens, int n, int rank, int *s_lens,
+                                            int *s_pick) {
+  const int n4 = (n + 3) & ~3;
+  for (int i = threadIdx.x; i < n4; i += blockDim.x)
+    s_lens[i] = i < n ? max(0, __ldg(lens + i)) : -1;  // -1 pads: never longer than a real one
+  if (threadIdx.x == 0) *s_pick = rank;
+  __syncthreads();
+  for (int i = threadIdx.x; i < n; i += blockDim.x) {
+    const int li = s_lens[i];
+    int r = 0;
+    for (int j = 0; j < n4; j += 4) {  // broadcast 16-byte reads: 4 lengths per load
+      const int4 l4 = *reinterpret_cast<const int4 *>(s_lens + j);
+      r += (l4.x > li) | ((l4.x == li) & (j < i));
+      r += (l4.y > li) | ((l4.y == li) & (j + 1 < i));
+      r += (l4.z > li) | ((l4.z == li) & (j + 2 < i));
+      r += (l4.w > li) | ((l4.w == li) & (j + 3 < i));
+    }
+    if (r == rank) *s_pick = i;
+  }
+  __syncthreads();
+  return *s_pick;
+}
 
 // ---------------------------------------------------------------------------------
 // Row bookkeeping shared by both paths.  Unit row rho (0 <= rho < rows) is query
@@ -210,7 +240,8 @@ struct FmaPath {
   }
 
   // Merge the lane groups of this warp, then publish the warp's state:
-  // mrg_m/mrg_l [RPC], mrg_acc [RPC][D] for this warp.
+  // mrg_m/mrg_l [RPC], mrg_acc [RPC][STRIDE] for this warp.
+  template <int STRIDE>
   __device__ __forceinline__ void publish(float *mrg_m, float *mrg_l, float *mrg_acc) {
     const int lane = threadIdx.x & 31;
 #pragma unroll
@@ -240,7 +271,7 @@ struct FmaPath {
         }
 #pragma unroll
         for (int jj = 0; jj < CH; ++jj) {
-          float4 *dst = reinterpret_cast<float4 *>(mrg_acc + r * D + chunk(jj) * 8);
+          float4 *dst = reinterpret_cast<float4 *>(mrg_acc + r * STRIDE + chunk(jj) * 8);
           dst[0] = make_float4(acc[r][jj * 8 + 0], acc[r][jj * 8 + 1], acc[r][jj * 8 + 2],
                                acc[r][jj * 8 + 3]);
           dst[1] = make_float4(acc[r][jj * 8 + 4], acc[r][jj * 8 + 5], acc[r][jj * 8 + 6],
@@ -296,20 +327,26 @@ struct MmaPath {
   __device__ __forceinline__ void tile(uint32_t kt, uint32_t vt, int tile_idx, float scale_log2) {
     const int lane = threadIdx.x & 31;
     const int mi = lane >> 3, ri = lane & 7;
-    float sc[2][4];
+    // S = Q K^T: B fragments (K rows = tokens, 8 dims each) by ldmatrix.  Even and
+    // odd k-steps accumulate separately (two independent mma chains), then add.
+    float sc[2][4], sd[2][4];
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-      for (int e = 0; e < 4; ++e) sc[nt][e] = 0.f;
-    // S = Q K^T: B fragments (K rows = tokens, 8 dims each) by ldmatrix
+      for (int e = 0; e < 4; ++e) sc[nt][e] = sd[nt][e] = 0.f;
 #pragma unroll
     for (int ks = 0; ks < KS; ++ks) {
       uint32_t b00, b01, b10, b11;
       const int tok = ri + ((mi >> 1) << 3), ch = 2 * ks + (mi & 1);
       ldmatrix_x4(kt + sw128_offset<kTileTokens>(tok, ch), b00, b01, b10, b11);
-      Elt<T>::mma16816(sc[0], qa[ks], b00, b01);
-      Elt<T>::mma16816(sc[1], qa[ks], b10, b11);
+      float (&acc)[2][4] = (ks & 1) ? sd : sc;
+      Elt<T>::mma16816(acc[0], qa[ks], b00, b01);
+      Elt<T>::mma16816(acc[1], qa[ks], b10, b11);
     }
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) sc[nt][e] += sd[nt][e];
     // scale to base-2 units, mask, row max over the 16 tokens (4 lanes per row)
     float mx[2];
 #pragma unroll
@@ -383,6 +420,7 @@ struct MmaPath {
     }
   }
 
+  template <int STRIDE>
   __device__ __forceinline__ void publish(float *mrg_m, float *mrg_l, float *mrg_acc) {
     const int lane = threadIdx.x & 31;
     const int g = lane >> 2, c2 = (lane & 3) * 2;
@@ -396,14 +434,18 @@ struct MmaPath {
       }
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt)
-        *reinterpret_cast<float2 *>(mrg_acc + (g + 8 * hr) * D + nt * 8 + c2) =
+        *reinterpret_cast<float2 *>(mrg_acc + (g + 8 * hr) * STRIDE + nt * 8 + c2) =
             make_float2(o[nt][2 * hr], o[nt][2 * hr + 1]);
     }
   }
 };
 
 // ---------------------------------------------------------------------------------
-// The kernel: work unit = (sequence, KV head, split) x row group.
+// The kernel: work unit = (sequence, KV head, split) x row group.  A unit may be
+// shared by the CTAs of one thread-block cluster (launched with cluster dimension
+// C > 1 along x): the C*NW warps take the unit's blocks round-robin, each CTA
+// merges its warps, then the CTAs merge through distributed shared memory.  This
+// splits one long sequence over several SMs without any global workspace.
 template <typename T, int D, int NW, int NSTAGE, class Path, bool PARTIAL>
 __global__ void __launch_bounds__(NW * 32)
     paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
@@ -411,7 +453,9 @@ __global__ void __launch_bounds__(NW * 32)
   constexpr int kTileBytes = kTileTokens * D * 2;  // one head of one block: 4 KiB at D = 128
   constexpr int kStageBytes = 2 * kTileBytes;      // K tile + V tile
   constexpr int RPC = Path::RPC;
-  static_assert(NW * RPC * (D + 2) * 4 <= NW * NSTAGE * kStageBytes, "merge area");
+  constexpr int kStride = D + 4;                   // merge-area row stride (floats), padded
+  static_assert((NW + 1) * RPC * (kStride + 2) * 4 + 64 <= NW * NSTAGE * kStageBytes,
+                "merge area");
 
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t bars[NW * NSTAGE];
@@ -422,17 +466,25 @@ __global__ void __launch_bounds__(NW * 32)
   const uint32_t smem_base = (smem_u32(smem_raw) + 1023u) & ~1023u;  // 128B-swizzle tiles: 1 KiB
   uint8_t *smem_gen = smem_raw + (smem_base - smem_u32(smem_raw));
 
-  const int unit = blockIdx.x;
+  const int csize = static_cast<int>(cluster_nctarank());  // 1 without a cluster launch
+  const int crank = static_cast<int>(cluster_ctarank());
+  const int unit = blockIdx.x / csize;
   const int kvh = unit % a.num_kv_heads;
   const int rest = unit / a.num_kv_heads;
   const int split = rest % a.num_splits;
-  const int seq = rest / a.num_splits;
+  int seq = rest / a.num_splits;
+  if (a.lpt) {
+    __shared__ __align__(16) int s_lens[kLptMaxSeqs];
+    __shared__ int s_pick;
+    seq = lpt_sequence(a.context_lens, a.num_seqs, seq, s_lens, &s_pick);
+  }
   const int row0 = blockIdx.y * RPC;
 
   const int L = max(0, __ldg(a.context_lens + seq));
   int nb = (L + kTileTokens - 1) / kTileTokens;
   if (nb > a.max_blocks_per_seq) {  // context longer than its block table
-    if (threadIdx.x == 0 && split == 0 && kvh == 0 && blockIdx.y == 0) record_error(a.err, kErrCheck);
+    if (threadIdx.x == 0 && split == 0 && kvh == 0 && blockIdx.y == 0 && crank == 0)
+      record_error(a.err, kErrCheck);
     nb = a.max_blocks_per_seq;
   }
   const int per = (nb + a.num_splits - 1) / a.num_splits;
@@ -455,16 +507,29 @@ __global__ void __launch_bounds__(NW * 32)
   Path path;
   path.init(a, seq, kvh, row0, L);
 
-  // this warp's tiles: j = tb + warp + NW * n, n = 0 .. n_my-1
-  const int n_my = (te - tb - warp > 0) ? (te - tb - warp + NW - 1) / NW : 0;
+  // This warp's tiles: the unit's ntiles blocks are visited from a starting offset
+  // `rot` that differs between the KV heads of a sequence, tile number
+  // k = gw + TW * n (gw: warp index in the cluster) being block
+  // tb + (k + rot) mod ntiles.  Staggered starts keep the CTAs of one wave in
+  // different phases (e.g. some on an L2-resident shared prefix, some on private
+  // blocks in HBM).  The order depends only on logical positions.
+  const int gw = crank * NW + warp;
+  const int TW = csize * NW;
+  const int ntiles = te - tb;
+  const int rot = ntiles > 0 ? (int)(((long long)kvh * ntiles) / a.num_kv_heads) : 0;
+  const int n_my = (ntiles - gw > 0) ? (ntiles - gw + TW - 1) / TW : 0;
+  auto tile_of = [&](int n) {
+    int k = gw + TW * n + rot;
+    if (k >= ntiles) k -= ntiles;
+    return tb + k;
+  };
   const int32_t *table = a.block_tables + (size_t)seq * a.max_blocks_per_seq;
   const uint32_t my_stages = smem_base + warp * NSTAGE * kStageBytes;
   int tbl = 0;  // lane i holds the block id of tile n = window + i
 
   auto issue = [&](int n) {
     if ((n & 31) == 0) {
-      const int j = tb + warp + NW * (n + lane);
-      tbl = (j < te) ? __ldg(table + j) : 0;
+      tbl = (n + lane < n_my) ? __ldg(table + tile_of(n + lane)) : 0;
     }
     const int phys = __shfl_sync(0xffffffffu, tbl, n & 31);
     if (lane == 0) {
@@ -500,7 +565,7 @@ __global__ void __launch_bounds__(NW * 32)
       failed = true;
       break;
     }
-    const int j = tb + warp + NW * n;
+    const int j = tile_of(n);
     const uint32_t kt = my_stages + s * kStageBytes;
     const uint32_t vt = kt + kTileBytes;
     if (j >= first_masked) {
@@ -510,6 +575,9 @@ __global__ void __launch_bounds__(NW * 32)
           const int row = nvalid + idx / (D / 8), ch = idx % (D / 8);
           sts128_zero(vt + sw128_offset<kTileTokens>(row, ch));
         }
+        // order these generic-proxy stores before any later TMA (async proxy) write
+        // into the same stage
+        fence_proxy_async_smem();
         __syncwarp();
       }
       path.template tile<true>(kt, vt, j, a.scale_log2);
@@ -529,34 +597,23 @@ __global__ void __launch_bounds__(NW * 32)
     }
   }
   __syncthreads();  // every stage consumed: the stage memory becomes the merge area
-  if (s_failed) return;
+  const bool cta_failed = s_failed != 0;
 
+  // merge area: per warp m[RPC], l[RPC], acc[RPC][kStride]; then the CTA's merged
+  // state cm[RPC], cl[RPC], cacc[RPC][kStride] (read by the cluster peers)
   float *mrg_m = reinterpret_cast<float *>(smem_gen);
   float *mrg_l = mrg_m + NW * RPC;
-  float *mrg_acc = mrg_l + NW * RPC;  // [NW][RPC][D], 16-byte aligned (NW*RPC*8 bytes before)
-  path.publish(mrg_m + warp * RPC, mrg_l + warp * RPC, mrg_acc + warp * RPC * D);
+  float *mrg_acc = mrg_l + NW * RPC;  // 16-byte aligned: NW*RPC*8 bytes before (NW even)
+  float *cta_acc = mrg_acc + NW * RPC * kStride;
+  float *cta_m = cta_acc + RPC * kStride;
+  float *cta_l = cta_m + RPC;
+  if (!cta_failed) path.template publish<kStride>(mrg_m + warp * RPC, mrg_l + warp * RPC,
+                                                   mrg_acc + warp * RPC * kStride);
   __syncthreads();
 
-  // merge the warps and write: (row, 8 dims) per item
-  for (int item = threadIdx.x; item < RPC * (D / 8); item += NW * 32) {
-    const int r = item / (D / 8), d8 = item % (D / 8);
+  auto emit = [&](int r, int d8, float M, float den, const float (&num)[8]) {
     const RowInfo ri = row_info(a, kvh, row0 + r);
-    if (!ri.valid) continue;
-    float M = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < NW; ++w) M = fmaxf(M, mrg_m[w * RPC + r]);
-    float den = 0.f, num[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-    for (int w = 0; w < NW; ++w) {
-      const float mw = mrg_m[w * RPC + r];
-      const float wt = (mw == -INFINITY) ? 0.f : fast_exp2(mw - M);
-      den += wt * mrg_l[w * RPC + r];
-      const float4 *src = reinterpret_cast<const float4 *>(mrg_acc + (w * RPC + r) * D + d8 * 8);
-      const float4 x0 = src[0], x1 = src[1];
-      num[0] += wt * x0.x; num[1] += wt * x0.y; num[2] += wt * x0.z; num[3] += wt * x0.w;
-      num[4] += wt * x1.x; num[5] += wt * x1.y; num[6] += wt * x1.z; num[7] += wt * x1.w;
-    }
-    const size_t orow = (size_t)(seq * a.q_len + ri.u) * a.num_q_heads + ri.h;  // row of out
+    if (!ri.valid) return;
     if constexpr (PARTIAL) {
       const size_t wrow = ((size_t)seq * a.num_splits + split) * (a.q_len * a.num_q_heads) +
                           (size_t)ri.u * a.num_q_heads + ri.h;
@@ -567,8 +624,8 @@ __global__ void __launch_bounds__(NW * 32)
         a.ws_m[wrow] = M;
         a.ws_l[wrow] = den;
       }
-      (void)orow;
     } else {
+      const size_t orow = (size_t)(seq * a.q_len + ri.u) * a.num_q_heads + ri.h;
       const float inv = den > 0.f ? 1.f / den : 0.f;
       uint4 packed;
       packed.x = Elt<T>::from_f2(num[0] * inv, num[1] * inv);
@@ -577,7 +634,68 @@ __global__ void __launch_bounds__(NW * 32)
       packed.w = Elt<T>::from_f2(num[6] * inv, num[7] * inv);
       *reinterpret_cast<uint4 *>(static_cast<T *>(a.out) + orow * D + d8 * 8) = packed;
     }
+  };
+
+  // level 1: merge this CTA's warps, item = (row, 8 dims)
+  if (!cta_failed) {
+    for (int item = threadIdx.x; item < RPC * (D / 8); item += NW * 32) {
+      const int r = item / (D / 8), d8 = item % (D / 8);
+      float M = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < NW; ++w) M = fmaxf(M, mrg_m[w * RPC + r]);
+      float den = 0.f, num[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int w = 0; w < NW; ++w) {
+        const float mw = mrg_m[w * RPC + r];
+        const float wt = (mw == -INFINITY) ? 0.f : fast_exp2(mw - M);
+        den += wt * mrg_l[w * RPC + r];
+        const float4 *src =
+            reinterpret_cast<const float4 *>(mrg_acc + (w * RPC + r) * kStride + d8 * 8);
+        const float4 x0 = src[0], x1 = src[1];
+        num[0] += wt * x0.x; num[1] += wt * x0.y; num[2] += wt * x0.z; num[3] += wt * x0.w;
+        num[4] += wt * x1.x; num[5] += wt * x1.y; num[6] += wt * x1.z; num[7] += wt * x1.w;
+      }
+      if (csize == 1) {
+        emit(r, d8, M, den, num);
+      } else {
+        float4 *dst = reinterpret_cast<float4 *>(cta_acc + r * kStride + d8 * 8);
+        dst[0] = make_float4(num[0], num[1], num[2], num[3]);
+        dst[1] = make_float4(num[4], num[5], num[6], num[7]);
+        if (d8 == 0) {
+          cta_m[r] = M;
+          cta_l[r] = den;
+        }
+      }
+    }
   }
+  if (csize == 1) return;
+
+  // level 2: merge the cluster's CTAs through distributed shared memory; CTA crank
+  // takes every csize-th item.  Every CTA reaches both cluster barriers.
+  cluster_sync_all();
+  bool any_failed = false;
+  for (int c = 0; c < csize; ++c)
+    any_failed |= dsmem_ld_s32(dsmem_map(smem_u32(&s_failed), c)) != 0;
+  if (!any_failed) {
+    for (int item = crank + csize * threadIdx.x; item < RPC * (D / 8); item += csize * NW * 32) {
+      const int r = item / (D / 8), d8 = item % (D / 8);
+      float M = -INFINITY;
+      for (int c = 0; c < csize; ++c)
+        M = fmaxf(M, dsmem_ld_f32(dsmem_map(smem_u32(cta_m + r), c)));
+      float den = 0.f, num[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      for (int c = 0; c < csize; ++c) {
+        const float mc = dsmem_ld_f32(dsmem_map(smem_u32(cta_m + r), c));
+        const float wt = (mc == -INFINITY) ? 0.f : fast_exp2(mc - M);
+        den += wt * dsmem_ld_f32(dsmem_map(smem_u32(cta_l + r), c));
+        const uint32_t src = dsmem_map(smem_u32(cta_acc + r * kStride + d8 * 8), c);
+        const float4 x0 = dsmem_ld_f32x4(src), x1 = dsmem_ld_f32x4(src + 16);
+        num[0] += wt * x0.x; num[1] += wt * x0.y; num[2] += wt * x0.z; num[3] += wt * x0.w;
+        num[4] += wt * x1.x; num[5] += wt * x1.y; num[6] += wt * x1.z; num[7] += wt * x1.w;
+      }
+      emit(r, d8, M, den, num);
+    }
+  }
+  cluster_sync_all();  // peers' shared memory stays alive until every read is done
 }
 
 // ---------------------------------------------------------------------------------
@@ -596,29 +714,43 @@ __global__ void __launch_bounds__(128) split_combine_kernel(const CombineArgs a)
   if (gw >= a.num_seqs * a.rows_per_seq) return;
   const int seq = gw / a.rows_per_seq, r = gw % a.rows_per_seq;
   const size_t base = (size_t)seq * a.num_splits * a.rows_per_seq + r;
+  const size_t pstride = a.rows_per_seq;
+  // statistics: lanes take partitions (all loads independent), then warp reductions
   float M = -INFINITY;
-  for (int p = 0; p < a.num_splits; ++p) {
-    const size_t w = base + (size_t)p * a.rows_per_seq;
+  for (int p = lane; p < a.num_splits; p += 32) {
+    const size_t w = base + p * pstride;
     if (a.ws_l[w] > 0.f) M = fmaxf(M, a.ws_m[w]);
   }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
   float den = 0.f, num[PER];
 #pragma unroll
   for (int k = 0; k < PER; ++k) num[k] = 0.f;
   if (M != -INFINITY) {
-    for (int p = 0; p < a.num_splits; ++p) {
-      const size_t w = base + (size_t)p * a.rows_per_seq;
-      const float lw = a.ws_l[w];
-      if (!(lw > 0.f)) continue;
-      const float wt = fast_exp2(a.ws_m[w] - M);
-      den += wt * lw;
-      const float *acc = a.ws_acc + w * D + lane * PER;
+    for (int p0 = 0; p0 < a.num_splits; p0 += 32) {
+      // lane holds the weight of partition p0 + lane
+      float wt = 0.f;
+      if (p0 + lane < a.num_splits) {
+        const size_t w = base + (p0 + lane) * pstride;
+        const float lw = a.ws_l[w];
+        wt = lw > 0.f ? fast_exp2(a.ws_m[w] - M) : 0.f;
+        den += wt * lw;
+      }
+      const int cnt = min(32, a.num_splits - p0);
+#pragma unroll 4
+      for (int k = 0; k < cnt; ++k) {
+        const float wk = __shfl_sync(0xffffffffu, wt, k);
+        const float *acc = a.ws_acc + (base + (p0 + k) * pstride) * D + lane * PER;
 #pragma unroll
-      for (int k = 0; k < PER; k += 2) {
-        const float2 x = *reinterpret_cast<const float2 *>(acc + k);
-        num[k] += wt * x.x;
-        num[k + 1] += wt * x.y;
+        for (int q = 0; q < PER; q += 2) {
+          const float2 x = *reinterpret_cast<const float2 *>(acc + q);
+          num[q] += wk * x.x;
+          num[q + 1] += wk * x.y;
+        }
       }
     }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
   }
   const float inv = den > 0.f ? 1.f / den : 0.f;
   T *o = static_cast<T *>(a.out) + ((size_t)seq * a.rows_per_seq + r) * D + lane * PER;

@@ -11,29 +11,70 @@ namespace pa {
 
 constexpr int kMaxDevices = 64;
 
-// Pipeline shape: warps per CTA, stages per warp.
+// Pipeline shape: warps per CTA, stages per warp (measured on GB300).  The single
+// pass uses 2 stages per warp, which fits 3 CTAs per SM (12 warps) and helps the
+// skewed-length workloads.  The split-KV partial pass gets the caller's
+// equal-size partitions; with 3 stages (2 CTAs per SM) its CTAs are deeper and
+// fewer, which measured faster there.
 constexpr int kWarps = 4;
-constexpr int kStages = 3;
+template <bool PARTIAL>
+constexpr int stages_for() { return PARTIAL ? 3 : 2; }
+constexpr int kMaxCluster = 8;  // portable cluster size limit
+
+// Per device: SM count and resident CTAs per SM of one kernel (cached).
+struct DeviceFit {
+  std::atomic<int> sms{0};
+  std::atomic<int> ctas_per_sm{0};
+};
 
 template <typename T, int D, class Path, bool PARTIAL>
 static cudaError_t launch_one(const CUtensorMap &kmap, const CUtensorMap &vmap,
                               const DecodeArgs &a, int units, int row_groups, cudaStream_t st) {
+  constexpr int kStages = stages_for<PARTIAL>();
   constexpr int kStageBytes = 2 * kTileTokens * D * 2;
   constexpr int kSmem = kWarps * kStages * kStageBytes + 1024;
   auto kern = paged_decode_kernel<T, D, kWarps, kStages, Path, PARTIAL>;
-  // the shared-memory opt-in is a per-device function attribute: set it once per device
-  static std::atomic<bool> configured[kMaxDevices];
+  static DeviceFit fit[kMaxDevices];
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  if (!configured[dev].load(std::memory_order_acquire)) {
+  DeviceFit &f = fit[dev];
+  if (f.ctas_per_sm.load(std::memory_order_acquire) == 0) {
+    // the shared-memory opt-in is a per-device function attribute
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     if (e != cudaSuccess) return e;
-    configured[dev].store(true, std::memory_order_release);
+    int sms = 0, per_sm = 0;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kWarps * 32, kSmem);
+    if (e != cudaSuccess) return e;
+    f.sms.store(sms, std::memory_order_relaxed);
+    f.ctas_per_sm.store(per_sm > 0 ? per_sm : 1, std::memory_order_release);
   }
-  kern<<<dim3(units, row_groups), kWarps * 32, kSmem, st>>>(kmap, vmap, a);
-  return cudaGetLastError();
+  // Single pass: when the units would fill fewer than two waves of resident CTAs,
+  // give each unit a cluster of 2, 4 or 8 CTAs so long sequences spread over
+  // several SMs.  The partial pass already has the caller's partitions (clusters
+  // measured slower there: each CTA's fixed cost outweighs the shorter tail).
+  int cluster = 1;
+  if (!PARTIAL) {
+    const long long slots = (long long)f.sms.load() * f.ctas_per_sm.load();
+    const long long work = (long long)units * row_groups;
+    while (cluster < kMaxCluster && work * cluster < 2 * slots) cluster *= 2;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)units * cluster, (unsigned)row_groups, 1);
+  cfg.blockDim = dim3(kWarps * 32, 1, 1);
+  cfg.dynamicSmemBytes = kSmem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = cluster;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = cluster > 1 ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, kmap, vmap, a);
 }
 
 template <typename T, int D, bool PARTIAL>
