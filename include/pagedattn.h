@@ -182,6 +182,16 @@ PA_API pa_status pa_decode_combine(void *out, const void *workspace, size_t work
 PA_API pa_status pa_device_error(void *stream, int clear);
 
 /*
+ * pa_selftest_wait_timeout -- diagnostic: launches one thread that waits, with the
+ * same bounded wait the attention kernels use for their TMA stages, on a
+ * shared-memory barrier that nothing ever completes.  After about two seconds the
+ * wait gives up and records PA_ERR_DEVICE_TIMEOUT in the device error word
+ * (read it with pa_device_error); the CUDA context stays usable.  Lets a caller
+ * check the failure path without faulting or hanging the GPU.
+ */
+PA_API pa_status pa_selftest_wait_timeout(void *stream);
+
+/*
  * pa_decode_split_noalloc -- the split-KV pair (pa_decode_partial, then
  * pa_decode_combine) with its workspace in a fixed device array that the library
  * owns, for callers that cannot allocate device memory where they run attention:

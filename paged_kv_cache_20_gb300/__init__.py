@@ -54,6 +54,7 @@ _SIGNATURES = {
     "pa_decode_combine": (_c_int, [_c_vp, _c_vp, _c_size, _c_int, _c_int, _c_int, _c_int,
                                    _c_int, _c_int, _c_vp]),
     "pa_device_error": (_c_int, [_c_vp, _c_int]),
+    "pa_selftest_wait_timeout": (_c_int, [_c_vp]),
     "pa_decode_split_noalloc": (_c_int, [_c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_int, _c_int,
                                          _c_int, _c_int, _c_int, _c_float, _c_int, _c_int,
                                          _c_int, _c_int, _c_int, _c_vp]),
@@ -234,6 +235,11 @@ def pa_decode_combine(out: torch.Tensor, workspace: torch.Tensor, num_splits: in
         _cuda(out, "out"), _cuda(workspace, "workspace"), nbytes, num_seqs, h_q, head_dim, q_len,
         num_splits, _elt(out, "out"), _stream(stream)))
     return out
+
+
+def pa_selftest_wait_timeout(stream=None) -> None:
+    """Launch the bounded-wait self-test (sets PA_ERR_DEVICE_TIMEOUT after ~2 s)."""
+    _check("pa_selftest_wait_timeout", load().pa_selftest_wait_timeout(_stream(stream)))
 
 
 def pa_device_error(stream=None, clear: bool = True) -> int:

@@ -79,6 +79,15 @@ __global__ void append_kv_kernel(uint16_t *k_cache, uint16_t *v_cache, const uin
   }
 }
 
+// A wait nobody satisfies: an mbarrier expecting one arrival that never comes.
+__global__ void wait_timeout_kernel(unsigned *err) {
+  __shared__ __align__(8) uint64_t bar;
+  const uint32_t b = pa::smem_u32(&bar);
+  pa::mbar_init(b, 1);
+  pa::fence_mbar_init();
+  if (!pa::mbar_wait_bounded(b, 0)) pa::record_error(err, pa::kErrTimeout);
+}
+
 // ---- host helpers --------------------------------------------------------------------
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
@@ -354,6 +363,13 @@ PA_API pa_status pa_decode_combine(void *out, const void *workspace, size_t work
   cudaError_t e = dtype == PA_FP16 ? pa::launch_combine_fp16(a, head_dim, s)
                                    : pa::launch_combine_bf16(a, head_dim, s);
   return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+PA_API pa_status pa_selftest_wait_timeout(void *stream) {
+  unsigned *err = error_word();
+  if (err == nullptr) return PA_ERR_CUDA;
+  wait_timeout_kernel<<<1, 1, 0, static_cast<cudaStream_t>(stream)>>>(err);
+  return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
 PA_API pa_status pa_device_error(void *stream, int clear) {

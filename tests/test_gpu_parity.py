@@ -283,3 +283,17 @@ def test_append_skips_negative_and_reports_out_of_pool_slots(pa):
     kc[0, :, 5] = 0
     vc[0, :, 5] = 0
     assert int(kc.abs().sum()) == 0 and int(vc.abs().sum()) == 0
+
+
+def test_device_wait_times_out_and_reports(pa):
+    """A device-side wait that nothing satisfies gives up after its limit, reports
+    PA_ERR_DEVICE_TIMEOUT, and leaves the context usable."""
+    import time
+    assert pa.pa_device_error() == 0
+    t0 = time.time()
+    pa.pa_selftest_wait_timeout()
+    assert pa.pa_device_error() == pa.PA_ERR_DEVICE_TIMEOUT
+    assert 1.0 < time.time() - t0 < 30.0
+    assert pa.pa_device_error() == 0                 # cleared
+    x = torch.ones(1024, device=DEV)
+    assert float(x.sum()) == 1024.0                  # context still works
