@@ -1,8 +1,11 @@
 """Benchmark: paged decode attention (append + attend) on GB300.
 
-One step = one pass of the whole hot path over one batch: pa_slot_mapping ->
-pa_append_kv -> pa_decode (or pa_decode_partial + pa_decode_combine for a
-split-KV workload), on one stream, with every input resident in HBM.
+One step = one pass of the whole hot path over one batch: slot mapping, append of
+the new K/V rows, attention (plus the combine for a split-KV workload), on one
+stream, with every input resident in HBM.  The timed step is the fused entry
+point pa_append_decode (one launch); the same step as separate launches
+(pa_slot_mapping -> pa_append_kv -> pa_decode, or the partial/combine pair) is
+timed too and reported as "separate_launches_ms_per_step".
 
 Metric: KV tokens/s = sum of context lengths / step time (a token is counted once
 per sequence, whatever the number of heads or query rows), with the achieved HBM
@@ -111,7 +114,10 @@ def algorithmic_bytes(w: workloads.Workload) -> dict:
         ws = 2 * rows * (c.head_dim + 2) * 4
     # the attention launch: reads unique KV, q, tables; writes out (or the workspace)
     decode = kv + q + tables + (ws // 2 if c.num_splits > 1 else out)
-    return {"per_token": per_token, "kv": kv, "decode_launch": decode,
+    # the fused step's attention launch(es): the above, plus the append it performs,
+    # plus (split-KV) the combine reading the workspace and writing out
+    fused = decode + append + (ws // 2 + out if c.num_splits > 1 else 0)
+    return {"per_token": per_token, "kv": kv, "decode_launch": decode, "fused_launch": fused,
             "step": kv + q + out + tables + append + ws + n_new * 8}
 
 
@@ -213,9 +219,33 @@ class Runner:
             nbytes = pa.pa_decode_workspace_size(c.num_seqs, c.num_q_heads, c.q_len, c.head_dim,
                                                  c.num_splits)
             self.ws = torch.empty(nbytes, dtype=torch.uint8, device=device)
-        self.launches_per_step = 3 + (1 if c.num_splits > 1 else 0)
+        self.fused = True
+        self.launches = {True: 1 + (1 if c.num_splits > 1 else 0),
+                         False: 3 + (1 if c.num_splits > 1 else 0)}
+
+    @property
+    def launches_per_step(self) -> int:
+        return self.launches[self.fused]
 
     def step(self, ev_pair=None):
+        if self.fused:
+            return self.step_fused(ev_pair)
+        return self.step_separate(ev_pair)
+
+    def step_fused(self, ev_pair=None):
+        """pa_append_decode: slot mapping, append and attention in one launch (plus the
+        combine for a split-KV workload); the events bracket the whole call."""
+        pa, d, c = self.pa, self.d, self.w.cfg
+        if ev_pair is not None:
+            ev_pair[0].record()
+        pa.pa_append_decode(self.out, d["q"], d["k_new"], d["v_new"], d["k_cache"], d["v_cache"],
+                            d["block_tables"], d["context_lens"], self.w.scale, c.q_len,
+                            c.num_splits, self.ws)
+        if ev_pair is not None:
+            ev_pair[1].record()
+
+    def step_separate(self, ev_pair=None):
+        """pa_slot_mapping, pa_append_kv, then the attention launch(es) on their own."""
         pa, d, c = self.pa, self.d, self.w.cfg
         pa.pa_slot_mapping(d["block_tables"], d["context_lens"], c.block_size, c.q_len,
                            out=self.slots)
@@ -329,6 +359,10 @@ def measure_config(pa, name, seed, device, steps, warmup, world, peaks, e2e=Fals
     over = {"num_seqs": num_seqs} if num_seqs else {}
     w = workloads.make(name, seed=seed, poison=False, **over)
     runner = Runner(pa, w, device)
+    # the unfused sequence first (reported for comparison), then the fused step
+    runner.fused = False
+    sep_ms, sep_kern_ms, _ = time_device(runner, steps, warmup, world)
+    runner.fused = True
     step_ms, kern_ms, wall = time_device(runner, steps, warmup, world)
     assert pa.pa_device_error() == 0, "device error during the timed run"
     ab = algorithmic_bytes(w)
@@ -336,8 +370,10 @@ def measure_config(pa, name, seed, device, steps, warmup, world, peaks, e2e=Fals
     tokens = sum_over_ranks(float(w.total_tokens), world, device)
     ms_per_step = total_ms / steps
     kern_avg = statistics.mean(kern_ms)
-    kern_name = "paged_decode_kernel" + ("(partial)" if w.cfg.num_splits > 1 else "")
-    achieved = ab["decode_launch"] / (kern_avg * 1e-3) / 1e9
+    split = w.cfg.num_splits > 1
+    kern_name = ("paged_decode_kernel(append+partial)+split_combine_kernel" if split
+                 else "paged_decode_kernel(append+attention)")
+    achieved = ab["fused_launch"] / (kern_avg * 1e-3) / 1e9
     peak = peaks.get("hbm_gbs")
     peak_src = "measured" if peak else "fallback"
     peak = peak or FALLBACK_HBM_GBS
@@ -350,9 +386,11 @@ def measure_config(pa, name, seed, device, steps, warmup, world, peaks, e2e=Fals
                      "frac_of_8tbs": achieved / NOMINAL_HBM_GBS,
                      "traffic": traffic_record(kern_name, name), "kernel": kern_name,
                      "kernel_us": kern_avg * 1e3,
-                     "bytes_per_launch": ab["decode_launch"],
-                     "bytes_per_kv_token": ab["per_token"]},
+                     "bytes_per_launch": ab["fused_launch"],
+                     "bytes_per_kv_token": ab["per_token"],
+                     "attention_only_kernel_us": statistics.mean(sep_kern_ms) * 1e3},
         "step_gbs": ab["step"] / (ms_per_step * 1e-3) / 1e9,
+        "separate_launches_ms_per_step": max_over_ranks(sum(sep_ms), world, device) / steps,
     }
     if e2e:
         ms, h2d, d2h = time_e2e(runner, steps, max(3, warmup))
@@ -395,6 +433,7 @@ def run_ours(args):
                 continue
             o = measure_config(pa, name, rank, device, args.steps, args.warmup, world, peaks)
             others[name] = {"value": o["value"], "unit": UNIT, "ms_per_step": o["ms_per_step"],
+                            "separate_launches_ms_per_step": o["separate_launches_ms_per_step"],
                             "roofline_frac": o["roofline"]["frac"],
                             "achieved_gbs": o["roofline"]["achieved"],
                             "kernel_us": o["roofline"]["kernel_us"],
@@ -414,15 +453,18 @@ def run_ours(args):
         "roofline": r["roofline"], "cpu_baseline": cpu, "e2e": r.get("e2e"),
         "gpu_launches": args.steps * r["runner"].launches_per_step,
         "clocks": clocks, "step_p10_p50_p90_ms": r["step_ms_p10_p50_p90"],
-        "step_algorithmic_gbs": r["step_gbs"], "other_configs": others,
+        "step_algorithmic_gbs": r["step_gbs"],
+        "separate_launches_ms_per_step": r["separate_launches_ms_per_step"],
+        "other_configs": others,
         "kernel_src_sha": kernel_source_sha(),
     }
     print(json.dumps(line))
 
 
 def _path(w):
-    return ("pa_slot_mapping+pa_append_kv+pa_decode_partial+pa_decode_combine"
-            if w.cfg.num_splits > 1 else "pa_slot_mapping+pa_append_kv+pa_decode")
+    return ("pa_append_decode (fused slot mapping + append + split-KV partial, then combine)"
+            if w.cfg.num_splits > 1 else
+            "pa_append_decode (fused slot mapping + append + attention, one launch)")
 
 
 # --------------------------------------------------------------------------- reference arm

@@ -173,6 +173,27 @@ PA_API pa_status pa_decode_combine(void *out, const void *workspace, size_t work
                                    int num_splits, pa_dtype dtype, void *stream);
 
 /*
+ * pa_append_decode -- one decode step fused: slot mapping, append of the new K/V
+ * rows and attention in one launch (a second launch, the combine, when
+ * num_splits > 1).  Kernel fusion of consecutive memory-bound steps follows
+ * [SB11] §11.8 ("Kernel Fusion").  Equivalent to pa_slot_mapping, then
+ * pa_append_kv of k_new/v_new (rows [num_seqs*q_len][num_kv_heads][head_dim], the
+ * last q_len positions of each sequence), then pa_decode (num_splits == 1;
+ * workspace may be NULL) or pa_decode_partial + pa_decode_combine (num_splits > 1;
+ * workspace as for pa_decode_partial).  The cache ends up bit-identical to the
+ * unfused sequence and out within the same tolerance.  New positions < 0 are
+ * skipped; new positions beyond the block table or the pool are skipped and set
+ * PA_ERR_DEVICE_CHECK.
+ */
+PA_API pa_status pa_append_decode(void *out, const void *q, const void *k_new, const void *v_new,
+                                  void *k_cache, void *v_cache, const int32_t *block_tables,
+                                  const int32_t *context_lens, int num_seqs, int num_q_heads,
+                                  int num_kv_heads, int head_dim, int block_size, float scale,
+                                  int max_blocks_per_seq, int num_blocks, int q_len,
+                                  pa_dtype dtype, int num_splits, void *workspace,
+                                  size_t workspace_bytes, void *stream);
+
+/*
  * pa_device_error -- synchronise `stream`, then return PA_OK or the first error
  * recorded by a kernel on the current device since the last clear
  * (PA_ERR_DEVICE_TIMEOUT takes precedence over PA_ERR_DEVICE_CHECK).  With

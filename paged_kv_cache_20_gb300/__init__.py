@@ -55,6 +55,9 @@ _SIGNATURES = {
                                    _c_int, _c_int, _c_vp]),
     "pa_device_error": (_c_int, [_c_vp, _c_int]),
     "pa_selftest_wait_timeout": (_c_int, [_c_vp]),
+    "pa_append_decode": (_c_int, [_c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_int,
+                                  _c_int, _c_int, _c_int, _c_int, _c_float, _c_int, _c_int,
+                                  _c_int, _c_int, _c_int, _c_vp, _c_size, _c_vp]),
     "pa_decode_split_noalloc": (_c_int, [_c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_int, _c_int,
                                          _c_int, _c_int, _c_int, _c_float, _c_int, _c_int,
                                          _c_int, _c_int, _c_int, _c_vp]),
@@ -247,19 +250,57 @@ def pa_device_error(stream=None, clear: bool = True) -> int:
     return int(load().pa_device_error(_stream(stream), 1 if clear else 0))
 
 
+def pa_append_decode(out: torch.Tensor, q: torch.Tensor, k_new: torch.Tensor,
+                     v_new: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                     block_tables: torch.Tensor, context_lens: torch.Tensor, scale: float,
+                     q_len: int = 1, num_splits: int = 1, workspace: torch.Tensor | None = None,
+                     stream=None) -> torch.Tensor:
+    """Fused step: slot mapping + append of k_new/v_new + attention (one launch)."""
+    num_blocks, h_kv, block_size, head_dim, num_seqs, h_q, maxb = _decode_dims(
+        q, k_cache, block_tables, context_lens, q_len)
+    if out.shape != q.shape or out.dtype != q.dtype or q.dtype != k_cache.dtype:
+        raise ValueError("out must match q; q must have the cache dtype")
+    if k_new.shape != (num_seqs * q_len, h_kv, head_dim) or v_new.shape != k_new.shape:
+        raise ValueError("k_new/v_new must be [num_seqs * q_len, num_kv_heads, head_dim]")
+    for t, nm in ((k_new, "k_new"), (v_new, "v_new"), (v_cache, "v_cache")):
+        if t.dtype != k_cache.dtype:
+            raise TypeError(f"{nm} must have the cache dtype {k_cache.dtype}")
+    ws_ptr, ws_bytes = None, 0
+    if num_splits > 1:
+        if workspace is None:
+            nbytes = pa_decode_workspace_size(num_seqs, h_q, q_len, head_dim, num_splits)
+            workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+        ws_ptr, ws_bytes = _cuda(workspace, "workspace"), workspace.numel() * workspace.element_size()
+    _check("pa_append_decode", load().pa_append_decode(
+        _cuda(out, "out"), _cuda(q, "q"), _cuda(k_new, "k_new"), _cuda(v_new, "v_new"),
+        _cuda(k_cache, "k_cache"), _cuda(v_cache, "v_cache"),
+        _cuda(block_tables, "block_tables", torch.int32),
+        _cuda(context_lens, "context_lens", torch.int32), num_seqs, h_q, h_kv, head_dim,
+        block_size, float(scale), maxb, num_blocks, q_len, _elt(k_cache, "k_cache"), num_splits,
+        ws_ptr, ws_bytes, _stream(stream)))
+    return out
+
+
 def paged_decode_step(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
                       k_cache: torch.Tensor, v_cache: torch.Tensor, block_tables: torch.Tensor,
                       context_lens: torch.Tensor, scale: float, q_len: int = 1,
                       num_splits: int = 1, out: torch.Tensor | None = None,
                       workspace: torch.Tensor | None = None,
-                      slot_mapping: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+                      slot_mapping: torch.Tensor | None = None, stream=None,
+                      fused: bool = False) -> torch.Tensor:
     """One decode step: slot mapping, KV append, then attention.
 
-    Runs pa_slot_mapping -> pa_append_kv -> pa_decode (num_splits == 1) or
-    pa_decode_partial + pa_decode_combine (num_splits > 1) on one stream.
+    fused=False runs pa_slot_mapping -> pa_append_kv -> pa_decode (num_splits == 1)
+    or pa_decode_partial + pa_decode_combine (num_splits > 1) on one stream;
+    fused=True runs the same step as pa_append_decode (one launch, two with splits).
     Optional ``out``, ``workspace`` and ``slot_mapping`` buffers are reused when
     given (no allocation on the hot path).
     """
+    if fused:
+        if out is None:
+            out = torch.empty_like(q)
+        return pa_append_decode(out, q, k_new, v_new, k_cache, v_cache, block_tables,
+                                context_lens, scale, q_len, num_splits, workspace, stream)
     block_size = int(k_cache.shape[2])
     slot_mapping = pa_slot_mapping(block_tables, context_lens, block_size, q_len,
                                    out=slot_mapping, stream=stream)

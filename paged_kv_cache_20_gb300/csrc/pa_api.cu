@@ -33,6 +33,8 @@ __global__ void slot_mapping_kernel(int64_t *out, const int32_t *block_tables,
                                     const int32_t *context_lens, int num_seqs,
                                     int max_blocks_per_seq, int block_size, int q_len,
                                     unsigned *err) {
+  pa::griddep_wait();  // inputs may come from the previous kernel on the stream
+  pa::griddep_launch_dependents();
   const int idx = blockIdx.x * blockDim.x + threadIdx.x;
   if (idx >= num_seqs * q_len) return;
   const int i = idx / q_len, u = idx % q_len;
@@ -55,6 +57,8 @@ template <int D>
 __global__ void append_kv_kernel(uint16_t *k_cache, uint16_t *v_cache, const uint16_t *k_new,
                                  const uint16_t *v_new, const int64_t *slot_mapping, int n_tokens,
                                  int num_kv_heads, int64_t num_slots, unsigned *err) {
+  pa::griddep_wait();  // the slot mapping may come from the previous kernel
+  pa::griddep_launch_dependents();
   constexpr int kChunks = D / 8;
   const int64_t total = (int64_t)n_tokens * num_kv_heads * kChunks;
   for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
@@ -187,7 +191,7 @@ pa_status decode_common(void *out, float *ws, const WsLayout *lay, const void *q
                         const int32_t *context_lens, int num_seqs, int num_q_heads,
                         int num_kv_heads, int head_dim, float scale, int num_splits,
                         int max_blocks_per_seq, int num_blocks, int q_len, pa_dtype dtype,
-                        void *stream) {
+                        void *stream, const void *k_new = nullptr, const void *v_new = nullptr) {
   const int64_t units = (int64_t)num_seqs * num_kv_heads * num_splits;
   if (units >= (int64_t)1 << 31) return PA_ERR_INVALID_ARG;
   CUtensorMap kmap, vmap;
@@ -215,6 +219,10 @@ pa_status decode_common(void *out, float *ws, const WsLayout *lay, const void *q
   a.num_blocks = num_blocks;
   a.num_splits = num_splits;
   a.lpt = num_seqs <= pa::kLptMaxSeqs ? 1 : 0;
+  a.k_new = static_cast<const uint16_t *>(k_new);
+  a.v_new = static_cast<const uint16_t *>(v_new);
+  a.k_cache = static_cast<uint16_t *>(const_cast<void *>(k_cache));
+  a.v_cache = static_cast<uint16_t *>(const_cast<void *>(v_cache));
   a.scale_log2 = scale * 1.4426950408889634f;  // log2(e)
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const bool partial = ws != nullptr;
@@ -256,10 +264,11 @@ PA_API pa_status pa_slot_mapping(int64_t *slot_mapping, const int32_t *block_tab
   unsigned *err = error_word();
   if (err == nullptr) return PA_ERR_CUDA;
   const int n = num_seqs * q_len;
-  slot_mapping_kernel<<<(n + 255) / 256, 256, 0, static_cast<cudaStream_t>(stream)>>>(
-      slot_mapping, block_tables, context_lens, num_seqs, max_blocks_per_seq, block_size, q_len,
-      err);
-  return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+  cudaError_t e = pa::launch_dependent(slot_mapping_kernel, (n + 255) / 256, 256,
+                                       static_cast<cudaStream_t>(stream), slot_mapping,
+                                       block_tables, context_lens, num_seqs, max_blocks_per_seq,
+                                       block_size, q_len, err);
+  return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
 PA_API pa_status pa_append_kv(void *k_cache, void *v_cache, const void *k_new, const void *v_new,
@@ -286,13 +295,14 @@ PA_API pa_status pa_append_kv(void *k_cache, void *v_cache, const void *k_new, c
   auto vc = static_cast<uint16_t *>(v_cache);
   auto kn = static_cast<const uint16_t *>(k_new);
   auto vn = static_cast<const uint16_t *>(v_new);
-  if (head_dim == 128)
-    append_kv_kernel<128><<<blocks, threads, 0, s>>>(kc, vc, kn, vn, slot_mapping, n_tokens,
-                                                     num_kv_heads, num_slots, err);
-  else
-    append_kv_kernel<64><<<blocks, threads, 0, s>>>(kc, vc, kn, vn, slot_mapping, n_tokens,
-                                                    num_kv_heads, num_slots, err);
-  return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+  cudaError_t e = head_dim == 128
+                      ? pa::launch_dependent(append_kv_kernel<128>, blocks, threads, s, kc, vc, kn,
+                                             vn, slot_mapping, n_tokens, num_kv_heads, num_slots,
+                                             err)
+                      : pa::launch_dependent(append_kv_kernel<64>, blocks, threads, s, kc, vc, kn,
+                                             vn, slot_mapping, n_tokens, num_kv_heads, num_slots,
+                                             err);
+  return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
 PA_API pa_status pa_decode(void *out, const void *q, const void *k_cache, const void *v_cache,
@@ -308,6 +318,36 @@ PA_API pa_status pa_decode(void *out, const void *q, const void *k_cache, const 
   return decode_common(out, nullptr, nullptr, q, k_cache, v_cache, block_tables, context_lens,
                        num_seqs, num_q_heads, num_kv_heads, head_dim, scale, 1,
                        max_blocks_per_seq, num_blocks, q_len, dtype, stream);
+}
+
+PA_API pa_status pa_append_decode(void *out, const void *q, const void *k_new, const void *v_new,
+                                  void *k_cache, void *v_cache, const int32_t *block_tables,
+                                  const int32_t *context_lens, int num_seqs, int num_q_heads,
+                                  int num_kv_heads, int head_dim, int block_size, float scale,
+                                  int max_blocks_per_seq, int num_blocks, int q_len,
+                                  pa_dtype dtype, int num_splits, void *workspace,
+                                  size_t workspace_bytes, void *stream) {
+  if (!out || !aligned16(out) || !k_new || !v_new || !aligned16(k_new) || !aligned16(v_new))
+    return PA_ERR_INVALID_ARG;
+  if (num_splits <= 0) return PA_ERR_INVALID_ARG;
+  pa_status st = check_decode(q, k_cache, v_cache, block_tables, context_lens, num_seqs,
+                              num_q_heads, num_kv_heads, head_dim, block_size, scale,
+                              max_blocks_per_seq, num_blocks, q_len, dtype);
+  if (st != PA_OK) return st;
+  if (num_splits == 1)
+    return decode_common(out, nullptr, nullptr, q, k_cache, v_cache, block_tables, context_lens,
+                         num_seqs, num_q_heads, num_kv_heads, head_dim, scale, 1,
+                         max_blocks_per_seq, num_blocks, q_len, dtype, stream, k_new, v_new);
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return PA_ERR_INVALID_ARG;
+  const WsLayout lay = ws_layout(num_seqs, num_q_heads, q_len, head_dim, num_splits);
+  if (workspace_bytes < lay.total) return PA_ERR_INVALID_ARG;
+  st = decode_common(nullptr, static_cast<float *>(workspace), &lay, q, k_cache, v_cache,
+                     block_tables, context_lens, num_seqs, num_q_heads, num_kv_heads, head_dim,
+                     scale, num_splits, max_blocks_per_seq, num_blocks, q_len, dtype, stream,
+                     k_new, v_new);
+  if (st != PA_OK) return st;
+  return pa_decode_combine(out, workspace, workspace_bytes, num_seqs, num_q_heads, head_dim,
+                           q_len, num_splits, dtype, stream);
 }
 
 PA_API size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int q_len, int head_dim,

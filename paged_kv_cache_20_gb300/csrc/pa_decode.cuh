@@ -59,6 +59,13 @@ struct DecodeArgs {
   int max_blocks_per_seq, num_blocks, num_splits;
   int lpt;                       // 1: take sequences longest first (num_seqs <= kLptMaxSeqs)
   float scale_log2;              // scale * log2(e): scores in base-2 units
+  // fused append (k_new == nullptr: none).  The unit writes its own KV head's rows
+  // of this step's new tokens -- positions context_len - q_len + u -- into the
+  // cache before reading it.
+  const uint16_t *k_new;         // [num_seqs * q_len][num_kv_heads][D]
+  const uint16_t *v_new;
+  uint16_t *k_cache;             // the memory the tensor maps describe
+  uint16_t *v_cache;
 };
 
 constexpr int kLptMaxSeqs = 256;
@@ -453,7 +460,7 @@ __global__ void __launch_bounds__(NW * 32)
   constexpr int kTileBytes = kTileTokens * D * 2;  // one head of one block: 4 KiB at D = 128
   constexpr int kStageBytes = 2 * kTileBytes;      // K tile + V tile
   constexpr int RPC = Path::RPC;
-  constexpr int kStride = D + 4;                   // merge-area row stride (floats), padded
+  constexpr int kStride = D + 8;  // merge-area row stride (floats): padded against bank conflicts
   static_assert((NW + 1) * RPC * (kStride + 2) * 4 + 64 <= NW * NSTAGE * kStageBytes,
                 "merge area");
 
@@ -465,6 +472,13 @@ __global__ void __launch_bounds__(NW * 32)
   const int warp = threadIdx.x >> 5;
   const uint32_t smem_base = (smem_u32(smem_raw) + 1023u) & ~1023u;  // 128B-swizzle tiles: 1 KiB
   uint8_t *smem_gen = smem_raw + (smem_base - smem_u32(smem_raw));
+
+  // Launched as a programmatic dependent of the previous kernel on the stream (for
+  // example the KV append): setup above this point overlaps that kernel's tail.
+  // Wait for it to complete before the first read of global memory: any input
+  // (cache, q, tables, lengths) may have been written by it.
+  griddep_wait();
+  griddep_launch_dependents();  // the next kernel may start its own setup
 
   const int csize = static_cast<int>(cluster_nctarank());  // 1 without a cluster launch
   const int crank = static_cast<int>(cluster_ctarank());
@@ -492,6 +506,37 @@ __global__ void __launch_bounds__(NW * 32)
   const int te = min(nb, tb + per);
   const int first_masked = (L - a.q_len + 1) / kTileTokens;  // tiles >= this need masking
 
+  // Fused append: every CTA whose block range holds a new token writes all of this
+  // unit's new rows itself (CTAs of one cluster, row group or neighbouring split
+  // write identical bytes), then orders those generic-proxy stores before its own
+  // TMA reads of the cache.
+  if (a.k_new != nullptr && te > tb && te * kTileTokens > L - a.q_len) {
+    const int64_t num_slots = (int64_t)a.num_blocks * kTileTokens;
+    for (int idx = threadIdx.x; idx < a.q_len * (D / 8); idx += NW * 32) {
+      const int u = idx / (D / 8), c = idx % (D / 8);
+      const int pos = L - a.q_len + u;
+      if (pos < 0) continue;
+      const int lb = pos / kTileTokens;
+      if (lb >= a.max_blocks_per_seq) {
+        record_error(a.err, kErrCheck);
+        continue;
+      }
+      const int64_t slot = (int64_t)__ldg(a.block_tables + (size_t)seq * a.max_blocks_per_seq + lb) *
+                               kTileTokens + pos % kTileTokens;
+      if (slot < 0 || slot >= num_slots) {
+        record_error(a.err, kErrCheck);
+        continue;
+      }
+      const int64_t blk = slot / kTileTokens, off = slot % kTileTokens;
+      const size_t dst = (size_t)(((blk * a.num_kv_heads + kvh) * kTileTokens + off) * D + c * 8);
+      const size_t src = ((size_t)(seq * a.q_len + u) * a.num_kv_heads + kvh) * D + c * 8;
+      *reinterpret_cast<uint4 *>(a.k_cache + dst) = __ldg(reinterpret_cast<const uint4 *>(a.k_new + src));
+      *reinterpret_cast<uint4 *>(a.v_cache + dst) = __ldg(reinterpret_cast<const uint4 *>(a.v_new + src));
+    }
+    fence_proxy_async_global();
+    __syncthreads();
+  }
+
   if (threadIdx.x == 0) {
     s_failed = 0;
     prefetch_tensormap(&kmap);
@@ -503,9 +548,6 @@ __global__ void __launch_bounds__(NW * 32)
     fence_mbar_init();
   }
   __syncwarp();
-
-  Path path;
-  path.init(a, seq, kvh, row0, L);
 
   // This warp's tiles: the unit's ntiles blocks are visited from a starting offset
   // `rot` that differs between the KV heads of a sequence, tile number
@@ -528,7 +570,7 @@ __global__ void __launch_bounds__(NW * 32)
   int tbl = 0;  // lane i holds the block id of tile n = window + i
 
   auto issue = [&](int n) {
-    if ((n & 31) == 0) {
+    if ((n & 31) == 0 && n > 0) {
       tbl = (n + lane < n_my) ? __ldg(table + tile_of(n + lane)) : 0;
     }
     const int phys = __shfl_sync(0xffffffffu, tbl, n & 31);
@@ -551,6 +593,11 @@ __global__ void __launch_bounds__(NW * 32)
       }
     }
   };
+
+  // the first block-table window and the q rows load concurrently
+  if (n_my > 0) tbl = (lane < n_my) ? __ldg(table + tile_of(lane)) : 0;
+  Path path;
+  path.init(a, seq, kvh, row0, L);
 
   const int prologue = min(NSTAGE, n_my);
   for (int n = 0; n < prologue; ++n) issue(n);
@@ -712,6 +759,8 @@ __global__ void __launch_bounds__(128) split_combine_kernel(const CombineArgs a)
   const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (gw >= a.num_seqs * a.rows_per_seq) return;
+  griddep_wait();  // the workspace comes from the partial pass just before
+  griddep_launch_dependents();
   const int seq = gw / a.rows_per_seq, r = gw % a.rows_per_seq;
   const size_t base = (size_t)seq * a.num_splits * a.rows_per_seq + r;
   const size_t pstride = a.rows_per_seq;

@@ -67,13 +67,17 @@ static cudaError_t launch_one(const CUtensorMap &kmap, const CUtensorMap &vmap,
   cfg.blockDim = dim3(kWarps * 32, 1, 1);
   cfg.dynamicSmemBytes = kSmem;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = cluster;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
+  // attribute 0: programmatic dependent launch (the kernel waits on griddepcontrol
+  // before reading global memory); attribute 1: the cluster shape, if any
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = cluster;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = cluster > 1 ? 1 : 0;
+  cfg.numAttrs = cluster > 1 ? 2 : 1;
   return cudaLaunchKernelEx(&cfg, kern, kmap, vmap, a);
 }
 
@@ -104,13 +108,9 @@ static cudaError_t launch_combine_t(const CombineArgs &a, int head_dim, cudaStre
   const long long warps = (long long)a.num_seqs * a.rows_per_seq;
   const int blocks = (int)((warps * 32 + 127) / 128);
   if (blocks == 0) return cudaSuccess;
-  if (head_dim == 128)
-    split_combine_kernel<T, 128><<<blocks, 128, 0, st>>>(a);
-  else if (head_dim == 64)
-    split_combine_kernel<T, 64><<<blocks, 128, 0, st>>>(a);
-  else
-    return cudaErrorInvalidValue;
-  return cudaGetLastError();
+  if (head_dim == 128) return launch_dependent(split_combine_kernel<T, 128>, blocks, 128, st, a);
+  if (head_dim == 64) return launch_dependent(split_combine_kernel<T, 64>, blocks, 128, st, a);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace pa

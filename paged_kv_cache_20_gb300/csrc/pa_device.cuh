@@ -74,6 +74,25 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// Orders this thread's earlier generic-proxy global-memory writes before later
+// asynchronous-proxy (TMA) reads of global memory.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// ---- programmatic dependent launch ------------------------------------------------
+// griddep_wait: block until the grids this launch depends on have completed and
+// their memory is visible (a no-op when the launch has no such dependency).
+// griddep_launch_dependents: allow the next dependent launch on the stream to start
+// its prologue early.
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---- TMA -------------------------------------------------------------------------
 // 3-D tiled bulk tensor load global -> shared, completion counted on `bar`.
 // Coordinates: x = element column (must be a multiple of 8 for 16-bit data so the

@@ -7,6 +7,25 @@
 
 namespace pa {
 
+// Launch `kern` as a programmatic dependent of the previous work on `stream`: it
+// may be scheduled before that work finishes, and must call griddepcontrol.wait
+// before touching global memory (every kernel of this library does).
+template <typename... Params, typename... Args>
+cudaError_t launch_dependent(void (*kern)(Params...), unsigned grid, unsigned block,
+                             cudaStream_t stream, Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid, 1, 1);
+  cfg.blockDim = dim3(block, 1, 1);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<Args &&>(args)...);
+}
+
 struct DecodeArgs;
 struct CombineArgs;
 

@@ -132,3 +132,18 @@ def test_product_and_oracle_share_nothing():
         if path.endswith((".py", ".c")):
             src = open(path).read()
             assert "paged_kv_cache_20_gb300" not in src and "pagedattn" not in src, path
+
+
+def test_append_decode_rejects_bad_arguments(lib):
+    base = [FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 2, 8, 2, 128, 16, 0.1, 4, 8, 1, 0]
+    ok_ws = lib.pa_decode_workspace_size(2, 8, 1, 128, 4)
+    call = lambda args, splits, ws, wsb: lib.pa_append_decode(*args, splits, ws, wsb, None)  # noqa: E731
+    bad_knew = list(base); bad_knew[2] = None
+    assert call(bad_knew, 1, None, 0) == -1
+    mis = list(base); mis[3] = FAKE + 8
+    assert call(mis, 1, None, 0) == -1
+    assert call(base, 0, None, 0) == -1                 # no splits
+    assert call(base, 4, None, 0) == -1                 # splits need a workspace
+    assert call(base, 4, FAKE, ok_ws - 1) == -1         # too small
+    d96 = list(base); d96[11] = 96
+    assert call(d96, 1, None, 0) == -2

@@ -42,12 +42,12 @@ def _f64(t: torch.Tensor) -> np.ndarray:
     return t.detach().cpu().to(torch.float64).numpy()
 
 
-def gpu_step(pa, w, num_splits=None):
+def gpu_step(pa, w, num_splits=None, fused=False):
     d = _dev(w)
     s = w.cfg.num_splits if num_splits is None else num_splits
     out = pa.paged_decode_step(d["q"], d["k_new"], d["v_new"], d["k_cache"], d["v_cache"],
                                d["block_tables"], d["context_lens"], w.scale, q_len=w.cfg.q_len,
-                               num_splits=s)
+                               num_splits=s, fused=fused)
     torch.cuda.synchronize()
     assert pa.pa_device_error() == 0
     return out, d
@@ -72,10 +72,11 @@ SMALL = [
 ]
 
 
+@pytest.mark.parametrize("fused", [False, True], ids=["separate", "fused"])
 @pytest.mark.parametrize("name,over", SMALL, ids=[s[0] for s in SMALL])
-def test_small_configs_every_element(pa, orc, name, over):
+def test_small_configs_every_element(pa, orc, name, over, fused):
     w = workloads.make(name, **over)
-    out, d = gpu_step(pa, w)
+    out, d = gpu_step(pa, w, fused=fused)
     ref, kc, vc, slots = oracle_step(orc, w)
     # append is bit-exact over the whole pool (NaN-poisoned slots included)
     assert np.array_equal(_u16(d["k_cache"]), kc)
@@ -86,10 +87,12 @@ def test_small_configs_every_element(pa, orc, name, over):
 FULL = ["llama7b_mha", "gqa", "long_split", "prefix_verify"]
 
 
+@pytest.mark.parametrize("fused", [False, True], ids=["separate", "fused"])
 @pytest.mark.parametrize("name", FULL)
-def test_full_size_sampled_rows(pa, orc, name):
+def test_full_size_sampled_rows(pa, orc, name, fused):
+    """Full-size workloads in the launch configuration bench.py times (fused)."""
     w = workloads.make(name)
-    out, d = gpu_step(pa, w)
+    out, d = gpu_step(pa, w, fused=fused)
     n_rows = w.cfg.num_seqs * w.cfg.q_len * w.cfg.num_q_heads
     rng = np.random.default_rng(1)
     rows = np.sort(rng.choice(n_rows, size=min(n_rows, 48), replace=False))
@@ -297,3 +300,63 @@ def test_device_wait_times_out_and_reports(pa):
     assert pa.pa_device_error() == 0                 # cleared
     x = torch.ones(1024, device=DEV)
     assert float(x.sum()) == 1024.0                  # context still works
+
+
+@pytest.mark.parametrize("h_q,h_kv,q_len,dtype", [(32, 1, 1, "bf16"), (32, 1, 2, "fp16"),
+                                                  (16, 16, 16, "fp16"), (64, 8, 4, "bf16")])
+def test_many_rows_per_kv_head(pa, orc, h_q, h_kv, q_len, dtype):
+    """MQA and long verify windows: 16-64 query rows per KV head (several row groups)."""
+    lens = [1, 15, 16, 40, 129, 700]
+    q, K, V = _logical_case(20, lens, h_q, h_kv, 128, dtype, q_len=q_len, qscale=1.5)
+    pc = Paged(orc, K, V, 16, dtype, perm_seed=21)
+    ref = pc.decode(orc, q, 0.0884, q_len=q_len)
+    _tol.check(_gpu_decode(pa, pc, q, 0.0884, q_len), ref, dtype, "single pass")
+    _tol.check(_gpu_decode(pa, pc, q, 0.0884, q_len, num_splits=5), ref, dtype, "split 5")
+
+
+def test_many_sequences_without_length_ranking(pa, orc):
+    """More sequences than the in-kernel longest-first ranking handles (300 > 256)."""
+    rng = np.random.default_rng(22)
+    lens = [int(x) for x in rng.integers(0, 90, size=300)]
+    q, K, V = _logical_case(23, lens, 8, 2, 64, "bf16")
+    pc = Paged(orc, K, V, 16, "bf16", perm_seed=24)
+    _tol.check(_gpu_decode(pa, pc, q, 0.125, 1), pc.decode(orc, q, 0.125), "bf16", "300 seqs")
+
+
+def test_wide_block_table_and_short_table(pa, orc):
+    q, K, V = _logical_case(25, [20, 50], 4, 4, 128, "fp16")
+    pc = Paged(orc, K, V, 16, "fp16", perm_seed=26)
+    ref = pc.decode(orc, q, 0.1)
+    # extra table columns (never read) pointing at the NaN-poisoned padding block
+    wide = np.concatenate([pc.tables, np.full((2, 5), pc.tables[0, -1], np.int32)], axis=1)
+    pc.tables = wide
+    _tol.check(_gpu_decode(pa, pc, q, 0.1, 1), ref, "fp16", "wide table")
+    # a context longer than its table: reported, the rest still finite
+    pc.tables = np.ascontiguousarray(wide[:, :2])
+    got = _gpu_decode_unchecked(pa, pc, q, 0.1, lens=[20, 50])
+    assert pa.pa_device_error() == pa.PA_ERR_DEVICE_CHECK
+    assert np.isfinite(got).all()
+
+
+def _gpu_decode_unchecked(pa, pc, q, scale, lens):
+    qd = _to_dev(q, pc.dtype)
+    out = torch.empty_like(qd)
+    pa.pa_decode(out, qd, _to_dev(pc.k, pc.dtype), _to_dev(pc.v, pc.dtype),
+                 torch.from_numpy(pc.tables).to(DEV),
+                 torch.from_numpy(np.asarray(lens, np.int32)).to(DEV), scale, 1)
+    torch.cuda.synchronize()
+    return _f64(out)
+
+
+@pytest.mark.parametrize("q_len,splits", [(1, 1), (4, 1), (4, 3), (16, 1), (2, 40)])
+def test_fused_append_decode_edges(pa, orc, q_len, splits):
+    """Fused step on edge lengths, including sequences shorter than q_len and new
+    tokens that straddle a block boundary or a split boundary."""
+    cfg = workloads.config("gqa", num_seqs=9, q_len=q_len,
+                           lens=("fixed", (0, 1, 3, 15, 16, 17, 33, 100, 257)), spare_blocks=3)
+    w = workloads.make(cfg)
+    out, d = gpu_step(pa, w, num_splits=splits, fused=True)
+    ref, kc, vc, slots = oracle_step(orc, w)
+    assert np.array_equal(_u16(d["k_cache"]), kc)
+    assert np.array_equal(_u16(d["v_cache"]), vc)
+    _tol.check(_f64(out), ref, w.cfg.dtype, f"fused q_len {q_len} splits {splits}")
