@@ -117,6 +117,21 @@ PA_API pa_status pa_append_kv(void *k_cache, void *v_cache, const void *k_new,
                               pa_dtype dtype, void *stream);
 
 /*
+ * pa_copy_blocks -- copy-on-write support: sequences that share physical blocks
+ * (parallel sampling, beam search, a cached prefix; [QA] Q2) keep sharing them
+ * until one of them writes; before that write it needs a private copy.  For each
+ * pair i, block src_blocks[i] (every head, every row, K and V) is copied bit for
+ * bit to block dst_blocks[i].  Pairs with an id outside [0, num_blocks) are skipped
+ * and set PA_ERR_DEVICE_CHECK.  A destination that is also a source or another
+ * pair's destination in the same call: undefined result.  src_blocks, dst_blocks:
+ * int32 [n_pairs] device arrays.  n_pairs == 0 is a no-op.
+ */
+PA_API pa_status pa_copy_blocks(void *k_cache, void *v_cache, const int32_t *src_blocks,
+                                const int32_t *dst_blocks, int n_pairs, int num_kv_heads,
+                                int head_dim, int block_size, int num_blocks, pa_dtype dtype,
+                                void *stream);
+
+/*
  * pa_decode -- attention of every query row over its sequence's paged K/V, in
  * one pass with online softmax ([ANIM] §5: running max m, running sum l,
  * unnormalised output rescaled by exp(m_old - m_new), output O / l at the end;

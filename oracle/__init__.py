@@ -73,6 +73,9 @@ class Oracle:
         lib.orc_append_kv.restype = None
         lib.orc_append_kv.argtypes = [_c_u16p, _c_u16p, _c_u16p, _c_u16p, _c_i64p, ctypes.c_int,
                                       ctypes.c_int, ctypes.c_int, ctypes.c_int]
+        lib.orc_copy_blocks.restype = ctypes.c_int
+        lib.orc_copy_blocks.argtypes = [_c_u16p, _c_u16p, _c_i32p, _c_i32p, ctypes.c_int,
+                                        ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int]
         lib.orc_decode.restype = ctypes.c_int
         lib.orc_decode.argtypes = [_c_f64p, _c_i64p, ctypes.c_int64, _c_u16p, _c_u16p, _c_u16p,
                                    _c_i32p, _c_i32p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
@@ -122,6 +125,16 @@ class Oracle:
         self.lib.orc_append_kv(_ptr(kc, _c_u16p), _ptr(vc, _c_u16p), _ptr(kn, _c_u16p),
                                _ptr(vn, _c_u16p), _ptr(sm, _c_i64p), sm.shape[0], h_kv,
                                head_dim, block_size)
+
+    # -- copy-on-write block copy (in place) ------------------------------------
+    def copy_blocks(self, k_cache: np.ndarray, v_cache: np.ndarray, src, dst) -> int:
+        kc, vc = k_cache.view(np.uint16), v_cache.view(np.uint16)
+        s = np.ascontiguousarray(src, dtype=np.int32)
+        d = np.ascontiguousarray(dst, dtype=np.int32)
+        num_blocks, h_kv, block_size, head_dim = kc.shape
+        return self.lib.orc_copy_blocks(_ptr(kc, _c_u16p), _ptr(vc, _c_u16p), _ptr(s, _c_i32p),
+                                        _ptr(d, _c_i32p), s.shape[0], h_kv, head_dim, block_size,
+                                        num_blocks)
 
     # -- attention --------------------------------------------------------------
     def decode(self, q, k_cache, v_cache, block_tables, context_lens, scale: float,

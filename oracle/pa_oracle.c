@@ -146,6 +146,29 @@ void orc_append_kv(uint16_t *k_cache, uint16_t *v_cache,
     }
 }
 
+/* ---- copy-on-write block copy ([QA] Q2: sequences share physical pages up to the
+ * point where they diverge; a writer first gives itself a private copy) ----
+ * For each pair i, every head's block_size rows of block src[i] are copied to block
+ * dst[i], in both caches.  Pairs with an id outside [0, num_blocks) are skipped
+ * (returns the number skipped).                                                 */
+int orc_copy_blocks(uint16_t *k_cache, uint16_t *v_cache, const int32_t *src, const int32_t *dst,
+                    int n_pairs, int num_kv_heads, int head_dim, int block_size, int num_blocks)
+{
+    int skipped = 0;
+    const int64_t block_elems = (int64_t)num_kv_heads * block_size * head_dim;
+    for (int i = 0; i < n_pairs; i++) {
+        if (src[i] < 0 || src[i] >= num_blocks || dst[i] < 0 || dst[i] >= num_blocks) {
+            skipped++;
+            continue;
+        }
+        for (int64_t e = 0; e < block_elems; e++) {
+            k_cache[(int64_t)dst[i] * block_elems + e] = k_cache[(int64_t)src[i] * block_elems + e];
+            v_cache[(int64_t)dst[i] * block_elems + e] = v_cache[(int64_t)src[i] * block_elems + e];
+        }
+    }
+    return skipped;
+}
+
 /* Shared description of one attention call. */
 typedef struct {
     const uint16_t *q;            /* [num_seqs][q_len][num_q_heads][head_dim] */

@@ -55,6 +55,8 @@ _SIGNATURES = {
                                    _c_int, _c_int, _c_vp]),
     "pa_device_error": (_c_int, [_c_vp, _c_int]),
     "pa_selftest_wait_timeout": (_c_int, [_c_vp]),
+    "pa_copy_blocks": (_c_int, [_c_vp, _c_vp, _c_vp, _c_vp, _c_int, _c_int, _c_int, _c_int,
+                                _c_int, _c_int, _c_vp]),
     "pa_append_decode": (_c_int, [_c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_int,
                                   _c_int, _c_int, _c_int, _c_int, _c_float, _c_int, _c_int,
                                   _c_int, _c_int, _c_int, _c_vp, _c_size, _c_vp]),
@@ -158,6 +160,21 @@ def pa_append_kv(k_cache: torch.Tensor, v_cache: torch.Tensor, k_new: torch.Tens
         _cuda(k_cache, "k_cache"), _cuda(v_cache, "v_cache"), _cuda(k_new, "k_new"),
         _cuda(v_new, "v_new"), _cuda(slot_mapping, "slot_mapping", torch.int64), n_tokens, h_kv,
         head_dim, block_size, num_blocks, dt, _stream(stream)))
+
+
+def pa_copy_blocks(k_cache: torch.Tensor, v_cache: torch.Tensor, src_blocks: torch.Tensor,
+                   dst_blocks: torch.Tensor, stream=None) -> None:
+    """Copy whole blocks src_blocks[i] -> dst_blocks[i] in both caches (copy-on-write)."""
+    num_blocks, h_kv, block_size, head_dim = _cache_dims(k_cache)
+    if v_cache.shape != k_cache.shape or v_cache.dtype != k_cache.dtype:
+        raise ValueError("v_cache must match k_cache")
+    n = int(src_blocks.shape[0])
+    if int(dst_blocks.shape[0]) != n:
+        raise ValueError("src_blocks and dst_blocks must have the same length")
+    _check("pa_copy_blocks", load().pa_copy_blocks(
+        _cuda(k_cache, "k_cache"), _cuda(v_cache, "v_cache"),
+        _cuda(src_blocks, "src_blocks", torch.int32), _cuda(dst_blocks, "dst_blocks", torch.int32),
+        n, h_kv, head_dim, block_size, num_blocks, _elt(k_cache, "k_cache"), _stream(stream)))
 
 
 def _decode_dims(q, k_cache, block_tables, context_lens, q_len):

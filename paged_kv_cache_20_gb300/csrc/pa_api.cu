@@ -83,6 +83,27 @@ __global__ void append_kv_kernel(uint16_t *k_cache, uint16_t *v_cache, const uin
   }
 }
 
+// Copy-on-write block copy: one thread per 16-byte chunk of a (pair, head, row).
+__global__ void copy_blocks_kernel(uint4 *k_cache, uint4 *v_cache, const int32_t *src,
+                                   const int32_t *dst, int n_pairs, int64_t chunks_per_block,
+                                   int num_blocks, unsigned *err) {
+  pa::griddep_wait();
+  pa::griddep_launch_dependents();
+  const int64_t total = (int64_t)n_pairs * chunks_per_block;
+  for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
+       idx += (int64_t)gridDim.x * blockDim.x) {
+    const int i = (int)(idx / chunks_per_block);
+    const int64_t c = idx % chunks_per_block;
+    const int s = __ldg(src + i), d = __ldg(dst + i);
+    if (s < 0 || s >= num_blocks || d < 0 || d >= num_blocks) {
+      if (c == 0) pa::record_error(err, pa::kErrCheck);
+      continue;
+    }
+    k_cache[(int64_t)d * chunks_per_block + c] = k_cache[(int64_t)s * chunks_per_block + c];
+    v_cache[(int64_t)d * chunks_per_block + c] = v_cache[(int64_t)s * chunks_per_block + c];
+  }
+}
+
 // A wait nobody satisfies: an mbarrier expecting one arrival that never comes.
 __global__ void wait_timeout_kernel(unsigned *err) {
   __shared__ __align__(8) uint64_t bar;
@@ -302,6 +323,31 @@ PA_API pa_status pa_append_kv(void *k_cache, void *v_cache, const void *k_new, c
                       : pa::launch_dependent(append_kv_kernel<64>, blocks, threads, s, kc, vc, kn,
                                              vn, slot_mapping, n_tokens, num_kv_heads, num_slots,
                                              err);
+  return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+PA_API pa_status pa_copy_blocks(void *k_cache, void *v_cache, const int32_t *src_blocks,
+                                const int32_t *dst_blocks, int n_pairs, int num_kv_heads,
+                                int head_dim, int block_size, int num_blocks, pa_dtype dtype,
+                                void *stream) {
+  if (!k_cache || !v_cache || !src_blocks || !dst_blocks) return PA_ERR_INVALID_ARG;
+  if (n_pairs < 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 || num_blocks <= 0)
+    return PA_ERR_INVALID_ARG;
+  if (!aligned16(k_cache) || !aligned16(v_cache)) return PA_ERR_INVALID_ARG;
+  if (!supported_dtype(dtype)) return PA_ERR_UNSUPPORTED;
+  if (head_dim != 64 && head_dim != 128) return PA_ERR_UNSUPPORTED;
+  if (block_size != kBlockSize) return PA_ERR_UNSUPPORTED;
+  if (n_pairs == 0) return PA_OK;
+  unsigned *err = error_word();
+  if (err == nullptr) return PA_ERR_CUDA;
+  const int64_t chunks = (int64_t)num_kv_heads * kBlockSize * head_dim * 2 / 16;
+  const int64_t total = (int64_t)n_pairs * chunks;
+  const int threads = 256;
+  const unsigned blocks = (unsigned)std::min<int64_t>((total + threads - 1) / threads, 1 << 20);
+  cudaError_t e = pa::launch_dependent(copy_blocks_kernel, blocks, threads,
+                                       static_cast<cudaStream_t>(stream),
+                                       static_cast<uint4 *>(k_cache), static_cast<uint4 *>(v_cache),
+                                       src_blocks, dst_blocks, n_pairs, chunks, num_blocks, err);
   return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 

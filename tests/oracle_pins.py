@@ -369,6 +369,29 @@ def pin_empty_context_zero(o):
     assert not np.any(np.isnan(got))
 
 
+def pin_copy_blocks_then_diverge(o):
+    # copy-on-write: two sequences share their first blocks; the second gets a
+    # private copy of the shared last block before appending into it.  Attention of
+    # every sequence is unchanged by the copy, and the copy holds the source bytes.
+    rng = np.random.default_rng(18)
+    H, D = 2, 16
+    K = [_bits(rng.standard_normal((40, H, D)), FP16)]
+    V = [_bits(rng.standard_normal((40, H, D)), FP16)]
+    pc = Paged(o, K, V, 16, FP16, perm_seed=19, spare=4)      # blocks of seq 0: 3
+    q = _bits(rng.standard_normal((1, 1, H, D)), FP16)
+    before = pc.decode(o, q, 0.25)
+    src = int(pc.tables[0, 2])
+    free = [b for b in range(pc.k.shape[0]) if b not in set(pc.tables[0].tolist())]
+    dst = free[0]
+    k0, v0 = pc.k.copy(), pc.v.copy()
+    assert o.copy_blocks(pc.k, pc.v, [src, -1], [dst, 0]) == 1   # second pair skipped
+    assert np.array_equal(pc.k[dst], pc.k[src]) and np.array_equal(pc.v[dst], pc.v[src])
+    changed = np.any(pc.k != k0, axis=(1, 2, 3)) | np.any(pc.v != v0, axis=(1, 2, 3))
+    assert set(np.nonzero(changed)[0].tolist()) <= {dst}
+    pc.tables[0, 2] = dst                                    # the table now points at the copy
+    assert np.array_equal(pc.decode(o, q, 0.25), before)
+
+
 PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_") and callable(v)]
 
 

@@ -147,3 +147,11 @@ def test_append_decode_rejects_bad_arguments(lib):
     assert call(base, 4, FAKE, ok_ws - 1) == -1         # too small
     d96 = list(base); d96[11] = 96
     assert call(d96, 1, None, 0) == -2
+
+
+def test_copy_blocks_rejects_bad_arguments(lib):
+    assert lib.pa_copy_blocks(None, FAKE, FAKE, FAKE, 2, 2, 128, 16, 8, 0, None) == -1
+    assert lib.pa_copy_blocks(FAKE, FAKE, FAKE, FAKE, -1, 2, 128, 16, 8, 0, None) == -1
+    assert lib.pa_copy_blocks(FAKE + 4, FAKE, FAKE, FAKE, 2, 2, 128, 16, 8, 0, None) == -1
+    assert lib.pa_copy_blocks(FAKE, FAKE, FAKE, FAKE, 2, 2, 100, 16, 8, 0, None) == -2
+    assert lib.pa_copy_blocks(FAKE, FAKE, FAKE, FAKE, 0, 2, 128, 16, 8, 0, None) == 0

@@ -360,3 +360,38 @@ def test_fused_append_decode_edges(pa, orc, q_len, splits):
     assert np.array_equal(_u16(d["k_cache"]), kc)
     assert np.array_equal(_u16(d["v_cache"]), vc)
     _tol.check(_f64(out), ref, w.cfg.dtype, f"fused q_len {q_len} splits {splits}")
+
+
+def test_copy_blocks_bit_exact_and_cow_decode(pa, orc):
+    """Copy-on-write: copies are bit-exact against the oracle on the whole pool, bad
+    pairs are skipped and reported, and a sequence redirected to its private copy
+    attends exactly as before."""
+    w = workloads.make("gqa", num_seqs=6)
+    d = _dev(w)
+    P = w.num_blocks
+    rng = np.random.default_rng(30)
+    src = rng.choice(P, size=20, replace=False).astype(np.int32)
+    dst = np.setdiff1d(np.arange(P), src)[:20].astype(np.int32)
+    src_b = np.concatenate([src, [P + 3]]).astype(np.int32)    # one bad pair
+    dst_b = np.concatenate([dst, [0]]).astype(np.int32)
+    pa.pa_copy_blocks(d["k_cache"], d["v_cache"], torch.from_numpy(src_b).to(DEV),
+                      torch.from_numpy(dst_b).to(DEV))
+    assert pa.pa_device_error() == pa.PA_ERR_DEVICE_CHECK
+    kc, vc = w.bits("k_cache").copy(), w.bits("v_cache").copy()
+    assert orc.copy_blocks(kc, vc, src_b, dst_b) == 1
+    assert np.array_equal(_u16(d["k_cache"]), kc) and np.array_equal(_u16(d["v_cache"]), vc)
+    # redirect sequence 0's last block to a fresh copy: attention unchanged (bit-exact)
+    out_a, _ = gpu_step(pa, w, fused=True)
+    d2 = _dev(w)
+    last = int((int(w.context_lens[0]) - 1) // 16)
+    old_blk = int(w.block_tables[0, last])
+    spare = int(np.setdiff1d(np.arange(P), w.block_tables.numpy().ravel())[0])
+    pa.pa_copy_blocks(d2["k_cache"], d2["v_cache"], torch.tensor([old_blk], dtype=torch.int32,
+                      device=DEV), torch.tensor([spare], dtype=torch.int32, device=DEV))
+    d2["block_tables"][0, last] = spare
+    out_b = pa.pa_append_decode(torch.empty_like(d2["q"]), d2["q"], d2["k_new"], d2["v_new"],
+                                d2["k_cache"], d2["v_cache"], d2["block_tables"],
+                                d2["context_lens"], w.scale, w.cfg.q_len)
+    torch.cuda.synchronize()
+    assert pa.pa_device_error() == 0
+    assert torch.equal(out_a, out_b)

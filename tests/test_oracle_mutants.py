@@ -47,6 +47,9 @@ MUTANTS = [
      "v = ldexp((double)(1024 + f), e - 24);"),
     ("bf16_subnormal_scale", "v = ldexp((double)f, -133);", "v = ldexp((double)f, -126);"),
     ("softmax_not_normalised", "double p = s[t] / den;", "double p = s[t];"),
+    ("copy_blocks_wrong_direction",
+     "k_cache[(int64_t)dst[i] * block_elems + e] = k_cache[(int64_t)src[i] * block_elems + e];",
+     "k_cache[(int64_t)src[i] * block_elems + e] = k_cache[(int64_t)dst[i] * block_elems + e];"),
 ]
 
 
