@@ -73,6 +73,22 @@ class Oracle:
         lib.orc_append_kv.restype = None
         lib.orc_append_kv.argtypes = [_c_u16p, _c_u16p, _c_u16p, _c_u16p, _c_i64p, ctypes.c_int,
                                       ctypes.c_int, ctypes.c_int, ctypes.c_int]
+        _c_u8p = ctypes.POINTER(ctypes.c_uint8)
+        _c_f32p = ctypes.POINTER(ctypes.c_float)
+        lib.orc_decode_e4m3.restype = None
+        lib.orc_decode_e4m3.argtypes = [_c_f64p, _c_u8p, ctypes.c_int64]
+        lib.orc_encode_e4m3.restype = None
+        lib.orc_encode_e4m3.argtypes = [_c_u8p, _c_f32p, ctypes.c_int64]
+        lib.orc_append_kv_fp8.restype = None
+        lib.orc_append_kv_fp8.argtypes = [_c_u8p, _c_u8p, _c_u16p, _c_u16p, _c_i64p, ctypes.c_int,
+                                          ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                          _c_f32p, _c_f32p]
+        lib.orc_decode_fp8.restype = ctypes.c_int
+        lib.orc_decode_fp8.argtypes = [_c_f64p, _c_i64p, ctypes.c_int64, _c_u16p, _c_u8p, _c_u8p,
+                                       _c_f32p, _c_f32p, _c_i32p, _c_i32p, ctypes.c_int,
+                                       ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                       ctypes.c_float, ctypes.c_int, ctypes.c_int, ctypes.c_int]
+        self._u8p, self._f32p = _c_u8p, _c_f32p
         lib.orc_copy_blocks.restype = ctypes.c_int
         lib.orc_copy_blocks.argtypes = [_c_u16p, _c_u16p, _c_i32p, _c_i32p, ctypes.c_int,
                                         ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int]
@@ -125,6 +141,62 @@ class Oracle:
         self.lib.orc_append_kv(_ptr(kc, _c_u16p), _ptr(vc, _c_u16p), _ptr(kn, _c_u16p),
                                _ptr(vn, _c_u16p), _ptr(sm, _c_i64p), sm.shape[0], h_kv,
                                head_dim, block_size)
+
+    # -- FP8 (e4m3) -------------------------------------------------------------
+    def decode_e4m3(self, codes: np.ndarray) -> np.ndarray:
+        c = np.ascontiguousarray(codes, dtype=np.uint8)
+        out = np.empty(c.shape, dtype=np.float64)
+        self.lib.orc_decode_e4m3(_ptr(out, _c_f64p), _ptr(c, self._u8p), c.size)
+        return out
+
+    def encode_e4m3(self, x: np.ndarray) -> np.ndarray:
+        f = np.ascontiguousarray(x, dtype=np.float32)
+        out = np.empty(f.shape, dtype=np.uint8)
+        self.lib.orc_encode_e4m3(_ptr(out, self._u8p), _ptr(f, self._f32p), f.size)
+        return out
+
+    def append_kv_fp8(self, k_cache: np.ndarray, v_cache: np.ndarray, k_new, v_new,
+                      slot_mapping, new_dtype, k_scale, v_scale) -> None:
+        """Quantising append into uint8 e4m3 caches [P, H, B, D] (in place)."""
+        for a in (k_cache, v_cache):
+            if not (a.flags.c_contiguous and a.dtype == np.uint8):
+                raise TypeError("FP8 caches must be contiguous uint8 arrays (modified in place)")
+        kn, vn = _u16(k_new), _u16(v_new)
+        sm = np.ascontiguousarray(slot_mapping, dtype=np.int64)
+        ks = np.ascontiguousarray(k_scale, dtype=np.float32)
+        vs = np.ascontiguousarray(v_scale, dtype=np.float32)
+        _, h_kv, block_size, head_dim = k_cache.shape
+        self.lib.orc_append_kv_fp8(_ptr(k_cache, self._u8p), _ptr(v_cache, self._u8p),
+                                   _ptr(kn, _c_u16p), _ptr(vn, _c_u16p), _ptr(sm, _c_i64p),
+                                   sm.shape[0], h_kv, head_dim, block_size,
+                                   _dtype_code(new_dtype), _ptr(ks, self._f32p),
+                                   _ptr(vs, self._f32p))
+
+    def decode_fp8(self, q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens,
+                   scale: float, dtype, q_len: int = 1, rows=None) -> np.ndarray:
+        """fp64 attention over e4m3 caches (value = code * per-KV-head scale)."""
+        qb = _u16(q)
+        kc = np.ascontiguousarray(k_cache, dtype=np.uint8)
+        vc = np.ascontiguousarray(v_cache, dtype=np.uint8)
+        ks = np.ascontiguousarray(k_scale, dtype=np.float32)
+        vs = np.ascontiguousarray(v_scale, dtype=np.float32)
+        bt = np.ascontiguousarray(block_tables, dtype=np.int32)
+        cl = np.ascontiguousarray(context_lens, dtype=np.int32)
+        num_seqs = cl.shape[0]
+        _, h_kv, block_size, head_dim = kc.shape
+        h_q = qb.size // (num_seqs * q_len * head_dim)
+        rows_arr = (np.arange(num_seqs * q_len * h_q, dtype=np.int64) if rows is None
+                    else np.ascontiguousarray(rows, dtype=np.int64))
+        out = np.empty((rows_arr.shape[0], head_dim), dtype=np.float64)
+        rc = self.lib.orc_decode_fp8(_ptr(out, _c_f64p), _ptr(rows_arr, _c_i64p),
+                                     rows_arr.shape[0], _ptr(qb, _c_u16p), _ptr(kc, self._u8p),
+                                     _ptr(vc, self._u8p), _ptr(ks, self._f32p),
+                                     _ptr(vs, self._f32p), _ptr(bt, _c_i32p), _ptr(cl, _c_i32p),
+                                     num_seqs, h_q, h_kv, head_dim, block_size, float(scale),
+                                     bt.shape[1], q_len, _dtype_code(dtype))
+        if rc != 0:
+            raise ValueError(f"oracle fp8 decode failed: {rc}")
+        return out.reshape(qb.shape) if rows is None else out
 
     # -- copy-on-write block copy (in place) ------------------------------------
     def copy_blocks(self, k_cache: np.ndarray, v_cache: np.ndarray, src, dst) -> int:

@@ -76,6 +76,58 @@ double orc_bf16_to_double(uint16_t b)
     return sign ? -v : v;
 }
 
+/* FP8 E4M3 ("e4m3fn"): 1 sign bit, 4 exponent bits (bias 7), 3 fraction bits, no
+ * infinities; S.1111.111 is NaN, so the largest finite magnitude is 1.75 * 2^8 = 448. */
+double orc_e4m3_to_double(uint8_t b)
+{
+    int sign = (b >> 7) & 1;
+    int e = (b >> 3) & 0xf;
+    int f = b & 0x7;
+    double v;
+    if (e == 0xf && f == 0x7)
+        return NAN;
+    if (e == 0)
+        v = ldexp((double)f, -9);               /* subnormal: f * 2^(1-7-3) */
+    else
+        v = ldexp((double)(8 + f), e - 10);     /* (1 + f/8) * 2^(e-7) */
+    return sign ? -v : v;
+}
+
+/* float -> e4m3, rounding to the nearest representable value, ties to the even
+ * code (fraction LSB 0), magnitudes beyond 448 saturating to 448, NaN -> 0x7F.
+ * Written as a search over the 127 finite non-negative codes. */
+uint8_t orc_e4m3_from_float(float x)
+{
+    if (x != x)
+        return 0x7F;
+    uint8_t sign = (x < 0.0f || (x == 0.0f && 1.0f / x < 0.0f)) ? 0x80 : 0x00;
+    double a = fabs((double)x);
+    if (a >= 448.0)
+        return (uint8_t)(sign | 0x7E);
+    int best = 0;
+    double best_err = a;                       /* code 0 is +0 */
+    for (int c = 1; c <= 0x7E; c++) {
+        double err = fabs(a - orc_e4m3_to_double((uint8_t)c));
+        if (err < best_err || (err == best_err && (c & 1) == 0 && (best & 1) == 1)) {
+            best = c;
+            best_err = err;
+        }
+    }
+    return (uint8_t)(sign | best);
+}
+
+void orc_decode_e4m3(double *out, const uint8_t *bits, int64_t n)
+{
+    for (int64_t i = 0; i < n; i++)
+        out[i] = orc_e4m3_to_double(bits[i]);
+}
+
+void orc_encode_e4m3(uint8_t *out, const float *x, int64_t n)
+{
+    for (int64_t i = 0; i < n; i++)
+        out[i] = orc_e4m3_from_float(x[i]);
+}
+
 static double elt(const uint16_t *base, size_t idx, int dtype)
 {
     return dtype == ORC_BF16 ? orc_bf16_to_double(base[idx]) : orc_fp16_to_double(base[idx]);
@@ -146,6 +198,35 @@ void orc_append_kv(uint16_t *k_cache, uint16_t *v_cache,
     }
 }
 
+/* ---- append into an FP8 (e4m3) cache with one scale per KV head ----
+ * Each new element x (fp16/bf16, exact in float) is stored as e4m3(x / scale[h]):
+ * the division in float, then nearest-even rounding with saturation.  The stored
+ * value stands for e4m3 * scale.                                               */
+void orc_append_kv_fp8(uint8_t *k_cache, uint8_t *v_cache,
+                       const uint16_t *k_new, const uint16_t *v_new,
+                       const int64_t *slot_mapping, int n_tokens, int num_kv_heads,
+                       int head_dim, int block_size, int new_dtype,
+                       const float *k_scale, const float *v_scale)
+{
+    for (int t = 0; t < n_tokens; t++) {
+        int64_t slot = slot_mapping[t];
+        if (slot < 0)
+            continue;
+        int64_t block = slot / block_size;
+        int64_t offset = slot % block_size;
+        for (int h = 0; h < num_kv_heads; h++) {
+            for (int d = 0; d < head_dim; d++) {
+                int64_t dst = ((block * num_kv_heads + h) * block_size + offset) * head_dim + d;
+                int64_t src = ((int64_t)t * num_kv_heads + h) * head_dim + d;
+                float kx = (float)elt(k_new, (size_t)src, new_dtype);
+                float vx = (float)elt(v_new, (size_t)src, new_dtype);
+                k_cache[dst] = orc_e4m3_from_float(kx / k_scale[h]);
+                v_cache[dst] = orc_e4m3_from_float(vx / v_scale[h]);
+            }
+        }
+    }
+}
+
 /* ---- copy-on-write block copy ([QA] Q2: sequences share physical pages up to the
  * point where they diverge; a writer first gives itself a private copy) ----
  * For each pair i, every head's block_size rows of block src[i] are copied to block
@@ -172,14 +253,26 @@ int orc_copy_blocks(uint16_t *k_cache, uint16_t *v_cache, const int32_t *src, co
 /* Shared description of one attention call. */
 typedef struct {
     const uint16_t *q;            /* [num_seqs][q_len][num_q_heads][head_dim] */
-    const uint16_t *k_cache;      /* [num_blocks][num_kv_heads][block_size][head_dim] */
-    const uint16_t *v_cache;
+    const void *k_cache;          /* [num_blocks][num_kv_heads][block_size][head_dim] */
+    const void *v_cache;          /* 16-bit patterns, or e4m3 bytes when kv_fp8 */
     const int32_t *block_tables;  /* [num_seqs][max_blocks_per_seq] */
     const int32_t *context_lens;  /* [num_seqs] */
     int num_seqs, num_q_heads, num_kv_heads, head_dim, block_size;
     int max_blocks_per_seq, q_len, dtype;
     double scale;
+    int kv_fp8;                   /* cache holds e4m3 codes */
+    const float *k_scale;         /* per KV head, kv_fp8 only: value = e4m3 * scale */
+    const float *v_scale;
 } orc_call;
+
+/* Element idx of a cache, in the units of q (dequantised for an FP8 cache). */
+static double cache_at(const orc_call *c, const void *cache, const float *scales, size_t idx,
+                       int kvh)
+{
+    if (c->kv_fp8)
+        return orc_e4m3_to_double(((const uint8_t *)cache)[idx]) * (double)scales[kvh];
+    return elt((const uint16_t *)cache, idx, c->dtype);
+}
 
 /* Address of token t (logical position) of sequence i, KV head h, in a cache. */
 static size_t token_row(const orc_call *c, int i, int h, int64_t t)
@@ -206,12 +299,12 @@ static void row_coords(const orc_call *c, int64_t r, int *i, int *u, int *h, int
 }
 
 /* scale * <q_row, k_token> in double. */
-static double score(const orc_call *c, int64_t r, size_t krow)
+static double score(const orc_call *c, int64_t r, size_t krow, int kvh)
 {
     const size_t qoff = (size_t)r * c->head_dim;
     double dot = 0.0;
     for (int d = 0; d < c->head_dim; d++)
-        dot += elt(c->q, qoff + d, c->dtype) * elt(c->k_cache, krow + d, c->dtype);
+        dot += elt(c->q, qoff + d, c->dtype) * cache_at(c, c->k_cache, c->k_scale, krow + d, kvh);
     return c->scale * dot;
 }
 
@@ -240,7 +333,7 @@ static int decode_rows(const orc_call *c, double *out, const int64_t *rows, int6
             continue;
         /* scores over the gathered, logically contiguous keys */
         for (int64_t t = 0; t < T; t++)
-            s[t] = score(c, r, token_row(c, i, kvh, t));
+            s[t] = score(c, r, token_row(c, i, kvh, t), kvh);
         /* softmax: exp(s - max) / sum */
         double mx = s[0];
         for (int64_t t = 1; t < T; t++)
@@ -256,7 +349,7 @@ static int decode_rows(const orc_call *c, double *out, const int64_t *rows, int6
             double p = s[t] / den;
             size_t vrow = token_row(c, i, kvh, t);
             for (int d = 0; d < c->head_dim; d++)
-                o[d] += p * elt(c->v_cache, vrow + d, c->dtype);
+                o[d] += p * cache_at(c, c->v_cache, c->v_scale, vrow + d, kvh);
         }
     }
     free(s);
@@ -271,7 +364,26 @@ int orc_decode(double *out, const int64_t *rows, int64_t n_rows,
 {
     orc_call c = {q, k_cache, v_cache, block_tables, context_lens, num_seqs, num_q_heads,
                   num_kv_heads, head_dim, block_size, max_blocks_per_seq, q_len, dtype,
-                  (double)scale};
+                  (double)scale, 0, NULL, NULL};
+    if (num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0 || block_size <= 0 || q_len <= 0)
+        return -2;
+    if (rows == NULL)
+        n_rows = (int64_t)num_seqs * q_len * num_q_heads;
+    return decode_rows(&c, out, rows, n_rows);
+}
+
+/* Attention over an FP8 (e4m3) cache: K = e4m3 * k_scale[kvh], V = e4m3 * v_scale[kvh];
+ * q and the arithmetic as in orc_decode. */
+int orc_decode_fp8(double *out, const int64_t *rows, int64_t n_rows,
+                   const uint16_t *q, const uint8_t *k_cache, const uint8_t *v_cache,
+                   const float *k_scale, const float *v_scale,
+                   const int32_t *block_tables, const int32_t *context_lens,
+                   int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                   int block_size, float scale, int max_blocks_per_seq, int q_len, int dtype)
+{
+    orc_call c = {q, k_cache, v_cache, block_tables, context_lens, num_seqs, num_q_heads,
+                  num_kv_heads, head_dim, block_size, max_blocks_per_seq, q_len, dtype,
+                  (double)scale, 1, k_scale, v_scale};
     if (num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0 || block_size <= 0 || q_len <= 0)
         return -2;
     if (rows == NULL)
@@ -296,7 +408,7 @@ int orc_decode_partitions(double *m_out, double *l_out, double *acc_out,
 {
     orc_call c = {q, k_cache, v_cache, block_tables, context_lens, num_seqs, num_q_heads,
                   num_kv_heads, head_dim, block_size, max_blocks_per_seq, q_len, dtype,
-                  (double)scale};
+                  (double)scale, 0, NULL, NULL};
     if (num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0 || num_splits <= 0 || q_len <= 0)
         return -2;
     const int64_t rows_per_seq = (int64_t)q_len * num_q_heads;
@@ -318,13 +430,13 @@ int orc_decode_partitions(double *m_out, double *l_out, double *acc_out,
             for (int d = 0; d < head_dim; d++)
                 acc[d] = 0.0;
             for (int64_t t = t0; t < t1; t++) {
-                double s = score(&c, r, token_row(&c, i, kvh, t));
+                double s = score(&c, r, token_row(&c, i, kvh, t), kvh);
                 if (s > m)
                     m = s;
             }
             for (int64_t t = t0; t < t1; t++) {
                 size_t row = token_row(&c, i, kvh, t);
-                double e = exp(score(&c, r, row) - m);
+                double e = exp(score(&c, r, row, kvh) - m);
                 l += e;
                 for (int d = 0; d < head_dim; d++)
                     acc[d] += e * elt(v_cache, row + d, dtype);

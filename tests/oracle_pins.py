@@ -392,6 +392,90 @@ def pin_copy_blocks_then_diverge(o):
     assert np.array_equal(pc.decode(o, q, 0.25), before)
 
 
+def _torch_e4m3_values(codes: np.ndarray) -> np.ndarray:
+    t = torch.from_numpy(np.ascontiguousarray(codes, dtype=np.uint8)).view(torch.float8_e4m3fn)
+    return t.to(torch.float64).numpy()
+
+
+def pin_e4m3_decoding(o):
+    codes = np.arange(256, dtype=np.uint8)
+    got, want = o.decode_e4m3(codes), _torch_e4m3_values(codes)
+    nan = np.isnan(want)
+    assert np.array_equal(np.isnan(got), nan) and np.array_equal(got[~nan], want[~nan])
+
+
+def pin_e4m3_encoding(o):
+    # torch rounds to nearest even but turns |x| > 464 into NaN; within +-464 the
+    # two must agree bit for bit (ties included), beyond it the oracle saturates.
+    f16 = np.arange(65536, dtype=np.uint16).view(np.float16).astype(np.float32)
+    rng = np.random.default_rng(31)
+    rnd = (rng.standard_normal(200000) * rng.choice([1e-3, 0.05, 1.0, 40.0, 300.0], 200000))
+    xs = np.concatenate([f16, rnd.astype(np.float32)])
+    fin = np.isfinite(xs) & (np.abs(xs) <= 464.0)
+    got = o.encode_e4m3(xs[fin])
+    want = torch.from_numpy(xs[fin]).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(got, want)
+    big = np.array([464.5, 500.0, 1e6, -465.0, -3e38], dtype=np.float32)
+    assert o.encode_e4m3(big).tolist() == [0x7E, 0x7E, 0x7E, 0xFE, 0xFE]
+    assert o.encode_e4m3(np.array([np.nan], dtype=np.float32))[0] == 0x7F
+
+
+def _fp8_case(o, seed, lens, h_q, h_kv, d, dtype):
+    """Logical rows quantised into an FP8 paged cache by the oracle's own append."""
+    rng = np.random.default_rng(seed)
+    K = [_bits(rng.standard_normal((L, h_kv, d)), dtype) for L in lens]
+    V = [_bits(rng.standard_normal((L, h_kv, d)), dtype) for L in lens]
+    q = _bits(rng.standard_normal((len(lens), 1, h_q, d)), dtype)
+    ks = (0.5 + rng.random(h_kv)).astype(np.float32) / 64
+    vs = (0.5 + rng.random(h_kv)).astype(np.float32) / 64
+    nb = [(L + 15) // 16 for L in lens]
+    pool = sum(nb) + 2
+    ids = rng.permutation(pool)
+    tables = np.full((len(lens), max(nb)), ids[-1], dtype=np.int32)
+    cur = 0
+    for i, n in enumerate(nb):
+        tables[i, :n] = ids[cur:cur + n]
+        cur += n
+    kc = np.full((pool, h_kv, 16, d), 0x7F, dtype=np.uint8)
+    vc = np.full((pool, h_kv, 16, d), 0x7F, dtype=np.uint8)
+    cl = np.array(lens, dtype=np.int32)
+    for i, L in enumerate(lens):
+        slots = o.slot_mapping(tables[i:i + 1], cl[i:i + 1], 16, q_len=L)
+        o.append_kv_fp8(kc, vc, K[i], V[i], slots, dtype, ks, vs)
+    return q, K, V, kc, vc, ks, vs, tables, cl
+
+
+def pin_fp8_append_quantises_per_head(o):
+    q, K, V, kc, vc, ks, vs, tables, cl = _fp8_case(o, 32, [5, 40], 4, 2, 16, BF16)
+    # the stored code of every appended element is e4m3(x / scale[h]) (float division)
+    for i, L in enumerate([5, 40]):
+        for t in range(L):
+            blk, off = tables[i, t // 16], t % 16
+            for h in range(2):
+                x = _vals(K[i][t, h], BF16).astype(np.float32)
+                want = torch.from_numpy(x / ks[h]).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+                assert np.array_equal(kc[blk, h, off], want)
+
+
+def pin_fp8_decode_matches_sdpa_on_dequantised(o):
+    lens = [1, 17, 60]
+    for dtype, h_q in ((FP16, 4), (BF16, 8)):
+        q, K, V, kc, vc, ks, vs, tables, cl = _fp8_case(o, 33, lens, h_q, 2, 32, dtype)
+        got = o.decode_fp8(q, kc, vc, ks, vs, tables, cl, 0.2, dtype)
+        for i, L in enumerate(lens):
+            rows_k = np.stack([kc[tables[i, t // 16], :, t % 16] for t in range(L)])   # [L, H, D]
+            rows_v = np.stack([vc[tables[i, t // 16], :, t % 16] for t in range(L)])
+            kd = _torch_e4m3_values(rows_k) * ks[None, :, None].astype(np.float64)
+            vd = _torch_e4m3_values(rows_v) * vs[None, :, None].astype(np.float64)
+            g = h_q // 2
+            qq = torch.from_numpy(_vals(q[i, 0], dtype))[:, None, :]               # [Hq, 1, D]
+            kk = torch.from_numpy(kd).permute(1, 0, 2).repeat_interleave(g, 0)
+            vv = torch.from_numpy(vd).permute(1, 0, 2).repeat_interleave(g, 0)
+            want = torch.nn.functional.scaled_dot_product_attention(
+                qq, kk, vv, scale=float(np.float32(0.2)))[:, 0].numpy()
+            assert np.abs(got[i, 0] - want).max() < 1e-12
+
+
 PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_") and callable(v)]
 
 

@@ -40,8 +40,18 @@ MUTANTS = [
     ("dot_drops_first_term",
      "    for (int d = 0; d < c->head_dim; d++)\n        dot +=",
      "    for (int d = 1; d < c->head_dim; d++)\n        dot +="),
-    ("keys_used_as_values", "o[d] += p * elt(c->v_cache, vrow + d, c->dtype);",
-     "o[d] += p * elt(c->k_cache, vrow + d, c->dtype);"),
+    ("keys_used_as_values", "o[d] += p * cache_at(c, c->v_cache, c->v_scale, vrow + d, kvh);",
+     "o[d] += p * cache_at(c, c->k_cache, c->v_scale, vrow + d, kvh);"),
+    ("e4m3_exponent_bias", "v = ldexp((double)(8 + f), e - 10);",
+     "v = ldexp((double)(8 + f), e - 9);"),
+    ("e4m3_ties_to_odd", "(err == best_err && (c & 1) == 0 && (best & 1) == 1)",
+     "(err == best_err && (c & 1) == 1 && (best & 1) == 0)"),
+    ("e4m3_no_saturation", "if (a >= 448.0)\n        return (uint8_t)(sign | 0x7E);",
+     "if (a >= 480.0)\n        return (uint8_t)(sign | 0x7F);"),
+    ("fp8_scales_swapped", "o[d] += p * cache_at(c, c->v_cache, c->v_scale, vrow + d, kvh);",
+     "o[d] += p * cache_at(c, c->v_cache, c->k_scale, vrow + d, kvh);"),
+    ("fp8_append_multiplies", "k_cache[dst] = orc_e4m3_from_float(kx / k_scale[h]);",
+     "k_cache[dst] = orc_e4m3_from_float(kx * k_scale[h]);"),
     ("append_writes_key_into_value", "v_cache[dst] = v_new[src];", "v_cache[dst] = k_new[src];"),
     ("fp16_exponent_bias", "v = ldexp((double)(1024 + f), e - 25);",
      "v = ldexp((double)(1024 + f), e - 24);"),
