@@ -46,7 +46,7 @@ import workloads  # noqa: E402
 METRIC = "paged decode attention: KV tokens/s and achieved HBM GB/s (% of GB300 peak)"
 UNIT = "KV tokens/s"
 DEFAULT_CONFIG = "llama7b_mha"
-OTHER_CONFIGS = ["gqa", "long_split", "prefix_verify"]
+OTHER_CONFIGS = ["gqa", "long_split", "prefix_verify", "llama7b_mha_fp8", "gqa_fp8"]
 L2_BYTES = 129 << 20             # GB300 L2; every workload's KV cache is several times larger
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
@@ -99,7 +99,8 @@ def measured_peaks() -> dict:
 def algorithmic_bytes(w: workloads.Workload) -> dict:
     """Bytes the step must move at minimum (unique KV once, q, out, tables, lens, append)."""
     c = w.cfg
-    per_token = 2 * c.num_kv_heads * c.head_dim * ELT          # K and V of one token, one layer
+    kv_elt = 1 if c.kv_fp8 else ELT
+    per_token = 2 * c.num_kv_heads * c.head_dim * kv_elt       # K and V of one token, one layer
     lens = w.context_lens.numpy().astype(np.int64)
     nb = (lens + c.block_size - 1) // c.block_size
     kv = w.info["unique_tokens"] * per_token
@@ -107,7 +108,7 @@ def algorithmic_bytes(w: workloads.Workload) -> dict:
     out = q
     tables = int(nb.sum()) * 4 + c.num_seqs * 4
     n_new = c.num_seqs * c.q_len
-    append = 2 * n_new * c.num_kv_heads * c.head_dim * ELT * 2   # read new rows + write slots
+    append = 2 * n_new * c.num_kv_heads * c.head_dim * (ELT + kv_elt)  # read rows, write slots
     ws = 0
     if c.num_splits > 1:   # partial writes, combine reads, per row: D + 2 floats
         rows = c.num_seqs * c.num_splits * c.q_len * c.num_q_heads
@@ -210,8 +211,10 @@ class Runner:
     def __init__(self, pa, w: workloads.Workload, device):
         self.pa, self.w, self.dev = pa, w, device
         c = w.cfg
-        self.d = {k: getattr(w, k).to(device) for k in
-                  ("q", "k_new", "v_new", "k_cache", "v_cache", "block_tables", "context_lens")}
+        names = ["q", "k_new", "v_new", "k_cache", "v_cache", "block_tables", "context_lens"]
+        if c.kv_fp8:
+            names += ["k_scale", "v_scale"]
+        self.d = {k: getattr(w, k).to(device) for k in names}
         self.out = torch.empty_like(self.d["q"])
         self.slots = torch.empty(c.num_seqs * c.q_len, dtype=torch.int64, device=device)
         self.ws = None
@@ -238,9 +241,14 @@ class Runner:
         pa, d, c = self.pa, self.d, self.w.cfg
         if ev_pair is not None:
             ev_pair[0].record()
-        pa.pa_append_decode(self.out, d["q"], d["k_new"], d["v_new"], d["k_cache"], d["v_cache"],
-                            d["block_tables"], d["context_lens"], self.w.scale, c.q_len,
-                            c.num_splits, self.ws)
+        if c.kv_fp8:
+            pa.pa_decode_fp8(self.out, d["q"], d["k_cache"], d["v_cache"], d["k_scale"],
+                             d["v_scale"], d["block_tables"], d["context_lens"], self.w.scale,
+                             c.q_len, c.num_splits, self.ws, k_new=d["k_new"], v_new=d["v_new"])
+        else:
+            pa.pa_append_decode(self.out, d["q"], d["k_new"], d["v_new"], d["k_cache"],
+                                d["v_cache"], d["block_tables"], d["context_lens"], self.w.scale,
+                                c.q_len, c.num_splits, self.ws)
         if ev_pair is not None:
             ev_pair[1].record()
 
@@ -249,6 +257,17 @@ class Runner:
         pa, d, c = self.pa, self.d, self.w.cfg
         pa.pa_slot_mapping(d["block_tables"], d["context_lens"], c.block_size, c.q_len,
                            out=self.slots)
+        if c.kv_fp8:
+            pa.pa_append_kv_fp8(d["k_cache"], d["v_cache"], d["k_new"], d["v_new"], self.slots,
+                                d["k_scale"], d["v_scale"])
+            if ev_pair is not None:
+                ev_pair[0].record()
+            pa.pa_decode_fp8(self.out, d["q"], d["k_cache"], d["v_cache"], d["k_scale"],
+                             d["v_scale"], d["block_tables"], d["context_lens"], self.w.scale,
+                             c.q_len, c.num_splits, self.ws)
+            if ev_pair is not None:
+                ev_pair[1].record()
+            return
         pa.pa_append_kv(d["k_cache"], d["v_cache"], d["k_new"], d["v_new"], self.slots)
         if ev_pair is not None:
             ev_pair[0].record()
@@ -404,11 +423,12 @@ def config_obj(w: workloads.Workload, path: str) -> dict:
     c = w.cfg
     return {"workload": c.name, "num_seqs": c.num_seqs, "num_q_heads": c.num_q_heads,
             "num_kv_heads": c.num_kv_heads, "head_dim": c.head_dim, "block_size": c.block_size,
-            "kv_dtype": c.dtype, "q_len": c.q_len, "num_splits": c.num_splits,
+            "kv_dtype": "e4m3 (per-KV-head scales)" if c.kv_fp8 else c.dtype,
+            "q_dtype": c.dtype, "q_len": c.q_len, "num_splits": c.num_splits,
             "context_tokens": w.total_tokens, "unique_kv_tokens": w.info["unique_tokens"],
             "pool_blocks": w.num_blocks, "path": path,
             "l2": ("not flushed: the KV cache read each step is "
-                   f"{w.info['unique_tokens'] * 2 * c.num_kv_heads * c.head_dim * ELT / 2**20:.0f} MiB,"
+                   f"{w.info['unique_tokens'] * 2 * c.num_kv_heads * c.head_dim * (1 if c.kv_fp8 else ELT) / 2**20:.0f} MiB,"
                    f" larger than the {L2_BYTES >> 20} MiB L2")}
 
 
@@ -462,6 +482,8 @@ def run_ours(args):
 
 
 def _path(w):
+    if w.cfg.kv_fp8:
+        return "pa_decode_fp8 with k_new/v_new (fused quantising append + attention, one launch)"
     return ("pa_append_decode (fused slot mapping + append + split-KV partial, then combine)"
             if w.cfg.num_splits > 1 else
             "pa_append_decode (fused slot mapping + append + attention, one launch)")

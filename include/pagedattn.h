@@ -209,6 +209,41 @@ PA_API pa_status pa_append_decode(void *out, const void *q, const void *k_new, c
                                   size_t workspace_bytes, void *stream);
 
 /*
+ * FP8 (e4m3) KV cache.  The pool holds one byte per element, same layout
+ * [num_blocks][num_kv_heads][block_size][head_dim]; an element stands for
+ * e4m3_value * scale[kv_head], with separate fp32 scales for K and V
+ * (k_scale, v_scale: device arrays [num_kv_heads]).  Quantisation ([QA] Q4: KV
+ * quantisation relieves KV memory; fewer bytes per token on a bandwidth-bound path)
+ * is code = e4m3(x / scale): fp32 division, round to nearest even, magnitudes above
+ * 448 saturate to 448.  head_dim 128 only.
+ *
+ * pa_append_kv_fp8 -- pa_append_kv for an FP8 cache: k_new/v_new are 16-bit rows of
+ * type new_dtype, quantised as above into their slots.
+ */
+PA_API pa_status pa_append_kv_fp8(void *k_cache, void *v_cache, const void *k_new,
+                                  const void *v_new, const int64_t *slot_mapping, int n_tokens,
+                                  int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                                  pa_dtype new_dtype, const float *k_scale, const float *v_scale,
+                                  void *stream);
+
+/*
+ * pa_decode_fp8 -- attention over an FP8 cache (q and out of type dtype; fp32
+ * arithmetic on the dequantised K, V).  With k_new/v_new (both non-NULL) the step's
+ * new rows are first quantised into the cache as pa_append_kv_fp8 would (slots of
+ * the last q_len positions, as pa_slot_mapping), in the same launch.  num_splits == 1:
+ * single pass, workspace may be NULL; num_splits > 1: split-KV partial pass into the
+ * workspace (layout of pa_decode_partial) and the combine.
+ */
+PA_API pa_status pa_decode_fp8(void *out, const void *q, const void *k_new, const void *v_new,
+                               void *k_cache, void *v_cache, const float *k_scale,
+                               const float *v_scale, const int32_t *block_tables,
+                               const int32_t *context_lens, int num_seqs, int num_q_heads,
+                               int num_kv_heads, int head_dim, int block_size, float scale,
+                               int max_blocks_per_seq, int num_blocks, int q_len, pa_dtype dtype,
+                               int num_splits, void *workspace, size_t workspace_bytes,
+                               void *stream);
+
+/*
  * pa_device_error -- synchronise `stream`, then return PA_OK or the first error
  * recorded by a kernel on the current device since the last clear
  * (PA_ERR_DEVICE_TIMEOUT takes precedence over PA_ERR_DEVICE_CHECK).  With

@@ -57,6 +57,11 @@ _SIGNATURES = {
     "pa_selftest_wait_timeout": (_c_int, [_c_vp]),
     "pa_copy_blocks": (_c_int, [_c_vp, _c_vp, _c_vp, _c_vp, _c_int, _c_int, _c_int, _c_int,
                                 _c_int, _c_int, _c_vp]),
+    "pa_append_kv_fp8": (_c_int, [_c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_int, _c_int, _c_int,
+                                  _c_int, _c_int, _c_int, _c_vp, _c_vp, _c_vp]),
+    "pa_decode_fp8": (_c_int, [_c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp,
+                               _c_vp, _c_int, _c_int, _c_int, _c_int, _c_int, _c_float, _c_int,
+                               _c_int, _c_int, _c_int, _c_int, _c_vp, _c_size, _c_vp]),
     "pa_append_decode": (_c_int, [_c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_int,
                                   _c_int, _c_int, _c_int, _c_int, _c_float, _c_int, _c_int,
                                   _c_int, _c_int, _c_int, _c_vp, _c_size, _c_vp]),
@@ -175,6 +180,66 @@ def pa_copy_blocks(k_cache: torch.Tensor, v_cache: torch.Tensor, src_blocks: tor
         _cuda(k_cache, "k_cache"), _cuda(v_cache, "v_cache"),
         _cuda(src_blocks, "src_blocks", torch.int32), _cuda(dst_blocks, "dst_blocks", torch.int32),
         n, h_kv, head_dim, block_size, num_blocks, _elt(k_cache, "k_cache"), _stream(stream)))
+
+
+_FP8_CACHE = (torch.uint8, getattr(torch, "float8_e4m3fn", torch.uint8))
+
+
+def _fp8_cache(t: torch.Tensor, name: str) -> int:
+    if t.dtype not in _FP8_CACHE:
+        raise TypeError(f"{name} must hold e4m3 codes (uint8 or float8_e4m3fn), got {t.dtype}")
+    return _cuda(t, name)
+
+
+def pa_append_kv_fp8(k_cache: torch.Tensor, v_cache: torch.Tensor, k_new: torch.Tensor,
+                     v_new: torch.Tensor, slot_mapping: torch.Tensor, k_scale: torch.Tensor,
+                     v_scale: torch.Tensor, stream=None) -> None:
+    """Quantise 16-bit rows k_new[t], v_new[t] into slot slot_mapping[t] of FP8 caches."""
+    num_blocks, h_kv, block_size, head_dim = _cache_dims(k_cache)
+    n_tokens = int(slot_mapping.shape[0])
+    if k_new.shape != (n_tokens, h_kv, head_dim) or v_new.shape != k_new.shape:
+        raise ValueError("k_new/v_new must be [n_tokens, num_kv_heads, head_dim]")
+    _check("pa_append_kv_fp8", load().pa_append_kv_fp8(
+        _fp8_cache(k_cache, "k_cache"), _fp8_cache(v_cache, "v_cache"), _cuda(k_new, "k_new"),
+        _cuda(v_new, "v_new"), _cuda(slot_mapping, "slot_mapping", torch.int64), n_tokens, h_kv,
+        head_dim, block_size, num_blocks, _elt(k_new, "k_new"),
+        _cuda(k_scale, "k_scale", torch.float32), _cuda(v_scale, "v_scale", torch.float32),
+        _stream(stream)))
+
+
+def pa_decode_fp8(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor,
+                  v_cache: torch.Tensor, k_scale: torch.Tensor, v_scale: torch.Tensor,
+                  block_tables: torch.Tensor, context_lens: torch.Tensor, scale: float,
+                  q_len: int = 1, num_splits: int = 1, workspace: torch.Tensor | None = None,
+                  k_new: torch.Tensor | None = None, v_new: torch.Tensor | None = None,
+                  stream=None) -> torch.Tensor:
+    """Attention over FP8 caches; with k_new/v_new the new rows are appended first
+    (quantised, same launch).  num_splits > 1 uses the split-KV pair."""
+    num_blocks, h_kv, block_size, head_dim, num_seqs, h_q, maxb = _decode_dims(
+        q, k_cache, block_tables, context_lens, q_len)
+    if out.shape != q.shape or out.dtype != q.dtype:
+        raise ValueError("out must match q")
+    kn = vn = None
+    if k_new is not None or v_new is not None:
+        if k_new is None or v_new is None or k_new.shape != (num_seqs * q_len, h_kv, head_dim) \
+                or v_new.shape != k_new.shape or k_new.dtype != q.dtype:
+            raise ValueError("k_new/v_new must both be [num_seqs * q_len, num_kv_heads, head_dim]"
+                             " of q's dtype")
+        kn, vn = _cuda(k_new, "k_new"), _cuda(v_new, "v_new")
+    ws_ptr, ws_bytes = None, 0
+    if num_splits > 1:
+        if workspace is None:
+            nbytes = pa_decode_workspace_size(num_seqs, h_q, q_len, head_dim, num_splits)
+            workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+        ws_ptr, ws_bytes = _cuda(workspace, "workspace"), workspace.numel() * workspace.element_size()
+    _check("pa_decode_fp8", load().pa_decode_fp8(
+        _cuda(out, "out"), _cuda(q, "q"), kn, vn, _fp8_cache(k_cache, "k_cache"),
+        _fp8_cache(v_cache, "v_cache"), _cuda(k_scale, "k_scale", torch.float32),
+        _cuda(v_scale, "v_scale", torch.float32), _cuda(block_tables, "block_tables", torch.int32),
+        _cuda(context_lens, "context_lens", torch.int32), num_seqs, h_q, h_kv, head_dim,
+        block_size, float(scale), maxb, num_blocks, q_len, _elt(q, "q"), num_splits, ws_ptr,
+        ws_bytes, _stream(stream)))
+    return out
 
 
 def _decode_dims(q, k_cache, block_tables, context_lens, q_len):

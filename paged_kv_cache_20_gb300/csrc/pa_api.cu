@@ -83,6 +83,39 @@ __global__ void append_kv_kernel(uint16_t *k_cache, uint16_t *v_cache, const uin
   }
 }
 
+// Quantising append into an FP8 cache: one thread per 8 values of a (token, head)
+// row; code = e4m3(x / scale[head]).
+template <typename T, int D>
+__global__ void append_kv_fp8_kernel(uint8_t *k_cache, uint8_t *v_cache, const uint16_t *k_new,
+                                     const uint16_t *v_new, const int64_t *slot_mapping,
+                                     int n_tokens, int num_kv_heads, int64_t num_slots,
+                                     const float *k_scale, const float *v_scale, unsigned *err) {
+  pa::griddep_wait();
+  pa::griddep_launch_dependents();
+  constexpr int kChunks = D / 8;
+  const int64_t total = (int64_t)n_tokens * num_kv_heads * kChunks;
+  for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
+       idx += (int64_t)gridDim.x * blockDim.x) {
+    const int c = (int)(idx % kChunks);
+    const int64_t th = idx / kChunks;
+    const int h = (int)(th % num_kv_heads);
+    const int64_t t = th / num_kv_heads;
+    const int64_t slot = slot_mapping[t];
+    if (slot < 0) continue;
+    if (slot >= num_slots) {
+      if (c == 0 && h == 0) pa::record_error(err, pa::kErrCheck);
+      continue;
+    }
+    const int64_t block = slot / kBlockSize, offset = slot % kBlockSize;
+    const int64_t dst = ((block * num_kv_heads + h) * kBlockSize + offset) * D + c * 8;
+    const int64_t src = (t * num_kv_heads + h) * D + c * 8;
+    const uint4 kv = __ldg(reinterpret_cast<const uint4 *>(k_new + src));
+    const uint4 vv = __ldg(reinterpret_cast<const uint4 *>(v_new + src));
+    *reinterpret_cast<uint2 *>(k_cache + dst) = pa::quantize8<T>(kv, __ldg(k_scale + h));
+    *reinterpret_cast<uint2 *>(v_cache + dst) = pa::quantize8<T>(vv, __ldg(v_scale + h));
+  }
+}
+
 // Copy-on-write block copy: one thread per 16-byte chunk of a (pair, head, row).
 __global__ void copy_blocks_kernel(uint4 *k_cache, uint4 *v_cache, const int32_t *src,
                                    const int32_t *dst, int n_pairs, int64_t chunks_per_block,
@@ -150,18 +183,19 @@ bool supported_dtype(pa_dtype d) { return d == PA_FP16 || d == PA_BF16; }
 // Tensor map over one cache: [num_blocks * num_kv_heads tiles][16 rows][head_dim],
 // box = 16 rows x 64 columns, 128-byte swizzle, zero fill outside.
 pa_status make_map(CUtensorMap *map, const void *cache, pa_dtype dtype, int head_dim,
-                   int num_blocks, int num_kv_heads) {
+                   int num_blocks, int num_kv_heads, bool fp8 = false) {
   std::call_once(g_encode_once, load_encode);
   if (g_encode == nullptr) return PA_ERR_CUDA;
+  const int elt = fp8 ? 1 : 2;
   cuuint64_t dims[3] = {(cuuint64_t)head_dim, (cuuint64_t)kBlockSize,
                         (cuuint64_t)num_blocks * (cuuint64_t)num_kv_heads};
-  cuuint64_t strides[2] = {(cuuint64_t)head_dim * 2, (cuuint64_t)kBlockSize * head_dim * 2};
-  cuuint32_t box[3] = {64, (cuuint32_t)kBlockSize, 1};
+  cuuint64_t strides[2] = {(cuuint64_t)head_dim * elt, (cuuint64_t)kBlockSize * head_dim * elt};
+  cuuint32_t box[3] = {(cuuint32_t)(128 / elt), (cuuint32_t)kBlockSize, 1};  // 128-byte rows
   cuuint32_t elem_strides[3] = {1, 1, 1};
-  CUresult r = g_encode(map,
-                        dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
-                                         : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
-                        3, const_cast<void *>(cache), dims, strides, box, elem_strides,
+  const CUtensorMapDataType ty = fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                     : (dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                         : CU_TENSOR_MAP_DATA_TYPE_FLOAT16);
+  CUresult r = g_encode(map, ty, 3, const_cast<void *>(cache), dims, strides, box, elem_strides,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? PA_OK : PA_ERR_CUDA;
@@ -212,13 +246,15 @@ pa_status decode_common(void *out, float *ws, const WsLayout *lay, const void *q
                         const int32_t *context_lens, int num_seqs, int num_q_heads,
                         int num_kv_heads, int head_dim, float scale, int num_splits,
                         int max_blocks_per_seq, int num_blocks, int q_len, pa_dtype dtype,
-                        void *stream, const void *k_new = nullptr, const void *v_new = nullptr) {
+                        void *stream, const void *k_new = nullptr, const void *v_new = nullptr,
+                        const float *k_scale = nullptr, const float *v_scale = nullptr) {
   const int64_t units = (int64_t)num_seqs * num_kv_heads * num_splits;
   if (units >= (int64_t)1 << 31) return PA_ERR_INVALID_ARG;
+  const bool fp8 = k_scale != nullptr;
   CUtensorMap kmap, vmap;
-  pa_status st = make_map(&kmap, k_cache, dtype, head_dim, num_blocks, num_kv_heads);
+  pa_status st = make_map(&kmap, k_cache, dtype, head_dim, num_blocks, num_kv_heads, fp8);
   if (st != PA_OK) return st;
-  st = make_map(&vmap, v_cache, dtype, head_dim, num_blocks, num_kv_heads);
+  st = make_map(&vmap, v_cache, dtype, head_dim, num_blocks, num_kv_heads, fp8);
   if (st != PA_OK) return st;
   pa::DecodeArgs a;
   a.q = q;
@@ -244,12 +280,18 @@ pa_status decode_common(void *out, float *ws, const WsLayout *lay, const void *q
   a.v_new = static_cast<const uint16_t *>(v_new);
   a.k_cache = static_cast<uint16_t *>(const_cast<void *>(k_cache));
   a.v_cache = static_cast<uint16_t *>(const_cast<void *>(v_cache));
+  a.k_scale = k_scale;
+  a.v_scale = v_scale;
   a.scale_log2 = scale * 1.4426950408889634f;  // log2(e)
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const bool partial = ws != nullptr;
-  cudaError_t e = dtype == PA_FP16
-                      ? pa::launch_decode_fp16(kmap, vmap, a, head_dim, partial, (int)units, s)
-                      : pa::launch_decode_bf16(kmap, vmap, a, head_dim, partial, (int)units, s);
+  cudaError_t e;
+  if (fp8)
+    e = dtype == PA_FP16 ? pa::launch_decode8_fp16(kmap, vmap, a, partial, (int)units, s)
+                         : pa::launch_decode8_bf16(kmap, vmap, a, partial, (int)units, s);
+  else
+    e = dtype == PA_FP16 ? pa::launch_decode_fp16(kmap, vmap, a, head_dim, partial, (int)units, s)
+                         : pa::launch_decode_bf16(kmap, vmap, a, head_dim, partial, (int)units, s);
   return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
@@ -391,6 +433,75 @@ PA_API pa_status pa_append_decode(void *out, const void *q, const void *k_new, c
                      block_tables, context_lens, num_seqs, num_q_heads, num_kv_heads, head_dim,
                      scale, num_splits, max_blocks_per_seq, num_blocks, q_len, dtype, stream,
                      k_new, v_new);
+  if (st != PA_OK) return st;
+  return pa_decode_combine(out, workspace, workspace_bytes, num_seqs, num_q_heads, head_dim,
+                           q_len, num_splits, dtype, stream);
+}
+
+PA_API pa_status pa_append_kv_fp8(void *k_cache, void *v_cache, const void *k_new,
+                                  const void *v_new, const int64_t *slot_mapping, int n_tokens,
+                                  int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                                  pa_dtype new_dtype, const float *k_scale, const float *v_scale,
+                                  void *stream) {
+  if (!k_cache || !v_cache || !k_new || !v_new || !slot_mapping || !k_scale || !v_scale)
+    return PA_ERR_INVALID_ARG;
+  if (n_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 || num_blocks <= 0)
+    return PA_ERR_INVALID_ARG;
+  if (!aligned16(k_cache) || !aligned16(v_cache) || !aligned16(k_new) || !aligned16(v_new))
+    return PA_ERR_INVALID_ARG;
+  if (!supported_dtype(new_dtype)) return PA_ERR_UNSUPPORTED;
+  if (head_dim != 128 || block_size != kBlockSize) return PA_ERR_UNSUPPORTED;
+  if (n_tokens == 0) return PA_OK;
+  unsigned *err = error_word();
+  if (err == nullptr) return PA_ERR_CUDA;
+  const int64_t total = (int64_t)n_tokens * num_kv_heads * (head_dim / 8);
+  const int threads = 256;
+  const unsigned blocks = (unsigned)std::min<int64_t>((total + threads - 1) / threads, 1 << 20);
+  const int64_t num_slots = (int64_t)num_blocks * kBlockSize;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  auto kc = static_cast<uint8_t *>(k_cache);
+  auto vc = static_cast<uint8_t *>(v_cache);
+  auto kn = static_cast<const uint16_t *>(k_new);
+  auto vn = static_cast<const uint16_t *>(v_new);
+  cudaError_t e = new_dtype == PA_FP16
+                      ? pa::launch_dependent(append_kv_fp8_kernel<__half, 128>, blocks, threads, s,
+                                             kc, vc, kn, vn, slot_mapping, n_tokens, num_kv_heads,
+                                             num_slots, k_scale, v_scale, err)
+                      : pa::launch_dependent(append_kv_fp8_kernel<__nv_bfloat16, 128>, blocks,
+                                             threads, s, kc, vc, kn, vn, slot_mapping, n_tokens,
+                                             num_kv_heads, num_slots, k_scale, v_scale, err);
+  return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+PA_API pa_status pa_decode_fp8(void *out, const void *q, const void *k_new, const void *v_new,
+                               void *k_cache, void *v_cache, const float *k_scale,
+                               const float *v_scale, const int32_t *block_tables,
+                               const int32_t *context_lens, int num_seqs, int num_q_heads,
+                               int num_kv_heads, int head_dim, int block_size, float scale,
+                               int max_blocks_per_seq, int num_blocks, int q_len, pa_dtype dtype,
+                               int num_splits, void *workspace, size_t workspace_bytes,
+                               void *stream) {
+  if (!out || !aligned16(out) || !k_scale || !v_scale) return PA_ERR_INVALID_ARG;
+  if ((k_new == nullptr) != (v_new == nullptr)) return PA_ERR_INVALID_ARG;
+  if (k_new && (!aligned16(k_new) || !aligned16(v_new))) return PA_ERR_INVALID_ARG;
+  if (num_splits <= 0) return PA_ERR_INVALID_ARG;
+  pa_status st = check_decode(q, k_cache, v_cache, block_tables, context_lens, num_seqs,
+                              num_q_heads, num_kv_heads, head_dim, block_size, scale,
+                              max_blocks_per_seq, num_blocks, q_len, dtype);
+  if (st != PA_OK) return st;
+  if (head_dim != 128) return PA_ERR_UNSUPPORTED;
+  if (num_splits == 1)
+    return decode_common(out, nullptr, nullptr, q, k_cache, v_cache, block_tables, context_lens,
+                         num_seqs, num_q_heads, num_kv_heads, head_dim, scale, 1,
+                         max_blocks_per_seq, num_blocks, q_len, dtype, stream, k_new, v_new,
+                         k_scale, v_scale);
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return PA_ERR_INVALID_ARG;
+  const WsLayout lay = ws_layout(num_seqs, num_q_heads, q_len, head_dim, num_splits);
+  if (workspace_bytes < lay.total) return PA_ERR_INVALID_ARG;
+  st = decode_common(nullptr, static_cast<float *>(workspace), &lay, q, k_cache, v_cache,
+                     block_tables, context_lens, num_seqs, num_q_heads, num_kv_heads, head_dim,
+                     scale, num_splits, max_blocks_per_seq, num_blocks, q_len, dtype, stream,
+                     k_new, v_new, k_scale, v_scale);
   if (st != PA_OK) return st;
   return pa_decode_combine(out, workspace, workspace_bytes, num_seqs, num_q_heads, head_dim,
                            q_len, num_splits, dtype, stream);

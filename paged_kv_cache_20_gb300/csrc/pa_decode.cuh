@@ -66,6 +66,9 @@ struct DecodeArgs {
   const uint16_t *v_new;
   uint16_t *k_cache;             // the memory the tensor maps describe
   uint16_t *v_cache;
+  // FP8 (e4m3) cache: value = code * scale of its KV head ([num_kv_heads] each)
+  const float *k_scale;
+  const float *v_scale;
 };
 
 constexpr int kLptMaxSeqs = 256;
@@ -139,7 +142,10 @@ struct FmaPath {
     return part * CH + (kRotate ? ((jj + rot) % CH) : jj);
   }
 
-  __device__ __forceinline__ void init(const DecodeArgs &a, int seq, int kvh, int row0, int L) {
+  static constexpr int kExtraBytes = 0;  // per-warp shared scratch beyond the stages
+
+  __device__ __forceinline__ void init(const DecodeArgs &a, int seq, int kvh, int row0, int L,
+                                       float sscale, uint32_t) {
     const int lane = threadIdx.x & 31;
     part = lane % K;
     tip = lane / K;
@@ -161,7 +167,7 @@ struct FmaPath {
         const float f[8] = {f0.x, f0.y, f1.x, f1.y, f2.x, f2.y, f3.x, f3.y};
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-          q[r][jj * 8 + e] = f[e] * a.scale_log2;
+          q[r][jj * 8 + e] = f[e] * sscale;
           acc[r][jj * 8 + e] = 0.f;
         }
       }
@@ -302,7 +308,10 @@ struct MmaPath {
   float m[2], l[2];
   int lim[2];
 
-  __device__ __forceinline__ void init(const DecodeArgs &a, int seq, int kvh, int row0, int L) {
+  static constexpr int kExtraBytes = 0;
+
+  __device__ __forceinline__ void init(const DecodeArgs &a, int seq, int kvh, int row0, int L,
+                                       float, uint32_t) {
     const int lane = threadIdx.x & 31;
     const int g = lane >> 2, c2 = (lane & 3) * 2;
     const T *qb = static_cast<const T *>(a.q);
@@ -447,21 +456,277 @@ struct MmaPath {
   }
 };
 
+// Eight 16-bit values -> eight e4m3 codes of value / scale (fp32 division, nearest
+// even, saturating): the quantising append of an FP8 cache.
+template <typename T>
+__device__ __forceinline__ uint2 quantize8(const uint4 v, float scale) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  uint16_t c[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 f = Elt<T>::to_f2(w[i]);
+    c[i] = f32x2_to_e4m3x2(f.x / scale, f.y / scale);
+  }
+  return make_uint2((uint32_t)c[0] | ((uint32_t)c[1] << 16), (uint32_t)c[2] | ((uint32_t)c[3] << 16));
+}
+
+// ---------------------------------------------------------------------------------
+// FP8 (e4m3) cache, CUDA-core path: head_dim 128, one 128-byte row per token,
+// 4 lanes per token, each lane 2 chunks of 16 codes.  The K scale is folded into q,
+// the V scale into the output.
+template <typename T, int R>
+struct Fma8Path {
+  static constexpr int D = 128;
+  static constexpr int RPC = R;
+  static constexpr int K = 4;                        // lanes per token
+  static constexpr int TPP = 32 / K;                 // tokens per pass
+  static constexpr int PASSES = kTileTokens / TPP;
+  static constexpr int CH = D / 16 / K;              // 16-code chunks per lane per token
+  static constexpr int kExtraBytes = 0;
+  // Under the 128-byte swizzle the 8 lanes of a shared-memory phase (2 tokens x 4
+  // parts) already land on 8 distinct bank groups: no rotation needed.
+
+  float q[R][CH * 16];
+  float acc[R][CH * 16];
+  float m[R], l[R];
+  int lim[R];
+  int part, tip;
+
+  __device__ __forceinline__ int chunk(int jj) const { return part * CH + jj; }
+
+  __device__ __forceinline__ void init(const DecodeArgs &a, int seq, int kvh, int row0, int L,
+                                       float sscale, uint32_t) {
+    const int lane = threadIdx.x & 31;
+    part = lane % K;
+    tip = lane / K;
+    const T *qb = static_cast<const T *>(a.q);
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      const RowInfo ri = row_info(a, kvh, row0 + r);
+      lim[r] = ri.valid ? (L - a.q_len + ri.u + 1) : 0;
+      m[r] = -INFINITY;
+      l[r] = 0.f;
+      const T *qrow = qb + ((size_t)(seq * a.q_len + ri.u) * a.num_q_heads + ri.h) * D;
+#pragma unroll
+      for (int jj = 0; jj < CH; ++jj) {
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          uint4 v = make_uint4(0, 0, 0, 0);
+          if (ri.valid)
+            v = __ldg(reinterpret_cast<const uint4 *>(qrow + chunk(jj) * 16 + half * 8));
+          const float2 f0 = Elt<T>::to_f2(v.x), f1 = Elt<T>::to_f2(v.y);
+          const float2 f2 = Elt<T>::to_f2(v.z), f3 = Elt<T>::to_f2(v.w);
+          const float f[8] = {f0.x, f0.y, f1.x, f1.y, f2.x, f2.y, f3.x, f3.y};
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            q[r][jj * 16 + half * 8 + e] = f[e] * sscale;
+            acc[r][jj * 16 + half * 8 + e] = 0.f;
+          }
+        }
+      }
+    }
+  }
+
+  template <bool MASKED>
+  __device__ __forceinline__ void tile(uint32_t kt, uint32_t vt, int tile_idx, float) {
+    float s[PASSES][R];
+#pragma unroll
+    for (int p = 0; p < PASSES; ++p) {
+      const int t = p * TPP + tip;
+#pragma unroll
+      for (int r = 0; r < R; ++r) s[p][r] = 0.f;
+#pragma unroll
+      for (int jj = 0; jj < CH; ++jj) {
+        float f[16];
+        e4m3x16_to_f32(lds128(kt + sw128_offset_row128(t, chunk(jj))), f);
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+#pragma unroll
+          for (int e = 0; e < 16; ++e) s[p][r] = fmaf(q[r][jj * 16 + e], f[e], s[p][r]);
+      }
+    }
+#pragma unroll
+    for (int p = 0; p < PASSES; ++p)
+#pragma unroll
+      for (int r = 0; r < R; ++r)
+#pragma unroll
+        for (int o = 1; o < K; o <<= 1) s[p][r] += __shfl_xor_sync(0xffffffffu, s[p][r], o);
+    if (MASKED) {
+#pragma unroll
+      for (int p = 0; p < PASSES; ++p) {
+        const int tg = tile_idx * kTileTokens + p * TPP + tip;
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+          if (tg >= lim[r]) s[p][r] = -INFINITY;
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      float mx = s[0][r];
+#pragma unroll
+      for (int p = 1; p < PASSES; ++p) mx = fmaxf(mx, s[p][r]);
+      if (mx > m[r]) {
+        const float c = fast_exp2(m[r] - mx);
+        l[r] *= c;
+#pragma unroll
+        for (int e = 0; e < CH * 16; ++e) acc[r][e] *= c;
+        m[r] = mx;
+      }
+#pragma unroll
+      for (int p = 0; p < PASSES; ++p) {
+        float pv;
+        if (MASKED)
+          pv = (s[p][r] == -INFINITY) ? 0.f : fast_exp2(s[p][r] - m[r]);
+        else
+          pv = fast_exp2(s[p][r] - m[r]);
+        s[p][r] = pv;
+        l[r] += pv;
+      }
+    }
+#pragma unroll
+    for (int p = 0; p < PASSES; ++p) {
+      const int t = p * TPP + tip;
+#pragma unroll
+      for (int jj = 0; jj < CH; ++jj) {
+        float f[16];
+        e4m3x16_to_f32(lds128(vt + sw128_offset_row128(t, chunk(jj))), f);
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+#pragma unroll
+          for (int e = 0; e < 16; ++e) acc[r][jj * 16 + e] = fmaf(s[p][r], f[e], acc[r][jj * 16 + e]);
+      }
+    }
+  }
+
+  template <int STRIDE>
+  __device__ __forceinline__ void publish(float *mrg_m, float *mrg_l, float *mrg_acc) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int o = K; o < 32; o <<= 1) {
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        const float mo = __shfl_xor_sync(0xffffffffu, m[r], o);
+        const float lo = __shfl_xor_sync(0xffffffffu, l[r], o);
+        const float mn = fmaxf(m[r], mo);
+        const float cs = (m[r] == -INFINITY) ? 0.f : fast_exp2(m[r] - mn);
+        const float co = (mo == -INFINITY) ? 0.f : fast_exp2(mo - mn);
+        l[r] = l[r] * cs + lo * co;
+#pragma unroll
+        for (int e = 0; e < CH * 16; ++e) {
+          const float ao = __shfl_xor_sync(0xffffffffu, acc[r][e], o);
+          acc[r][e] = acc[r][e] * cs + ao * co;
+        }
+        m[r] = mn;
+      }
+    }
+    if (lane < K) {
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        if (lane == 0) {
+          mrg_m[r] = m[r];
+          mrg_l[r] = l[r];
+        }
+#pragma unroll
+        for (int jj = 0; jj < CH; ++jj)
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4)
+            reinterpret_cast<float4 *>(mrg_acc + r * STRIDE + chunk(jj) * 16)[q4] =
+                make_float4(acc[r][jj * 16 + 4 * q4], acc[r][jj * 16 + 4 * q4 + 1],
+                            acc[r][jj * 16 + 4 * q4 + 2], acc[r][jj * 16 + 4 * q4 + 3]);
+      }
+    }
+  }
+};
+
+// FP8 (e4m3) cache, tensor-core path: each warp widens its FP8 K and V tiles into
+// 16-bit tiles of q's type in its own shared scratch (same 128-byte swizzled
+// layout as a 16-bit cache tile), then runs the 16-bit tensor-core tile.
+template <typename T>
+struct Mma8Path {
+  static constexpr int D = 128;
+  static constexpr int RPC = 16;
+  static constexpr int kTile16 = kTileTokens * D * 2;  // one widened tile
+  static constexpr int kExtraBytes = 2 * kTile16;      // widened K and V
+  MmaPath<T, D> inner;
+  uint32_t wk, wv;  // widened tiles (this warp's scratch)
+
+  __device__ __forceinline__ void init(const DecodeArgs &a, int seq, int kvh, int row0, int L,
+                                       float sscale, uint32_t scratch) {
+    inner.init(a, seq, kvh, row0, L, sscale, 0);
+    wk = scratch;
+    wv = scratch + kTile16;
+  }
+
+  __device__ __forceinline__ void widen(uint32_t src8, uint32_t dst16) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int i = 0; i < (kTileTokens * 8) / 32; ++i) {  // 128 chunks of 16 codes
+      const int idx = lane + 32 * i;
+      const int row = idx >> 3, c8 = idx & 7;
+      const uint4 v = lds128(src8 + sw128_offset_row128(row, c8));
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+      uint32_t o[8];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const uint32_t lo = e4m3x2_to_f16x2(static_cast<uint16_t>(w[k] & 0xffffu));
+        const uint32_t hi = e4m3x2_to_f16x2(static_cast<uint16_t>(w[k] >> 16));
+        if constexpr (sizeof(T) == 2 && Elt<T>::kMantBits == 10) {
+          o[2 * k] = lo;
+          o[2 * k + 1] = hi;
+        } else {  // fp16 -> bf16 through fp32 (exact for every e4m3 value)
+          const float2 a = __half22float2(*reinterpret_cast<const __half2 *>(&lo));
+          const float2 b = __half22float2(*reinterpret_cast<const __half2 *>(&hi));
+          o[2 * k] = Elt<T>::from_f2(a.x, a.y);
+          o[2 * k + 1] = Elt<T>::from_f2(b.x, b.y);
+        }
+      }
+      asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
+                       dst16 + sw128_offset<kTileTokens>(row, 2 * c8)),
+                   "r"(o[0]), "r"(o[1]), "r"(o[2]), "r"(o[3])
+                   : "memory");
+      asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
+                       dst16 + sw128_offset<kTileTokens>(row, 2 * c8 + 1)),
+                   "r"(o[4]), "r"(o[5]), "r"(o[6]), "r"(o[7])
+                   : "memory");
+    }
+  }
+
+  template <bool MASKED>
+  __device__ __forceinline__ void tile(uint32_t kt, uint32_t vt, int tile_idx, float sscale) {
+    widen(kt, wk);
+    widen(vt, wv);
+    __syncwarp();
+    inner.template tile<MASKED>(wk, wv, tile_idx, sscale);
+    __syncwarp();  // the scratch is rewritten by the next tile
+  }
+
+  template <int STRIDE>
+  __device__ __forceinline__ void publish(float *mrg_m, float *mrg_l, float *mrg_acc) {
+    inner.template publish<STRIDE>(mrg_m, mrg_l, mrg_acc);
+  }
+};
+
 // ---------------------------------------------------------------------------------
 // The kernel: work unit = (sequence, KV head, split) x row group.  A unit may be
 // shared by the CTAs of one thread-block cluster (launched with cluster dimension
 // C > 1 along x): the C*NW warps take the unit's blocks round-robin, each CTA
 // merges its warps, then the CTAs merge through distributed shared memory.  This
 // splits one long sequence over several SMs without any global workspace.
-template <typename T, int D, int NW, int NSTAGE, class Path, bool PARTIAL>
+template <typename T, int D, int NW, int NSTAGE, class Path, bool PARTIAL, bool KV8>
 __global__ void __launch_bounds__(NW * 32)
     paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
                         const __grid_constant__ CUtensorMap vmap, const DecodeArgs a) {
-  constexpr int kTileBytes = kTileTokens * D * 2;  // one head of one block: 4 KiB at D = 128
+  // one head of one block: 4 KiB at D = 128 (16-bit cache), 2 KiB (FP8 cache)
+  constexpr int kEltBytes = KV8 ? 1 : 2;
+  constexpr int kTileBytes = kTileTokens * D * kEltBytes;
   constexpr int kStageBytes = 2 * kTileBytes;      // K tile + V tile
+  constexpr int kBoxCols = 128 / kEltBytes;        // one TMA box = 16 rows x 128 bytes
+  constexpr int kRowChunks = D * kEltBytes / 16;   // 16-byte chunks per cached row
   constexpr int RPC = Path::RPC;
   constexpr int kStride = D + 8;  // merge-area row stride (floats): padded against bank conflicts
-  static_assert((NW + 1) * RPC * (kStride + 2) * 4 + 64 <= NW * NSTAGE * kStageBytes,
+  static_assert(!KV8 || D == 128, "FP8 cache: head_dim 128");
+  static_assert((NW + 1) * RPC * (kStride + 2) * 4 + 64 <=
+                    NW * NSTAGE * kStageBytes + NW * Path::kExtraBytes,
                 "merge area");
 
   extern __shared__ uint8_t smem_raw[];
@@ -505,6 +770,9 @@ __global__ void __launch_bounds__(NW * 32)
   const int tb = min(nb, split * per);
   const int te = min(nb, tb + per);
   const int first_masked = (L - a.q_len + 1) / kTileTokens;  // tiles >= this need masking
+  // base-2 score scale (times the K scale of an FP8 cache) and the V scale
+  const float sscale = a.scale_log2 * (KV8 ? __ldg(a.k_scale + kvh) : 1.f);
+  const float vscale = KV8 ? __ldg(a.v_scale + kvh) : 1.f;
 
   // Fused append: every CTA whose block range holds a new token writes all of this
   // unit's new rows itself (CTAs of one cluster, row group or neighbouring split
@@ -530,8 +798,16 @@ __global__ void __launch_bounds__(NW * 32)
       const int64_t blk = slot / kTileTokens, off = slot % kTileTokens;
       const size_t dst = (size_t)(((blk * a.num_kv_heads + kvh) * kTileTokens + off) * D + c * 8);
       const size_t src = ((size_t)(seq * a.q_len + u) * a.num_kv_heads + kvh) * D + c * 8;
-      *reinterpret_cast<uint4 *>(a.k_cache + dst) = __ldg(reinterpret_cast<const uint4 *>(a.k_new + src));
-      *reinterpret_cast<uint4 *>(a.v_cache + dst) = __ldg(reinterpret_cast<const uint4 *>(a.v_new + src));
+      const uint4 kv = __ldg(reinterpret_cast<const uint4 *>(a.k_new + src));
+      const uint4 vv = __ldg(reinterpret_cast<const uint4 *>(a.v_new + src));
+      if constexpr (KV8) {  // quantise: e4m3(x / scale), 8 codes per chunk
+        uint8_t *kc = reinterpret_cast<uint8_t *>(a.k_cache), *vc = reinterpret_cast<uint8_t *>(a.v_cache);
+        *reinterpret_cast<uint2 *>(kc + dst) = quantize8<T>(kv, __ldg(a.k_scale + kvh));
+        *reinterpret_cast<uint2 *>(vc + dst) = quantize8<T>(vv, __ldg(a.v_scale + kvh));
+      } else {
+        *reinterpret_cast<uint4 *>(a.k_cache + dst) = kv;
+        *reinterpret_cast<uint4 *>(a.v_cache + dst) = vv;
+      }
     }
     fence_proxy_async_global();
     __syncthreads();
@@ -587,9 +863,9 @@ __global__ void __launch_bounds__(NW * 32)
       }
       mbar_arrive_expect_tx(bar, kStageBytes);
 #pragma unroll
-      for (int hh = 0; hh < D / 64; ++hh) {
-        tma_load_3d(kdst + hh * (kTileTokens * 128), &kmap, hh * 64, 0, z, bar);
-        tma_load_3d(kdst + kTileBytes + hh * (kTileTokens * 128), &vmap, hh * 64, 0, z, bar);
+      for (int hh = 0; hh < kTileBytes / (kTileTokens * 128); ++hh) {
+        tma_load_3d(kdst + hh * (kTileTokens * 128), &kmap, hh * kBoxCols, 0, z, bar);
+        tma_load_3d(kdst + kTileBytes + hh * (kTileTokens * 128), &vmap, hh * kBoxCols, 0, z, bar);
       }
     }
   };
@@ -597,7 +873,8 @@ __global__ void __launch_bounds__(NW * 32)
   // the first block-table window and the q rows load concurrently
   if (n_my > 0) tbl = (lane < n_my) ? __ldg(table + tile_of(lane)) : 0;
   Path path;
-  path.init(a, seq, kvh, row0, L);
+  path.init(a, seq, kvh, row0, L, sscale,
+            smem_base + NW * NSTAGE * kStageBytes + warp * Path::kExtraBytes);
 
   const int prologue = min(NSTAGE, n_my);
   for (int n = 0; n < prologue; ++n) issue(n);
@@ -618,18 +895,18 @@ __global__ void __launch_bounds__(NW * 32)
     if (j >= first_masked) {
       const int nvalid = L - j * kTileTokens;  // rows >= nvalid are past the context
       if (nvalid < kTileTokens) {
-        for (int idx = lane; idx < (kTileTokens - nvalid) * (D / 8); idx += 32) {
-          const int row = nvalid + idx / (D / 8), ch = idx % (D / 8);
-          sts128_zero(vt + sw128_offset<kTileTokens>(row, ch));
+        for (int idx = lane; idx < (kTileTokens - nvalid) * kRowChunks; idx += 32) {
+          const int row = nvalid + idx / kRowChunks, ch = idx % kRowChunks;
+          sts128_zero(vt + (KV8 ? sw128_offset_row128(row, ch) : sw128_offset<kTileTokens>(row, ch)));
         }
         // order these generic-proxy stores before any later TMA (async proxy) write
         // into the same stage
         fence_proxy_async_smem();
         __syncwarp();
       }
-      path.template tile<true>(kt, vt, j, a.scale_log2);
+      path.template tile<true>(kt, vt, j, sscale);
     } else {
-      path.template tile<false>(kt, vt, j, a.scale_log2);
+      path.template tile<false>(kt, vt, j, sscale);
     }
     __syncwarp();
     if (n + NSTAGE < n_my) issue(n + NSTAGE);
@@ -665,15 +942,15 @@ __global__ void __launch_bounds__(NW * 32)
       const size_t wrow = ((size_t)seq * a.num_splits + split) * (a.q_len * a.num_q_heads) +
                           (size_t)ri.u * a.num_q_heads + ri.h;
       float4 *dst = reinterpret_cast<float4 *>(a.ws_acc + wrow * D + d8 * 8);
-      dst[0] = make_float4(num[0], num[1], num[2], num[3]);
-      dst[1] = make_float4(num[4], num[5], num[6], num[7]);
+      dst[0] = make_float4(num[0] * vscale, num[1] * vscale, num[2] * vscale, num[3] * vscale);
+      dst[1] = make_float4(num[4] * vscale, num[5] * vscale, num[6] * vscale, num[7] * vscale);
       if (d8 == 0) {
         a.ws_m[wrow] = M;
         a.ws_l[wrow] = den;
       }
     } else {
       const size_t orow = (size_t)(seq * a.q_len + ri.u) * a.num_q_heads + ri.h;
-      const float inv = den > 0.f ? 1.f / den : 0.f;
+      const float inv = den > 0.f ? vscale / den : 0.f;
       uint4 packed;
       packed.x = Elt<T>::from_f2(num[0] * inv, num[1] * inv);
       packed.y = Elt<T>::from_f2(num[2] * inv, num[3] * inv);

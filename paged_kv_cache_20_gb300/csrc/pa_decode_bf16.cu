@@ -10,4 +10,9 @@ cudaError_t launch_decode_bf16(const CUtensorMap &kmap, const CUtensorMap &vmap,
 cudaError_t launch_combine_bf16(const CombineArgs &args, int head_dim, cudaStream_t stream) {
   return launch_combine_t<__nv_bfloat16>(args, head_dim, stream);
 }
+cudaError_t launch_decode8_bf16(const CUtensorMap &kmap, const CUtensorMap &vmap,
+                                const DecodeArgs &args, bool partial, int units,
+                                cudaStream_t stream) {
+  return launch_decode8_t<__nv_bfloat16>(kmap, vmap, args, partial, units, stream);
+}
 }  // namespace pa

@@ -10,4 +10,9 @@ cudaError_t launch_decode_fp16(const CUtensorMap &kmap, const CUtensorMap &vmap,
 cudaError_t launch_combine_fp16(const CombineArgs &args, int head_dim, cudaStream_t stream) {
   return launch_combine_t<__half>(args, head_dim, stream);
 }
+cudaError_t launch_decode8_fp16(const CUtensorMap &kmap, const CUtensorMap &vmap,
+                                const DecodeArgs &args, bool partial, int units,
+                                cudaStream_t stream) {
+  return launch_decode8_t<__half>(kmap, vmap, args, partial, units, stream);
+}
 }  // namespace pa

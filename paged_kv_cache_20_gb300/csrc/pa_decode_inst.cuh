@@ -27,13 +27,13 @@ struct DeviceFit {
   std::atomic<int> ctas_per_sm{0};
 };
 
-template <typename T, int D, class Path, bool PARTIAL>
+template <typename T, int D, class Path, bool PARTIAL, bool KV8 = false>
 static cudaError_t launch_one(const CUtensorMap &kmap, const CUtensorMap &vmap,
                               const DecodeArgs &a, int units, int row_groups, cudaStream_t st) {
   constexpr int kStages = stages_for<PARTIAL>();
-  constexpr int kStageBytes = 2 * kTileTokens * D * 2;
-  constexpr int kSmem = kWarps * kStages * kStageBytes + 1024;
-  auto kern = paged_decode_kernel<T, D, kWarps, kStages, Path, PARTIAL>;
+  constexpr int kStageBytes = 2 * kTileTokens * D * (KV8 ? 1 : 2);
+  constexpr int kSmem = kWarps * (kStages * kStageBytes + Path::kExtraBytes) + 1024;
+  auto kern = paged_decode_kernel<T, D, kWarps, kStages, Path, PARTIAL, KV8>;
   static DeviceFit fit[kMaxDevices];
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -88,6 +88,23 @@ static cudaError_t launch_paths(const CUtensorMap &kmap, const CUtensorMap &vmap
   if (a.rows == 2) return launch_one<T, D, FmaPath<T, D, 8, 2>, PARTIAL>(kmap, vmap, a, units, 1, st);
   const int groups = (a.rows + 15) / 16;
   return launch_one<T, D, MmaPath<T, D>, PARTIAL>(kmap, vmap, a, units, groups, st);
+}
+
+template <typename T, bool PARTIAL>
+static cudaError_t launch_paths8(const CUtensorMap &kmap, const CUtensorMap &vmap,
+                                 const DecodeArgs &a, int units, cudaStream_t st) {
+  if (a.rows == 1) return launch_one<T, 128, Fma8Path<T, 1>, PARTIAL, true>(kmap, vmap, a, units, 1, st);
+  if (a.rows == 2) return launch_one<T, 128, Fma8Path<T, 2>, PARTIAL, true>(kmap, vmap, a, units, 1, st);
+  const int groups = (a.rows + 15) / 16;
+  return launch_one<T, 128, Mma8Path<T>, PARTIAL, true>(kmap, vmap, a, units, groups, st);
+}
+
+// FP8 (e4m3) cache, head_dim 128; T is the type of q and out.
+template <typename T>
+static cudaError_t launch_decode8_t(const CUtensorMap &kmap, const CUtensorMap &vmap,
+                                    const DecodeArgs &a, bool partial, int units, cudaStream_t st) {
+  return partial ? launch_paths8<T, true>(kmap, vmap, a, units, st)
+                 : launch_paths8<T, false>(kmap, vmap, a, units, st);
 }
 
 template <typename T>

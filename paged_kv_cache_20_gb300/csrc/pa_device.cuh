@@ -248,6 +248,45 @@ struct Elt<__nv_bfloat16> {
   }
 };
 
+// ---- FP8 (e4m3) --------------------------------------------------------------------
+// Two e4m3 codes (low byte = first element) -> two fp16 in one 32-bit register
+// (low half = first element).  Every e4m3 value is exact in fp16.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t v) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(v));
+  return r;
+}
+
+// Two floats -> two e4m3 codes (low byte = `lo`), round to nearest even, magnitudes
+// beyond 448 saturate to 448, NaN stays NaN.
+__device__ __forceinline__ uint16_t f32x2_to_e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// 16 e4m3 codes (one 16-byte chunk) -> 16 floats.
+__device__ __forceinline__ void e4m3x16_to_f32(const uint4 v, float (&f)[16]) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t lo = e4m3x2_to_f16x2(static_cast<uint16_t>(w[i] & 0xffffu));
+    const uint32_t hi = e4m3x2_to_f16x2(static_cast<uint16_t>(w[i] >> 16));
+    const float2 a = __half22float2(*reinterpret_cast<const __half2 *>(&lo));
+    const float2 b = __half22float2(*reinterpret_cast<const __half2 *>(&hi));
+    f[4 * i + 0] = a.x;
+    f[4 * i + 1] = a.y;
+    f[4 * i + 2] = b.x;
+    f[4 * i + 3] = b.y;
+  }
+}
+
+// Byte offset of (row, 16-byte chunk) in a [rows][128 B] tile written by TMA with
+// 128-byte swizzling (an FP8 head of 128 dims is exactly one such row).
+__device__ __forceinline__ uint32_t sw128_offset_row128(int row, int chunk) {
+  return static_cast<uint32_t>(row * 128 + ((chunk ^ (row & 7)) << 4));
+}
+
 __device__ __forceinline__ float fast_exp2(float x) {
   return exp2f(x);
 }

@@ -37,6 +37,13 @@ cudaError_t launch_decode_fp16(const CUtensorMap &kmap, const CUtensorMap &vmap,
 cudaError_t launch_decode_bf16(const CUtensorMap &kmap, const CUtensorMap &vmap,
                                const DecodeArgs &args, int head_dim, bool partial, int units,
                                cudaStream_t stream);
+// FP8 (e4m3) cache, head_dim 128; the suffix names the type of q and out.
+cudaError_t launch_decode8_fp16(const CUtensorMap &kmap, const CUtensorMap &vmap,
+                                const DecodeArgs &args, bool partial, int units,
+                                cudaStream_t stream);
+cudaError_t launch_decode8_bf16(const CUtensorMap &kmap, const CUtensorMap &vmap,
+                                const DecodeArgs &args, bool partial, int units,
+                                cudaStream_t stream);
 cudaError_t launch_combine_fp16(const CombineArgs &args, int head_dim, cudaStream_t stream);
 cudaError_t launch_combine_bf16(const CombineArgs &args, int head_dim, cudaStream_t stream);
 

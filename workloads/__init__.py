@@ -19,6 +19,10 @@ Workloads (shapes from the configurations the library is measured on):
   prefix_verify   128 seqs sharing a 1024-token prefix (the same 64 physical
                   blocks), private tails of U[64, 2048] tokens, 4 causal query
                   positions per seq, 32 q / 8 KV heads, head_dim 128, fp16
+  llama7b_mha_fp8, gqa_fp8
+                  the same shapes over an FP8 (e4m3) cache with one scale per KV
+                  head (K and V separately, drawn in [0.02, 0.05]); q and the new
+                  rows stay in the 16-bit type
 
 Every value in q, the pool and the new rows is N(0, 1), rounded to nearest even
 into the 16-bit type.  Physical block ids are a seeded random permutation of the
@@ -64,6 +68,7 @@ class Config:
     pool_blocks: int | None = None   # fixed pool size; None = exactly what is needed + spare
     shared_prefix: int = 0     # tokens of a prefix whose blocks all sequences share
     spare_blocks: int = 8      # free (never referenced) blocks added to the pool
+    kv_fp8: bool = False       # cache holds FP8 (e4m3) codes with per-KV-head scales
 
     @property
     def group(self) -> int:
@@ -80,6 +85,11 @@ CONFIGS: dict[str, Config] = {
                          lens=("fixed", (32768,) * 4), num_splits=16),
     "prefix_verify": Config("prefix_verify", 128, 32, 8, 128, 16, "fp16", q_len=4,
                             lens=("prefix", 1024, 64, 2048), shared_prefix=1024),
+    # the same shapes over an FP8 (e4m3) cache, q and new rows in the 16-bit type
+    "llama7b_mha_fp8": Config("llama7b_mha_fp8", 32, 32, 32, 128, 16, "fp16",
+                              lens=("uniform", 512, 4096), kv_fp8=True),
+    "gqa_fp8": Config("gqa_fp8", 64, 32, 8, 128, 16, "bf16",
+                      lens=("lognormal", 1500.0, 0.5, 8192), kv_fp8=True),
 }
 
 
@@ -153,6 +163,8 @@ class Workload:
     v_cache: torch.Tensor
     padding_block: int           # block id used for table entries past a sequence's end
     info: dict = field(default_factory=dict)
+    k_scale: torch.Tensor | None = None   # [H_kv] float32, FP8 caches only (uint8 codes)
+    v_scale: torch.Tensor | None = None
 
     @property
     def num_blocks(self) -> int:
@@ -167,8 +179,12 @@ class Workload:
         return int(self.context_lens.to(torch.int64).sum())
 
     def bits(self, name: str) -> np.ndarray:
-        """A 16-bit tensor field as a numpy uint16 bit-pattern array (shares memory)."""
-        return getattr(self, name).view(torch.int16).numpy().view(np.uint16)
+        """A 16-bit tensor field as a numpy uint16 bit-pattern array (shares memory);
+        FP8 caches come back as their uint8 codes."""
+        t = getattr(self, name)
+        if t.dtype == torch.uint8:
+            return t.numpy()
+        return t.view(torch.int16).numpy().view(np.uint16)
 
 
 def make(cfg: Config | str, seed: int = 0, poison: bool = True, **overrides) -> Workload:
@@ -217,6 +233,17 @@ def make(cfg: Config | str, seed: int = 0, poison: bool = True, **overrides) -> 
     v_new = normal_tensor((n_new, H_kv, D), cfg.dtype, seed, _S_VNEW)
     k_cache = normal_tensor((pool, H_kv, B, D), cfg.dtype, seed, _S_KCACHE)
     v_cache = normal_tensor((pool, H_kv, B, D), cfg.dtype, seed, _S_VCACHE)
+    k_scale = v_scale = None
+    if cfg.kv_fp8:
+        # FP8 pool: codes of N(0,1) values under a per-head scale drawn in
+        # [0.02, 0.05] (|value / scale| stays well inside e4m3's +-448); the codes
+        # are made with torch's float8 conversion.
+        srng = _rng(seed, _S_PERM + 100)
+        k_scale = torch.from_numpy(srng.uniform(0.02, 0.05, H_kv).astype(np.float32))
+        v_scale = torch.from_numpy(srng.uniform(0.02, 0.05, H_kv).astype(np.float32))
+        k_cache = (k_cache.float() / k_scale[None, :, None, None]).to(torch.float8_e4m3fn)
+        v_cache = (v_cache.float() / v_scale[None, :, None, None]).to(torch.float8_e4m3fn)
+        k_cache, v_cache = k_cache.view(torch.uint8), v_cache.view(torch.uint8)
 
     if poison:
         # filled[block] = how many leading slots of the block carry a token written
@@ -231,12 +258,13 @@ def make(cfg: Config | str, seed: int = 0, poison: bool = True, **overrides) -> 
                     break
                 b = tables[i, j]
                 filled[b] = max(filled[b], min(B, old - first))
+        nan = 0x7F if cfg.kv_fp8 else float("nan")      # e4m3 NaN code
         empty = torch.from_numpy(np.nonzero(filled == 0)[0])
-        k_cache[empty] = float("nan")
-        v_cache[empty] = float("nan")
+        k_cache[empty] = nan
+        v_cache[empty] = nan
         for b in np.nonzero((filled > 0) & (filled < B))[0]:
-            k_cache[int(b), :, int(filled[b]):, :] = float("nan")
-            v_cache[int(b), :, int(filled[b]):, :] = float("nan")
+            k_cache[int(b), :, int(filled[b]):, :] = nan
+            v_cache[int(b), :, int(filled[b]):, :] = nan
 
     info = {
         "pool_blocks": pool,
@@ -248,4 +276,4 @@ def make(cfg: Config | str, seed: int = 0, poison: bool = True, **overrides) -> 
                     context_lens=torch.from_numpy(lens.copy()),
                     block_tables=torch.from_numpy(tables.astype(np.int32)),
                     q=q, k_new=k_new, v_new=v_new, k_cache=k_cache, v_cache=v_cache,
-                    padding_block=padding_block, info=info)
+                    padding_block=padding_block, info=info, k_scale=k_scale, v_scale=v_scale)
