@@ -306,16 +306,17 @@ struct MmaPath {
   uint32_t qa[KS][4];  // A fragments of Q
   float o[NT][4];      // O: rows (lane/4, lane/4 + 8), dims nt*8 + (lane%4)*2 + {0,1}
   float m[2], l[2];
+  float rs[2];         // base-2 score scale of each of this lane's two rows
   int lim[2];
 
   static constexpr int kExtraBytes = 0;
 
-  __device__ __forceinline__ void init(const DecodeArgs &a, int seq, int kvh, int row0, int L,
-                                       float, uint32_t) {
-    const int lane = threadIdx.x & 31;
-    const int g = lane >> 2, c2 = (lane & 3) * 2;
-    const T *qb = static_cast<const T *>(a.q);
-    const T *qrow[2];
+  // Row bookkeeping; returns this lane's two q rows (nullptr for padding rows).
+  template <typename TQ>
+  __device__ __forceinline__ void init_rows(const DecodeArgs &a, int seq, int kvh, int row0, int L,
+                                            float sscale, const TQ *(&qrow)[2]) {
+    const int g = (threadIdx.x & 31) >> 2;
+    const TQ *qb = static_cast<const TQ *>(a.q);
 #pragma unroll
     for (int hr = 0; hr < 2; ++hr) {
       const RowInfo ri = row_info(a, kvh, row0 + g + 8 * hr);
@@ -324,7 +325,19 @@ struct MmaPath {
                           : nullptr;
       m[hr] = -INFINITY;
       l[hr] = 0.f;
+      rs[hr] = sscale;
     }
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) o[nt][e] = 0.f;
+  }
+
+  __device__ __forceinline__ void init(const DecodeArgs &a, int seq, int kvh, int row0, int L,
+                                       float sscale, uint32_t) {
+    const int c2 = (threadIdx.x & 3) * 2;
+    const T *qrow[2];
+    init_rows<T>(a, seq, kvh, row0, L, sscale, qrow);
 #pragma unroll
     for (int ks = 0; ks < KS; ++ks) {
 #pragma unroll
@@ -333,14 +346,10 @@ struct MmaPath {
         qa[ks][i] = qrow[hr] ? __ldg(reinterpret_cast<const uint32_t *>(qrow[hr] + col)) : 0u;
       }
     }
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) o[nt][e] = 0.f;
   }
 
   template <bool MASKED>
-  __device__ __forceinline__ void tile(uint32_t kt, uint32_t vt, int tile_idx, float scale_log2) {
+  __device__ __forceinline__ void tile(uint32_t kt, uint32_t vt, int tile_idx, float) {
     const int lane = threadIdx.x & 31;
     const int mi = lane >> 3, ri = lane & 7;
     // S = Q K^T: B fragments (K rows = tokens, 8 dims each) by ldmatrix.  Even and
@@ -363,6 +372,16 @@ struct MmaPath {
     for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
       for (int e = 0; e < 4; ++e) sc[nt][e] += sd[nt][e];
+    softmax_pv<MASKED>(sc, vt, tile_idx);
+  }
+
+  // Online-softmax update of this tile's scores S (C fragments: rows lane/4 and
+  // lane/4 + 8, tokens nt*8 + (lane%4)*2 + {0,1}) and O += P V with V^T fragments
+  // from the 16-bit tile at vt.
+  template <bool MASKED>
+  __device__ __forceinline__ void softmax_pv(float (&sc)[2][4], uint32_t vt, int tile_idx) {
+    const int lane = threadIdx.x & 31;
+    const int mi = lane >> 3, ri = lane & 7;
     // scale to base-2 units, mask, row max over the 16 tokens (4 lanes per row)
     float mx[2];
 #pragma unroll
@@ -371,7 +390,7 @@ struct MmaPath {
       for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
-          float v = sc[nt][2 * hr + e] * scale_log2;
+          float v = sc[nt][2 * hr + e] * rs[hr];
           if (MASKED) {
             const int tg = tile_idx * kTileTokens + nt * 8 + (lane & 3) * 2 + e;
             if (tg >= lim[hr]) v = -INFINITY;
@@ -639,22 +658,60 @@ struct Fma8Path {
 };
 
 // FP8 (e4m3) cache, tensor-core path: each warp widens its FP8 K and V tiles into
-// 16-bit tiles of q's type in its own shared scratch (same 128-byte swizzled
-// layout as a 16-bit cache tile), then runs the 16-bit tensor-core tile.
+// fp16 tiles in its own shared scratch (same 128-byte swizzled layout as a 16-bit
+// cache tile; every e4m3 value is exact in fp16), then runs the fp16 tensor-core
+// tile whatever q's type.  A bf16 q row is brought into fp16 range by an exact
+// power-of-two factor 2^-e (e: exponent of the row's largest |q|), and 2^e goes
+// into that row's score scale.  P is then fp16 too: no hi/lo split is needed.
 template <typename T>
 struct Mma8Path {
   static constexpr int D = 128;
   static constexpr int RPC = 16;
   static constexpr int kTile16 = kTileTokens * D * 2;  // one widened tile
-  static constexpr int kExtraBytes = 2 * kTile16;      // widened K and V
-  MmaPath<T, D> inner;
-  uint32_t wk, wv;  // widened tiles (this warp's scratch)
+  static constexpr int kExtraBytes = kTile16;          // widened V
+  MmaPath<__half, D> inner;
+  uint32_t wv;  // widened V tile (this warp's scratch)
 
+  // The contraction over head dims is permuted inside each 16-dim k-step so that a
+  // lane's four k slots {2c, 2c+1, 2c+8, 2c+9} (c = lane % 4) are dims 4c..4c+3:
+  // four consecutive e4m3 codes, one 32-bit shared load.  Q's A fragments use the
+  // same permutation, so S is unchanged.
   __device__ __forceinline__ void init(const DecodeArgs &a, int seq, int kvh, int row0, int L,
                                        float sscale, uint32_t scratch) {
-    inner.init(a, seq, kvh, row0, L, sscale, 0);
-    wk = scratch;
-    wv = scratch + kTile16;
+    const int c4 = (threadIdx.x & 3) * 4;
+    const T *qrow[2];
+    inner.template init_rows<T>(a, seq, kvh, row0, L, sscale, qrow);
+    float2 qf[MmaPath<__half, D>::KS][4];
+    float mx[2] = {0.f, 0.f};
+#pragma unroll
+    for (int ks = 0; ks < MmaPath<__half, D>::KS; ++ks)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int hr = i & 1, col = ks * 16 + c4 + (i >> 1) * 2;
+        const uint32_t v = qrow[hr] ? __ldg(reinterpret_cast<const uint32_t *>(qrow[hr] + col)) : 0u;
+        qf[ks][i] = Elt<T>::to_f2(v);
+        mx[hr] = fmaxf(mx[hr], fmaxf(fabsf(qf[ks][i].x), fabsf(qf[ks][i].y)));
+      }
+#pragma unroll
+    for (int hr = 0; hr < 2; ++hr) {  // the 4 lanes holding a row agree on its maximum
+      mx[hr] = fmaxf(mx[hr], __shfl_xor_sync(0xffffffffu, mx[hr], 1));
+      mx[hr] = fmaxf(mx[hr], __shfl_xor_sync(0xffffffffu, mx[hr], 2));
+    }
+    float down[2];
+#pragma unroll
+    for (int hr = 0; hr < 2; ++hr) {
+      const int e = (mx[hr] > 0.f && isfinite(mx[hr])) ? ilogbf(mx[hr]) : 0;
+      down[hr] = ldexpf(1.f, -e);           // |q| * down < 2: well inside fp16
+      inner.rs[hr] = sscale * ldexpf(1.f, e);
+    }
+#pragma unroll
+    for (int ks = 0; ks < MmaPath<__half, D>::KS; ++ks)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float d = down[i & 1];
+        inner.qa[ks][i] = Elt<__half>::from_f2(qf[ks][i].x * d, qf[ks][i].y * d);
+      }
+    wv = scratch;
   }
 
   __device__ __forceinline__ void widen(uint32_t src8, uint32_t dst16) {
@@ -668,17 +725,8 @@ struct Mma8Path {
       uint32_t o[8];
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
-        const uint32_t lo = e4m3x2_to_f16x2(static_cast<uint16_t>(w[k] & 0xffffu));
-        const uint32_t hi = e4m3x2_to_f16x2(static_cast<uint16_t>(w[k] >> 16));
-        if constexpr (sizeof(T) == 2 && Elt<T>::kMantBits == 10) {
-          o[2 * k] = lo;
-          o[2 * k + 1] = hi;
-        } else {  // fp16 -> bf16 through fp32 (exact for every e4m3 value)
-          const float2 a = __half22float2(*reinterpret_cast<const __half2 *>(&lo));
-          const float2 b = __half22float2(*reinterpret_cast<const __half2 *>(&hi));
-          o[2 * k] = Elt<T>::from_f2(a.x, a.y);
-          o[2 * k + 1] = Elt<T>::from_f2(b.x, b.y);
-        }
+        o[2 * k] = e4m3x2_to_f16x2(static_cast<uint16_t>(w[k] & 0xffffu));
+        o[2 * k + 1] = e4m3x2_to_f16x2(static_cast<uint16_t>(w[k] >> 16));
       }
       asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
                        dst16 + sw128_offset<kTileTokens>(row, 2 * c8)),
@@ -692,11 +740,35 @@ struct Mma8Path {
   }
 
   template <bool MASKED>
-  __device__ __forceinline__ void tile(uint32_t kt, uint32_t vt, int tile_idx, float sscale) {
-    widen(kt, wk);
+  __device__ __forceinline__ void tile(uint32_t kt, uint32_t vt, int tile_idx, float) {
+    const int lane = threadIdx.x & 31;
     widen(vt, wv);
-    __syncwarp();
-    inner.template tile<MASKED>(wk, wv, tile_idx, sscale);
+    // S = Q K^T with K's B fragments widened in registers from the FP8 tile
+    float sc[2][4], sd[2][4];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) sc[nt][e] = sd[nt][e] = 0.f;
+#pragma unroll
+    for (int ks = 0; ks < MmaPath<__half, D>::KS; ++ks) {
+      float (&acc)[2][4] = (ks & 1) ? sd : sc;
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        uint32_t w;
+        asm volatile("ld.shared.b32 %0, [%1];"
+                     : "=r"(w)
+                     : "r"(kt + sw128_offset_row128(nt * 8 + (lane >> 2), ks) + 4 * (lane & 3)));
+        const uint32_t b0 = e4m3x2_to_f16x2(static_cast<uint16_t>(w & 0xffffu));
+        const uint32_t b1 = e4m3x2_to_f16x2(static_cast<uint16_t>(w >> 16));
+        Elt<__half>::mma16816(acc[nt], inner.qa[ks], b0, b1);
+      }
+    }
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) sc[nt][e] += sd[nt][e];
+    __syncwarp();  // widened V visible to every lane
+    inner.template softmax_pv<MASKED>(sc, wv, tile_idx);
     __syncwarp();  // the scratch is rewritten by the next tile
   }
 

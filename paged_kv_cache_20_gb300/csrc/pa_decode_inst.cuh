@@ -19,6 +19,11 @@ constexpr int kMaxDevices = 64;
 constexpr int kWarps = 4;
 template <bool PARTIAL>
 constexpr int stages_for() { return PARTIAL ? 3 : 2; }
+// An FP8 stage carries half the bytes, so FP8 keeps more stages per warp in flight:
+// 4 on the CUDA-core path, 3 on the tensor-core path (which also holds a 4 KiB
+// widened V tile per warp), both measured best and both still 3 CTAs per SM.
+template <class Path, bool PARTIAL, bool KV8>
+constexpr int stages_of() { return KV8 ? (Path::RPC == 16 ? 3 : 4) : stages_for<PARTIAL>(); }
 constexpr int kMaxCluster = 8;  // portable cluster size limit
 
 // Per device: SM count and resident CTAs per SM of one kernel (cached).
@@ -30,7 +35,7 @@ struct DeviceFit {
 template <typename T, int D, class Path, bool PARTIAL, bool KV8 = false>
 static cudaError_t launch_one(const CUtensorMap &kmap, const CUtensorMap &vmap,
                               const DecodeArgs &a, int units, int row_groups, cudaStream_t st) {
-  constexpr int kStages = stages_for<PARTIAL>();
+  constexpr int kStages = stages_of<Path, PARTIAL, KV8>();
   constexpr int kStageBytes = 2 * kTileTokens * D * (KV8 ? 1 : 2);
   constexpr int kSmem = kWarps * (kStages * kStageBytes + Path::kExtraBytes) + 1024;
   auto kern = paged_decode_kernel<T, D, kWarps, kStages, Path, PARTIAL, KV8>;
