@@ -46,7 +46,9 @@ import workloads  # noqa: E402
 METRIC = "paged decode attention: KV tokens/s and achieved HBM GB/s (% of GB300 peak)"
 UNIT = "KV tokens/s"
 DEFAULT_CONFIG = "llama7b_mha"
-OTHER_CONFIGS = ["gqa", "long_split", "prefix_verify", "llama7b_mha_fp8", "gqa_fp8"]
+OTHER_CONFIGS = ["gqa", "long_split", "prefix_verify", "llama7b_mha_fp8", "gqa_fp8",
+                 "chunked_prefill"]
+DECODE_MAX_QLEN = 16              # more query rows per sequence go to the prefill kernel
 L2_BYTES = 129 << 20             # GB300 L2; every workload's KV cache is several times larger
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
@@ -120,6 +122,16 @@ def algorithmic_bytes(w: workloads.Workload) -> dict:
     fused = decode + append + (ws // 2 + out if c.num_splits > 1 else 0)
     return {"per_token": per_token, "kv": kv, "decode_launch": decode, "fused_launch": fused,
             "step": kv + q + out + tables + append + ws + n_new * 8}
+
+
+def attention_flops(w: workloads.Workload) -> float:
+    """Multiply-adds of the attention proper, x2: for every query row, 2*D for its
+    scores and 2*D for P.V per visible position (causal window)."""
+    c = w.cfg
+    lens = w.context_lens.numpy().astype(np.int64)
+    u = np.arange(c.q_len, dtype=np.int64)
+    visible = np.clip(lens[:, None] - c.q_len + u[None, :] + 1, 0, None)
+    return float(4 * c.head_dim * c.num_q_heads * int(visible.sum()))
 
 
 def traffic_record(kernel_name: str, config: str):
@@ -222,18 +234,47 @@ class Runner:
             nbytes = pa.pa_decode_workspace_size(c.num_seqs, c.num_q_heads, c.q_len, c.head_dim,
                                                  c.num_splits)
             self.ws = torch.empty(nbytes, dtype=torch.uint8, device=device)
-        self.fused = True
-        self.launches = {True: 1 + (1 if c.num_splits > 1 else 0),
-                         False: 3 + (1 if c.num_splits > 1 else 0)}
+        split = 1 if c.num_splits > 1 else 0
+        prefill = 1 if c.q_len > DECODE_MAX_QLEN else 0       # separate append launch
+        self.mode = "fused"
+        self.launches = {"fused": 1 + prefill + split, "separate": 3 + split,
+                         "cascade": 3 + prefill}
+        if c.shared_prefix:
+            self.cascade_ws = torch.empty(
+                pa.pa_decode_workspace_size(c.num_seqs, c.num_q_heads, c.q_len, c.head_dim, 2),
+                dtype=torch.uint8, device=device)
+
+    @property
+    def fused(self) -> bool:
+        return self.mode == "fused"
+
+    @fused.setter
+    def fused(self, value: bool):
+        self.mode = "fused" if value else "separate"
 
     @property
     def launches_per_step(self) -> int:
-        return self.launches[self.fused]
+        return self.launches[self.mode]
 
     def step(self, ev_pair=None):
-        if self.fused:
+        if self.mode == "fused":
             return self.step_fused(ev_pair)
+        if self.mode == "cascade":
+            return self.step_cascade(ev_pair)
         return self.step_separate(ev_pair)
+
+    def step_cascade(self, ev_pair=None):
+        """pa_decode_cascade with the append: the shared prefix once for all query
+        rows, each sequence's own blocks, then the combine."""
+        pa, d, c = self.pa, self.d, self.w.cfg
+        if ev_pair is not None:
+            ev_pair[0].record()
+        pa.pa_decode_cascade(self.out, d["q"], d["k_cache"], d["v_cache"], d["block_tables"],
+                             d["context_lens"], self.w.scale, c.shared_prefix // c.block_size,
+                             q_len=c.q_len, tail_splits=1, k_new=d["k_new"], v_new=d["v_new"],
+                             workspace=self.cascade_ws)
+        if ev_pair is not None:
+            ev_pair[1].record()
 
     def step_fused(self, ev_pair=None):
         """pa_append_decode: slot mapping, append and attention in one launch (plus the
@@ -411,6 +452,29 @@ def measure_config(pa, name, seed, device, steps, warmup, world, peaks, e2e=Fals
         "step_gbs": ab["step"] / (ms_per_step * 1e-3) / 1e9,
         "separate_launches_ms_per_step": max_over_ranks(sum(sep_ms), world, device) / steps,
     }
+    if w.cfg.q_len > DECODE_MAX_QLEN:
+        # many query rows: the attention is a dense contraction; report it against
+        # the tensor-core peak as well
+        fl = attention_flops(w)
+        tpeak = peaks.get("bf16_tflops")
+        res["tensor_roofline"] = {
+            "bound": "tensor", "flops_per_step": fl,
+            "achieved": fl / (kern_avg * 1e-3) / 1e12,
+            "peak": tpeak or 1900.0, "unit": "TFLOP/s",
+            "frac": fl / (kern_avg * 1e-3) / 1e12 / (tpeak or 1900.0),
+            "peak_source": "measured bf16 dense (burst)" if tpeak else "fallback",
+            "kernel": "append_step_kernel+paged_prefill_kernel (mma.sync m16n8k16)"}
+        res["roofline"]["kernel"] = "append_step_kernel+paged_prefill_kernel"
+    if w.cfg.shared_prefix:
+        runner.mode = "cascade"
+        c_ms, c_kern, _ = time_device(runner, steps, warmup, world)
+        assert pa.pa_device_error() == 0, "device error during the timed cascade run"
+        c_step = max_over_ranks(sum(c_ms), world, device) / steps
+        res["cascade"] = {"ms_per_step": c_step, "value": tokens / (c_step * 1e-3),
+                          "kernel_us": statistics.mean(c_kern) * 1e3,
+                          "path": "pa_decode_cascade (shared-prefix pass, tail pass with "
+                                  "fused append, combine: 3 launches)"}
+        runner.mode = "fused"
     if e2e:
         ms, h2d, d2h = time_e2e(runner, steps, max(3, warmup))
         e_ms = max_over_ranks(sum(ms), world, device) / steps
@@ -459,6 +523,9 @@ def run_ours(args):
                             "kernel_us": o["roofline"]["kernel_us"],
                             "frac_of_8tbs": o["roofline"]["frac_of_8tbs"],
                             "config": config_obj(o["w"], _path(o["w"]))}
+            for extra in ("cascade", "tensor_roofline"):
+                if extra in o:
+                    others[name][extra] = o[extra]
             del o
     cpu = cpu_baseline(r["w"]) if (rank == 0 and not args.no_cpu) else None
     if rank != 0:
@@ -482,6 +549,9 @@ def run_ours(args):
 
 
 def _path(w):
+    if w.cfg.q_len > DECODE_MAX_QLEN:
+        return ("pa_append_decode with q_len > 16: append launch, then the prefill kernel "
+                "(64 query rows per CTA share each K/V tile)")
     if w.cfg.kv_fp8:
         return "pa_decode_fp8 with k_new/v_new (fused quantising append + attention, one launch)"
     return ("pa_append_decode (fused slot mapping + append + split-KV partial, then combine)"

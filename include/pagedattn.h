@@ -42,7 +42,10 @@
  *    AttentionWithKVCache.forward updates the cache before computing scores).
  *  - GQA: query head h reads KV head h / (num_q_heads / num_kv_heads)
  *    (contiguous groups; [QA] Q7, [ANIM] §1 figure).
- *  - Supported now: block_size 16; head_dim 64 or 128; q_len 1..16.
+ *  - Supported now: block_size 16; head_dim 64 or 128; q_len 1..4096 with a
+ *    16-bit cache (up to 16 query rows per sequence go to the decode kernel, more
+ *    to a kernel that shares each K/V tile among 64 query rows: chunked prefill,
+ *    [QA] Q14, [SB11] §11.3 "Continuous Batching"); q_len 1..16 with an FP8 cache.
  *  - Alignment: every pointer 16-byte aligned.
  *
  * Errors: argument checks run on the host before any launch and return
@@ -198,7 +201,8 @@ PA_API pa_status pa_decode_combine(void *out, const void *workspace, size_t work
  * workspace as for pa_decode_partial).  The cache ends up bit-identical to the
  * unfused sequence and out within the same tolerance.  New positions < 0 are
  * skipped; new positions beyond the block table or the pool are skipped and set
- * PA_ERR_DEVICE_CHECK.
+ * PA_ERR_DEVICE_CHECK.  With q_len > 16 the append is a launch of its own before
+ * the attention (a CTA's rows then depend on rows other CTAs would write).
  */
 PA_API pa_status pa_append_decode(void *out, const void *q, const void *k_new, const void *v_new,
                                   void *k_cache, void *v_cache, const int32_t *block_tables,
@@ -207,6 +211,35 @@ PA_API pa_status pa_append_decode(void *out, const void *q, const void *k_new, c
                                   int max_blocks_per_seq, int num_blocks, int q_len,
                                   pa_dtype dtype, int num_splits, void *workspace,
                                   size_t workspace_bytes, void *stream);
+
+/*
+ * pa_decode_cascade -- attention of a batch whose sequences all begin with the
+ * same prefix_blocks physical blocks (a shared prompt: [QA] Q2 copy-on-write page
+ * sharing and Q3 prefix caching; [SB11] §11.4 "Prefix Caching": the shared
+ * prefix's KV is stored once).  Same result as pa_append_decode, computed in
+ * three launches over a workspace of 1 + tail_splits partitions
+ * (pa_decode_workspace_size(num_seqs, num_q_heads, q_len, head_dim,
+ * 1 + tail_splits) bytes, 256-byte aligned, layout as for pa_decode_partial):
+ *   partition 0      every query row of every sequence against the prefix blocks,
+ *                    read once per KV head for all num_seqs * q_len * group rows;
+ *                    the prefix is the first prefix_blocks entries of block-table
+ *                    row 0;
+ *   partitions 1..   each sequence's blocks from prefix_blocks on (with this
+ *                    step's append when k_new/v_new are given), cut into
+ *                    tail_splits equal parts;
+ * then the combine.  The causal limit applies in both passes.
+ * Caller's contract: for every sequence, table entries [0, prefix_blocks) equal
+ * those of row 0, and this step's new tokens lie at or past position
+ * prefix_blocks * block_size (so the append never writes a shared block).
+ * k_new and v_new are both NULL (no append) or both given.  16-bit caches only.
+ */
+PA_API pa_status pa_decode_cascade(void *out, const void *q, const void *k_new, const void *v_new,
+                                   void *k_cache, void *v_cache, const int32_t *block_tables,
+                                   const int32_t *context_lens, int num_seqs, int num_q_heads,
+                                   int num_kv_heads, int head_dim, int block_size, float scale,
+                                   int max_blocks_per_seq, int num_blocks, int q_len,
+                                   pa_dtype dtype, int prefix_blocks, int tail_splits,
+                                   void *workspace, size_t workspace_bytes, void *stream);
 
 /*
  * FP8 (e4m3) KV cache.  The pool holds one byte per element, same layout

@@ -65,6 +65,9 @@ _SIGNATURES = {
     "pa_append_decode": (_c_int, [_c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_int,
                                   _c_int, _c_int, _c_int, _c_int, _c_float, _c_int, _c_int,
                                   _c_int, _c_int, _c_int, _c_vp, _c_size, _c_vp]),
+    "pa_decode_cascade": (_c_int, [_c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_int,
+                                   _c_int, _c_int, _c_int, _c_int, _c_float, _c_int, _c_int,
+                                   _c_int, _c_int, _c_int, _c_int, _c_vp, _c_size, _c_vp]),
     "pa_decode_split_noalloc": (_c_int, [_c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_int, _c_int,
                                          _c_int, _c_int, _c_int, _c_float, _c_int, _c_int,
                                          _c_int, _c_int, _c_int, _c_vp]),
@@ -360,6 +363,43 @@ def pa_append_decode(out: torch.Tensor, q: torch.Tensor, k_new: torch.Tensor,
         _cuda(context_lens, "context_lens", torch.int32), num_seqs, h_q, h_kv, head_dim,
         block_size, float(scale), maxb, num_blocks, q_len, _elt(k_cache, "k_cache"), num_splits,
         ws_ptr, ws_bytes, _stream(stream)))
+    return out
+
+
+def pa_decode_cascade(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor,
+                      v_cache: torch.Tensor, block_tables: torch.Tensor,
+                      context_lens: torch.Tensor, scale: float, prefix_blocks: int,
+                      q_len: int = 1, tail_splits: int = 1, k_new: torch.Tensor | None = None,
+                      v_new: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+                      stream=None) -> torch.Tensor:
+    """Attention of a batch sharing its first ``prefix_blocks`` blocks (block-table row
+    0): one pass over the shared prefix for all rows, one over each sequence's own
+    blocks (with the append of k_new/v_new when given), then the combine."""
+    num_blocks, h_kv, block_size, head_dim, num_seqs, h_q, maxb = _decode_dims(
+        q, k_cache, block_tables, context_lens, q_len)
+    if out.shape != q.shape or out.dtype != q.dtype or q.dtype != k_cache.dtype:
+        raise ValueError("out must match q; q must have the cache dtype")
+    if (k_new is None) != (v_new is None):
+        raise ValueError("give both k_new and v_new, or neither")
+    if k_new is not None:
+        if k_new.shape != (num_seqs * q_len, h_kv, head_dim) or v_new.shape != k_new.shape:
+            raise ValueError("k_new/v_new must be [num_seqs * q_len, num_kv_heads, head_dim]")
+        for t, nm in ((k_new, "k_new"), (v_new, "v_new")):
+            if t.dtype != k_cache.dtype:
+                raise TypeError(f"{nm} must have the cache dtype {k_cache.dtype}")
+    if workspace is None:
+        nbytes = pa_decode_workspace_size(num_seqs, h_q, q_len, head_dim, 1 + tail_splits)
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+    _check("pa_decode_cascade", load().pa_decode_cascade(
+        _cuda(out, "out"), _cuda(q, "q"),
+        None if k_new is None else _cuda(k_new, "k_new"),
+        None if v_new is None else _cuda(v_new, "v_new"),
+        _cuda(k_cache, "k_cache"), _cuda(v_cache, "v_cache"),
+        _cuda(block_tables, "block_tables", torch.int32),
+        _cuda(context_lens, "context_lens", torch.int32), num_seqs, h_q, h_kv, head_dim,
+        block_size, float(scale), maxb, num_blocks, q_len, _elt(k_cache, "k_cache"),
+        int(prefix_blocks), int(tail_splits), _cuda(workspace, "workspace"),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
     return out
 
 

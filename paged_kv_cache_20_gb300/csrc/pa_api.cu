@@ -11,6 +11,7 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <mutex>
@@ -23,7 +24,8 @@ namespace {
 
 constexpr int kBlockSize = 16;
 constexpr int kMaxDevices = 64;
-constexpr int kMaxQLen = 16;
+constexpr int kMaxQLen = 4096;       // query rows per sequence accepted by the ABI
+constexpr int kMaxDecodeQLen = 16;   // at most this many go to the decode kernel
 
 __device__ unsigned int g_error_word;  // one per device (module global)
 
@@ -80,6 +82,46 @@ __global__ void append_kv_kernel(uint16_t *k_cache, uint16_t *v_cache, const uin
     const uint4 vv = __ldg(reinterpret_cast<const uint4 *>(v_new + src));
     *reinterpret_cast<uint4 *>(k_cache + dst) = kv;
     *reinterpret_cast<uint4 *>(v_cache + dst) = vv;
+  }
+}
+
+// Append of one step's new rows straight from the block tables: token u of
+// sequence i sits at position context_lens[i] - q_len + u (the slot of the slot
+// mapping kernel, computed in place).  One thread per 16-byte chunk.
+template <int D>
+__global__ void append_step_kernel(uint16_t *k_cache, uint16_t *v_cache, const uint16_t *k_new,
+                                   const uint16_t *v_new, const int32_t *block_tables,
+                                   const int32_t *context_lens, int num_seqs, int q_len,
+                                   int num_kv_heads, int max_blocks_per_seq, int64_t num_slots,
+                                   unsigned *err) {
+  pa::griddep_wait();
+  pa::griddep_launch_dependents();
+  constexpr int kChunks = D / 8;
+  const int64_t total = (int64_t)num_seqs * q_len * num_kv_heads * kChunks;
+  for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
+       idx += (int64_t)gridDim.x * blockDim.x) {
+    const int c = (int)(idx % kChunks);
+    const int64_t th = idx / kChunks;
+    const int h = (int)(th % num_kv_heads);
+    const int64_t t = th / num_kv_heads;  // token row of k_new: seq * q_len + u
+    const int i = (int)(t / q_len), u = (int)(t % q_len);
+    const int64_t pos = (int64_t)context_lens[i] - q_len + u;
+    if (pos < 0) continue;
+    const int64_t lb = pos / kBlockSize;
+    if (lb >= max_blocks_per_seq) {
+      if (c == 0) pa::record_error(err, pa::kErrCheck);
+      continue;
+    }
+    const int64_t slot =
+        (int64_t)block_tables[(int64_t)i * max_blocks_per_seq + lb] * kBlockSize + pos % kBlockSize;
+    if (slot < 0 || slot >= num_slots) {
+      if (c == 0) pa::record_error(err, pa::kErrCheck);
+      continue;
+    }
+    const int64_t dst = (((slot / kBlockSize) * num_kv_heads + h) * kBlockSize + slot % kBlockSize) * D + c * 8;
+    const int64_t src = (t * num_kv_heads + h) * D + c * 8;
+    *reinterpret_cast<uint4 *>(k_cache + dst) = __ldg(reinterpret_cast<const uint4 *>(k_new + src));
+    *reinterpret_cast<uint4 *>(v_cache + dst) = __ldg(reinterpret_cast<const uint4 *>(v_new + src));
   }
 }
 
@@ -241,16 +283,31 @@ pa_status check_decode(const void *q, const void *k_cache, const void *v_cache,
   return PA_OK;
 }
 
+// Where a launch's partitions go inside a workspace shared with other passes (the
+// cascade): the sequence's partitions start at its block first_block, and the
+// launch writes workspace partitions [ws_split0, ws_split0 + num_splits) of
+// ws_splits.  shared_prefix > 0 selects the shared-prefix pass.
+struct Placement {
+  int first_block = 0;
+  int ws_splits = 0;  // 0: num_splits
+  int ws_split0 = 0;
+  int shared_prefix = 0;
+};
+
 pa_status decode_common(void *out, float *ws, const WsLayout *lay, const void *q,
                         const void *k_cache, const void *v_cache, const int32_t *block_tables,
                         const int32_t *context_lens, int num_seqs, int num_q_heads,
                         int num_kv_heads, int head_dim, float scale, int num_splits,
                         int max_blocks_per_seq, int num_blocks, int q_len, pa_dtype dtype,
                         void *stream, const void *k_new = nullptr, const void *v_new = nullptr,
-                        const float *k_scale = nullptr, const float *v_scale = nullptr) {
+                        const float *k_scale = nullptr, const float *v_scale = nullptr,
+                        const Placement &place = Placement()) {
   const int64_t units = (int64_t)num_seqs * num_kv_heads * num_splits;
   if (units >= (int64_t)1 << 31) return PA_ERR_INVALID_ARG;
   const bool fp8 = k_scale != nullptr;
+  // many query rows (or the shared-prefix pass): the CTA-shared pipeline kernel
+  const bool prefill = place.shared_prefix > 0 || q_len > kMaxDecodeQLen;
+  if (prefill && fp8) return PA_ERR_UNSUPPORTED;
   CUtensorMap kmap, vmap;
   pa_status st = make_map(&kmap, k_cache, dtype, head_dim, num_blocks, num_kv_heads, fp8);
   if (st != PA_OK) return st;
@@ -282,11 +339,37 @@ pa_status decode_common(void *out, float *ws, const WsLayout *lay, const void *q
   a.v_cache = static_cast<uint16_t *>(const_cast<void *>(v_cache));
   a.k_scale = k_scale;
   a.v_scale = v_scale;
+  a.first_block = place.first_block;
+  a.ws_splits = place.ws_splits > 0 ? place.ws_splits : num_splits;
+  a.ws_split0 = place.ws_split0;
+  a.shared_prefix = place.shared_prefix;
   a.scale_log2 = scale * 1.4426950408889634f;  // log2(e)
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const bool partial = ws != nullptr;
   cudaError_t e;
-  if (fp8)
+  if (prefill) {
+    if (k_new != nullptr) {
+      // The rows of a CTA depend on new tokens that other CTAs' rows own, so the
+      // append runs as its own launch first (ordered by the stream).
+      const int64_t total = (int64_t)num_seqs * q_len * num_kv_heads * (head_dim / 8);
+      const unsigned blocks = (unsigned)std::min<int64_t>((total + 255) / 256, 1 << 20);
+      const int64_t num_slots = (int64_t)num_blocks * kBlockSize;
+      auto kc = static_cast<uint16_t *>(const_cast<void *>(k_cache));
+      auto vc = static_cast<uint16_t *>(const_cast<void *>(v_cache));
+      auto kn = static_cast<const uint16_t *>(k_new);
+      auto vn = static_cast<const uint16_t *>(v_new);
+      e = head_dim == 128
+              ? pa::launch_dependent(append_step_kernel<128>, blocks, 256, s, kc, vc, kn, vn,
+                                     block_tables, context_lens, num_seqs, q_len, num_kv_heads,
+                                     max_blocks_per_seq, num_slots, a.err)
+              : pa::launch_dependent(append_step_kernel<64>, blocks, 256, s, kc, vc, kn, vn,
+                                     block_tables, context_lens, num_seqs, q_len, num_kv_heads,
+                                     max_blocks_per_seq, num_slots, a.err);
+      if (e != cudaSuccess) return PA_ERR_CUDA;
+      a.k_new = a.v_new = nullptr;
+    }
+    e = pa::launch_prefill(kmap, vmap, a, head_dim, dtype == PA_FP16, partial, s);
+  } else if (fp8)
     e = dtype == PA_FP16 ? pa::launch_decode8_fp16(kmap, vmap, a, partial, (int)units, s)
                          : pa::launch_decode8_bf16(kmap, vmap, a, partial, (int)units, s);
   else
@@ -438,6 +521,52 @@ PA_API pa_status pa_append_decode(void *out, const void *q, const void *k_new, c
                            q_len, num_splits, dtype, stream);
 }
 
+PA_API pa_status pa_decode_cascade(void *out, const void *q, const void *k_new, const void *v_new,
+                                   void *k_cache, void *v_cache, const int32_t *block_tables,
+                                   const int32_t *context_lens, int num_seqs, int num_q_heads,
+                                   int num_kv_heads, int head_dim, int block_size, float scale,
+                                   int max_blocks_per_seq, int num_blocks, int q_len,
+                                   pa_dtype dtype, int prefix_blocks, int tail_splits,
+                                   void *workspace, size_t workspace_bytes, void *stream) {
+  if (!out || !aligned16(out)) return PA_ERR_INVALID_ARG;
+  if ((k_new == nullptr) != (v_new == nullptr)) return PA_ERR_INVALID_ARG;
+  if (k_new && (!aligned16(k_new) || !aligned16(v_new))) return PA_ERR_INVALID_ARG;
+  if (tail_splits <= 0 || prefix_blocks <= 0) return PA_ERR_INVALID_ARG;
+  pa_status st = check_decode(q, k_cache, v_cache, block_tables, context_lens, num_seqs,
+                              num_q_heads, num_kv_heads, head_dim, block_size, scale,
+                              max_blocks_per_seq, num_blocks, q_len, dtype);
+  if (st != PA_OK) return st;
+  if (prefix_blocks > max_blocks_per_seq) return PA_ERR_INVALID_ARG;
+  if (tail_splits >= (1 << 20)) return PA_ERR_INVALID_ARG;
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return PA_ERR_INVALID_ARG;
+  const int parts = 1 + tail_splits;
+  const WsLayout lay = ws_layout(num_seqs, num_q_heads, q_len, head_dim, parts);
+  if (workspace_bytes < lay.total) return PA_ERR_INVALID_ARG;
+  float *ws = static_cast<float *>(workspace);
+  // 1. the shared prefix: every query row of every sequence against the first
+  //    prefix_blocks blocks of table row 0 -> workspace partition 0
+  Placement head;
+  head.ws_splits = parts;
+  head.shared_prefix = prefix_blocks;
+  st = decode_common(nullptr, ws, &lay, q, k_cache, v_cache, block_tables, context_lens, num_seqs,
+                     num_q_heads, num_kv_heads, head_dim, scale, 1, max_blocks_per_seq,
+                     num_blocks, q_len, dtype, stream, nullptr, nullptr, nullptr, nullptr, head);
+  if (st != PA_OK) return st;
+  // 2. each sequence's own blocks past the prefix (with this step's append, if
+  //    given) -> partitions 1 .. tail_splits
+  Placement tail;
+  tail.first_block = prefix_blocks;
+  tail.ws_splits = parts;
+  tail.ws_split0 = 1;
+  st = decode_common(nullptr, ws, &lay, q, k_cache, v_cache, block_tables, context_lens, num_seqs,
+                     num_q_heads, num_kv_heads, head_dim, scale, tail_splits, max_blocks_per_seq,
+                     num_blocks, q_len, dtype, stream, k_new, v_new, nullptr, nullptr, tail);
+  if (st != PA_OK) return st;
+  // 3. merge the partitions
+  return pa_decode_combine(out, workspace, workspace_bytes, num_seqs, num_q_heads, head_dim, q_len,
+                           parts, dtype, stream);
+}
+
 PA_API pa_status pa_append_kv_fp8(void *k_cache, void *v_cache, const void *k_new,
                                   const void *v_new, const int64_t *slot_mapping, int n_tokens,
                                   int num_kv_heads, int head_dim, int block_size, int num_blocks,
@@ -489,7 +618,7 @@ PA_API pa_status pa_decode_fp8(void *out, const void *q, const void *k_new, cons
                               num_q_heads, num_kv_heads, head_dim, block_size, scale,
                               max_blocks_per_seq, num_blocks, q_len, dtype);
   if (st != PA_OK) return st;
-  if (head_dim != 128) return PA_ERR_UNSUPPORTED;
+  if (head_dim != 128 || q_len > kMaxDecodeQLen) return PA_ERR_UNSUPPORTED;
   if (num_splits == 1)
     return decode_common(out, nullptr, nullptr, q, k_cache, v_cache, block_tables, context_lens,
                          num_seqs, num_q_heads, num_kv_heads, head_dim, scale, 1,

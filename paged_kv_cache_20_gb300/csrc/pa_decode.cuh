@@ -69,6 +69,14 @@ struct DecodeArgs {
   // FP8 (e4m3) cache: value = code * scale of its KV head ([num_kv_heads] each)
   const float *k_scale;
   const float *v_scale;
+  // Partitioning of each sequence's blocks: blocks before first_block are skipped
+  // (a shared prefix handled elsewhere); the partial pass writes partitions
+  // ws_split0 .. ws_split0 + num_splits - 1 of a workspace laid out for ws_splits.
+  int first_block;
+  int ws_splits, ws_split0;
+  // Prefill kernel, shared-prefix mode (> 0): the query rows of every sequence
+  // attend to the first `shared_prefix` blocks of block-table row 0.
+  int shared_prefix;
 };
 
 constexpr int kLptMaxSeqs = 256;
@@ -331,6 +339,31 @@ struct MmaPath {
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
       for (int e = 0; e < 4; ++e) o[nt][e] = 0.f;
+  }
+
+  // Rows given directly: this lane's two q rows (nullptr = padding) and how many
+  // leading positions each may see.
+  __device__ __forceinline__ void init_explicit(const T *(&qrow)[2], const int (&limit)[2],
+                                                float sscale) {
+    const int c2 = (threadIdx.x & 3) * 2;
+#pragma unroll
+    for (int hr = 0; hr < 2; ++hr) {
+      lim[hr] = limit[hr];
+      m[hr] = -INFINITY;
+      l[hr] = 0.f;
+      rs[hr] = sscale;
+    }
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) o[nt][e] = 0.f;
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int hr = i & 1, col = ks * 16 + c2 + (i >> 1) * 8;
+        qa[ks][i] = qrow[hr] ? __ldg(reinterpret_cast<const uint32_t *>(qrow[hr] + col)) : 0u;
+      }
   }
 
   __device__ __forceinline__ void init(const DecodeArgs &a, int seq, int kvh, int row0, int L,
@@ -838,8 +871,9 @@ __global__ void __launch_bounds__(NW * 32)
       record_error(a.err, kErrCheck);
     nb = a.max_blocks_per_seq;
   }
-  const int per = (nb + a.num_splits - 1) / a.num_splits;
-  const int tb = min(nb, split * per);
+  const int fb = min(nb, a.first_block);
+  const int per = (nb - fb + a.num_splits - 1) / a.num_splits;
+  const int tb = min(nb, fb + split * per);
   const int te = min(nb, tb + per);
   const int first_masked = (L - a.q_len + 1) / kTileTokens;  // tiles >= this need masking
   // base-2 score scale (times the K scale of an FP8 cache) and the V scale
@@ -1011,7 +1045,7 @@ __global__ void __launch_bounds__(NW * 32)
     const RowInfo ri = row_info(a, kvh, row0 + r);
     if (!ri.valid) return;
     if constexpr (PARTIAL) {
-      const size_t wrow = ((size_t)seq * a.num_splits + split) * (a.q_len * a.num_q_heads) +
+      const size_t wrow = ((size_t)seq * a.ws_splits + a.ws_split0 + split) * (a.q_len * a.num_q_heads) +
                           (size_t)ri.u * a.num_q_heads + ri.h;
       float4 *dst = reinterpret_cast<float4 *>(a.ws_acc + wrow * D + d8 * 8);
       dst[0] = make_float4(num[0] * vscale, num[1] * vscale, num[2] * vscale, num[3] * vscale);

@@ -1,0 +1,70 @@
+// pa_prefill.cu -- host launchers of the many-row (chunked-prefill / shared-prefix)
+// kernel, both element types.
+#include <atomic>
+
+#include "pa_launch.h"
+#include "pa_prefill.cuh"
+
+namespace pa {
+
+namespace {
+
+constexpr int kPrefillWarps = 4;   // consumer warps: 64 query rows per CTA
+constexpr int kPrefillStages = 4;  // K/V tile pairs in flight per CTA
+
+template <typename T, int D, bool PARTIAL>
+cudaError_t launch_prefill_t(const CUtensorMap &kmap, const CUtensorMap &vmap, const DecodeArgs &a,
+                             cudaStream_t st) {
+  constexpr int kRows = 16 * kPrefillWarps;
+  constexpr int kSmem = kPrefillStages * 2 * kTileTokens * D * 2 + 1024;
+  auto kern = paged_prefill_kernel<T, D, kPrefillWarps, kPrefillStages, PARTIAL>;
+  static std::atomic<unsigned long long> opted{0};  // bit per device: smem opt-in done
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!(opted.load(std::memory_order_acquire) & (1ull << dev))) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    if (e != cudaSuccess) return e;
+    opted.fetch_or(1ull << dev, std::memory_order_acq_rel);
+  }
+  const long long rows_per_seq = (long long)a.q_len * a.group;
+  const long long rows = a.shared_prefix > 0 ? rows_per_seq * a.num_seqs : rows_per_seq;
+  const long long nz = a.shared_prefix > 0 ? a.num_splits : (long long)a.num_seqs * a.num_splits;
+  const long long gx = (rows + kRows - 1) / kRows * nz;
+  if (gx <= 0) return cudaSuccess;
+  if (gx > 0x7fffffffLL || a.num_kv_heads > 65535) return cudaErrorInvalidConfiguration;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)gx, (unsigned)a.num_kv_heads, 1);
+  cfg.blockDim = dim3((kPrefillWarps + 1) * 32, 1, 1);
+  cfg.dynamicSmemBytes = kSmem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, kmap, vmap, a);
+}
+
+template <typename T>
+cudaError_t dispatch(const CUtensorMap &kmap, const CUtensorMap &vmap, const DecodeArgs &a,
+                     int head_dim, bool partial, cudaStream_t st) {
+  if (head_dim == 128)
+    return partial ? launch_prefill_t<T, 128, true>(kmap, vmap, a, st)
+                   : launch_prefill_t<T, 128, false>(kmap, vmap, a, st);
+  if (head_dim == 64)
+    return partial ? launch_prefill_t<T, 64, true>(kmap, vmap, a, st)
+                   : launch_prefill_t<T, 64, false>(kmap, vmap, a, st);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+cudaError_t launch_prefill(const CUtensorMap &kmap, const CUtensorMap &vmap, const DecodeArgs &args,
+                           int head_dim, bool fp16, bool partial, cudaStream_t stream) {
+  return fp16 ? dispatch<__half>(kmap, vmap, args, head_dim, partial, stream)
+              : dispatch<__nv_bfloat16>(kmap, vmap, args, head_dim, partial, stream);
+}
+
+}  // namespace pa

@@ -208,6 +208,8 @@ def pin_matches_sdpa(o):
         (3, 8, 2, 32, BF16, [5, 33, 64], 1),
         (4, 6, 3, 16, FP16, [9, 20, 40], 4),
         (5, 4, 1, 32, BF16, [4, 31], 2),
+        # chunked prefill: many query rows; L == q_len is a plain causal prefill
+        (18, 4, 2, 16, FP16, [40, 57, 100], 40),
     ]
     for seed, h_q, h_kv, d, dtype, lens, q_len in cases:
         q, K, V = _rand_case(seed, len(lens), h_q, h_kv, d, dtype, lens, q_len=q_len)

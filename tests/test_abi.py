@@ -88,7 +88,7 @@ def _decode(lib, **kw):
     ({"n": 0}, -1), ({"hq": 6, "hkv": 4}, -1), ({"hkv": 0}, -1), ({"qlen": 0}, -1),
     ({"maxb": 0}, -1), ({"nblocks": -1}, -1), ({"q": FAKE + 2}, -1), ({"out": FAKE + 8}, -1),
     ({"scale": float("nan")}, -1), ({"d": 96}, -2), ({"d": 256}, -2), ({"bs": 32}, -2),
-    ({"qlen": 17}, -2), ({"dtype": 5}, -2), ({"nblocks": 1 << 30, "hkv": 4, "hq": 4}, -1),
+    ({"qlen": 4097}, -2), ({"dtype": 5}, -2), ({"nblocks": 1 << 30, "hkv": 4, "hq": 4}, -1),
 ])
 def test_decode_rejects_bad_arguments(lib, kw, status):
     assert _decode(lib, **kw) == status
@@ -155,3 +155,28 @@ def test_copy_blocks_rejects_bad_arguments(lib):
     assert lib.pa_copy_blocks(FAKE + 4, FAKE, FAKE, FAKE, 2, 2, 128, 16, 8, 0, None) == -1
     assert lib.pa_copy_blocks(FAKE, FAKE, FAKE, FAKE, 2, 2, 100, 16, 8, 0, None) == -2
     assert lib.pa_copy_blocks(FAKE, FAKE, FAKE, FAKE, 0, 2, 128, 16, 8, 0, None) == 0
+
+
+def test_cascade_rejects_bad_arguments(lib):
+    # out, q, k_new, v_new, k, v, tables, lens, n, hq, hkv, d, bs, scale, maxb, nblocks, qlen, dtype
+    base = [FAKE, FAKE, None, None, FAKE, FAKE, FAKE, FAKE, 2, 8, 2, 128, 16, 0.1, 4, 8, 1, 0]
+    ws_ok = lib.pa_decode_workspace_size(2, 8, 1, 128, 3)
+    call = lambda args, prefix, tail, ws, wsb: lib.pa_decode_cascade(  # noqa: E731
+        *args, prefix, tail, ws, wsb, None)
+    assert call(base, 0, 2, FAKE, ws_ok) == -1          # no prefix
+    assert call(base, 5, 2, FAKE, ws_ok) == -1          # prefix longer than the table
+    assert call(base, 2, 0, FAKE, ws_ok) == -1          # no tail partition
+    assert call(base, 2, 2, None, ws_ok) == -1          # workspace required
+    assert call(base, 2, 2, FAKE + 16, ws_ok) == -1     # 256-byte alignment
+    assert call(base, 2, 2, FAKE, ws_ok - 1) == -1      # 1 + tail_splits partitions
+    one_new = list(base); one_new[2] = FAKE
+    assert call(one_new, 2, 2, FAKE, ws_ok) == -1       # k_new without v_new
+    d96 = list(base); d96[11] = 96
+    assert call(d96, 2, 2, FAKE, ws_ok) == -2
+
+
+def test_fp8_keeps_the_decode_row_limit(lib):
+    # an FP8 cache goes only through the decode kernel: q_len <= 16
+    args = [FAKE, FAKE, None, None, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 2, 8, 2, 128, 16, 0.1, 4,
+            8]
+    assert lib.pa_decode_fp8(*args, 17, 0, 1, None, 0, None) == -2

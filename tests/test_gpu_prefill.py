@@ -1,0 +1,162 @@
+"""Many query rows per sequence (chunked prefill) and cascade shared-prefix attention,
+CUDA library vs the fp64 oracle through the C ABI (needs a GPU).
+
+Both reach the same attention as pa_decode -- softmax(scale q K^T) V over each
+row's causal window -- so each is compared with the oracle's plain definition:
+every element at small sizes, sampled rows at full size, and the appended cache
+bit for bit.
+"""
+import numpy as np
+import pytest
+import torch
+
+import workloads
+from tests import _tol
+from tests.oracle_pins import Paged
+from tests.test_gpu_parity import (DEV, _dev, _f64, _gpu_decode, _logical_case, _u16,
+                                   gpu_step, oracle_step)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def pa():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import paged_kv_cache_20_gb300 as pa
+    pa.load()
+    assert pa.pa_device_error() == 0
+    return pa
+
+
+# ------------------------------------------------------------------- chunked prefill
+PREFILL_SMALL = [
+    ("chunked_prefill", {"num_seqs": 2, "q_len": 100, "lens": ("fixed", (100, 357))}),
+    ("llama7b_mha", {"num_seqs": 2, "q_len": 40, "lens": ("fixed", (40, 700))}),
+    ("tiny", {"q_len": 17, "lens": ("fixed", (17, 33, 60))}),
+    ("gqa", {"num_seqs": 3, "q_len": 64, "lens": ("fixed", (64, 65, 1000))}),
+]
+
+
+@pytest.mark.parametrize("splits", [1, 3])
+@pytest.mark.parametrize("fused", [False, True], ids=["separate", "fused"])
+@pytest.mark.parametrize("name,over", PREFILL_SMALL, ids=[c[0] for c in PREFILL_SMALL])
+def test_chunked_prefill_every_element(pa, orc, name, over, fused, splits):
+    w = workloads.make(name, **over)
+    out, d = gpu_step(pa, w, num_splits=splits, fused=fused)
+    ref, kc, vc, _ = oracle_step(orc, w)
+    assert np.array_equal(_u16(d["k_cache"]), kc)
+    assert np.array_equal(_u16(d["v_cache"]), vc)
+    _tol.check(_f64(out), ref, w.cfg.dtype, f"{name} q_len {w.cfg.q_len}")
+
+
+@pytest.mark.parametrize("fused", [False, True], ids=["separate", "fused"])
+def test_chunked_prefill_full_size_sampled_rows(pa, orc, fused):
+    """The full chunked-prefill workload in the launch configuration bench.py times."""
+    w = workloads.make("chunked_prefill")
+    out, d = gpu_step(pa, w, fused=fused)
+    n_rows = w.cfg.num_seqs * w.cfg.q_len * w.cfg.num_q_heads
+    rng = np.random.default_rng(2)
+    rows = np.sort(rng.choice(n_rows, size=64, replace=False))
+    ref, kc, vc, _ = oracle_step(orc, w, rows=rows)
+    _tol.check(_f64(out).reshape(n_rows, -1)[rows], ref, w.cfg.dtype, "chunked_prefill")
+    assert np.array_equal(_u16(d["k_cache"]), kc)
+    assert np.array_equal(_u16(d["v_cache"]), vc)
+
+
+PREFILL_LENS = [0, 1, 15, 16, 17, 33, 100, 257]
+
+
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("h_q,h_kv,q_len", [(8, 8, 17), (8, 2, 33), (12, 4, 64)])
+def test_prefill_edge_lengths(pa, orc, dtype, d, h_q, h_kv, q_len):
+    # contexts shorter than q_len: the first rows see nothing (zeros), later ones a
+    # prefix of the context
+    q, K, V = _logical_case(21, PREFILL_LENS, h_q, h_kv, d, dtype, q_len=q_len, qscale=2.0)
+    pc = Paged(orc, K, V, 16, dtype, perm_seed=9)
+    scale = float(np.float32(1.0) / np.sqrt(np.float32(d)))
+    ref = pc.decode(orc, q, scale, q_len=q_len)
+    _tol.check(_gpu_decode(pa, pc, q, scale, q_len), ref, dtype, f"{dtype} d{d} q_len {q_len}")
+    for S in (2, 7):
+        _tol.check(_gpu_decode(pa, pc, q, scale, q_len, num_splits=S), ref, dtype, f"split {S}")
+
+
+def test_prefill_paging_permutation_is_bit_invariant(pa, orc):
+    lens = [64, 511, 1000]
+    q, K, V = _logical_case(22, lens, 32, 8, 128, "bf16", q_len=40)
+    outs = [_gpu_decode(pa, Paged(orc, K, V, 16, "bf16", perm_seed=s), q, 0.0884, 40)
+            for s in (None, 13, 14)]
+    assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[0], outs[2])
+
+
+def test_prefill_peaked_scores(pa, orc):
+    lens = [300, 900]
+    q, K, V = _logical_case(23, lens, 8, 2, 128, "fp16", q_len=48, qscale=8.0)
+    pc = Paged(orc, K, V, 16, "fp16", perm_seed=15)
+    _tol.check(_gpu_decode(pa, pc, q, 0.0884, 48), pc.decode(orc, q, 0.0884, q_len=48), "fp16",
+               "peaked prefill")
+
+
+# -------------------------------------------------------------------------- cascade
+def gpu_cascade(pa, w, tail_splits=1, fused=True):
+    d = _dev(w)
+    P = w.cfg.shared_prefix // w.cfg.block_size
+    out = torch.empty_like(d["q"])
+    if fused:
+        pa.pa_decode_cascade(out, d["q"], d["k_cache"], d["v_cache"], d["block_tables"],
+                             d["context_lens"], w.scale, P, q_len=w.cfg.q_len,
+                             tail_splits=tail_splits, k_new=d["k_new"], v_new=d["v_new"])
+    else:
+        slots = pa.pa_slot_mapping(d["block_tables"], d["context_lens"], 16, w.cfg.q_len)
+        pa.pa_append_kv(d["k_cache"], d["v_cache"], d["k_new"], d["v_new"], slots)
+        pa.pa_decode_cascade(out, d["q"], d["k_cache"], d["v_cache"], d["block_tables"],
+                             d["context_lens"], w.scale, P, q_len=w.cfg.q_len,
+                             tail_splits=tail_splits)
+    torch.cuda.synchronize()
+    assert pa.pa_device_error() == 0
+    return out, d
+
+
+CASCADE_SMALL = [
+    ("prefix_verify", {"num_seqs": 4}),
+    ("prefix_verify", {"num_seqs": 3, "q_len": 40, "lens": ("prefix", 1024, 64, 300)}),
+    ("prefix_verify", {"num_seqs": 5, "q_len": 1, "num_q_heads": 8, "num_kv_heads": 8,
+                       "head_dim": 64, "dtype": "bf16", "shared_prefix": 48,
+                       "lens": ("prefix", 48, 1, 100)}),
+]
+
+
+@pytest.mark.parametrize("tail_splits", [1, 3])
+@pytest.mark.parametrize("fused", [False, True], ids=["separate", "fused"])
+@pytest.mark.parametrize("case", range(len(CASCADE_SMALL)))
+def test_cascade_every_element(pa, orc, case, fused, tail_splits):
+    name, over = CASCADE_SMALL[case]
+    w = workloads.make(name, **over)
+    out, d = gpu_cascade(pa, w, tail_splits=tail_splits, fused=fused)
+    ref, kc, vc, _ = oracle_step(orc, w)
+    assert np.array_equal(_u16(d["k_cache"]), kc)
+    assert np.array_equal(_u16(d["v_cache"]), vc)
+    _tol.check(_f64(out), ref, w.cfg.dtype, f"cascade {case}")
+
+
+def test_cascade_full_size_sampled_rows(pa, orc):
+    """prefix_verify at full size, in the launch configuration bench.py times."""
+    w = workloads.make("prefix_verify")
+    out, d = gpu_cascade(pa, w)
+    n_rows = w.cfg.num_seqs * w.cfg.q_len * w.cfg.num_q_heads
+    rows = np.sort(np.random.default_rng(3).choice(n_rows, size=64, replace=False))
+    ref, kc, vc, _ = oracle_step(orc, w, rows=rows)
+    _tol.check(_f64(out).reshape(n_rows, -1)[rows], ref, w.cfg.dtype, "cascade full")
+    assert np.array_equal(_u16(d["k_cache"]), kc)
+    assert np.array_equal(_u16(d["v_cache"]), vc)
+
+
+def test_cascade_equals_plain_decode_closely(pa):
+    """Same inputs through pa_append_decode and pa_decode_cascade: both are the same
+    attention, so they agree to a few output ulps."""
+    w = workloads.make("prefix_verify", num_seqs=16)
+    plain, _ = gpu_step(pa, w, fused=True)
+    casc, _ = gpu_cascade(pa, w)
+    diff = (plain.double() - casc.double()).abs().max().item()
+    assert diff <= 2e-3, diff

@@ -19,6 +19,9 @@ Workloads (shapes from the configurations the library is measured on):
   prefix_verify   128 seqs sharing a 1024-token prefix (the same 64 physical
                   blocks), private tails of U[64, 2048] tokens, 4 causal query
                   positions per seq, 32 q / 8 KV heads, head_dim 128, fp16
+  chunked_prefill 16 seqs, each appending a chunk of 512 new tokens (8192 tokens a
+                  step) at the end of a context uniform in [512, 8192], causal;
+                  32 q / 8 KV heads, head_dim 128, bf16
   llama7b_mha_fp8, gqa_fp8
                   the same shapes over an FP8 (e4m3) cache with one scale per KV
                   head (K and V separately, drawn in [0.02, 0.05]); q and the new
@@ -85,6 +88,8 @@ CONFIGS: dict[str, Config] = {
                          lens=("fixed", (32768,) * 4), num_splits=16),
     "prefix_verify": Config("prefix_verify", 128, 32, 8, 128, 16, "fp16", q_len=4,
                             lens=("prefix", 1024, 64, 2048), shared_prefix=1024),
+    "chunked_prefill": Config("chunked_prefill", 16, 32, 8, 128, 16, "bf16", q_len=512,
+                              lens=("uniform", 512, 8192)),
     # the same shapes over an FP8 (e4m3) cache, q and new rows in the 16-bit type
     "llama7b_mha_fp8": Config("llama7b_mha_fp8", 32, 32, 32, 128, 16, "fp16",
                               lens=("uniform", 512, 4096), kv_fp8=True),
