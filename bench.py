@@ -545,6 +545,9 @@ def run_ours(args):
         "other_configs": others,
         "kernel_src_sha": kernel_source_sha(),
     }
+    for extra in ("cascade", "tensor_roofline"):
+        if extra in r:
+            line[extra] = r[extra]
     print(json.dumps(line))
 
 

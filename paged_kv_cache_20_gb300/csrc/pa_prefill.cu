@@ -1,23 +1,21 @@
 // pa_prefill.cu -- host launchers of the many-row (chunked-prefill / shared-prefix)
-// kernel, both element types.
+// tensor-core kernel, both element types.
 #include <atomic>
 
 #include "pa_launch.h"
-#include "pa_prefill.cuh"
+#include "pa_prefill_tc.cuh"
 
 namespace pa {
 
 namespace {
 
-constexpr int kPrefillWarps = 4;   // consumer warps: 64 query rows per CTA
-constexpr int kPrefillStages = 4;  // K/V tile pairs in flight per CTA
+constexpr int kTcStages = 5;  // chunks in flight per CTA in each of the K and V rings
 
 template <typename T, int D, bool PARTIAL>
 cudaError_t launch_prefill_t(const CUtensorMap &kmap, const CUtensorMap &vmap, const DecodeArgs &a,
                              cudaStream_t st) {
-  constexpr int kRows = 16 * kPrefillWarps;
-  constexpr int kSmem = kPrefillStages * 2 * kTileTokens * D * 2 + 1024;
-  auto kern = paged_prefill_kernel<T, D, kPrefillWarps, kPrefillStages, PARTIAL>;
+  constexpr int kSmem = TcLayout<T, D>::smem_bytes(kTcStages);
+  auto kern = paged_prefill_tc_kernel<T, D, kTcStages, PARTIAL>;
   static std::atomic<unsigned long long> opted{0};  // bit per device: smem opt-in done
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -31,12 +29,12 @@ cudaError_t launch_prefill_t(const CUtensorMap &kmap, const CUtensorMap &vmap, c
   const long long rows_per_seq = (long long)a.q_len * a.group;
   const long long rows = a.shared_prefix > 0 ? rows_per_seq * a.num_seqs : rows_per_seq;
   const long long nz = a.shared_prefix > 0 ? a.num_splits : (long long)a.num_seqs * a.num_splits;
-  const long long gx = (rows + kRows - 1) / kRows * nz;
+  const long long gx = (rows + kTcTiles * kTcRows - 1) / (kTcTiles * kTcRows) * nz;
   if (gx <= 0) return cudaSuccess;
   if (gx > 0x7fffffffLL || a.num_kv_heads > 65535) return cudaErrorInvalidConfiguration;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)gx, (unsigned)a.num_kv_heads, 1);
-  cfg.blockDim = dim3((kPrefillWarps + 1) * 32, 1, 1);
+  cfg.blockDim = dim3(kTcThreads, 1, 1);
   cfg.dynamicSmemBytes = kSmem;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];

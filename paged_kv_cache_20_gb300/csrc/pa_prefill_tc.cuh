@@ -1,0 +1,549 @@
+// pa_prefill_tc.cuh -- paged attention for many query rows per KV head on the
+// 5th-generation tensor cores: chunked prefill (q_len new tokens of a sequence,
+// causal) and the shared-prefix pass of cascade attention (the query rows of every
+// sequence against prefix blocks that all sequences share).
+//
+// What is computed is the attention of pa_decode: softmax(scale q K^T) V over each
+// row's visible positions ("LLM 推理优化全景实战" §2.4; the causal offset of
+// "09-inference-optimization.md", AttentionWithKVCache.forward), accumulated with
+// online softmax ("推理机制动态图解（进阶）" §5: running max, running sum, output
+// rescaled when the max moves, divided by the sum at the end).  Chunked prefill is
+// "LLM推理与服务：面试问题与推荐回答" Q14; one physical copy of a shared prefix is
+// Q2-Q3 of the same page and "Scaling Book 入门第 11 章" §11.4.
+//
+// One CTA = one KV head x two tiles of 128 query rows (the MMA's M) that share
+// every K/V chunk; the cache is walked in chunks of 64 positions (4 blocks):
+//   warps 0, 1  TMA producers: the K (warp 0) and V (warp 1) tiles of a chunk's 4
+//               blocks into rings of NS stages each (zero fill for blocks past the
+//               walk or bad ids).  A K stage is released as soon as the S MMAs that
+//               read it complete, a V stage after P V: K runs several chunks ahead;
+//   warp 2      owns tensor memory and issues the MMAs from one thread: for each
+//               tile, S_j = Q K_j^T into one of two S accumulators (fp32, TMEM),
+//               then O += P_j V_j into the tile's O accumulator (fp32, TMEM) with
+//               P_j read from tensor memory;
+//   warps 3-10  softmax, 4 warps per tile, one thread per query row (TMEM lane):
+//               read S_j, mask, online-softmax update, write P_j (16-bit) over the
+//               S_j columns it came from, rescale O in TMEM when the row max has
+//               grown by more than 2^8 since the last rescale (until then P is taken
+//               against the older max, at most 2^8, and the final O / l is the same
+//               quotient); at the end O / l (or the partial statistics).
+// The tensor core executes one thread's MMAs in issue order, so S_{j+2} (issued
+// after P_j V_j) never overwrites P_j before it is read.
+// Each SM sub-partition runs two softmax warps (one per tile), which hide each
+// other's latency while the tensor core works on the other tile.  bf16 P is split
+// into hi + lo bf16 parts, both multiplied by V, so that P keeps ~16 significant
+// bits as the fp16 path does.  Every wait is bounded.
+#pragma once
+
+#include "pa_decode.cuh"
+#include "pa_tc.cuh"
+
+namespace pa {
+
+constexpr int kTcRows = 128;                       // query rows per tile (MMA M)
+constexpr int kTcTiles = 2;                        // tiles per CTA
+constexpr int kTcChunk = 64;                       // positions per chunk
+constexpr int kTcBlocks = kTcChunk / kTileTokens;  // cache blocks per chunk
+constexpr int kTcCtl = 3;                          // K producer, V producer, MMA warps
+constexpr int kTcThreads = 32 * kTcCtl + kTcTiles * 128;
+constexpr float kTcRescale = 8.f;                  // base-2 growth that forces a rescale
+
+template <typename T, int D>
+struct TcLayout {
+  static constexpr int kHalves = D / 64;           // 128-byte column groups of a row
+  static constexpr bool kSplitP = Elt<T>::kMantBits < 10;
+  static constexpr int kQBytes = kHalves * kTcRows * 128;    // per tile: [half][128 rows][128 B]
+  static constexpr int kKVBytes = kHalves * kTcChunk * 128;  // [half][64 positions][128 B]
+  static constexpr int kOffStages = kTcTiles * kQBytes;      // K ring, then V ring
+  // per tile 256 columns: O at [0, D), S buffers at [128, 192) and [192, 256); P_j
+  // (packed 16-bit pairs) replaces S_j: hi in the buffer's first 32 columns, lo
+  // (bf16 only) in the next 32
+  static constexpr int kTmemCols = 256 * kTcTiles;
+  static constexpr int kColS = 128;
+  static constexpr int smem_bytes(int ns) { return kOffStages + 2 * ns * kKVBytes + 1024; }
+};
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+// 2^x (PTX ex2.approx, flushing subnormal results to zero: a weight below 2^-126
+// of the row maximum contributes nothing at fp32 accumulation anyway)
+__device__ __forceinline__ float ex2_ftz(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+template <typename T, int D, int NS, bool PARTIAL>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
+                            const __grid_constant__ CUtensorMap vmap, const DecodeArgs a) {
+  using Lay = TcLayout<T, D>;
+  constexpr int H = Lay::kHalves;
+  constexpr bool kBf16 = Elt<T>::kMantBits < 10;
+  constexpr int kRowsCta = kTcTiles * kTcRows;
+  static_assert(NS >= 2, "ring depth");
+  static_assert(D == 64 || D == 128, "head_dim");
+
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t k_full[NS];
+  __shared__ __align__(8) uint64_t k_empty[NS];
+  __shared__ __align__(8) uint64_t v_full[NS];
+  __shared__ __align__(8) uint64_t v_empty[NS];
+  __shared__ __align__(8) uint64_t s_full[kTcTiles][2];
+  __shared__ __align__(8) uint64_t p_full[kTcTiles];
+  __shared__ __align__(8) uint64_t o_done[kTcTiles];
+  __shared__ __align__(8) uint64_t q_ready;
+  __shared__ __align__(8) uint64_t mma_fin;
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_failed;
+  __shared__ int s_maxlim;
+
+  griddep_wait();
+  griddep_launch_dependents();
+
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  const uint32_t sK = base + Lay::kOffStages;          // K ring: NS x kKVBytes
+  const uint32_t sV = sK + NS * Lay::kKVBytes;          // V ring
+
+  // ---- the unit: grid.x = (sequence, partition, row block), row block fastest ----
+  const bool shared = a.shared_prefix > 0;
+  const int kvh = blockIdx.y;
+  const int rows_per_seq = a.q_len * a.group;
+  const int rows_total = shared ? a.num_seqs * rows_per_seq : rows_per_seq;
+  const int nrb = (rows_total + kRowsCta - 1) / kRowsCta;
+  const int zz = blockIdx.x / nrb;
+  const int split = zz % a.num_splits;
+  const int zseq = zz / a.num_splits;
+  // the last row blocks see the most positions (causal): they are scheduled first
+  const int row_base = (nrb - 1 - (int)(blockIdx.x % nrb)) * kRowsCta;
+  const int tseq = shared ? 0 : zseq;  // block-table row that is walked
+  // tiles holding at least one real row
+  const int ntile = min(kTcTiles, (rows_total - row_base + kTcRows - 1) / kTcRows);
+
+  int nb;
+  const int Lt = max(0, __ldg(a.context_lens + tseq));
+  if (shared) {
+    nb = min(a.shared_prefix, a.max_blocks_per_seq);
+  } else {
+    nb = (Lt + kTileTokens - 1) / kTileTokens;
+    if (nb > a.max_blocks_per_seq) {
+      if (threadIdx.x == 0 && kvh == 0) record_error(a.err, kErrCheck);
+      nb = a.max_blocks_per_seq;
+    }
+  }
+  // blocks before first_block belong to another pass (a cascade's shared prefix);
+  // the rest is cut into num_splits equal partitions
+  const int fb = shared ? 0 : min(nb, a.first_block);
+  const int per = (nb - fb + a.num_splits - 1) / a.num_splits;
+  const int tb = min(nb, fb + split * per);
+  const int te = min(nb, tb + per);
+
+  if (threadIdx.x == 0) {
+    s_failed = 0;
+    s_maxlim = 0;
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(smem_u32(&k_full[s]), 1);
+      mbar_init(smem_u32(&k_empty[s]), 1);
+      mbar_init(smem_u32(&v_full[s]), 1);
+      mbar_init(smem_u32(&v_empty[s]), 1);
+    }
+    for (int t = 0; t < kTcTiles; ++t) {
+      for (int b = 0; b < 2; ++b) mbar_init(smem_u32(&s_full[t][b]), 1);
+      mbar_init(smem_u32(&p_full[t]), 4);
+      mbar_init(smem_u32(&o_done[t]), 1);
+    }
+    mbar_init(smem_u32(&q_ready), 4 * kTcTiles);
+    mbar_init(smem_u32(&mma_fin), 1);
+    fence_mbar_init();
+    prefetch_tensormap(&kmap);
+    prefetch_tensormap(&vmap);
+  }
+  if (warp == 2) {
+    tc::alloc(smem_u32(&s_tmem), Lay::kTmemCols);
+    tc::relinquish();
+  }
+  __syncthreads();  // s_maxlim, barriers initialised
+
+  // ---- this thread's query row (softmax warps): tile t, row = TMEM lane ----
+  const bool sm_warp = warp >= kTcCtl;
+  const int tile = sm_warp ? (warp - kTcCtl) >> 2 : 0;
+  const int row = 32 * (warp & 3) + lane;
+  const T *qrow = nullptr;
+  int lim = 0, rseq = 0, ru = 0, rh = 0;
+  if (sm_warp) {
+    const int rho = row_base + tile * kTcRows + row;
+    if (rho < rows_total) {
+      const int sq = shared ? rho / rows_per_seq : zseq;
+      const int rr = rho % rows_per_seq;
+      const int u = rr / a.group, h = kvh * a.group + rr % a.group;
+      const int L = max(0, __ldg(a.context_lens + sq));
+      int visible = L - a.q_len + u + 1;  // causal limit
+      if (shared) visible = min(visible, nb * kTileTokens);
+      rseq = sq;
+      ru = u;
+      rh = h;
+      lim = visible;
+      qrow = static_cast<const T *>(a.q) + ((size_t)(sq * a.q_len + u) * a.num_q_heads + h) * D;
+      atomicMax(&s_maxlim, visible);
+    }
+  }
+  tc::fence_before();
+  __syncthreads();
+  tc::fence_after();
+  const uint32_t tmem = s_tmem;
+  // blocks any row of this CTA can see, and the chunks covering them
+  const int t_end = min(te, max(tb, (s_maxlim + kTileTokens - 1) / kTileTokens));
+  const int nch = (t_end - tb + kTcBlocks - 1) / kTcBlocks;
+  const int vis_end = min(te * kTileTokens, s_maxlim);  // no row uses a position past it
+  volatile int *failed = &s_failed;
+
+  if (warp < 2) {
+    // ------------------------------------------------------------ TMA producers
+    const bool is_k = warp == 0;
+    const CUtensorMap *map = is_k ? &kmap : &vmap;
+    const uint32_t ring = is_k ? sK : sV;
+    uint64_t *full = is_k ? k_full : v_full;
+    uint64_t *empty = is_k ? k_empty : v_empty;
+    const int32_t *table = a.block_tables + (size_t)tseq * a.max_blocks_per_seq;
+    int issued = 0;
+    bool ok = true;
+    for (int ch = 0; ch < nch; ++ch) {
+      const int s = ch % NS;
+      // a fresh barrier counts as released (parity 1 of the phase before the first)
+      bool fr = mbar_wait_bounded(smem_u32(&empty[s]), ((ch / NS) & 1) ^ 1);
+      fr = __all_sync(0xffffffffu, fr);
+      if (!fr || *failed) {
+        ok = fr;
+        break;
+      }
+      const int blk = tb + ch * kTcBlocks + lane;
+      int z = -1;  // outside the tensor map: zero fill
+      if (lane < kTcBlocks && blk < t_end) {
+        const int phys = __ldg(table + blk);
+        if (phys >= 0 && phys < a.num_blocks)
+          z = phys * a.num_kv_heads + kvh;
+        else if (is_k)
+          record_error(a.err, kErrCheck);
+      }
+      const uint32_t bar = smem_u32(&full[s]);
+      if (lane == 0) mbar_arrive_expect_tx(bar, Lay::kKVBytes);
+      __syncwarp();
+      if (lane < kTcBlocks) {
+        const uint32_t dst = ring + s * Lay::kKVBytes + lane * (kTileTokens * 128);
+#pragma unroll
+        for (int hh = 0; hh < H; ++hh) tma_load_3d(dst + hh * (kTcChunk * 128), map, hh * 64, 0, z, bar);
+      }
+      issued = ch + 1;
+    }
+    if (!ok && lane == 0) {
+      record_error(a.err, kErrTimeout);
+      atomicExch(&s_failed, 1);
+    }
+    if (*failed) {
+      // the loads still in flight land before the CTA may exit (bounded)
+      for (int k = max(0, issued - NS); k < issued; ++k)
+        (void)mbar_wait_bounded(smem_u32(&full[k % NS]), (k / NS) & 1);
+    }
+  } else if (warp == 2) {
+    // ------------------------------------------------------------ MMA issue
+    constexpr uint32_t kIdS = tc::idesc_f16(kTcRows, kTcChunk, kBf16, false);
+    constexpr uint32_t kIdO = tc::idesc_f16(kTcRows, D, kBf16, true);
+    // descriptors of the first stage / tile; the others differ only in the start
+    // address field (bits 0-13, address / 16), so an offset is a plain addition
+    const uint64_t dQ = tc::sdesc_sw128(base, 16, 1024);
+    const uint64_t dK = tc::sdesc_sw128(sK, 16, 1024);
+    const uint64_t dV = tc::sdesc_sw128(sV, kTcChunk * 128, 1024);
+    bool ok = true;
+    if (nch > 0) {
+      ok = mbar_wait_bounded(smem_u32(&q_ready), 0);
+      ok = __all_sync(0xffffffffu, ok);
+    }
+    // S_j = Q K_j^T of every tile, into S buffer j % 2 (free: P_{j-2} V_{j-2}, the
+    // last reader of that buffer, was issued before)
+    auto issue_s = [&](int j) -> bool {
+      const int s = j % NS, b = j & 1;
+      bool w = mbar_wait_bounded(smem_u32(&k_full[s]), (j / NS) & 1);
+      w = __all_sync(0xffffffffu, w);
+      if (!w || *failed) return false;
+      tc::fence_after();
+      if (lane == 0) {
+        const uint64_t kd = dK + (uint64_t)((s * Lay::kKVBytes) >> 4);
+        for (int t = 0; t < ntile; ++t) {
+          const uint64_t qd = dQ + (uint64_t)((t * Lay::kQBytes) >> 4);
+          const uint32_t dst = tmem + t * 256 + Lay::kColS + kTcChunk * b;
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            // a K step of 16 columns: +32 bytes inside the 128-byte row, +one
+            // column-group block every 4 steps (descriptor addresses count 16 bytes)
+            tc::mma_f16(dst, qd + (uint64_t)(((kk >> 2) * (kTcRows * 128) + (kk & 3) * 32) >> 4),
+                        kd + (uint64_t)(((kk >> 2) * (kTcChunk * 128) + (kk & 3) * 32) >> 4), kIdS,
+                        kk > 0 ? 1u : 0u);
+          }
+          tc::commit(smem_u32(&s_full[t][b]));
+        }
+        tc::commit(smem_u32(&k_empty[s]));  // K chunk j is no longer read
+      }
+      __syncwarp();
+      return true;
+    };
+    // O_t += P_t,j V_j of every tile, P from tensor memory; the V stage is released
+    // after the last
+    auto issue_pv = [&](int j) -> bool {
+      const int s = j % NS, b = j & 1;
+      {
+        bool w = mbar_wait_bounded(smem_u32(&v_full[s]), (j / NS) & 1);
+        w = __all_sync(0xffffffffu, w);
+        if (!w || *failed) return false;
+      }
+      const uint64_t vd = dV + (uint64_t)((s * Lay::kKVBytes) >> 4);
+      for (int t = 0; t < ntile; ++t) {
+        bool w = mbar_wait_bounded(smem_u32(&p_full[t]), j & 1);
+        w = __all_sync(0xffffffffu, w);
+        if (!w || *failed) return false;
+        tc::fence_after();
+        if (lane == 0) {
+          const uint32_t pa = tmem + t * 256 + Lay::kColS + kTcChunk * b;
+#pragma unroll
+          for (int kk = 0; kk < kTcChunk / 16; ++kk) {
+            // V is N-major (head_dim contiguous): atoms of 64 columns kTcChunk*128
+            // bytes apart (the descriptor's leading offset), groups of 8 positions
+            // 1024 bytes apart; a K step of 16 positions is 2048 bytes of V and 8
+            // tensor-memory columns of P
+            const uint64_t bd = vd + (uint64_t)((kk * (16 * 128)) >> 4);
+            tc::mma_f16_ts(tmem + t * 256, pa + kk * 8, bd, kIdO, (j > 0 || kk > 0) ? 1u : 0u);
+            if (Lay::kSplitP) tc::mma_f16_ts(tmem + t * 256, pa + 32 + kk * 8, bd, kIdO, 1u);
+          }
+          tc::commit(smem_u32(&o_done[t]));
+          if (t == ntile - 1) tc::commit(smem_u32(&v_empty[s]));
+        }
+        __syncwarp();
+      }
+      return true;
+    };
+    if (ok && nch > 0) ok = issue_s(0);
+    if (ok && nch > 1) ok = issue_s(1);
+    for (int j = 0; ok && j < nch; ++j) {
+      ok = issue_pv(j);
+      if (ok && j + 2 < nch) ok = issue_s(j + 2);
+    }
+    if (!ok && lane == 0) {
+      record_error(a.err, kErrTimeout);
+      atomicExch(&s_failed, 1);
+    }
+    // every MMA issued has completed before tensor memory is released
+    if (lane == 0) tc::commit(smem_u32(&mma_fin));
+    __syncwarp();
+    (void)mbar_wait_bounded(smem_u32(&mma_fin), 0);
+  } else {
+    // ------------------------------------------------------------ softmax rows
+    const uint32_t trow = tmem + tile * 256 + ((uint32_t)(32 * (warp & 3)) << 16);
+    const uint32_t sQ = base + tile * Lay::kQBytes;
+    // Q row -> shared memory in the swizzled K-major layout of the MMA's A operand
+#pragma unroll
+    for (int c = 0; c < D / 8; ++c) {
+      uint4 v = make_uint4(0u, 0u, 0u, 0u);
+      if (qrow) v = __ldg(reinterpret_cast<const uint4 *>(qrow) + c);
+      const int hh = c >> 3, cc = c & 7;
+      const uint32_t addr = sQ + hh * (kTcRows * 128) + row * 128 + ((cc ^ (row & 7)) << 4);
+      asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y),
+                   "r"(v.z), "r"(v.w)
+                   : "memory");
+    }
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(&q_ready));
+
+    const bool active = tile < ntile;  // a tile of padding rows only: no MMA, no softmax
+    const int my_nch = active ? nch : 0;
+    const float rs = a.scale_log2;
+    const int lim_row = min(lim, te * kTileTokens);  // padding rows: 0
+    float m_run = -INFINITY, l = 0.f;
+    bool ok = true;
+    const int tid = ((warp - kTcCtl) & 3) * 32 + lane;  // 0..127 within the tile
+    for (int j = 0; j < my_nch; ++j) {
+      const int b = j & 1;
+      bool w = mbar_wait_bounded(smem_u32(&s_full[tile][b]), (j >> 1) & 1);
+      w = __all_sync(0xffffffffu, w);
+      if (!w) {
+        ok = false;
+        break;
+      }
+      tc::fence_after();
+      float sv[kTcChunk];
+      tc::ld64(trow + Lay::kColS + kTcChunk * b, sv);
+
+      const int c0 = (tb + j * kTcBlocks) * kTileTokens;
+      // scale to base-2 units and mask; the row max as a tree of 8 partial maxima
+      if (c0 + kTcChunk <= lim_row) {
+#pragma unroll
+        for (int c = 0; c < kTcChunk; ++c) sv[c] *= rs;
+      } else {
+#pragma unroll
+        for (int c = 0; c < kTcChunk; ++c) sv[c] = (c0 + c < lim_row) ? sv[c] * rs : -INFINITY;
+      }
+      float pm[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) pm[i] = sv[i];
+#pragma unroll
+      for (int c = 8; c < kTcChunk; ++c) pm[c & 7] = fmaxf(pm[c & 7], sv[c]);
+      const float mx = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])),
+                             fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7])));
+      const float m_new = fmaxf(m_run, mx);
+      const bool need = m_new > m_run + kTcRescale;  // false while both are -inf
+      const float f = need ? ex2_ftz(m_run - m_new) : 1.f;  // 0 when m_run = -inf
+      if (need) {
+        l *= f;
+        m_run = m_new;
+      }
+      // P_j over the S_j columns (the exponentials overlap the tensor core's
+      // P_{j-1} V_{j-1})
+      const float mb = (m_run == -INFINITY) ? 0.f : m_run;
+      float ps[4] = {0.f, 0.f, 0.f, 0.f};
+      {
+        uint32_t hw[kTcChunk / 2];
+#pragma unroll
+        for (int e = 0; e < kTcChunk / 2; ++e) {
+          const float p0 = ex2_ftz(sv[2 * e] - mb);
+          const float p1 = ex2_ftz(sv[2 * e + 1] - mb);
+          if constexpr (Lay::kSplitP) {
+            // hi = p truncated to bf16 (exact); lo = the remainder, rounded, kept in sv
+            const uint32_t u0 = __float_as_uint(p0), u1 = __float_as_uint(p1);
+            hw[e] = __byte_perm(u0, u1, 0x7632);
+            sv[2 * e] = p0 - __uint_as_float(u0 & 0xffff0000u);
+            sv[2 * e + 1] = p1 - __uint_as_float(u1 & 0xffff0000u);
+            ps[e & 3] += p0 + p1;
+          } else {
+            hw[e] = Elt<T>::from_f2(p0, p1);
+            // the sum of the rounded weights P V is taken with: the quotient O / l
+            // is then an exact convex combination of V rows (a dominant weight's
+            // rounding cancels)
+            const float2 hf = Elt<T>::to_f2(hw[e]);
+            ps[e & 3] += hf.x + hf.y;
+          }
+        }
+        tc::st32u(trow + Lay::kColS + kTcChunk * b, hw);
+      }
+      if constexpr (Lay::kSplitP) {
+        uint32_t lw[kTcChunk / 2];
+#pragma unroll
+        for (int e = 0; e < kTcChunk / 2; ++e) lw[e] = Elt<T>::from_f2(sv[2 * e], sv[2 * e + 1]);
+        tc::st32u(trow + Lay::kColS + kTcChunk * b + 32, lw);
+      }
+      l += (ps[0] + ps[1]) + (ps[2] + ps[3]);
+      // P_{j-1} V_{j-1} complete before P_j is announced: O may be rescaled below,
+      // and the MMA thread has taken P_{j-1} before this barrier moves again
+      if (j > 0) {
+        w = mbar_wait_bounded(smem_u32(&o_done[tile]), (j - 1) & 1);
+        w = __all_sync(0xffffffffu, w);
+        if (!w) {
+          ok = false;
+          break;
+        }
+        tc::fence_after();
+        if (__any_sync(0xffffffffu, need)) {
+#pragma unroll
+          for (int q = 0; q < D / 32; ++q) {
+            float o[32];
+            tc::ld32(trow + 32 * q, o);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] *= f;
+            tc::st32(trow + 32 * q, o);
+          }
+        }
+      }
+      if (c0 + kTcChunk > vis_end) {
+        // V rows at or past vis_end may be unused slots holding anything; P is 0
+        // there but 0 * NaN is not 0, so they become zeros before P V (each tile
+        // writes the same zeros before its own P V)
+        const int s = j % NS;
+        w = mbar_wait_bounded(smem_u32(&v_full[s]), (j / NS) & 1);
+        w = __all_sync(0xffffffffu, w);
+        if (!w) {
+          ok = false;
+          break;
+        }
+        const int first = max(0, vis_end - c0);
+        const uint32_t vb = sV + s * Lay::kKVBytes;
+        for (int idx = tid; idx < (kTcChunk - first) * H * 8; idx += kTcRows) {
+          const int r = first + idx / (H * 8), rem = idx % (H * 8);
+          const int hh = rem >> 3, cc = rem & 7;
+          sts128_zero(vb + hh * (kTcChunk * 128) + r * 128 + ((cc ^ (r & 7)) << 4));
+        }
+        fence_proxy_async_smem();  // the zeros visible to the tensor core
+      }
+      tc::st_wait();        // P_j (and a rescaled O) are in tensor memory
+      tc::fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&p_full[tile]));
+    }
+    if (!ok && lane == 0) {
+      record_error(a.err, kErrTimeout);
+      atomicExch(&s_failed, 1);
+    }
+    // ---- epilogue: O / l, or the unnormalised partial with its statistics ----
+    bool have = ok && my_nch > 0;
+    if (have) {
+      bool w = mbar_wait_bounded(smem_u32(&o_done[tile]), (my_nch - 1) & 1);
+      w = __all_sync(0xffffffffu, w);
+      if (!w) {
+        have = false;
+        ok = false;
+        if (lane == 0) {
+          record_error(a.err, kErrTimeout);
+          atomicExch(&s_failed, 1);
+        }
+      } else {
+        tc::fence_after();
+      }
+    }
+    const bool write = ok && qrow != nullptr;
+    const float inv = l > 0.f ? 1.f / l : 0.f;
+    size_t wrow = 0;
+    if (PARTIAL)
+      wrow = ((size_t)rseq * a.ws_splits + a.ws_split0 + split) * (a.q_len * a.num_q_heads) +
+             (size_t)ru * a.num_q_heads + rh;
+    const size_t orow = (size_t)(rseq * a.q_len + ru) * a.num_q_heads + rh;
+#pragma unroll
+    for (int q = 0; q < D / 32; ++q) {
+      float o[32];
+      if (have) {
+        tc::ld32(trow + 32 * q, o);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) o[i] = 0.f;
+      }
+      if (!write) continue;
+      if constexpr (PARTIAL) {
+        float4 *dst = reinterpret_cast<float4 *>(a.ws_acc + wrow * D + 32 * q);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) dst[i] = make_float4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+      } else {
+        uint4 *dst = reinterpret_cast<uint4 *>(static_cast<T *>(a.out) + orow * D + 32 * q);
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          dst[i] = make_uint4(Elt<T>::from_f2(o[8 * i] * inv, o[8 * i + 1] * inv),
+                              Elt<T>::from_f2(o[8 * i + 2] * inv, o[8 * i + 3] * inv),
+                              Elt<T>::from_f2(o[8 * i + 4] * inv, o[8 * i + 5] * inv),
+                              Elt<T>::from_f2(o[8 * i + 6] * inv, o[8 * i + 7] * inv));
+      }
+    }
+    if (PARTIAL && write) {
+      a.ws_m[wrow] = have ? m_run : -INFINITY;
+      a.ws_l[wrow] = have ? l : 0.f;
+    }
+  }
+
+  // ---- teardown: every tensor-memory access is complete; release it ----
+  tc::fence_before();
+  __syncthreads();
+  if (warp == 2) {
+    tc::fence_after();
+    tc::dealloc(tmem, Lay::kTmemCols);
+  }
+}
+
+}  // namespace pa
