@@ -9,7 +9,7 @@ namespace pa {
 
 namespace {
 
-constexpr int kTcStages = 5;  // chunks in flight per CTA in each of the K and V rings
+constexpr int kTcStages = 2;  // chunks in flight per CTA in each of the K and V rings
 
 template <typename T, int D, bool PARTIAL>
 cudaError_t launch_prefill_t(const CUtensorMap &kmap, const CUtensorMap &vmap, const DecodeArgs &a,

@@ -12,27 +12,28 @@
 // Q2-Q3 of the same page and "Scaling Book 入门第 11 章" §11.4.
 //
 // One CTA = one KV head x two tiles of 128 query rows (the MMA's M) that share
-// every K/V chunk; the cache is walked in chunks of 64 positions (4 blocks):
-//   warps 0, 1  TMA producers: the K (warp 0) and V (warp 1) tiles of a chunk's 4
+// every K/V chunk; the cache is walked in chunks of 128 positions (8 blocks):
+//   warps 0, 1  TMA producers: the K (warp 0) and V (warp 1) tiles of a chunk's 8
 //               blocks into rings of NS stages each (zero fill for blocks past the
 //               walk or bad ids).  A K stage is released as soon as the S MMAs that
-//               read it complete, a V stage after P V: K runs several chunks ahead;
-//   warp 2      owns tensor memory and issues the MMAs from one thread: for each
-//               tile, S_j = Q K_j^T into one of two S accumulators (fp32, TMEM),
-//               then O += P_j V_j into the tile's O accumulator (fp32, TMEM) with
-//               P_j read from tensor memory;
+//               read it complete, a V stage after P V;
+//   warp 2      owns tensor memory and issues the MMAs from one thread.  Per tile
+//               and chunk j: O += P_j V_j (P_j read from tensor memory), then
+//               S_{j+1} = Q K_{j+1}^T into the same columns P_j occupied; the two
+//               tiles alternate, so the tensor core works on one tile while the
+//               other tile's softmax runs;
 //   warps 3-10  softmax, 4 warps per tile, one thread per query row (TMEM lane):
 //               read S_j, mask, online-softmax update, write P_j (16-bit) over the
 //               S_j columns it came from, rescale O in TMEM when the row max has
 //               grown by more than 2^8 since the last rescale (until then P is taken
 //               against the older max, at most 2^8, and the final O / l is the same
 //               quotient); at the end O / l (or the partial statistics).
-// The tensor core executes one thread's MMAs in issue order, so S_{j+2} (issued
-// after P_j V_j) never overwrites P_j before it is read.
-// Each SM sub-partition runs two softmax warps (one per tile), which hide each
-// other's latency while the tensor core works on the other tile.  bf16 P is split
-// into hi + lo bf16 parts, both multiplied by V, so that P keeps ~16 significant
-// bits as the fp16 path does.  Every wait is bounded.
+// The tensor core executes one thread's MMAs in issue order, and a commit fires
+// only once every earlier MMA has completed: S_{j+1} never overwrites P_j before
+// P_j V_j has read it, and when S_{j+1} is complete so is P_j V_j (O may be
+// rescaled then).  bf16 P is split into hi + lo bf16 parts, both multiplied by V,
+// so that P keeps ~16 significant bits as the fp16 path does.  Every wait is
+// bounded.
 #pragma once
 
 #include "pa_decode.cuh"
@@ -42,7 +43,7 @@ namespace pa {
 
 constexpr int kTcRows = 128;                       // query rows per tile (MMA M)
 constexpr int kTcTiles = 2;                        // tiles per CTA
-constexpr int kTcChunk = 64;                       // positions per chunk
+constexpr int kTcChunk = 128;                      // positions per chunk (S MMA N)
 constexpr int kTcBlocks = kTcChunk / kTileTokens;  // cache blocks per chunk
 constexpr int kTcCtl = 3;                          // K producer, V producer, MMA warps
 constexpr int kTcThreads = 32 * kTcCtl + kTcTiles * 128;
@@ -53,11 +54,11 @@ struct TcLayout {
   static constexpr int kHalves = D / 64;           // 128-byte column groups of a row
   static constexpr bool kSplitP = Elt<T>::kMantBits < 10;
   static constexpr int kQBytes = kHalves * kTcRows * 128;    // per tile: [half][128 rows][128 B]
-  static constexpr int kKVBytes = kHalves * kTcChunk * 128;  // [half][64 positions][128 B]
+  static constexpr int kKVBytes = kHalves * kTcChunk * 128;  // [half][128 positions][128 B]
   static constexpr int kOffStages = kTcTiles * kQBytes;      // K ring, then V ring
-  // per tile 256 columns: O at [0, D), S buffers at [128, 192) and [192, 256); P_j
-  // (packed 16-bit pairs) replaces S_j: hi in the buffer's first 32 columns, lo
-  // (bf16 only) in the next 32
+  // per tile 256 columns: O at [0, D), S at [128, 256).  P_j (packed 16-bit pairs)
+  // replaces S_j half by half: positions [64h, 64h + 64) in columns 128 + 64h +
+  // [0, 32) (hi) and [32, 64) (lo, bf16 only)
   static constexpr int kTmemCols = 256 * kTcTiles;
   static constexpr int kColS = 128;
   static constexpr int smem_bytes(int ns) { return kOffStages + 2 * ns * kKVBytes + 1024; }
@@ -91,7 +92,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   __shared__ __align__(8) uint64_t k_empty[NS];
   __shared__ __align__(8) uint64_t v_full[NS];
   __shared__ __align__(8) uint64_t v_empty[NS];
-  __shared__ __align__(8) uint64_t s_full[kTcTiles][2];
+  __shared__ __align__(8) uint64_t s_full[kTcTiles];
   __shared__ __align__(8) uint64_t p_full[kTcTiles];
   __shared__ __align__(8) uint64_t o_done[kTcTiles];
   __shared__ __align__(8) uint64_t q_ready;
@@ -152,7 +153,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       mbar_init(smem_u32(&v_empty[s]), 1);
     }
     for (int t = 0; t < kTcTiles; ++t) {
-      for (int b = 0; b < 2; ++b) mbar_init(smem_u32(&s_full[t][b]), 1);
+      mbar_init(smem_u32(&s_full[t]), 1);
       mbar_init(smem_u32(&p_full[t]), 4);
       mbar_init(smem_u32(&o_done[t]), 1);
     }
@@ -262,73 +263,78 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       ok = mbar_wait_bounded(smem_u32(&q_ready), 0);
       ok = __all_sync(0xffffffffu, ok);
     }
-    // S_j = Q K_j^T of every tile, into S buffer j % 2 (free: P_{j-2} V_{j-2}, the
-    // last reader of that buffer, was issued before)
-    auto issue_s = [&](int j) -> bool {
-      const int s = j % NS, b = j & 1;
-      bool w = mbar_wait_bounded(smem_u32(&k_full[s]), (j / NS) & 1);
-      w = __all_sync(0xffffffffu, w);
-      if (!w || *failed) return false;
-      tc::fence_after();
-      if (lane == 0) {
-        const uint64_t kd = dK + (uint64_t)((s * Lay::kKVBytes) >> 4);
-        for (int t = 0; t < ntile; ++t) {
-          const uint64_t qd = dQ + (uint64_t)((t * Lay::kQBytes) >> 4);
-          const uint32_t dst = tmem + t * 256 + Lay::kColS + kTcChunk * b;
+    // S_t,j = Q_t K_j^T into tile t's S columns
+    auto mma_s = [&](int t, int j) {
+      const uint64_t kd = dK + (uint64_t)(((j % NS) * Lay::kKVBytes) >> 4);
+      const uint64_t qd = dQ + (uint64_t)((t * Lay::kQBytes) >> 4);
+      const uint32_t dst = tmem + t * 256 + Lay::kColS;
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            // a K step of 16 columns: +32 bytes inside the 128-byte row, +one
-            // column-group block every 4 steps (descriptor addresses count 16 bytes)
-            tc::mma_f16(dst, qd + (uint64_t)(((kk >> 2) * (kTcRows * 128) + (kk & 3) * 32) >> 4),
-                        kd + (uint64_t)(((kk >> 2) * (kTcChunk * 128) + (kk & 3) * 32) >> 4), kIdS,
-                        kk > 0 ? 1u : 0u);
-          }
-          tc::commit(smem_u32(&s_full[t][b]));
-        }
-        tc::commit(smem_u32(&k_empty[s]));  // K chunk j is no longer read
+      for (int kk = 0; kk < D / 16; ++kk) {
+        // a K step of 16 columns: +32 bytes inside the 128-byte row, +one
+        // column-group block every 4 steps (descriptor addresses count 16 bytes)
+        tc::mma_f16(dst, qd + (uint64_t)(((kk >> 2) * (kTcRows * 128) + (kk & 3) * 32) >> 4),
+                    kd + (uint64_t)(((kk >> 2) * (kTcChunk * 128) + (kk & 3) * 32) >> 4), kIdS,
+                    kk > 0 ? 1u : 0u);
       }
-      __syncwarp();
-      return true;
+      tc::commit(smem_u32(&s_full[t]));
     };
-    // O_t += P_t,j V_j of every tile, P from tensor memory; the V stage is released
-    // after the last
-    auto issue_pv = [&](int j) -> bool {
-      const int s = j % NS, b = j & 1;
-      {
-        bool w = mbar_wait_bounded(smem_u32(&v_full[s]), (j / NS) & 1);
-        w = __all_sync(0xffffffffu, w);
-        if (!w || *failed) return false;
+    // O_t += P_t,j V_j, P from tile t's S columns
+    auto mma_pv = [&](int t, int j) {
+      const uint64_t vd = dV + (uint64_t)(((j % NS) * Lay::kKVBytes) >> 4);
+      const uint32_t pa = tmem + t * 256 + Lay::kColS;
+#pragma unroll
+      for (int kk = 0; kk < kTcChunk / 16; ++kk) {
+        // V is N-major (head_dim contiguous): atoms of 64 columns kTcChunk*128 bytes
+        // apart (the descriptor's leading offset), groups of 8 positions 1024 bytes
+        // apart; a K step of 16 positions is 2048 bytes of V and 8 tensor-memory
+        // columns of P (positions 64h.. in columns 64h.., hi then lo)
+        const uint64_t bd = vd + (uint64_t)((kk * (16 * 128)) >> 4);
+        const uint32_t pc = pa + (kk >> 2) * 64 + (kk & 3) * 8;
+        tc::mma_f16_ts(tmem + t * 256, pc, bd, kIdO, (j > 0 || kk > 0) ? 1u : 0u);
+        if (Lay::kSplitP) tc::mma_f16_ts(tmem + t * 256, pc + 32, bd, kIdO, 1u);
       }
-      const uint64_t vd = dV + (uint64_t)((s * Lay::kKVBytes) >> 4);
-      for (int t = 0; t < ntile; ++t) {
-        bool w = mbar_wait_bounded(smem_u32(&p_full[t]), j & 1);
-        w = __all_sync(0xffffffffu, w);
-        if (!w || *failed) return false;
+      tc::commit(smem_u32(&o_done[t]));
+    };
+    auto wait_all = [&](uint64_t *bar, int parity) -> bool {
+      bool w = mbar_wait_bounded(smem_u32(bar), parity);
+      w = __all_sync(0xffffffffu, w);
+      return w && !*failed;
+    };
+    if (ok && nch > 0) {
+      ok = wait_all(&k_full[0], 0);
+      if (ok) {
         tc::fence_after();
         if (lane == 0) {
-          const uint32_t pa = tmem + t * 256 + Lay::kColS + kTcChunk * b;
-#pragma unroll
-          for (int kk = 0; kk < kTcChunk / 16; ++kk) {
-            // V is N-major (head_dim contiguous): atoms of 64 columns kTcChunk*128
-            // bytes apart (the descriptor's leading offset), groups of 8 positions
-            // 1024 bytes apart; a K step of 16 positions is 2048 bytes of V and 8
-            // tensor-memory columns of P
-            const uint64_t bd = vd + (uint64_t)((kk * (16 * 128)) >> 4);
-            tc::mma_f16_ts(tmem + t * 256, pa + kk * 8, bd, kIdO, (j > 0 || kk > 0) ? 1u : 0u);
-            if (Lay::kSplitP) tc::mma_f16_ts(tmem + t * 256, pa + 32 + kk * 8, bd, kIdO, 1u);
-          }
-          tc::commit(smem_u32(&o_done[t]));
-          if (t == ntile - 1) tc::commit(smem_u32(&v_empty[s]));
+          for (int t = 0; t < ntile; ++t) mma_s(t, 0);
+          tc::commit(smem_u32(&k_empty[0]));
         }
         __syncwarp();
       }
-      return true;
-    };
-    if (ok && nch > 0) ok = issue_s(0);
-    if (ok && nch > 1) ok = issue_s(1);
+    }
     for (int j = 0; ok && j < nch; ++j) {
-      ok = issue_pv(j);
-      if (ok && j + 2 < nch) ok = issue_s(j + 2);
+      const bool next = j + 1 < nch;
+      ok = wait_all(&v_full[j % NS], (j / NS) & 1);
+      for (int t = 0; ok && t < ntile; ++t) {
+        ok = wait_all(&p_full[t], j & 1);
+        if (!ok) break;
+        tc::fence_after();
+        if (lane == 0) {
+          mma_pv(t, j);
+          if (t == ntile - 1) tc::commit(smem_u32(&v_empty[j % NS]));
+        }
+        __syncwarp();
+        if (!next) continue;
+        if (t == 0) {
+          ok = wait_all(&k_full[(j + 1) % NS], ((j + 1) / NS) & 1);
+          if (!ok) break;
+          tc::fence_after();
+        }
+        if (lane == 0) {
+          mma_s(t, j + 1);  // into the columns P_t,j V_j reads: issued after it
+          if (t == ntile - 1) tc::commit(smem_u32(&k_empty[(j + 1) % NS]));
+        }
+        __syncwarp();
+      }
     }
     if (!ok && lane == 0) {
       record_error(a.err, kErrTimeout);
@@ -364,34 +370,48 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     float m_run = -INFINITY, l = 0.f;
     bool ok = true;
     const int tid = ((warp - kTcCtl) & 3) * 32 + lane;  // 0..127 within the tile
+    const uint32_t ts = trow + Lay::kColS;  // this row's S / P columns
     for (int j = 0; j < my_nch; ++j) {
-      const int b = j & 1;
-      bool w = mbar_wait_bounded(smem_u32(&s_full[tile][b]), (j >> 1) & 1);
+      // S_j complete; so is P_{j-1} V_{j-1}, issued before it
+      bool w = mbar_wait_bounded(smem_u32(&s_full[tile]), j & 1);
       w = __all_sync(0xffffffffu, w);
       if (!w) {
         ok = false;
         break;
       }
       tc::fence_after();
-      float sv[kTcChunk];
-      tc::ld64(trow + Lay::kColS + kTcChunk * b, sv);
-
       const int c0 = (tb + j * kTcBlocks) * kTileTokens;
-      // scale to base-2 units and mask; the row max as a tree of 8 partial maxima
-      if (c0 + kTcChunk <= lim_row) {
+      const bool full = c0 + kTcChunk <= lim_row;  // no position of the chunk masked
+      // scale to base-2 units (two lanes per instruction) and mask positions
+      // [c0 + 64h, c0 + 64h + 64)
+      const uint64_t rs2 = tc::f2pack(rs, rs);
+      auto scale_mask = [&](float (&v)[64], int h) {
 #pragma unroll
-        for (int c = 0; c < kTcChunk; ++c) sv[c] *= rs;
-      } else {
+        for (int c = 0; c < 64; c += 2) {
+          const uint64_t x = tc::fmul2(tc::f2pack(v[c], v[c + 1]), rs2);
+          tc::f2unpack(x, v[c], v[c + 1]);
+        }
+        if (!full) {
 #pragma unroll
-        for (int c = 0; c < kTcChunk; ++c) sv[c] = (c0 + c < lim_row) ? sv[c] * rs : -INFINITY;
-      }
-      float pm[8];
+          for (int c = 0; c < 64; ++c) v[c] = (c0 + 64 * h + c < lim_row) ? v[c] : -INFINITY;
+        }
+      };
+      auto max64 = [](const float (&v)[64]) {
+        float pm[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) pm[i] = sv[i];
+        for (int i = 0; i < 8; ++i) pm[i] = v[i];
 #pragma unroll
-      for (int c = 8; c < kTcChunk; ++c) pm[c & 7] = fmaxf(pm[c & 7], sv[c]);
-      const float mx = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])),
-                             fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7])));
+        for (int c = 8; c < 64; ++c) pm[c & 7] = fmaxf(pm[c & 7], v[c]);
+        return fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])),
+                     fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7])));
+      };
+      float sv[64];
+      tc::ld64(ts, sv);  // first half: only its maximum now
+      scale_mask(sv, 0);
+      float mx = max64(sv);
+      tc::ld64(ts + 64, sv);  // second half: kept
+      scale_mask(sv, 1);
+      mx = fmaxf(mx, max64(sv));
       const float m_new = fmaxf(m_run, mx);
       const bool need = m_new > m_run + kTcRescale;  // false while both are -inf
       const float f = need ? ex2_ftz(m_run - m_new) : 1.f;  // 0 when m_run = -inf
@@ -399,60 +419,64 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         l *= f;
         m_run = m_new;
       }
-      // P_j over the S_j columns (the exponentials overlap the tensor core's
-      // P_{j-1} V_{j-1})
       const float mb = (m_run == -INFINITY) ? 0.f : m_run;
-      float ps[4] = {0.f, 0.f, 0.f, 0.f};
+      const uint64_t nmb2 = tc::f2pack(-mb, -mb);
+      uint64_t ps2[2] = {0ull, 0ull};  // packed partial sums (+0.0f, +0.0f)
+      // P of one half over the S columns of that half: hi words in its first 32
+      // columns, lo words (bf16) in the next 32
+      auto emit_p = [&](const float (&v)[64], int h) {
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {  // 16 positions (8 columns) at a time
+          uint32_t hw[8], lw[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const int c = 16 * g + 2 * e;
+            float x0, x1;
+            tc::f2unpack(tc::fadd2(tc::f2pack(v[c], v[c + 1]), nmb2), x0, x1);
+            const float p0 = ex2_ftz(x0), p1 = ex2_ftz(x1);
+            if constexpr (Lay::kSplitP) {
+              // hi = p truncated to bf16 (exact); lo = p - hi (exact in fp32), rounded
+              const uint32_t u0 = __float_as_uint(p0), u1 = __float_as_uint(p1);
+              hw[e] = __byte_perm(u0, u1, 0x7632);
+              const uint64_t pp = tc::f2pack(p0, p1);
+              const uint64_t hh = tc::f2pack(__uint_as_float(u0 & 0xffff0000u),
+                                             __uint_as_float(u1 & 0xffff0000u));
+              float l0, l1;
+              tc::f2unpack(tc::ffma2(hh, tc::f2pack(-1.f, -1.f), pp), l0, l1);
+              lw[e] = Elt<T>::from_f2(l0, l1);
+              ps2[e & 1] = tc::fadd2(ps2[e & 1], pp);
+            } else {
+              hw[e] = Elt<T>::from_f2(p0, p1);
+              // the sum of the rounded weights P V is taken with: the quotient O / l
+              // is then an exact convex combination of V rows (a dominant weight's
+              // rounding cancels)
+              const float2 hf = Elt<T>::to_f2(hw[e]);
+              ps2[e & 1] = tc::fadd2(ps2[e & 1], tc::f2pack(hf.x, hf.y));
+            }
+          }
+          tc::st8u(ts + 64 * h + 8 * g, hw);
+          if constexpr (Lay::kSplitP) tc::st8u(ts + 64 * h + 32 + 8 * g, lw);
+        }
+      };
+      emit_p(sv, 1);     // second half from registers (its S columns are read)
+      tc::ld64(ts, sv);  // first half again (its columns are still S)
+      scale_mask(sv, 0);
+      emit_p(sv, 0);
       {
-        uint32_t hw[kTcChunk / 2];
-#pragma unroll
-        for (int e = 0; e < kTcChunk / 2; ++e) {
-          const float p0 = ex2_ftz(sv[2 * e] - mb);
-          const float p1 = ex2_ftz(sv[2 * e + 1] - mb);
-          if constexpr (Lay::kSplitP) {
-            // hi = p truncated to bf16 (exact); lo = the remainder, rounded, kept in sv
-            const uint32_t u0 = __float_as_uint(p0), u1 = __float_as_uint(p1);
-            hw[e] = __byte_perm(u0, u1, 0x7632);
-            sv[2 * e] = p0 - __uint_as_float(u0 & 0xffff0000u);
-            sv[2 * e + 1] = p1 - __uint_as_float(u1 & 0xffff0000u);
-            ps[e & 3] += p0 + p1;
-          } else {
-            hw[e] = Elt<T>::from_f2(p0, p1);
-            // the sum of the rounded weights P V is taken with: the quotient O / l
-            // is then an exact convex combination of V rows (a dominant weight's
-            // rounding cancels)
-            const float2 hf = Elt<T>::to_f2(hw[e]);
-            ps[e & 3] += hf.x + hf.y;
-          }
-        }
-        tc::st32u(trow + Lay::kColS + kTcChunk * b, hw);
+        float a0, a1, b0, b1;
+        tc::f2unpack(ps2[0], a0, a1);
+        tc::f2unpack(ps2[1], b0, b1);
+        l += (a0 + a1) + (b0 + b1);
       }
-      if constexpr (Lay::kSplitP) {
-        uint32_t lw[kTcChunk / 2];
+      if (j > 0 && __any_sync(0xffffffffu, need)) {
+        // P_{j-1} V_{j-1} is complete (see above), P_j V_j not yet issued
 #pragma unroll
-        for (int e = 0; e < kTcChunk / 2; ++e) lw[e] = Elt<T>::from_f2(sv[2 * e], sv[2 * e + 1]);
-        tc::st32u(trow + Lay::kColS + kTcChunk * b + 32, lw);
-      }
-      l += (ps[0] + ps[1]) + (ps[2] + ps[3]);
-      // P_{j-1} V_{j-1} complete before P_j is announced: O may be rescaled below,
-      // and the MMA thread has taken P_{j-1} before this barrier moves again
-      if (j > 0) {
-        w = mbar_wait_bounded(smem_u32(&o_done[tile]), (j - 1) & 1);
-        w = __all_sync(0xffffffffu, w);
-        if (!w) {
-          ok = false;
-          break;
-        }
-        tc::fence_after();
-        if (__any_sync(0xffffffffu, need)) {
+        for (int q = 0; q < D / 32; ++q) {
+          float o[32];
+          tc::ld32(trow + 32 * q, o);
 #pragma unroll
-          for (int q = 0; q < D / 32; ++q) {
-            float o[32];
-            tc::ld32(trow + 32 * q, o);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] *= f;
-            tc::st32(trow + 32 * q, o);
-          }
+          for (int i = 0; i < 32; ++i) o[i] *= f;
+          tc::st32(trow + 32 * q, o);
         }
       }
       if (c0 + kTcChunk > vis_end) {
@@ -475,7 +499,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         fence_proxy_async_smem();  // the zeros visible to the tensor core
       }
-      tc::st_wait();        // P_j (and a rescaled O) are in tensor memory
+      tc::st_wait();  // P_j (and a rescaled O) are in tensor memory
       tc::fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&p_full[tile]));
