@@ -9,13 +9,16 @@ namespace pa {
 
 namespace {
 
-constexpr int kTcStages = 2;  // chunks in flight per CTA in each of the K and V rings
+// K and V ring depths (chunks in flight per CTA); with head_dim 128 the rings fill
+// what shared memory remains after Q (227 KiB per CTA at most)
+template <int D> constexpr int kRingK = D == 128 ? 3 : 4;
+template <int D> constexpr int kRingV = D == 128 ? 2 : 4;
 
 template <typename T, int D, bool PARTIAL>
 cudaError_t launch_prefill_t(const CUtensorMap &kmap, const CUtensorMap &vmap, const DecodeArgs &a,
                              cudaStream_t st) {
-  constexpr int kSmem = TcLayout<T, D>::smem_bytes(kTcStages);
-  auto kern = paged_prefill_tc_kernel<T, D, kTcStages, PARTIAL>;
+  constexpr int kSmem = TcLayout<T, D>::smem_bytes(kRingK<D>, kRingV<D>);
+  auto kern = paged_prefill_tc_kernel<T, D, kRingK<D>, kRingV<D>, PARTIAL>;
   static std::atomic<unsigned long long> opted{0};  // bit per device: smem opt-in done
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -29,7 +32,7 @@ cudaError_t launch_prefill_t(const CUtensorMap &kmap, const CUtensorMap &vmap, c
   const long long rows_per_seq = (long long)a.q_len * a.group;
   const long long rows = a.shared_prefix > 0 ? rows_per_seq * a.num_seqs : rows_per_seq;
   const long long nz = a.shared_prefix > 0 ? a.num_splits : (long long)a.num_seqs * a.num_splits;
-  const long long gx = (rows + kTcTiles * kTcRows - 1) / (kTcTiles * kTcRows) * nz;
+  const long long gx = (rows + kTcRows - 1) / kTcRows * nz;
   if (gx <= 0) return cudaSuccess;
   if (gx > 0x7fffffffLL || a.num_kv_heads > 65535) return cudaErrorInvalidConfiguration;
   cudaLaunchConfig_t cfg = {};
