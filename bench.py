@@ -134,13 +134,22 @@ def attention_flops(w: workloads.Workload) -> float:
     return float(4 * c.head_dim * c.num_q_heads * int(visible.sum()))
 
 
+# the sources each timed kernel is built from (its traffic record is void once any
+# of them changes)
+_COMMON_SRC = ("pa_device.cuh", "pa_launch.h", "pa_api.cu", "pa_decode.cuh")
+KERNEL_SOURCES = {
+    "decode": _COMMON_SRC + ("pa_decode_inst.cuh", "pa_decode_fp16.cu", "pa_decode_bf16.cu"),
+    "prefill": _COMMON_SRC + ("pa_prefill_tc.cuh", "pa_tc.cuh", "pa_prefill.cu"),
+}
+
+
 def traffic_record(kernel_name: str, config: str):
     """dram bytes per launch from the committed ncu summary, if the kernel source is
     unchanged since the counters were taken (else None)."""
     path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
     if not os.path.exists(path):
         return None
-    want_sha = kernel_source_sha()
+    want_sha = kernel_source_sha("prefill" if "prefill" in kernel_name else "decode")
     for line in open(path):
         line = line.strip()
         if not line or line.startswith("#"):
@@ -152,13 +161,12 @@ def traffic_record(kernel_name: str, config: str):
     return None
 
 
-def kernel_source_sha() -> str:
+def kernel_source_sha(kernel: str = "decode") -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "paged_kv_cache_20_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode() + f.read())
+    for name in sorted(KERNEL_SOURCES[kernel]):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
 
 
@@ -463,8 +471,9 @@ def measure_config(pa, name, seed, device, steps, warmup, world, peaks, e2e=Fals
             "peak": tpeak or 1900.0, "unit": "TFLOP/s",
             "frac": fl / (kern_avg * 1e-3) / 1e12 / (tpeak or 1900.0),
             "peak_source": "measured bf16 dense (burst)" if tpeak else "fallback",
-            "kernel": "append_step_kernel+paged_prefill_kernel (mma.sync m16n8k16)"}
+            "kernel": "append_step_kernel+paged_prefill_tc_kernel (tcgen05.mma, M = 128)"}
         res["roofline"]["kernel"] = "append_step_kernel+paged_prefill_kernel"
+        res["roofline"]["traffic"] = traffic_record("paged_prefill_tc_kernel", name)
     if w.cfg.shared_prefix:
         runner.mode = "cascade"
         c_ms, c_kern, _ = time_device(runner, steps, warmup, world)
@@ -543,7 +552,7 @@ def run_ours(args):
         "step_algorithmic_gbs": r["step_gbs"],
         "separate_launches_ms_per_step": r["separate_launches_ms_per_step"],
         "other_configs": others,
-        "kernel_src_sha": kernel_source_sha(),
+        "kernel_src_sha": {k: kernel_source_sha(k) for k in KERNEL_SOURCES},
     }
     for extra in ("cascade", "tensor_roofline"):
         if extra in r:
