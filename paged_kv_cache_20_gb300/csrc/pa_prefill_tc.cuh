@@ -17,11 +17,12 @@
 //               blocks into rings of NK and NV stages (zero fill for blocks past the
 //               walk or bad ids).  A K stage is released as soon as the S MMA that
 //               reads it completes, a V stage after P V;
-//   warp 2      owns tensor memory and issues the MMAs from one thread:
-//               S_{j+2} = Q K_{j+2}^T into S buffer (j+2) % 3 (fp32, TMEM), then
-//               O += P_j V_j into the O accumulator (fp32, TMEM) with P_j read from
-//               tensor memory (buffer j % 3);
-//   warps 3-10  softmax, two warps per group of 32 rows (TMEM lanes), one per half
+//   warp 2      owns tensor memory and issues O += P_j V_j (fp32 accumulator in
+//               TMEM, P_j read from tensor memory) from one thread;
+//   warp 3      issues S_j = Q K_j^T into S buffer j % 3 (fp32, TMEM) from one
+//               thread, as soon as K_j has landed and P_{j-3} V_{j-3} has freed the
+//               buffer: the scores run ahead of the softmax independently of P V;
+//   warps 4-11  softmax, two warps per group of 32 rows (TMEM lanes), one per half
 //               of the chunk's 128 columns: read S_j, mask, exchange the half-row
 //               maxima with the partner warp, online-softmax update, write P_j
 //               (16-bit) over the S_j columns it came from, rescale its half of O in
@@ -29,10 +30,8 @@
 //               rescale (until then P is taken against the older max, at most 2^8,
 //               and the final O / l is the same quotient); at the end O / l (or
 //               the partial statistics) for its half of the columns.
-// S_{j+1} and S_{j+2} are computed while the softmax works on S_j.  The tensor core
-// executes one thread's MMAs in issue order and a commit fires only once every
-// earlier MMA has completed, so S_{j+3} (issued after P_j V_j) never overwrites P_j
-// before it is read.  bf16 P is split into hi + lo bf16 parts, both multiplied by V, so
+// S_{j+1} and S_{j+2} are computed while the softmax works on S_j.  S_{j+3} is issued
+// only after the commit of P_j V_j (the last reader of buffer j % 3) has fired.  bf16 P is split into hi + lo bf16 parts, both multiplied by V, so
 // that P keeps ~16 significant bits as the fp16 path does.  Every wait is bounded.
 #pragma once
 
@@ -44,7 +43,7 @@ namespace pa {
 constexpr int kTcRows = 128;                       // query rows per CTA (MMA M)
 constexpr int kTcChunk = 128;                      // positions per chunk (S MMA N)
 constexpr int kTcBlocks = kTcChunk / kTileTokens;  // cache blocks per chunk
-constexpr int kTcCtl = 3;                          // K producer, V producer, MMA warps
+constexpr int kTcCtl = 4;                          // K, V producers; P V and S issuers
 constexpr int kTcSoft = 8;                         // softmax warps
 constexpr int kTcThreads = 32 * (kTcCtl + kTcSoft);
 constexpr float kTcRescale = 8.f;                  // base-2 growth that forces a rescale
@@ -96,6 +95,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   __shared__ __align__(8) uint64_t p_full;
   __shared__ __align__(8) uint64_t p_ack;        // the MMA thread has taken P_j
   __shared__ __align__(8) uint64_t o_done[2];   // P_j V_j complete, j even / odd
+  __shared__ __align__(8) uint64_t bfree[3];    // P_j V_j complete, by S/P buffer j % 3
   __shared__ __align__(8) uint64_t q_ready;
   __shared__ __align__(8) uint64_t mma_fin;
   __shared__ __align__(8) uint64_t xbar[4];      // partner exchange, per group of 32 rows
@@ -160,8 +160,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     mbar_init(smem_u32(&p_ack), 1);
     mbar_init(smem_u32(&o_done[0]), 1);
     mbar_init(smem_u32(&o_done[1]), 1);
+    for (int b = 0; b < 3; ++b) mbar_init(smem_u32(&bfree[b]), 1);
     mbar_init(smem_u32(&q_ready), kTcSoft);
-    mbar_init(smem_u32(&mma_fin), 1);
+    mbar_init(smem_u32(&mma_fin), 2);  // one commit from each issuing thread
     for (int q = 0; q < 4; ++q) mbar_init(smem_u32(&xbar[q]), 2);
     fence_mbar_init();
     prefetch_tensormap(&kmap);
@@ -218,8 +219,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int32_t *table = a.block_tables + (size_t)tseq * a.max_blocks_per_seq;
     int issued = 0;
     bool ok = true;
+    // block-table window: lane l holds entry tb + 32w + l of window w (4 chunks);
+    // the next window is loaded a whole window ahead, so no TMA issue waits on a
+    // table load
+    auto table_at = [&](int w) -> int {
+      const int blk = tb + 32 * w + lane;
+      return blk < t_end ? __ldg(table + blk) : -1;
+    };
+    int win_cur = table_at(0), win_nxt = table_at(1);
     for (int ch = 0; ch < nch; ++ch) {
       const int s = ch % NS;
+      if (ch > 0 && (ch & 3) == 0) {  // next window of 32 entries
+        win_cur = win_nxt;
+        win_nxt = table_at((ch >> 2) + 1);
+      }
       // a fresh barrier counts as released (parity 1 of the phase before the first)
       bool fr = mbar_wait_bounded(smem_u32(&empty[s]), ((ch / NS) & 1) ^ 1);
       fr = __all_sync(0xffffffffu, fr);
@@ -228,9 +241,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         break;
       }
       const int blk = tb + ch * kTcBlocks + lane;
+      const int phys = __shfl_sync(0xffffffffu, win_cur, ((ch & 3) * kTcBlocks + lane) & 31);
       int z = -1;  // outside the tensor map: zero fill
       if (lane < kTcBlocks && blk < t_end) {
-        const int phys = __ldg(table + blk);
         if (phys >= 0 && phys < a.num_blocks)
           z = phys * a.num_kv_heads + kvh;
         else if (is_k)
@@ -255,7 +268,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       for (int k = max(0, issued - NS); k < issued; ++k)
         (void)mbar_wait_bounded(smem_u32(&full[k % NS]), (k / NS) & 1);
     }
-  } else if (warp == 2) {
+  } else if (warp == 2 || warp == 3) {
     // ------------------------------------------------------------ MMA issue
     constexpr uint32_t kIdS = tc::idesc_f16(kTcRows, kTcChunk, kBf16, false);
     constexpr uint32_t kIdO = tc::idesc_f16(kTcRows, D, kBf16, true);
@@ -270,66 +283,66 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       w = __all_sync(0xffffffffu, w);
       return w && !*failed;
     };
-    // S_j = Q K_j^T into S buffer j % 3
-    auto issue_s = [&](int j) -> bool {
-      if (!wait_all(&k_full[j % NK], (j / NK) & 1)) return false;
-      tc::fence_after();
-      if (lane == 0) {
-        const uint64_t kd = dK + (uint64_t)(((j % NK) * Lay::kKVBytes) >> 4);
-        const uint32_t dst = tmem + Lay::kColS + kTcChunk * (j % 3);
+    if (warp == 3) {
+      // S_j = Q K_j^T into S buffer j % 3
+      if (nch > 0) ok = wait_all(&q_ready, 0);
+      for (int j = 0; ok && j < nch; ++j) {
+        ok = wait_all(&k_full[j % NK], (j / NK) & 1);
+        // the buffer's last reader, P_{j-3} V_{j-3}, has completed (its barrier is at
+        // most one phase behind: P_j V_j needs S_j first)
+        if (ok && j >= 3) ok = wait_all(&bfree[j % 3], ((j - 3) / 3) & 1);
+        if (!ok) break;
+        tc::fence_after();
+        if (lane == 0) {
+          const uint64_t kd = dK + (uint64_t)(((j % NK) * Lay::kKVBytes) >> 4);
+          const uint32_t dst = tmem + Lay::kColS + kTcChunk * (j % 3);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          // a K step of 16 columns: +32 bytes inside the 128-byte row, +one
-          // column-group block every 4 steps (descriptor addresses count 16 bytes)
-          tc::mma_f16(dst, dQ + (uint64_t)(((kk >> 2) * (kTcRows * 128) + (kk & 3) * 32) >> 4),
-                      kd + (uint64_t)(((kk >> 2) * (kTcChunk * 128) + (kk & 3) * 32) >> 4), kIdS,
-                      kk > 0 ? 1u : 0u);
+          for (int kk = 0; kk < D / 16; ++kk) {
+            // a K step of 16 columns: +32 bytes inside the 128-byte row, +one
+            // column-group block every 4 steps (descriptor addresses count 16 bytes)
+            tc::mma_f16(dst, dQ + (uint64_t)(((kk >> 2) * (kTcRows * 128) + (kk & 3) * 32) >> 4),
+                        kd + (uint64_t)(((kk >> 2) * (kTcChunk * 128) + (kk & 3) * 32) >> 4), kIdS,
+                        kk > 0 ? 1u : 0u);
+          }
+          tc::commit(smem_u32(&s_full[j % 3]));
+          tc::commit(smem_u32(&k_empty[j % NK]));
         }
-        tc::commit(smem_u32(&s_full[j % 3]));
-        tc::commit(smem_u32(&k_empty[j % NK]));
+        __syncwarp();
       }
-      __syncwarp();
-      return true;
-    };
-    // O += P_j V_j, P from S buffer j % 3
-    auto issue_pv = [&](int j) -> bool {
-      if (!wait_all(&v_full[j % NV], (j / NV) & 1)) return false;
-      if (!wait_all(&p_full, j & 1)) return false;
-      tc::fence_after();
-      if (lane == 0) {
-        mbar_arrive(smem_u32(&p_ack));  // the softmax may announce P_{j+1}
-        const uint64_t vd = dV + (uint64_t)(((j % NV) * Lay::kKVBytes) >> 4);
-        const uint32_t pa = tmem + Lay::kColS + kTcChunk * (j % 3);
+    } else {
+      // O += P_j V_j, P from S buffer j % 3
+      for (int j = 0; ok && j < nch; ++j) {
+        ok = wait_all(&v_full[j % NV], (j / NV) & 1);
+        if (ok) ok = wait_all(&p_full, j & 1);
+        if (!ok) break;
+        tc::fence_after();
+        if (lane == 0) {
+          mbar_arrive(smem_u32(&p_ack));  // the softmax may announce P_{j+1}
+          const uint64_t vd = dV + (uint64_t)(((j % NV) * Lay::kKVBytes) >> 4);
+          const uint32_t pa = tmem + Lay::kColS + kTcChunk * (j % 3);
 #pragma unroll
-        for (int kk = 0; kk < kTcChunk / 16; ++kk) {
-          // V is N-major (head_dim contiguous): atoms of 64 columns kTcChunk*128
-          // bytes apart (the descriptor's leading offset), groups of 8 positions
-          // 1024 bytes apart; a K step of 16 positions is 2048 bytes of V and 8
-          // tensor-memory columns of P (positions 64h.. in columns 64h.., hi then lo)
-          const uint64_t bd = vd + (uint64_t)((kk * (16 * 128)) >> 4);
-          const uint32_t pc = pa + (kk >> 2) * 64 + (kk & 3) * 8;
-          tc::mma_f16_ts(tmem, pc, bd, kIdO, (j > 0 || kk > 0) ? 1u : 0u);
-          if (Lay::kSplitP) tc::mma_f16_ts(tmem, pc + 32, bd, kIdO, 1u);
+          for (int kk = 0; kk < kTcChunk / 16; ++kk) {
+            // V is N-major (head_dim contiguous): atoms of 64 columns kTcChunk*128
+            // bytes apart (the descriptor's leading offset), groups of 8 positions
+            // 1024 bytes apart; a K step of 16 positions is 2048 bytes of V and 8
+            // tensor-memory columns of P (positions 64h.. in columns 64h.., hi then lo)
+            const uint64_t bd = vd + (uint64_t)((kk * (16 * 128)) >> 4);
+            const uint32_t pc = pa + (kk >> 2) * 64 + (kk & 3) * 8;
+            tc::mma_f16_ts(tmem, pc, bd, kIdO, (j > 0 || kk > 0) ? 1u : 0u);
+            if (Lay::kSplitP) tc::mma_f16_ts(tmem, pc + 32, bd, kIdO, 1u);
+          }
+          tc::commit(smem_u32(&o_done[j & 1]));
+          tc::commit(smem_u32(&v_empty[j % NV]));
+          tc::commit(smem_u32(&bfree[j % 3]));
         }
-        tc::commit(smem_u32(&o_done[j & 1]));
-        tc::commit(smem_u32(&v_empty[j % NV]));
+        __syncwarp();
       }
-      __syncwarp();
-      return true;
-    };
-    if (nch > 0) ok = wait_all(&q_ready, 0);
-    if (ok && nch > 0) ok = issue_s(0);
-    if (ok && nch > 1) ok = issue_s(1);
-    for (int j = 0; ok && j < nch; ++j) {
-      // buffer (j + 2) % 3 was last read by P_{j-1} V_{j-1}, issued before
-      if (j + 2 < nch) ok = issue_s(j + 2);
-      if (ok) ok = issue_pv(j);
     }
     if (!ok && lane == 0) {
       record_error(a.err, kErrTimeout);
       atomicExch(&s_failed, 1);
     }
-    // every MMA issued has completed before tensor memory is released
+    // every MMA this thread issued has completed before tensor memory is released
     if (lane == 0) tc::commit(smem_u32(&mma_fin));
     __syncwarp();
     (void)mbar_wait_bounded(smem_u32(&mma_fin), 0);
