@@ -243,6 +243,24 @@ pa_status make_map(CUtensorMap *map, const void *cache, pa_dtype dtype, int head
   return r == CUDA_SUCCESS ? PA_OK : PA_ERR_CUDA;
 }
 
+// Tensor map over q [tokens][num_q_heads][head_dim] as [head_dim, num_q_heads,
+// tokens], box = 64 columns x `group` heads x 128/group tokens: the 128 query rows
+// (token, head) of one KV head's row block, 128-byte swizzle, zero fill outside.
+pa_status make_q_map(CUtensorMap *map, const void *q, pa_dtype dtype, int head_dim,
+                     int num_q_heads, int64_t tokens, int group) {
+  std::call_once(g_encode_once, load_encode);
+  if (g_encode == nullptr) return PA_ERR_CUDA;
+  cuuint64_t dims[3] = {(cuuint64_t)head_dim, (cuuint64_t)num_q_heads, (cuuint64_t)tokens};
+  cuuint64_t strides[2] = {(cuuint64_t)head_dim * 2, (cuuint64_t)num_q_heads * head_dim * 2};
+  cuuint32_t box[3] = {64u, (cuuint32_t)group, (cuuint32_t)(128 / group)};
+  cuuint32_t elem_strides[3] = {1, 1, 1};
+  CUresult r = g_encode(map, dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                        3, const_cast<void *>(q), dims, strides, box, elem_strides,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? PA_OK : PA_ERR_CUDA;
+}
+
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct WsLayout {
@@ -343,6 +361,7 @@ pa_status decode_common(void *out, float *ws, const WsLayout *lay, const void *q
   a.ws_splits = place.ws_splits > 0 ? place.ws_splits : num_splits;
   a.ws_split0 = place.ws_split0;
   a.shared_prefix = place.shared_prefix;
+  a.q_tma = 0;
   a.scale_log2 = scale * 1.4426950408889634f;  // log2(e)
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const bool partial = ws != nullptr;
@@ -368,7 +387,15 @@ pa_status decode_common(void *out, float *ws, const WsLayout *lay, const void *q
       if (e != cudaSuccess) return PA_ERR_CUDA;
       a.k_new = a.v_new = nullptr;
     }
-    e = pa::launch_prefill(kmap, vmap, a, head_dim, dtype == PA_FP16, partial, s);
+    CUtensorMap qmap;
+    a.q_tma = (128 % a.group == 0) ? 1 : 0;
+    if (a.q_tma) {
+      st = make_q_map(&qmap, q, dtype, head_dim, num_q_heads, (int64_t)num_seqs * q_len, a.group);
+      if (st != PA_OK) return st;
+    } else {
+      qmap = kmap;  // unused
+    }
+    e = pa::launch_prefill(kmap, vmap, qmap, a, head_dim, dtype == PA_FP16, partial, s);
   } else if (fp8)
     e = dtype == PA_FP16 ? pa::launch_decode8_fp16(kmap, vmap, a, partial, (int)units, s)
                          : pa::launch_decode8_bf16(kmap, vmap, a, partial, (int)units, s);

@@ -77,6 +77,9 @@ struct DecodeArgs {
   // Prefill kernel, shared-prefix mode (> 0): the query rows of every sequence
   // attend to the first `shared_prefix` blocks of block-table row 0.
   int shared_prefix;
+  // Prefill kernel: q rows arrive by TMA through the kernel's q tensor map (the KV
+  // group size divides 128); otherwise each thread loads its own row
+  int q_tma;
 };
 
 constexpr int kLptMaxSeqs = 256;

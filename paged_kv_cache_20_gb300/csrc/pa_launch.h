@@ -47,8 +47,9 @@ cudaError_t launch_decode8_bf16(const CUtensorMap &kmap, const CUtensorMap &vmap
 // Many query rows per KV head (q_len above the decode kernel's limit, or the
 // shared-prefix pass of a cascade when args.shared_prefix > 0): 64 rows per CTA,
 // grid ([num_seqs x] num_splits x row blocks, num_kv_heads).
-cudaError_t launch_prefill(const CUtensorMap &kmap, const CUtensorMap &vmap, const DecodeArgs &args,
-                           int head_dim, bool fp16, bool partial, cudaStream_t stream);
+cudaError_t launch_prefill(const CUtensorMap &kmap, const CUtensorMap &vmap, const CUtensorMap &qmap,
+                           const DecodeArgs &args, int head_dim, bool fp16, bool partial,
+                           cudaStream_t stream);
 cudaError_t launch_combine_fp16(const CombineArgs &args, int head_dim, cudaStream_t stream);
 cudaError_t launch_combine_bf16(const CombineArgs &args, int head_dim, cudaStream_t stream);
 

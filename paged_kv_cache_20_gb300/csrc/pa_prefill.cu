@@ -15,8 +15,8 @@ template <int D> constexpr int kRingK = D == 128 ? 3 : 4;
 template <int D> constexpr int kRingV = D == 128 ? 2 : 4;
 
 template <typename T, int D, bool PARTIAL>
-cudaError_t launch_prefill_t(const CUtensorMap &kmap, const CUtensorMap &vmap, const DecodeArgs &a,
-                             cudaStream_t st) {
+cudaError_t launch_prefill_t(const CUtensorMap &kmap, const CUtensorMap &vmap, const CUtensorMap &qmap,
+                             const DecodeArgs &a, cudaStream_t st) {
   constexpr int kSmem = TcLayout<T, D>::smem_bytes(kRingK<D>, kRingV<D>);
   auto kern = paged_prefill_tc_kernel<T, D, kRingK<D>, kRingV<D>, PARTIAL>;
   static std::atomic<unsigned long long> opted{0};  // bit per device: smem opt-in done
@@ -45,27 +45,28 @@ cudaError_t launch_prefill_t(const CUtensorMap &kmap, const CUtensorMap &vmap, c
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, kmap, vmap, a);
+  return cudaLaunchKernelEx(&cfg, kern, kmap, vmap, qmap, a);
 }
 
 template <typename T>
-cudaError_t dispatch(const CUtensorMap &kmap, const CUtensorMap &vmap, const DecodeArgs &a,
-                     int head_dim, bool partial, cudaStream_t st) {
+cudaError_t dispatch(const CUtensorMap &kmap, const CUtensorMap &vmap, const CUtensorMap &qmap,
+                     const DecodeArgs &a, int head_dim, bool partial, cudaStream_t st) {
   if (head_dim == 128)
-    return partial ? launch_prefill_t<T, 128, true>(kmap, vmap, a, st)
-                   : launch_prefill_t<T, 128, false>(kmap, vmap, a, st);
+    return partial ? launch_prefill_t<T, 128, true>(kmap, vmap, qmap, a, st)
+                   : launch_prefill_t<T, 128, false>(kmap, vmap, qmap, a, st);
   if (head_dim == 64)
-    return partial ? launch_prefill_t<T, 64, true>(kmap, vmap, a, st)
-                   : launch_prefill_t<T, 64, false>(kmap, vmap, a, st);
+    return partial ? launch_prefill_t<T, 64, true>(kmap, vmap, qmap, a, st)
+                   : launch_prefill_t<T, 64, false>(kmap, vmap, qmap, a, st);
   return cudaErrorInvalidValue;
 }
 
 }  // namespace
 
-cudaError_t launch_prefill(const CUtensorMap &kmap, const CUtensorMap &vmap, const DecodeArgs &args,
-                           int head_dim, bool fp16, bool partial, cudaStream_t stream) {
-  return fp16 ? dispatch<__half>(kmap, vmap, args, head_dim, partial, stream)
-              : dispatch<__nv_bfloat16>(kmap, vmap, args, head_dim, partial, stream);
+cudaError_t launch_prefill(const CUtensorMap &kmap, const CUtensorMap &vmap, const CUtensorMap &qmap,
+                           const DecodeArgs &args, int head_dim, bool fp16, bool partial,
+                           cudaStream_t stream) {
+  return fp16 ? dispatch<__half>(kmap, vmap, qmap, args, head_dim, partial, stream)
+              : dispatch<__nv_bfloat16>(kmap, vmap, qmap, args, head_dim, partial, stream);
 }
 
 }  // namespace pa

@@ -78,7 +78,8 @@ __device__ __forceinline__ float ex2_ftz(float x) {
 template <typename T, int D, int NK, int NV, bool PARTIAL>
 __global__ void __launch_bounds__(kTcThreads, 1)
     paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
-                            const __grid_constant__ CUtensorMap vmap, const DecodeArgs a) {
+                            const __grid_constant__ CUtensorMap vmap,
+                            const __grid_constant__ CUtensorMap qmap, const DecodeArgs a) {
   using Lay = TcLayout<T, D>;
   constexpr int H = Lay::kHalves;
   constexpr bool kBf16 = Elt<T>::kMantBits < 10;
@@ -96,7 +97,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   __shared__ __align__(8) uint64_t p_ack;        // the MMA thread has taken P_j
   __shared__ __align__(8) uint64_t o_done[2];   // P_j V_j complete, j even / odd
   __shared__ __align__(8) uint64_t bfree[3];    // P_j V_j complete, by S/P buffer j % 3
-  __shared__ __align__(8) uint64_t q_ready;
+  __shared__ __align__(8) uint64_t q_ready;      // Q written by the softmax threads
+  __shared__ __align__(8) uint64_t q_full;       // Q landed by TMA
   __shared__ __align__(8) uint64_t mma_fin;
   __shared__ __align__(8) uint64_t xbar[4];      // partner exchange, per group of 32 rows
   __shared__ float xval[2][2][kTcRows];           // [parity][column half][row]
@@ -162,11 +164,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     mbar_init(smem_u32(&o_done[1]), 1);
     for (int b = 0; b < 3; ++b) mbar_init(smem_u32(&bfree[b]), 1);
     mbar_init(smem_u32(&q_ready), kTcSoft);
+    mbar_init(smem_u32(&q_full), 1);
     mbar_init(smem_u32(&mma_fin), 2);  // one commit from each issuing thread
     for (int q = 0; q < 4; ++q) mbar_init(smem_u32(&xbar[q]), 2);
     fence_mbar_init();
     prefetch_tensormap(&kmap);
     prefetch_tensormap(&vmap);
+    if (a.q_tma) prefetch_tensormap(&qmap);
   }
   if (warp == 2) {
     tc::alloc(smem_u32(&s_tmem), Lay::kTmemCols);
@@ -207,6 +211,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int nch = (t_end - tb + kTcBlocks - 1) / kTcBlocks;
   const int vis_end = min(te * kTileTokens, s_maxlim);  // no row uses a position past it
   volatile int *failed = &s_failed;
+  if (a.q_tma && nch > 0 && threadIdx.x == 0) {
+    // the row block's 128 query rows (token, head): tokens [t0, t0 + 128/g) of heads
+    // [kvh*g, kvh*g + g) (rows past the sequence's last token are never written
+    // back; past the tensor they are zero-filled).  The S thread waits for them.
+    const int t0 = (shared ? 0 : zseq * a.q_len) + row_base / a.group;
+    const uint32_t bar = smem_u32(&q_full);
+    mbar_arrive_expect_tx(bar, Lay::kQBytes);
+#pragma unroll
+    for (int hh = 0; hh < H; ++hh) tma_load_3d(base + hh * (kTcRows * 128), &qmap, hh * 64, kvh * a.group, t0, bar);
+  }
 
   if (warp < 2) {
     // ------------------------------------------------------------ TMA producers
@@ -285,7 +299,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     };
     if (warp == 3) {
       // S_j = Q K_j^T into S buffer j % 3
-      if (nch > 0) ok = wait_all(&q_ready, 0);
+      if (nch > 0) ok = a.q_tma ? wait_all(&q_full, 0) : wait_all(&q_ready, 0);
       for (int j = 0; ok && j < nch; ++j) {
         ok = wait_all(&k_full[j % NK], (j / NK) & 1);
         // the buffer's last reader, P_{j-3} V_{j-3}, has completed (its barrier is at
@@ -350,9 +364,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // ------------------------------------------------------------ softmax rows
     const uint32_t trow = tmem + ((uint32_t)(32 * q4) << 16);
     // Q row -> shared memory in the swizzled K-major layout of the MMA's A operand
-    // (each warp of the pair writes half of the row's 16-byte chunks)
+    // (each warp of the pair writes half of the row's 16-byte chunks), unless TMA
+    // brings it
 #pragma unroll
-    for (int ci = 0; ci < D / 16; ++ci) {
+    for (int ci = 0; ci < (a.q_tma ? 0 : D / 16); ++ci) {
       const int c = hc * (D / 16) + ci;
       uint4 v = make_uint4(0u, 0u, 0u, 0u);
       if (qrow) v = __ldg(reinterpret_cast<const uint4 *>(qrow) + c);
