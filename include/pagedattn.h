@@ -227,7 +227,9 @@ PA_API pa_status pa_append_decode(void *out, const void *q, const void *k_new, c
  *   partitions 1..   each sequence's blocks from prefix_blocks on (with this
  *                    step's append when k_new/v_new are given), cut into
  *                    tail_splits equal parts;
- * then the combine.  The causal limit applies in both passes.
+ * then the combine.  With tail_splits == 1 and q_len <= 16 the tail pass is a
+ * single pass that merges partition 0 into its result (no combine launch).  The
+ * causal limit applies in both passes.
  * Caller's contract: for every sequence, table entries [0, prefix_blocks) equal
  * those of row 0, and this step's new tokens lie at or past position
  * prefix_blocks * block_size (so the append never writes a shared block).

@@ -310,6 +310,11 @@ struct Placement {
   int ws_splits = 0;  // 0: num_splits
   int ws_split0 = 0;
   int shared_prefix = 0;
+  // single pass: merge partition 0 of this workspace (prior_splits partitions) into
+  // the result
+  const float *prior_ws = nullptr;
+  const WsLayout *prior_lay = nullptr;
+  int prior_splits = 0;
 };
 
 pa_status decode_common(void *out, float *ws, const WsLayout *lay, const void *q,
@@ -362,6 +367,15 @@ pa_status decode_common(void *out, float *ws, const WsLayout *lay, const void *q
   a.ws_split0 = place.ws_split0;
   a.shared_prefix = place.shared_prefix;
   a.q_tma = 0;
+  a.prior_splits = place.prior_splits;
+  if (place.prior_ws != nullptr) {
+    const char *pb = reinterpret_cast<const char *>(place.prior_ws);
+    a.prior_acc = reinterpret_cast<const float *>(pb + place.prior_lay->acc_off);
+    a.prior_m = reinterpret_cast<const float *>(pb + place.prior_lay->m_off);
+    a.prior_l = reinterpret_cast<const float *>(pb + place.prior_lay->l_off);
+  } else {
+    a.prior_acc = a.prior_m = a.prior_l = nullptr;
+  }
   a.scale_log2 = scale * 1.4426950408889634f;  // log2(e)
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const bool partial = ws != nullptr;
@@ -580,9 +594,20 @@ PA_API pa_status pa_decode_cascade(void *out, const void *q, const void *k_new, 
                      num_blocks, q_len, dtype, stream, nullptr, nullptr, nullptr, nullptr, head);
   if (st != PA_OK) return st;
   // 2. each sequence's own blocks past the prefix (with this step's append, if
-  //    given) -> partitions 1 .. tail_splits
+  //    given).  One tail partition and q_len <= 16: a single pass of the decode
+  //    kernel that merges partition 0 into its result and writes out.  Otherwise:
+  //    partitions 1 .. tail_splits, then the combine.
   Placement tail;
   tail.first_block = prefix_blocks;
+  if (tail_splits == 1 && q_len <= kMaxDecodeQLen) {  // (the decode kernel merges)
+    tail.prior_ws = ws;
+    tail.prior_lay = &lay;
+    tail.prior_splits = parts;
+    return decode_common(out, nullptr, nullptr, q, k_cache, v_cache, block_tables, context_lens,
+                         num_seqs, num_q_heads, num_kv_heads, head_dim, scale, 1,
+                         max_blocks_per_seq, num_blocks, q_len, dtype, stream, k_new, v_new,
+                         nullptr, nullptr, tail);
+  }
   tail.ws_splits = parts;
   tail.ws_split0 = 1;
   st = decode_common(nullptr, ws, &lay, q, k_cache, v_cache, block_tables, context_lens, num_seqs,

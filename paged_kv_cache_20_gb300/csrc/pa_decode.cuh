@@ -80,6 +80,12 @@ struct DecodeArgs {
   // Prefill kernel: q rows arrive by TMA through the kernel's q tensor map (the KV
   // group size divides 128); otherwise each thread loads its own row
   int q_tma;
+  // Single pass only: a partition of the same rows computed by another pass (the
+  // shared prefix of a cascade), merged into the result before it is written.
+  // Workspace layout of pa_decode_partial with prior_splits partitions; the prior
+  // is partition 0.  prior_m == nullptr: none.
+  const float *prior_acc, *prior_m, *prior_l;
+  int prior_splits;
 };
 
 constexpr int kLptMaxSeqs = 256;
@@ -1059,12 +1065,32 @@ __global__ void __launch_bounds__(NW * 32)
       }
     } else {
       const size_t orow = (size_t)(seq * a.q_len + ri.u) * a.num_q_heads + ri.h;
-      const float inv = den > 0.f ? vscale / den : 0.f;
+      float inv = den > 0.f ? vscale / den : 0.f;
+      float o[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) o[i] = num[i] * inv;
+      if (a.prior_m != nullptr) {
+        // merge the prior partition (m0, l0, acc0): the same rescale as the online
+        // softmax, once more
+        const size_t prow = (size_t)seq * a.prior_splits * (a.q_len * a.num_q_heads) +
+                            (size_t)ri.u * a.num_q_heads + ri.h;
+        const float m0 = __ldg(a.prior_m + prow), l0 = __ldg(a.prior_l + prow);
+        const float Mx = fmaxf(M, m0);
+        const float w1 = (M == -INFINITY) ? 0.f : fast_exp2(M - Mx);
+        const float w0 = (m0 == -INFINITY) ? 0.f : fast_exp2(m0 - Mx);
+        const float dd = w1 * den + w0 * l0;
+        inv = dd > 0.f ? 1.f / dd : 0.f;
+        const float4 *src = reinterpret_cast<const float4 *>(a.prior_acc + prow * D + d8 * 8);
+        const float4 p0 = __ldg(src), p1 = __ldg(src + 1);
+        const float pv[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+#pragma unroll
+        for (int i = 0; i < 8; ++i) o[i] = (w1 * num[i] * vscale + w0 * pv[i]) * inv;
+      }
       uint4 packed;
-      packed.x = Elt<T>::from_f2(num[0] * inv, num[1] * inv);
-      packed.y = Elt<T>::from_f2(num[2] * inv, num[3] * inv);
-      packed.z = Elt<T>::from_f2(num[4] * inv, num[5] * inv);
-      packed.w = Elt<T>::from_f2(num[6] * inv, num[7] * inv);
+      packed.x = Elt<T>::from_f2(o[0], o[1]);
+      packed.y = Elt<T>::from_f2(o[2], o[3]);
+      packed.z = Elt<T>::from_f2(o[4], o[5]);
+      packed.w = Elt<T>::from_f2(o[6], o[7]);
       *reinterpret_cast<uint4 *>(static_cast<T *>(a.out) + orow * D + d8 * 8) = packed;
     }
   };
