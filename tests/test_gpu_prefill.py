@@ -13,7 +13,7 @@ import torch
 import workloads
 from tests import _tol
 from tests.oracle_pins import Paged
-from tests.test_gpu_parity import (DEV, _dev, _f64, _gpu_decode, _logical_case, _u16,
+from tests.test_gpu_parity import (DEV, _dev, _f64, _gpu_decode, _logical_case, _to_dev, _u16,
                                    gpu_step, oracle_step)
 
 pytestmark = pytest.mark.gpu
@@ -160,3 +160,104 @@ def test_cascade_equals_plain_decode_closely(pa):
     casc, _ = gpu_cascade(pa, w)
     diff = (plain.double() - casc.double()).abs().max().item()
     assert diff <= 2e-3, diff
+
+
+# ------------------------------------------------------------------- more edges
+def test_prefill_partial_statistics_match_oracle_partitions(pa, orc):
+    """The many-row kernel's partial pass writes each partition's (m, l, acc): the
+    normalised partition outputs and log-sum-exps equal the oracle's partitions."""
+    lens = [40, 300, 700, 33]
+    q_len, S = 33, 3
+    q, K, V = _logical_case(24, lens, 8, 2, 128, "bf16", q_len=q_len)
+    pc = Paged(orc, K, V, 16, "bf16", perm_seed=16)
+    m, l, acc = orc.decode_partitions(q, pc.k, pc.v, pc.tables, pc.lens, 0.0884, "bf16", S,
+                                      q_len=q_len)
+    qd = _to_dev(q, "bf16")
+    nbytes = pa.pa_decode_workspace_size(4, 8, q_len, 128, S)
+    ws = torch.full((nbytes,), 0x7F, dtype=torch.uint8, device=DEV)  # garbage-filled
+    pa.pa_decode_partial(ws, qd, _to_dev(pc.k, "bf16"), _to_dev(pc.v, "bf16"),
+                         torch.from_numpy(pc.tables).to(DEV), torch.from_numpy(pc.lens).to(DEV),
+                         0.0884, S, q_len)
+    torch.cuda.synchronize()
+    assert pa.pa_device_error() == 0
+    g_acc, g_m, g_l = (t.double().cpu().numpy() for t in pa.workspace_views(ws, 4, 8, q_len, 128, S))
+    empty = l == 0
+    assert np.array_equal(g_l == 0, empty)
+    assert np.all(np.isneginf(g_m[empty])) and np.all(g_acc[empty] == 0)
+    ok = ~empty
+    _tol.check(g_acc[ok] / g_l[ok][:, None], acc[ok] / l[ok][:, None], "bf16", "partition output")
+    lse_g = g_m[ok] * np.log(2.0) + np.log(g_l[ok])
+    assert np.abs(lse_g - (m[ok] + np.log(l[ok]))).max() < 1e-4
+
+
+def test_prefill_longest_chunk_sampled_rows(pa, orc):
+    """q_len at the library's limit (4096): one sequence, GQA, sampled rows."""
+    w = workloads.make("chunked_prefill", num_seqs=1, q_len=4096, lens=("fixed", (4400,)))
+    out, d = gpu_step(pa, w, fused=True)
+    n_rows = w.cfg.q_len * w.cfg.num_q_heads
+    rows = np.sort(np.random.default_rng(4).choice(n_rows, size=48, replace=False))
+    rows = np.unique(np.concatenate([rows, [0, n_rows - 1]]))   # first and last query rows
+    ref, kc, vc, _ = oracle_step(orc, w, rows=rows)
+    _tol.check(_f64(out).reshape(n_rows, -1)[rows], ref, w.cfg.dtype, "q_len 4096")
+    assert np.array_equal(_u16(d["k_cache"]), kc)
+
+
+def test_prefill_bad_block_id_is_reported_not_faulted(pa, orc):
+    q, K, V = _logical_case(25, [100, 100], 8, 2, 128, "fp16", q_len=40)
+    pc = Paged(orc, K, V, 16, "fp16", perm_seed=17)
+    pc.tables[1, 2] = pc.k.shape[0] + 7                  # beyond the pool
+    qd = _to_dev(q, "fp16")
+    out = torch.empty_like(qd)
+    pa.pa_decode(out, qd, _to_dev(pc.k, "fp16"), _to_dev(pc.v, "fp16"),
+                 torch.from_numpy(pc.tables).to(DEV), torch.from_numpy(pc.lens).to(DEV), 0.1, 40)
+    assert pa.pa_device_error() == pa.PA_ERR_DEVICE_CHECK
+    assert pa.pa_device_error() == 0                     # cleared
+    got = _f64(out)
+    assert np.isfinite(got).all()
+    ref = pc.decode(orc, q, 0.1, q_len=40)
+    _tol.check(got[0], ref[0], "fp16", "unaffected sequence")
+
+
+def test_prefill_append_reports_positions_beyond_the_table(pa):
+    """The table-driven append (q_len > 16) skips and reports new positions past a
+    sequence's block table."""
+    H, D, q_len = 2, 128, 20
+    kc = torch.zeros((8, H, 16, D), dtype=torch.float16, device=DEV)
+    vc = torch.zeros_like(kc)
+    q = torch.randn((1, q_len, 2, D), dtype=torch.float16, device=DEV)
+    kn = torch.randn((q_len, H, D), dtype=torch.float16, device=DEV)
+    vn = torch.randn_like(kn)
+    bt = torch.tensor([[3]], dtype=torch.int32, device=DEV)      # one block: 16 positions
+    cl = torch.tensor([q_len], dtype=torch.int32, device=DEV)    # needs two
+    out = torch.empty_like(q)
+    pa.pa_append_decode(out, q, kn, vn, kc, vc, bt, cl, 0.1, q_len)
+    torch.cuda.synchronize()
+    assert pa.pa_device_error() == pa.PA_ERR_DEVICE_CHECK
+    assert torch.equal(kc[3].transpose(0, 1), kn[:16])           # positions 0..15 written
+    assert int(kc[torch.arange(8, device=DEV) != 3].abs().sum()) == 0
+
+
+def test_cascade_without_append_any_lengths(pa, orc):
+    """Without an append the cascade is exact for any context lengths, including
+    sequences shorter than the shared prefix (each row's causal limit cuts the
+    prefix pass)."""
+    w = workloads.make("prefix_verify", num_seqs=4, lens=("prefix", 1024, 64, 300))
+    d = _dev(w)
+    # shorten two sequences into the prefix; their tables keep the prefix blocks
+    lens = w.context_lens.clone()
+    lens[1] = 500
+    lens[3] = 4
+    kc, vc = w.bits("k_cache").copy(), w.bits("v_cache").copy()
+    # the pool as a finished prefill left it (slots before each new position)
+    slots = orc.slot_mapping(w.block_tables.numpy(), w.context_lens.numpy(), 16, w.cfg.q_len)
+    orc.append_kv(kc, vc, w.bits("k_new"), w.bits("v_new"), slots)
+    ref = orc.decode(w.bits("q"), kc, vc, w.block_tables.numpy(), lens.numpy(), w.scale,
+                     w.cfg.dtype, q_len=w.cfg.q_len)
+    kt = torch.from_numpy(kc.view(np.int16)).view(torch.float16).to(DEV)
+    vt = torch.from_numpy(vc.view(np.int16)).view(torch.float16).to(DEV)
+    out = torch.empty_like(d["q"])
+    pa.pa_decode_cascade(out, d["q"], kt, vt, d["block_tables"], lens.to(DEV), w.scale,
+                         w.cfg.shared_prefix // 16, q_len=w.cfg.q_len)
+    torch.cuda.synchronize()
+    assert pa.pa_device_error() == 0
+    _tol.check(_f64(out), ref, w.cfg.dtype, "cascade, short sequences")
