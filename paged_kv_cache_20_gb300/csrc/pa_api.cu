@@ -367,6 +367,7 @@ pa_status decode_common(void *out, float *ws, const WsLayout *lay, const void *q
   a.ws_split0 = place.ws_split0;
   a.shared_prefix = place.shared_prefix;
   a.q_tma = 0;
+  a.s_negate = 0;
   a.prior_splits = place.prior_splits;
   if (place.prior_ws != nullptr) {
     const char *pb = reinterpret_cast<const char *>(place.prior_ws);
@@ -401,6 +402,15 @@ pa_status decode_common(void *out, float *ws, const WsLayout *lay, const void *q
       if (e != cudaSuccess) return PA_ERR_CUDA;
       a.k_new = a.v_new = nullptr;
     }
+    // The prefill kernel scales scores inside exp2's argument (one multiply-add),
+    // which needs a positive scale: a negative one negates Q K^T in the MMA instead,
+    // and a zero one (every visible weight equal) becomes one too small to move an
+    // exponent of a finite score
+    if (a.scale_log2 < 0.f) {
+      a.s_negate = 1;
+      a.scale_log2 = -a.scale_log2;
+    }
+    if (a.scale_log2 == 0.f) a.scale_log2 = 1e-30f;
     CUtensorMap qmap;
     a.q_tma = (128 % a.group == 0) ? 1 : 0;
     if (a.q_tma) {

@@ -80,6 +80,9 @@ struct DecodeArgs {
   // Prefill kernel: q rows arrive by TMA through the kernel's q tensor map (the KV
   // group size divides 128); otherwise each thread loads its own row
   int q_tma;
+  // Prefill kernel: the score MMA negates Q K^T (scale_log2 then holds |scale| *
+  // log2(e)), so that the kernel's base-2 scale is always positive
+  int s_negate;
   // Single pass only: a partition of the same rows computed by another pass (the
   // shared prefix of a cascade), merged into the result before it is written.
   // Workspace layout of pa_decode_partial with prior_splits partitions; the prior

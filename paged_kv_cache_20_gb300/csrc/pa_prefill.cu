@@ -1,5 +1,6 @@
 // pa_prefill.cu -- host launchers of the many-row (chunked-prefill / shared-prefix)
 // tensor-core kernel, both element types.
+#include <algorithm>
 #include <atomic>
 
 #include "pa_launch.h"
@@ -32,11 +33,21 @@ cudaError_t launch_prefill_t(const CUtensorMap &kmap, const CUtensorMap &vmap, c
   const long long rows_per_seq = (long long)a.q_len * a.group;
   const long long rows = a.shared_prefix > 0 ? rows_per_seq * a.num_seqs : rows_per_seq;
   const long long nz = a.shared_prefix > 0 ? a.num_splits : (long long)a.num_seqs * a.num_splits;
-  const long long gx = (rows + kTcRows - 1) / kTcRows * nz;
-  if (gx <= 0) return cudaSuccess;
-  if (gx > 0x7fffffffLL || a.num_kv_heads > 65535) return cudaErrorInvalidConfiguration;
+  const long long units = (rows + kTcRows - 1) / kTcRows * nz * a.num_kv_heads;
+  if (units <= 0) return cudaSuccess;
+  if (units > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  // persistent CTAs, one per SM (the shared memory and tensor memory of one CTA
+  // fill an SM): each walks a list of units
+  static std::atomic<int> sm_count[64];
+  int sms = sm_count[dev].load(std::memory_order_relaxed);
+  if (sms <= 0) {
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    sm_count[dev].store(sms, std::memory_order_relaxed);
+  }
+  const long long gx = std::min<long long>(units, std::max(1, sms));
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)gx, (unsigned)a.num_kv_heads, 1);
+  cfg.gridDim = dim3((unsigned)gx, 1, 1);
   cfg.blockDim = dim3(kTcThreads, 1, 1);
   cfg.dynamicSmemBytes = kSmem;
   cfg.stream = st;

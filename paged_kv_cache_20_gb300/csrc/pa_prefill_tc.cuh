@@ -11,8 +11,12 @@
 // "LLM推理与服务：面试问题与推荐回答" Q14; one physical copy of a shared prefix is
 // Q2-Q3 of the same page and "Scaling Book 入门第 11 章" §11.4.
 //
-// One CTA = one KV head x 128 query rows (the MMA's M); the cache is walked in
-// chunks of 128 positions (8 blocks):
+// A unit = one KV head x one partition of the walked blocks x 128 query rows (the
+// MMA's M).  The CTAs are persistent, one per SM, and each walks its own list of
+// units (longest first, see tc_unit); the cache is walked in chunks of 128
+// positions (8 blocks), and every ring, buffer and barrier runs on through the
+// chunks of all the CTA's units, so the next unit's loads and scores start while
+// the previous one is finishing:
 //   warps 0, 1  TMA producers: the K (warp 0) and V (warp 1) tiles of a chunk's 8
 //               blocks into rings of NK and NV stages (zero fill for blocks past the
 //               walk or bad ids).  A K stage is released as soon as the S MMA that
@@ -31,8 +35,13 @@
 //               and the final O / l is the same quotient); at the end O / l (or
 //               the partial statistics) for its half of the columns.
 // S_{j+1} and S_{j+2} are computed while the softmax works on S_j.  S_{j+3} is issued
-// only after the commit of P_j V_j (the last reader of buffer j % 3) has fired.  bf16 P is split into hi + lo bf16 parts, both multiplied by V, so
-// that P keeps ~16 significant bits as the fp16 path does.  Every wait is bounded.
+// only after the commit of P_j V_j (the last reader of buffer j % 3) has fired.  A
+// unit's Q replaces the previous one once that unit's last S MMA has completed
+// (by TMA from the S thread, or written by the softmax warps before the previous
+// unit's epilogue); a unit's first P V overwrites O, which the softmax warps have
+// read out before they announce that unit's first P.  bf16 P is split into hi + lo
+// bf16 parts, both multiplied by V, so that P keeps ~16 significant bits as the
+// fp16 path does.  Every wait is bounded.
 #pragma once
 
 #include "pa_decode.cuh"
@@ -47,6 +56,7 @@ constexpr int kTcCtl = 4;                          // K, V producers; P V and S 
 constexpr int kTcSoft = 8;                         // softmax warps
 constexpr int kTcThreads = 32 * (kTcCtl + kTcSoft);
 constexpr float kTcRescale = 8.f;                  // base-2 growth that forces a rescale
+constexpr int kTcScrBytes = 32 * 64;               // epilogue scratch per softmax warp
 
 template <typename T, int D>
 struct TcLayout {
@@ -60,11 +70,23 @@ struct TcLayout {
   // 64h + [0, 32) (hi) and [32, 64) (lo, bf16 only) of the buffer
   static constexpr int kTmemCols = 512;
   static constexpr int kColS = 128;
-  static constexpr int smem_bytes(int nk, int nv) { return kOffStages + (nk + nv) * kKVBytes + 1024; }
+  // after the rings: a 2 KiB scratch per softmax warp (the epilogue's transpose)
+  static constexpr int kScrBytes = kTcSoft * kTcScrBytes;
+  static constexpr int smem_bytes(int nk, int nv) {
+    return kOffStages + (nk + nv) * kKVBytes + kScrBytes + 1024;
+  }
 };
 
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+// max(a, b, c) in one instruction (sm_100 and later); NaN inputs are ignored as
+// by fmaxf
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
 }
 
 // 2^x (PTX ex2.approx, flushing subnormal results to zero: a weight below 2^-126
@@ -73,6 +95,151 @@ __device__ __forceinline__ float ex2_ftz(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+
+// n / d for 0 <= n < 2^31 by a multiply and a shift (Granlund and Montgomery,
+// "Division by invariant integers using multiplication", 1994): with l = ceil(log2 d)
+// and m = ceil(2^(31+l) / d) < 2^32, floor(n m / 2^(31+l)) = floor(n / d), because
+// the rounding of m adds less than n / 2^(31+l) < 1 / d to n / d.
+struct FastDiv {
+  uint32_t m;
+  int s, d;
+  __device__ __forceinline__ void init(int dv) {
+    d = dv;
+    m = 0u;
+    s = 0;
+    if (dv > 1) {
+      const int l = 32 - __clz(dv - 1);
+      m = (uint32_t)(((1ull << (31 + l)) + (unsigned long long)(dv - 1)) / (unsigned long long)dv);
+      s = l - 1;
+    }
+  }
+  __device__ __forceinline__ int div(int n) const {
+    return d <= 1 ? n : (int)(__umulhi((uint32_t)n, m) >> s);
+  }
+};
+
+// The launch's unit geometry, computed once per thread.
+struct TcGeo {
+  FastDiv kvh, splits, nrb, group, rps;
+  int rows_per_seq, rows_total, nrb_n;
+  long long units;
+  __device__ __forceinline__ void init(const DecodeArgs &a) {
+    const bool shared = a.shared_prefix > 0;
+    rows_per_seq = a.q_len * a.group;
+    rows_total = shared ? a.num_seqs * rows_per_seq : rows_per_seq;
+    nrb_n = (rows_total + kTcRows - 1) / kTcRows;
+    units = (long long)nrb_n * a.num_splits * (shared ? 1 : a.num_seqs) * a.num_kv_heads;
+    kvh.init(a.num_kv_heads);
+    splits.init(a.num_splits);
+    nrb.init(nrb_n);
+    group.init(a.group);
+    rps.init(rows_per_seq);
+  }
+};
+
+// One unit of work: a KV head x a partition of the walked blocks x 128 query rows.
+// Every warp derives it from the unit's index alone, so the roles agree on it
+// without exchanging anything.
+struct TcUnit {
+  int valid;
+  int kvh, zseq, split, row_base, tseq;
+  int tb, te;      // the partition: blocks [tb, te) of the walked table row
+  int t_end, nch;  // blocks any row of the unit sees, and the chunks covering them
+  int vis_end;     // no row of the unit uses a position at or past it
+  // the caller's row of the unit (row >= 0)
+  int rvalid, rseq, ru, rh, vis;
+};
+
+// Units are numbered longest first: sequences by decreasing context length
+// (s_order), within a sequence the last row block (the one that sees the most
+// positions) first, then partition, then KV head.  CTA c takes units
+// c, 2G - 1 - c, 2G + c, 4G - 1 - c, ... of G CTAs (back and forth), so every CTA
+// gets one long and one short unit of each pair of rounds.  All lanes of the warp
+// call it (the shared-prefix limit is a warp maximum).
+__device__ __forceinline__ TcUnit tc_unit(const DecodeArgs &a, const TcGeo &geo, int k,
+                                          const int *s_order, const int *lens, int lane, int row,
+                                          bool rec) {
+  TcUnit t;
+  const int G = gridDim.x;
+  const bool shared = a.shared_prefix > 0;
+  const long long id = (long long)k * G + ((k & 1) ? G - 1 - (int)blockIdx.x : (int)blockIdx.x);
+  t.valid = id < geo.units;
+  t.nch = 0;
+  t.rvalid = 0;
+  if (!t.valid) return t;
+  int r = (int)id;  // units < 2^31 (host check)
+  int q = geo.kvh.div(r);
+  t.kvh = r - q * a.num_kv_heads;
+  r = q;
+  q = geo.splits.div(r);
+  t.split = r - q * a.num_splits;
+  r = q;
+  q = geo.nrb.div(r);
+  const int rbi = r - q * geo.nrb_n;
+  r = q;
+  t.zseq = shared ? 0 : (a.lpt ? s_order[r] : r);
+  t.row_base = (geo.nrb_n - 1 - rbi) * kTcRows;
+  t.tseq = t.zseq;  // block-table row that is walked (row 0 for a shared prefix)
+
+  int nb;
+  const int Lt = max(0, lens[t.tseq]);
+  if (shared) {
+    nb = min(a.shared_prefix, a.max_blocks_per_seq);
+  } else {
+    nb = (Lt + kTileTokens - 1) / kTileTokens;
+    if (nb > a.max_blocks_per_seq) {
+      if (rec && t.kvh == 0 && t.split == 0) record_error(a.err, kErrCheck);
+      nb = a.max_blocks_per_seq;
+    }
+  }
+  // blocks before first_block belong to another pass (a cascade's shared prefix);
+  // the rest is cut into num_splits equal partitions
+  const int fb = shared ? 0 : min(nb, a.first_block);
+  const int per = (nb - fb + a.num_splits - 1) / a.num_splits;
+  t.tb = min(nb, fb + t.split * per);
+  t.te = min(nb, t.tb + per);
+
+  // the largest causal limit of the unit's rows: its last row's (one sequence), or
+  // the largest over the sequences whose rows it holds (shared prefix)
+  const int row_last = min(t.row_base + kTcRows, geo.rows_total) - 1;
+  int mx;
+  if (!shared) {
+    mx = max(0, Lt - a.q_len + geo.group.div(row_last) + 1);
+  } else {
+    const int rps = geo.rows_per_seq;
+    const int s0 = geo.rps.div(t.row_base), s1 = geo.rps.div(row_last);
+    mx = 0;
+    for (int sq = s0 + lane; sq <= s1; sq += 32) {
+      const int last = min(row_last, sq * rps + rps - 1) - sq * rps;
+      const int visible = min(max(0, lens[sq]) - a.q_len + geo.group.div(last) + 1, nb * kTileTokens);
+      mx = max(mx, visible);
+    }
+    mx = __reduce_max_sync(0xffffffffu, mx);
+  }
+  t.t_end = min(t.te, max(t.tb, (mx + kTileTokens - 1) / kTileTokens));
+  t.nch = (t.t_end - t.tb + kTcBlocks - 1) / kTcBlocks;
+  t.vis_end = min(t.te * kTileTokens, mx);
+
+  t.rseq = t.ru = t.rh = t.vis = 0;
+  const int rho = t.row_base + row;
+  if (row >= 0 && rho < geo.rows_total) {
+    int sq = t.zseq, rr = rho;
+    if (shared) {
+      sq = geo.rps.div(rho);
+      rr = rho - sq * geo.rows_per_seq;
+    }
+    const int u = geo.group.div(rr);
+    const int L = shared ? max(0, lens[sq]) : Lt;
+    int visible = L - a.q_len + u + 1;  // causal limit
+    if (shared) visible = min(visible, nb * kTileTokens);
+    t.rvalid = 1;
+    t.rseq = sq;
+    t.ru = u;
+    t.rh = t.kvh * a.group + (rr - u * a.group);
+    t.vis = visible;
+  }
+  return t;
 }
 
 template <typename T, int D, int NK, int NV, bool PARTIAL>
@@ -99,12 +266,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   __shared__ __align__(8) uint64_t bfree[3];    // P_j V_j complete, by S/P buffer j % 3
   __shared__ __align__(8) uint64_t q_ready;      // Q written by the softmax threads
   __shared__ __align__(8) uint64_t q_full;       // Q landed by TMA
+  __shared__ __align__(8) uint64_t q_free;       // a unit's last S MMA has read Q
   __shared__ __align__(8) uint64_t mma_fin;
   __shared__ __align__(8) uint64_t xbar[4];      // partner exchange, per group of 32 rows
   __shared__ float xval[2][2][kTcRows];           // [parity][column half][row]
+  __shared__ int s_order[kLptMaxSeqs];            // rank -> sequence, longest first
+  __shared__ int s_lens[kLptMaxSeqs];
   __shared__ uint32_t s_tmem;
   __shared__ int s_failed;
-  __shared__ int s_maxlim;
 
   griddep_wait();
   griddep_launch_dependents();
@@ -114,41 +283,33 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
   const uint32_t sK = base + Lay::kOffStages;  // K ring: NK x kKVBytes
   const uint32_t sV = sK + NK * Lay::kKVBytes;  // V ring: NV x kKVBytes
-
-  // ---- the unit: grid.x = (sequence, partition, row block), row block fastest ----
+  const uint32_t sScr = sV + NV * Lay::kKVBytes;  // epilogue scratch
   const bool shared = a.shared_prefix > 0;
-  const int kvh = blockIdx.y;
-  const int rows_per_seq = a.q_len * a.group;
-  const int rows_total = shared ? a.num_seqs * rows_per_seq : rows_per_seq;
-  const int nrb = (rows_total + kTcRows - 1) / kTcRows;
-  const int zz = blockIdx.x / nrb;
-  const int split = zz % a.num_splits;
-  const int zseq = zz / a.num_splits;
-  // the last row blocks see the most positions (causal): they are scheduled first
-  const int row_base = (nrb - 1 - (int)(blockIdx.x % nrb)) * kTcRows;
-  const int tseq = shared ? 0 : zseq;  // block-table row that is walked
 
-  int nb;
-  const int Lt = max(0, __ldg(a.context_lens + tseq));
-  if (shared) {
-    nb = min(a.shared_prefix, a.max_blocks_per_seq);
-  } else {
-    nb = (Lt + kTileTokens - 1) / kTileTokens;
-    if (nb > a.max_blocks_per_seq) {
-      if (threadIdx.x == 0 && kvh == 0) record_error(a.err, kErrCheck);
-      nb = a.max_blocks_per_seq;
+  // the context lengths (read at every unit: a global load there would stall each
+  // role between units) and their longest-first order (rank by counting; ties by
+  // index)
+  const int *lens = a.context_lens;
+  if (a.num_seqs <= kLptMaxSeqs) {
+    const int n = a.num_seqs;
+    for (int i = threadIdx.x; i < n; i += blockDim.x) s_lens[i] = max(0, __ldg(a.context_lens + i));
+    lens = s_lens;
+    __syncthreads();
+  }
+  if (!shared && a.lpt) {
+    const int n = a.num_seqs;
+    for (int i = threadIdx.x; i < n; i += blockDim.x) {
+      const int li = s_lens[i];
+      int rk = 0;
+      for (int j = 0; j < n; ++j) {
+        const int lj = s_lens[j];
+        rk += (lj > li) | ((lj == li) & (j < i));
+      }
+      s_order[rk] = i;
     }
   }
-  // blocks before first_block belong to another pass (a cascade's shared prefix);
-  // the rest is cut into num_splits equal partitions
-  const int fb = shared ? 0 : min(nb, a.first_block);
-  const int per = (nb - fb + a.num_splits - 1) / a.num_splits;
-  const int tb = min(nb, fb + split * per);
-  const int te = min(nb, tb + per);
-
   if (threadIdx.x == 0) {
     s_failed = 0;
-    s_maxlim = 0;
     for (int s = 0; s < NK; ++s) {
       mbar_init(smem_u32(&k_full[s]), 1);
       mbar_init(smem_u32(&k_empty[s]), 1);
@@ -165,6 +326,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     for (int b = 0; b < 3; ++b) mbar_init(smem_u32(&bfree[b]), 1);
     mbar_init(smem_u32(&q_ready), kTcSoft);
     mbar_init(smem_u32(&q_full), 1);
+    mbar_init(smem_u32(&q_free), 1);
     mbar_init(smem_u32(&mma_fin), 2);  // one commit from each issuing thread
     for (int q = 0; q < 4; ++q) mbar_init(smem_u32(&xbar[q]), 2);
     fence_mbar_init();
@@ -176,51 +338,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     tc::alloc(smem_u32(&s_tmem), Lay::kTmemCols);
     tc::relinquish();
   }
-  __syncthreads();  // s_maxlim, barriers initialised
-
-  // ---- this thread's query row (softmax warps): row = TMEM lane ----
-  const bool sm_warp = warp >= kTcCtl;
-  const int hc = sm_warp ? (warp - kTcCtl) >> 2 : 0;  // column half of this warp
-  const int q4 = warp & 3;                            // lane group (TMEM access rule)
-  const int row = 32 * q4 + lane;
-  const T *qrow = nullptr;
-  int lim = 0, rseq = 0, ru = 0, rh = 0;
-  if (sm_warp) {
-    const int rho = row_base + row;
-    if (rho < rows_total) {
-      const int sq = shared ? rho / rows_per_seq : zseq;
-      const int rr = rho % rows_per_seq;
-      const int u = rr / a.group, h = kvh * a.group + rr % a.group;
-      const int L = max(0, __ldg(a.context_lens + sq));
-      int visible = L - a.q_len + u + 1;  // causal limit
-      if (shared) visible = min(visible, nb * kTileTokens);
-      rseq = sq;
-      ru = u;
-      rh = h;
-      lim = visible;
-      qrow = static_cast<const T *>(a.q) + ((size_t)(sq * a.q_len + u) * a.num_q_heads + h) * D;
-      if (hc == 0) atomicMax(&s_maxlim, visible);
-    }
-  }
   tc::fence_before();
-  __syncthreads();
+  __syncthreads();  // order, barriers and tensor memory ready
   tc::fence_after();
   const uint32_t tmem = s_tmem;
-  // blocks any row of this CTA can see, and the chunks covering them
-  const int t_end = min(te, max(tb, (s_maxlim + kTileTokens - 1) / kTileTokens));
-  const int nch = (t_end - tb + kTcBlocks - 1) / kTcBlocks;
-  const int vis_end = min(te * kTileTokens, s_maxlim);  // no row uses a position past it
   volatile int *failed = &s_failed;
-  if (a.q_tma && nch > 0 && threadIdx.x == 0) {
-    // the row block's 128 query rows (token, head): tokens [t0, t0 + 128/g) of heads
-    // [kvh*g, kvh*g + g) (rows past the sequence's last token are never written
-    // back; past the tensor they are zero-filled).  The S thread waits for them.
-    const int t0 = (shared ? 0 : zseq * a.q_len) + row_base / a.group;
-    const uint32_t bar = smem_u32(&q_full);
-    mbar_arrive_expect_tx(bar, Lay::kQBytes);
-#pragma unroll
-    for (int hh = 0; hh < H; ++hh) tma_load_3d(base + hh * (kTcRows * 128), &qmap, hh * 64, kvh * a.group, t0, bar);
-  }
+  TcGeo geo;
+  geo.init(a);
 
   if (warp < 2) {
     // ------------------------------------------------------------ TMA producers
@@ -230,61 +354,71 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     uint64_t *full = is_k ? k_full : v_full;
     uint64_t *empty = is_k ? k_empty : v_empty;
     const int NS = is_k ? NK : NV;
-    const int32_t *table = a.block_tables + (size_t)tseq * a.max_blocks_per_seq;
-    int issued = 0;
+    int g = 0, issued = 0;  // chunks of this CTA so far (all units), loads issued
     bool ok = true;
-    // block-table window: lane l holds entry tb + 32w + l of window w (4 chunks);
-    // the next window is loaded a whole window ahead, so no TMA issue waits on a
-    // table load
-    auto table_at = [&](int w) -> int {
-      const int blk = tb + 32 * w + lane;
-      return blk < t_end ? __ldg(table + blk) : -1;
-    };
-    int win_cur = table_at(0), win_nxt = table_at(1);
-    for (int ch = 0; ch < nch; ++ch) {
-      const int s = ch % NS;
-      if (ch > 0 && (ch & 3) == 0) {  // next window of 32 entries
-        win_cur = win_nxt;
-        win_nxt = table_at((ch >> 2) + 1);
+    for (int k = 0; ok; ++k) {
+      const TcUnit t = tc_unit(a, geo, k, s_order, lens, lane, -1, is_k && lane == 0);
+      if (!t.valid) break;
+      const int32_t *table = a.block_tables + (size_t)t.tseq * a.max_blocks_per_seq;
+      // block-table window: lane l holds entry tb + 32w + l of window w (4 chunks);
+      // the next window is loaded a whole window ahead, so no TMA issue waits on a
+      // table load
+      auto table_at = [&](int w) -> int {
+        const int blk = t.tb + 32 * w + lane;
+        return blk < t.t_end ? __ldg(table + blk) : -1;
+      };
+      int win_cur = 0, win_nxt = 0;
+      if (t.nch > 0) {
+        win_cur = table_at(0);
+        win_nxt = table_at(1);
       }
-      // a fresh barrier counts as released (parity 1 of the phase before the first)
-      bool fr = mbar_wait_bounded(smem_u32(&empty[s]), ((ch / NS) & 1) ^ 1);
-      fr = __all_sync(0xffffffffu, fr);
-      if (!fr || *failed) {
-        ok = fr;
-        break;
-      }
-      const int blk = tb + ch * kTcBlocks + lane;
-      const int phys = __shfl_sync(0xffffffffu, win_cur, ((ch & 3) * kTcBlocks + lane) & 31);
-      int z = -1;  // outside the tensor map: zero fill
-      if (lane < kTcBlocks && blk < t_end) {
-        if (phys >= 0 && phys < a.num_blocks)
-          z = phys * a.num_kv_heads + kvh;
-        else if (is_k)
-          record_error(a.err, kErrCheck);
-      }
-      const uint32_t bar = smem_u32(&full[s]);
-      if (lane == 0) mbar_arrive_expect_tx(bar, Lay::kKVBytes);
-      __syncwarp();
-      if (lane < kTcBlocks) {
-        const uint32_t dst = ring + s * Lay::kKVBytes + lane * (kTileTokens * 128);
+      for (int ch = 0; ch < t.nch; ++ch) {
+        const int gg = g + ch;
+        const int s = gg % NS;
+        if (ch > 0 && (ch & 3) == 0) {  // next window of 32 entries
+          win_cur = win_nxt;
+          win_nxt = table_at((ch >> 2) + 1);
+        }
+        // a fresh barrier counts as released (parity 1 of the phase before the first)
+        bool fr = mbar_wait_bounded(smem_u32(&empty[s]), ((gg / NS) & 1) ^ 1);
+        fr = __all_sync(0xffffffffu, fr);
+        if (!fr || *failed) {
+          ok = false;
+          if (!fr && lane == 0) {
+            record_error(a.err, kErrTimeout);
+            atomicExch(&s_failed, 1);
+          }
+          break;
+        }
+        const int blk = t.tb + ch * kTcBlocks + lane;
+        const int phys = __shfl_sync(0xffffffffu, win_cur, ((ch & 3) * kTcBlocks + lane) & 31);
+        int z = -1;  // outside the tensor map: zero fill
+        if (lane < kTcBlocks && blk < t.t_end) {
+          if (phys >= 0 && phys < a.num_blocks)
+            z = phys * a.num_kv_heads + t.kvh;
+          else if (is_k)
+            record_error(a.err, kErrCheck);
+        }
+        const uint32_t bar = smem_u32(&full[s]);
+        if (lane == 0) mbar_arrive_expect_tx(bar, Lay::kKVBytes);
+        __syncwarp();
+        if (lane < kTcBlocks) {
+          const uint32_t dst = ring + s * Lay::kKVBytes + lane * (kTileTokens * 128);
 #pragma unroll
-        for (int hh = 0; hh < H; ++hh) tma_load_3d(dst + hh * (kTcChunk * 128), map, hh * 64, 0, z, bar);
+          for (int hh = 0; hh < H; ++hh) tma_load_3d(dst + hh * (kTcChunk * 128), map, hh * 64, 0, z, bar);
+        }
+        issued = gg + 1;
       }
-      issued = ch + 1;
+      g += t.nch;
     }
-    if (!ok && lane == 0) {
-      record_error(a.err, kErrTimeout);
-      atomicExch(&s_failed, 1);
-    }
-    if (*failed) {
-      // the loads still in flight land before the CTA may exit (bounded)
-      for (int k = max(0, issued - NS); k < issued; ++k)
-        (void)mbar_wait_bounded(smem_u32(&full[k % NS]), (k / NS) & 1);
-    }
+    // the last loads have landed before the CTA may exit (bounded; at once unless a
+    // consumer gave up)
+    for (int k = max(0, issued - NS); k < issued; ++k)
+      (void)mbar_wait_bounded(smem_u32(&full[k % NS]), (k / NS) & 1);
   } else if (warp == 2 || warp == 3) {
     // ------------------------------------------------------------ MMA issue
-    constexpr uint32_t kIdS = tc::idesc_f16(kTcRows, kTcChunk, kBf16, false);
+    // bit 13 of the instruction descriptor negates A (Q): S = -Q K^T for a negative scale
+    const uint32_t kIdS = tc::idesc_f16(kTcRows, kTcChunk, kBf16, false) | (a.s_negate ? (1u << 13) : 0u);
     constexpr uint32_t kIdO = tc::idesc_f16(kTcRows, D, kBf16, true);
     // descriptors of the first stage; the others differ only in the start address
     // field (bits 0-13, address / 16), so an offset is a plain addition
@@ -297,59 +431,101 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       w = __all_sync(0xffffffffu, w);
       return w && !*failed;
     };
+    int g = 0;
     if (warp == 3) {
-      // S_j = Q K_j^T into S buffer j % 3
-      if (nch > 0) ok = a.q_tma ? wait_all(&q_full, 0) : wait_all(&q_ready, 0);
-      for (int j = 0; ok && j < nch; ++j) {
-        ok = wait_all(&k_full[j % NK], (j / NK) & 1);
-        // the buffer's last reader, P_{j-3} V_{j-3}, has completed (its barrier is at
-        // most one phase behind: P_j V_j needs S_j first)
-        if (ok && j >= 3) ok = wait_all(&bfree[j % 3], ((j - 3) / 3) & 1);
-        if (!ok) break;
-        tc::fence_after();
-        if (lane == 0) {
-          const uint64_t kd = dK + (uint64_t)(((j % NK) * Lay::kKVBytes) >> 4);
-          const uint32_t dst = tmem + Lay::kColS + kTcChunk * (j % 3);
+      // S_j = Q K_j^T into S buffer j % 3 (j counts the chunks of all units)
+      int qn = 0;            // units with chunks so far: the phase of q_full / q_ready / q_free
+      bool q_flight = false;  // a Q load issued and not yet seen landed
+      for (int k = 0; ok; ++k) {
+        const TcUnit t = tc_unit(a, geo, k, s_order, lens, lane, -1, false);
+        if (!t.valid) break;
+        if (t.nch == 0) continue;
+        if (a.q_tma) {
+          // the unit's 128 query rows (token, head): tokens [t0, t0 + 128/g) of heads
+          // [kvh*g, kvh*g + g) (rows past the sequence's last token are never written
+          // back; past the tensor they are zero-filled), once the previous unit's S
+          // MMAs have finished reading the buffer
+          if (qn > 0) ok = wait_all(&q_free, (qn - 1) & 1);
+          if (!ok) break;
+          if (lane == 0) {
+            const int t0 = (shared ? 0 : t.zseq * a.q_len) + t.row_base / a.group;
+            const uint32_t bar = smem_u32(&q_full);
+            mbar_arrive_expect_tx(bar, Lay::kQBytes);
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            // a K step of 16 columns: +32 bytes inside the 128-byte row, +one
-            // column-group block every 4 steps (descriptor addresses count 16 bytes)
-            tc::mma_f16(dst, dQ + (uint64_t)(((kk >> 2) * (kTcRows * 128) + (kk & 3) * 32) >> 4),
-                        kd + (uint64_t)(((kk >> 2) * (kTcChunk * 128) + (kk & 3) * 32) >> 4), kIdS,
-                        kk > 0 ? 1u : 0u);
+            for (int hh = 0; hh < H; ++hh)
+              tma_load_3d(base + hh * (kTcRows * 128), &qmap, hh * 64, t.kvh * a.group, t0, bar);
           }
-          tc::commit(smem_u32(&s_full[j % 3]));
-          tc::commit(smem_u32(&k_empty[j % NK]));
+          __syncwarp();
+          q_flight = true;
+          ok = wait_all(&q_full, qn & 1);
+          if (!ok) break;
+          q_flight = false;
+        } else {
+          ok = wait_all(&q_ready, qn & 1);
+          if (!ok) break;
         }
-        __syncwarp();
+        for (int j = 0; ok && j < t.nch; ++j) {
+          const int gg = g + j;
+          ok = wait_all(&k_full[gg % NK], (gg / NK) & 1);
+          // the buffer's last reader, P_{j-3} V_{j-3}, has completed (its barrier is at
+          // most one phase behind: P_j V_j needs S_j first)
+          if (ok && gg >= 3) ok = wait_all(&bfree[gg % 3], ((gg - 3) / 3) & 1);
+          if (!ok) break;
+          tc::fence_after();
+          if (lane == 0) {
+            const uint64_t kd = dK + (uint64_t)(((gg % NK) * Lay::kKVBytes) >> 4);
+            const uint32_t dst = tmem + Lay::kColS + kTcChunk * (gg % 3);
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+              // a K step of 16 columns: +32 bytes inside the 128-byte row, +one
+              // column-group block every 4 steps (descriptor addresses count 16 bytes)
+              tc::mma_f16(dst, dQ + (uint64_t)(((kk >> 2) * (kTcRows * 128) + (kk & 3) * 32) >> 4),
+                          kd + (uint64_t)(((kk >> 2) * (kTcChunk * 128) + (kk & 3) * 32) >> 4), kIdS,
+                          kk > 0 ? 1u : 0u);
+            }
+            tc::commit(smem_u32(&s_full[gg % 3]));
+            tc::commit(smem_u32(&k_empty[gg % NK]));
+            if (j == t.nch - 1) tc::commit(smem_u32(&q_free));  // Q may be replaced
+          }
+          __syncwarp();
+        }
+        g += t.nch;
+        ++qn;
       }
+      if (q_flight) (void)mbar_wait_bounded(smem_u32(&q_full), (qn & 1));  // lands before exit
     } else {
-      // O += P_j V_j, P from S buffer j % 3
-      for (int j = 0; ok && j < nch; ++j) {
-        ok = wait_all(&v_full[j % NV], (j / NV) & 1);
-        if (ok) ok = wait_all(&p_full, j & 1);
-        if (!ok) break;
-        tc::fence_after();
-        if (lane == 0) {
-          mbar_arrive(smem_u32(&p_ack));  // the softmax may announce P_{j+1}
-          const uint64_t vd = dV + (uint64_t)(((j % NV) * Lay::kKVBytes) >> 4);
-          const uint32_t pa = tmem + Lay::kColS + kTcChunk * (j % 3);
+      // O += P_j V_j, P from S buffer j % 3; a unit's first chunk overwrites O
+      for (int k = 0; ok; ++k) {
+        const TcUnit t = tc_unit(a, geo, k, s_order, lens, lane, -1, false);
+        if (!t.valid) break;
+        for (int j = 0; ok && j < t.nch; ++j) {
+          const int gg = g + j;
+          ok = wait_all(&v_full[gg % NV], (gg / NV) & 1);
+          if (ok) ok = wait_all(&p_full, gg & 1);
+          if (!ok) break;
+          tc::fence_after();
+          if (lane == 0) {
+            mbar_arrive(smem_u32(&p_ack));  // the softmax may announce P_{j+1}
+            const uint64_t vd = dV + (uint64_t)(((gg % NV) * Lay::kKVBytes) >> 4);
+            const uint32_t pa = tmem + Lay::kColS + kTcChunk * (gg % 3);
 #pragma unroll
-          for (int kk = 0; kk < kTcChunk / 16; ++kk) {
-            // V is N-major (head_dim contiguous): atoms of 64 columns kTcChunk*128
-            // bytes apart (the descriptor's leading offset), groups of 8 positions
-            // 1024 bytes apart; a K step of 16 positions is 2048 bytes of V and 8
-            // tensor-memory columns of P (positions 64h.. in columns 64h.., hi then lo)
-            const uint64_t bd = vd + (uint64_t)((kk * (16 * 128)) >> 4);
-            const uint32_t pc = pa + (kk >> 2) * 64 + (kk & 3) * 8;
-            tc::mma_f16_ts(tmem, pc, bd, kIdO, (j > 0 || kk > 0) ? 1u : 0u);
-            if (Lay::kSplitP) tc::mma_f16_ts(tmem, pc + 32, bd, kIdO, 1u);
+            for (int kk = 0; kk < kTcChunk / 16; ++kk) {
+              // V is N-major (head_dim contiguous): atoms of 64 columns kTcChunk*128
+              // bytes apart (the descriptor's leading offset), groups of 8 positions
+              // 1024 bytes apart; a K step of 16 positions is 2048 bytes of V and 8
+              // tensor-memory columns of P (positions 64h.. in columns 64h.., hi then lo)
+              const uint64_t bd = vd + (uint64_t)((kk * (16 * 128)) >> 4);
+              const uint32_t pc = pa + (kk >> 2) * 64 + (kk & 3) * 8;
+              tc::mma_f16_ts(tmem, pc, bd, kIdO, (j > 0 || kk > 0) ? 1u : 0u);
+              if (Lay::kSplitP) tc::mma_f16_ts(tmem, pc + 32, bd, kIdO, 1u);
+            }
+            tc::commit(smem_u32(&o_done[gg & 1]));
+            tc::commit(smem_u32(&v_empty[gg % NV]));
+            tc::commit(smem_u32(&bfree[gg % 3]));
           }
-          tc::commit(smem_u32(&o_done[j & 1]));
-          tc::commit(smem_u32(&v_empty[j % NV]));
-          tc::commit(smem_u32(&bfree[j % 3]));
+          __syncwarp();
         }
-        __syncwarp();
+        g += t.nch;
       }
     }
     if (!ok && lane == 0) {
@@ -362,32 +538,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     (void)mbar_wait_bounded(smem_u32(&mma_fin), 0);
   } else {
     // ------------------------------------------------------------ softmax rows
+    const int hc = (warp - kTcCtl) >> 2;  // column half of this warp
+    const int q4 = warp & 3;              // lane group (TMEM access rule)
+    const int row = 32 * q4 + lane;       // = TMEM lane
     const uint32_t trow = tmem + ((uint32_t)(32 * q4) << 16);
-    // Q row -> shared memory in the swizzled K-major layout of the MMA's A operand
-    // (each warp of the pair writes half of the row's 16-byte chunks), unless TMA
-    // brings it
-#pragma unroll
-    for (int ci = 0; ci < (a.q_tma ? 0 : D / 16); ++ci) {
-      const int c = hc * (D / 16) + ci;
-      uint4 v = make_uint4(0u, 0u, 0u, 0u);
-      if (qrow) v = __ldg(reinterpret_cast<const uint4 *>(qrow) + c);
-      const int hh = c >> 3, cc = c & 7;
-      const uint32_t addr = base + hh * (kTcRows * 128) + row * 128 + ((cc ^ (row & 7)) << 4);
-      asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y),
-                   "r"(v.z), "r"(v.w)
-                   : "memory");
-    }
-    fence_proxy_async_smem();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(smem_u32(&q_ready));
-
+    const int tid = (warp - kTcCtl) * 32 + lane;  // 0..255
     const float rs = a.scale_log2;
     const uint64_t rs2 = tc::f2pack(rs, rs);
-    const int lim_row = min(lim, te * kTileTokens);  // padding rows: 0
-    float m_run = -INFINITY, l = 0.f;
     bool ok = true;
     int xph = 0;  // exchanges done (phase of xbar[q4])
-    const int tid = (warp - kTcCtl) * 32 + lane;  // 0..255
     // max (or, at the end, sum) of this warp's value and the partner warp's
     auto exchange = [&](float v, bool is_max) -> float {
       xval[xph & 1][hc][row] = v;
@@ -400,206 +559,327 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       ++xph;
       return is_max ? fmaxf(v, o) : v + o;
     };
-    for (int j = 0; j < nch; ++j) {
-      const int b = j % 3;
-      const uint32_t ts = trow + Lay::kColS + kTcChunk * b + 64 * hc;  // this warp's columns
-      bool w = mbar_wait_bounded(smem_u32(&s_full[b]), (j / 3) & 1);
-      w = __all_sync(0xffffffffu, w);
-      if (!w) {
-        ok = false;
-        break;
+    auto q_ptr = [&](const TcUnit &t) -> const T * {
+      return t.rvalid ? static_cast<const T *>(a.q) +
+                            ((size_t)(t.rseq * a.q_len + t.ru) * a.num_q_heads + t.rh) * D
+                      : nullptr;
+    };
+    // Q row -> shared memory in the swizzled K-major layout of the MMA's A operand
+    // (each warp of the pair writes half of the row's 16-byte chunks)
+    auto write_q = [&](const TcUnit &t) {
+      const T *qrow = q_ptr(t);
+#pragma unroll
+      for (int ci = 0; ci < D / 16; ++ci) {
+        const int c = hc * (D / 16) + ci;
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (qrow) v = __ldg(reinterpret_cast<const uint4 *>(qrow) + c);
+        const int hh = c >> 3, cc = c & 7;
+        const uint32_t addr = base + hh * (kTcRows * 128) + row * 128 + ((cc ^ (row & 7)) << 4);
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y),
+                     "r"(v.z), "r"(v.w)
+                     : "memory");
       }
-      tc::fence_after();
-      const int c0 = (tb + j * kTcBlocks) * kTileTokens + 64 * hc;  // first position here
-      float sv[64];
-      tc::ld64(ts, sv);
-      // scale to base-2 units (two lanes per instruction), mask, row maximum
-#pragma unroll
-      for (int c = 0; c < 64; c += 2) {
-        const uint64_t x = tc::fmul2(tc::f2pack(sv[c], sv[c + 1]), rs2);
-        tc::f2unpack(x, sv[c], sv[c + 1]);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&q_ready));
+    };
+
+    // ---- epilogue of a finished unit: O / l (or the unnormalised partial and its
+    // statistics) from tensor memory to global memory.  The warp's 32 rows pass
+    // through its shared-memory scratch, so that a store instruction writes 64-byte
+    // pieces of 8 rows instead of 16 bytes of 32 rows (32 lines an instruction).
+    // roff: the row's output (or workspace) row, -1 for padding rows.
+    const uint32_t scr = sScr + (uint32_t)(warp - kTcCtl) * kTcScrBytes;
+    auto epilogue = [&](bool have, int gl, float sc, float m_fin, long long roff) -> bool {
+      if (have) {
+        // the unit's last P V (and with it every earlier one) has completed; the next
+        // P V to commit to that barrier needs a P this warp has not announced yet
+        bool w = mbar_wait_bounded(smem_u32(&o_done[gl & 1]), (gl >> 1) & 1);
+        w = __all_sync(0xffffffffu, w);
+        if (!w) return false;
+        tc::fence_after();
       }
-      if (c0 + 64 > lim_row) {
+      constexpr int kEsz = PARTIAL ? 4 : (int)sizeof(T);
+      char *gbase = PARTIAL ? reinterpret_cast<char *>(a.ws_acc) : static_cast<char *>(a.out);
+      long long rj[4];  // rows 8 j + lane / 4: the ones this lane stores
 #pragma unroll
-        for (int c = 0; c < 64; ++c) sv[c] = (c0 + c < lim_row) ? sv[c] : -INFINITY;
-      }
-      float pm[8];
+      for (int j = 0; j < 4; ++j) rj[j] = __shfl_sync(0xffffffffu, roff, 8 * j + (lane >> 2));
 #pragma unroll
-      for (int i = 0; i < 8; ++i) pm[i] = sv[i];
+      for (int qq = 0; qq < kOCols / 32; ++qq) {
+        float o[32];
+        if (have) {
+          tc::ld32(trow + hc * kOCols + 32 * qq, o);
+        } else {
 #pragma unroll
-      for (int c = 8; c < 64; ++c) pm[c & 7] = fmaxf(pm[c & 7], sv[c]);
-      float mx = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])),
-                       fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7])));
-      mx = exchange(mx, true);  // the whole chunk's row maximum
-      if (!ok) break;
-      const float m_new = fmaxf(m_run, mx);
-      const bool need = m_new > m_run + kTcRescale;  // false while both are -inf
-      const float f = need ? ex2_ftz(m_run - m_new) : 1.f;  // 0 when m_run = -inf
-      if (need) {
-        l *= f;
-        m_run = m_new;
-      }
-      const float mb = (m_run == -INFINITY) ? 0.f : m_run;
-      const uint64_t nmb2 = tc::f2pack(-mb, -mb);
-      uint64_t ps2[2] = {0ull, 0ull};  // packed partial sums (+0.0f, +0.0f)
-      {
-        // P over these S columns: hi words in the first 32, lo words (bf16) next
-        uint32_t hw[32];
+          for (int i = 0; i < 32; ++i) o[i] = 0.f;
+        }
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          float x0, x1;
-          tc::f2unpack(tc::fadd2(tc::f2pack(sv[2 * e], sv[2 * e + 1]), nmb2), x0, x1);
-          const float p0 = ex2_ftz(x0), p1 = ex2_ftz(x1);
-          if constexpr (Lay::kSplitP) {
-            // hi = p truncated to bf16 (exact); lo = p - hi (exact in fp32), kept in sv
-            const uint32_t u0 = __float_as_uint(p0), u1 = __float_as_uint(p1);
-            hw[e] = __byte_perm(u0, u1, 0x7632);
-            const uint64_t pp = tc::f2pack(p0, p1);
-            const uint64_t hh = tc::f2pack(__uint_as_float(u0 & 0xffff0000u),
-                                           __uint_as_float(u1 & 0xffff0000u));
-            tc::f2unpack(tc::ffma2(hh, tc::f2pack(-1.f, -1.f), pp), sv[2 * e], sv[2 * e + 1]);
-            ps2[e & 1] = tc::fadd2(ps2[e & 1], pp);
+        for (int h2 = 0; h2 < 32 * kEsz / 64; ++h2) {  // 64-byte pieces of these columns
+          uint32_t wv[16];
+          if constexpr (PARTIAL) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) wv[i] = __float_as_uint(o[16 * h2 + i]);
           } else {
-            hw[e] = Elt<T>::from_f2(p0, p1);
-            // the sum of the rounded weights P V is taken with: the quotient O / l
-            // is then an exact convex combination of V rows (a dominant weight's
-            // rounding cancels)
-            const float2 hf = Elt<T>::to_f2(hw[e]);
-            ps2[e & 1] = tc::fadd2(ps2[e & 1], tc::f2pack(hf.x, hf.y));
-          }
-        }
-        tc::st32u(ts, hw);
-        if constexpr (Lay::kSplitP) {
 #pragma unroll
-          for (int e = 0; e < 32; ++e) hw[e] = Elt<T>::from_f2(sv[2 * e], sv[2 * e + 1]);
-          tc::st32u(ts + 32, hw);
+            for (int i = 0; i < 16; ++i) wv[i] = Elt<T>::from_f2(o[2 * i] * sc, o[2 * i + 1] * sc);
+          }
+          // row `lane`, 16-byte chunk c at position c ^ ((lane >> 1) & 3): no bank
+          // conflict when written by row or read by column
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const uint32_t addr = scr + lane * 64 + ((c ^ ((lane >> 1) & 3)) << 4);
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(wv[4 * c]),
+                         "r"(wv[4 * c + 1]), "r"(wv[4 * c + 2]), "r"(wv[4 * c + 3])
+                         : "memory");
+          }
+          __syncwarp();
+          const int c = lane & 3;
+          const int col_b = (hc * kOCols + 32 * qq) * kEsz + 64 * h2 + 16 * c;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int r = 8 * j + (lane >> 2);
+            uint4 v;
+            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                         : "r"(scr + r * 64 + ((c ^ ((r >> 1) & 3)) << 4))
+                         : "memory");
+            if (rj[j] >= 0) *reinterpret_cast<uint4 *>(gbase + rj[j] * (D * kEsz) + col_b) = v;
+          }
+          __syncwarp();  // read before the next piece is written
         }
       }
-      {
-        float a0, a1, b0, b1;
-        tc::f2unpack(ps2[0], a0, a1);
-        tc::f2unpack(ps2[1], b0, b1);
-        l += (a0 + a1) + (b0 + b1);
+      if (PARTIAL && hc == 0 && roff >= 0) {
+        a.ws_m[roff] = have ? m_fin : -INFINITY;
+        a.ws_l[roff] = have ? sc : 0.f;
       }
-      // O rescale: P_{j-1} V_{j-1} (and with it every earlier P V) must be complete.
-      // S_j's completion implies P_{j-3} V_{j-3}'s and P_j V_j is not issued yet, so
-      // the barrier of odd / even chunks that P_{j-1} V_{j-1} commits to is at most
-      // one phase behind: a parity wait is exact
-      if (j > 0 && __any_sync(0xffffffffu, need)) {  // (the pair decides alike)
-        w = mbar_wait_bounded(smem_u32(&o_done[(j - 1) & 1]), ((j - 1) >> 1) & 1);
+      return true;
+    };
+    // a finished unit whose epilogue waits for the next unit's first chunk
+    bool pend = false;
+    int pend_gl = 0;
+    float pend_sc = 0.f, pend_m = 0.f;
+    long long pend_roff = -1;
+
+    int g = 0;   // chunks of this CTA so far (all units)
+    int qn = 0;  // Q buffers written (without TMA)
+    TcUnit cu = tc_unit(a, geo, 0, s_order, lens, lane, row, false);
+    if (!a.q_tma && cu.valid && cu.nch > 0) {
+      write_q(cu);
+      qn = 1;
+    }
+    for (int k = 0; ok && cu.valid; ++k) {
+      const int lim_row = cu.rvalid ? min(cu.vis, cu.te * kTileTokens) : 0;  // padding rows: 0
+      float m_run = -INFINITY, l = 0.f;
+      for (int j = 0; j < cu.nch; ++j) {
+        const int gg = g + j;
+        const int b = gg % 3;
+        const uint32_t ts = trow + Lay::kColS + kTcChunk * b + 64 * hc;  // this warp's columns
+        bool w = mbar_wait_bounded(smem_u32(&s_full[b]), (gg / 3) & 1);
         w = __all_sync(0xffffffffu, w);
         if (!w) {
           ok = false;
           break;
         }
         tc::fence_after();
+        const int c0 = (cu.tb + j * kTcBlocks) * kTileTokens + 64 * hc;  // first position here
+        float sv[64];
+        tc::ld64(ts, sv);
+        // mask, then the row maximum of the raw scores (three-input max, eight
+        // independent chains); the scale is positive, so scaling the maximum gives
+        // the maximum in base-2 units
+        if (c0 + 64 > lim_row) {
+#pragma unroll
+          for (int c = 0; c < 64; ++c) sv[c] = (c0 + c < lim_row) ? sv[c] : -INFINITY;
+        }
+        float pm[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) pm[i] = fmax3(sv[i], sv[8 + i], sv[16 + i]);  // 0..23
+#pragma unroll
+        for (int c = 24; c < 56; c += 16) {  // 24..55
+#pragma unroll
+          for (int i = 0; i < 8; ++i) pm[i] = fmax3(pm[i], sv[c + i], sv[c + 8 + i]);
+        }
+        // the eight chains and 56..63
+        const float q0 = fmax3(pm[0], pm[1], sv[56]), q1 = fmax3(pm[2], pm[3], sv[57]);
+        const float q2 = fmax3(pm[4], pm[5], sv[58]), q3 = fmax3(pm[6], pm[7], sv[59]);
+        float mx = fmax3(fmax3(q0, q1, sv[60]), fmax3(q2, q3, sv[61]), fmaxf(sv[62], sv[63]));
+        mx = exchange(mx * rs, true);  // the whole chunk's row maximum
+        if (!ok) break;
+        const float m_new = fmaxf(m_run, mx);
+        const bool need = m_new > m_run + kTcRescale;  // false while both are -inf
+        const float f = need ? ex2_ftz(m_run - m_new) : 1.f;  // 0 when m_run = -inf
+        if (need) {
+          l *= f;
+          m_run = m_new;
+        }
+        const float mb = (m_run == -INFINITY) ? 0.f : m_run;
+        const uint64_t nmb2 = tc::f2pack(-mb, -mb);
+        uint64_t ps2[2] = {0ull, 0ull};  // packed partial sums (+0.0f, +0.0f)
         {
-          const uint64_t f2 = tc::f2pack(f, f);
+          // P over these S columns: hi words in the first 32, lo words (bf16) next
+          uint32_t hw[32];
 #pragma unroll
-          for (int qq = 0; qq < kOCols / 32; ++qq) {
-            float o[32];
-            const uint32_t oc = trow + hc * kOCols + 32 * qq;
-            tc::ld32(oc, o);
-#pragma unroll
-            for (int i = 0; i < 32; i += 2) {
-              const uint64_t x = tc::fmul2(tc::f2pack(o[i], o[i + 1]), f2);
-              tc::f2unpack(x, o[i], o[i + 1]);
+          for (int e = 0; e < 32; ++e) {
+            float x0, x1;
+            tc::f2unpack(tc::ffma2(tc::f2pack(sv[2 * e], sv[2 * e + 1]), rs2, nmb2), x0, x1);
+            const float p0 = ex2_ftz(x0), p1 = ex2_ftz(x1);
+            if constexpr (Lay::kSplitP) {
+              // hi = p truncated to bf16 (exact); lo = p - hi (exact in fp32), kept in sv
+              const uint32_t u0 = __float_as_uint(p0), u1 = __float_as_uint(p1);
+              hw[e] = __byte_perm(u0, u1, 0x7632);
+              const uint64_t pp = tc::f2pack(p0, p1);
+              const uint64_t hh = tc::f2pack(__uint_as_float(u0 & 0xffff0000u),
+                                             __uint_as_float(u1 & 0xffff0000u));
+              tc::f2unpack(tc::ffma2(hh, tc::f2pack(-1.f, -1.f), pp), sv[2 * e], sv[2 * e + 1]);
+              ps2[e & 1] = tc::fadd2(ps2[e & 1], pp);
+            } else {
+              hw[e] = Elt<T>::from_f2(p0, p1);
+              // the sum of the rounded weights P V is taken with: the quotient O / l
+              // is then an exact convex combination of V rows (a dominant weight's
+              // rounding cancels)
+              const float2 hf = Elt<T>::to_f2(hw[e]);
+              ps2[e & 1] = tc::fadd2(ps2[e & 1], tc::f2pack(hf.x, hf.y));
             }
-            tc::st32(oc, o);
+          }
+          tc::st32u(ts, hw);
+          if constexpr (Lay::kSplitP) {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) hw[e] = Elt<T>::from_f2(sv[2 * e], sv[2 * e + 1]);
+            tc::st32u(ts + 32, hw);
           }
         }
+        {
+          float a0, a1, b0, b1;
+          tc::f2unpack(ps2[0], a0, a1);
+          tc::f2unpack(ps2[1], b0, b1);
+          l += (a0 + a1) + (b0 + b1);
+        }
+        // O rescale: P_{j-1} V_{j-1} (and with it every earlier P V) must be complete.
+        // S_j's completion implies P_{j-3} V_{j-3}'s and P_j V_j is not issued yet, so
+        // the barrier of odd / even chunks that P_{j-1} V_{j-1} commits to is at most
+        // one phase behind: a parity wait is exact.  (A unit's first chunk overwrites O.)
+        if (j > 0 && __any_sync(0xffffffffu, need)) {  // (the pair decides alike)
+          w = mbar_wait_bounded(smem_u32(&o_done[(gg - 1) & 1]), ((gg - 1) >> 1) & 1);
+          w = __all_sync(0xffffffffu, w);
+          if (!w) {
+            ok = false;
+            break;
+          }
+          tc::fence_after();
+          {
+            const uint64_t f2 = tc::f2pack(f, f);
+#pragma unroll
+            for (int qq = 0; qq < kOCols / 32; ++qq) {
+              float o[32];
+              const uint32_t oc = trow + hc * kOCols + 32 * qq;
+              tc::ld32(oc, o);
+#pragma unroll
+              for (int i = 0; i < 32; i += 2) {
+                const uint64_t x = tc::fmul2(tc::f2pack(o[i], o[i + 1]), f2);
+                tc::f2unpack(x, o[i], o[i + 1]);
+              }
+              tc::st32(oc, o);
+            }
+          }
+        }
+        if (j == 0 && pend) {
+          // the previous unit's epilogue: its last P V has been completing under this
+          // chunk's softmax.  This unit's first P V overwrites O, and is announced
+          // only below.
+          if (!epilogue(true, pend_gl, pend_sc, pend_m, pend_roff)) {
+            ok = false;
+            break;
+          }
+          pend = false;
+        }
+        const int cs = (cu.tb + j * kTcBlocks) * kTileTokens;  // the chunk's first position
+        if (cs + kTcChunk > cu.vis_end) {
+          // V rows at or past vis_end may be unused slots holding anything; P is 0
+          // there but 0 * NaN is not 0, so they become zeros before P V
+          const int s = gg % NV;
+          w = mbar_wait_bounded(smem_u32(&v_full[s]), (gg / NV) & 1);
+          w = __all_sync(0xffffffffu, w);
+          if (!w) {
+            ok = false;
+            break;
+          }
+          const int first = max(0, cu.vis_end - cs);
+          const uint32_t vb = sV + s * Lay::kKVBytes;
+          for (int idx = tid; idx < (kTcChunk - first) * H * 8; idx += 32 * kTcSoft) {
+            const int r = first + idx / (H * 8), rem = idx % (H * 8);
+            const int hh = rem >> 3, cc = rem & 7;
+            sts128_zero(vb + hh * (kTcChunk * 128) + r * 128 + ((cc ^ (r & 7)) << 4));
+          }
+          fence_proxy_async_smem();  // the zeros visible to the tensor core
+        }
+        tc::st_wait();  // P_j (and a rescaled O) are in tensor memory
+        // the MMA thread has taken P_{j-1}: p_full may move on
+        if (gg > 0) {
+          w = mbar_wait_bounded(smem_u32(&p_ack), (gg - 1) & 1);
+          w = __all_sync(0xffffffffu, w);
+          if (!w) {
+            ok = false;
+            break;
+          }
+        }
+        tc::fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&p_full));
       }
-      const int cs = (tb + j * kTcBlocks) * kTileTokens;  // the chunk's first position
-      if (cs + kTcChunk > vis_end) {
-        // V rows at or past vis_end may be unused slots holding anything; P is 0
-        // there but 0 * NaN is not 0, so they become zeros before P V
-        const int s = j % NV;
-        w = mbar_wait_bounded(smem_u32(&v_full[s]), (j / NV) & 1);
-        w = __all_sync(0xffffffffu, w);
-        if (!w) {
+      if (!ok) break;
+
+      // the next unit's Q (without TMA) goes in while this unit's P V drains: its
+      // buffer is free once this unit's last S MMA has completed
+      const TcUnit nu = tc_unit(a, geo, k + 1, s_order, lens, lane, row, false);
+      if (!a.q_tma && nu.valid && nu.nch > 0) {
+        if (qn > 0) {
+          bool w = mbar_wait_bounded(smem_u32(&q_free), (qn - 1) & 1);
+          w = __all_sync(0xffffffffu, w);
+          if (!w) {
+            ok = false;
+            break;
+          }
+        }
+        write_q(nu);
+        ++qn;
+      }
+
+      // ---- the unit's results: deferred to the next unit's first chunk ----
+      long long roff = -1;
+      if (cu.rvalid)
+        roff = PARTIAL ? (long long)(((size_t)cu.rseq * a.ws_splits + a.ws_split0 + cu.split) *
+                                         (a.q_len * a.num_q_heads) +
+                                     (size_t)cu.ru * a.num_q_heads + cu.rh)
+                       : (long long)((size_t)(cu.rseq * a.q_len + cu.ru) * a.num_q_heads + cu.rh);
+      if (cu.nch > 0) {
+        l = exchange(l, false);  // the row sum over both column halves
+        if (!ok) break;
+        pend = true;
+        pend_gl = g + cu.nch - 1;
+        pend_sc = PARTIAL ? l : (l > 0.f ? 1.f / l : 0.f);
+        pend_m = m_run;
+        pend_roff = roff;
+      } else {
+        // no position in this unit's partition: zeros (empty statistics)
+        if (pend) {
+          if (!epilogue(true, pend_gl, pend_sc, pend_m, pend_roff)) {
+            ok = false;
+            break;
+          }
+          pend = false;
+        }
+        if (!epilogue(false, 0, 0.f, 0.f, roff)) {
           ok = false;
           break;
         }
-        const int first = max(0, vis_end - cs);
-        const uint32_t vb = sV + s * Lay::kKVBytes;
-        for (int idx = tid; idx < (kTcChunk - first) * H * 8; idx += 32 * kTcSoft) {
-          const int r = first + idx / (H * 8), rem = idx % (H * 8);
-          const int hh = rem >> 3, cc = rem & 7;
-          sts128_zero(vb + hh * (kTcChunk * 128) + r * 128 + ((cc ^ (r & 7)) << 4));
-        }
-        fence_proxy_async_smem();  // the zeros visible to the tensor core
       }
-      tc::st_wait();  // P_j (and a rescaled O) are in tensor memory
-      // the MMA thread has taken P_{j-1}: p_full may move on
-      if (j > 0) {
-        w = mbar_wait_bounded(smem_u32(&p_ack), (j - 1) & 1);
-        w = __all_sync(0xffffffffu, w);
-        if (!w) {
-          ok = false;
-          break;
-        }
-      }
-      tc::fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&p_full));
+      g += cu.nch;
+      cu = nu;
     }
+    if (ok && pend) ok = epilogue(true, pend_gl, pend_sc, pend_m, pend_roff);
     if (!ok && lane == 0) {
       record_error(a.err, kErrTimeout);
       atomicExch(&s_failed, 1);
-    }
-    // ---- epilogue: O / l, or the unnormalised partial with its statistics ----
-    bool have = ok && nch > 0;
-    if (have) {
-      // every MMA of this CTA has completed
-      bool w = mbar_wait_bounded(smem_u32(&mma_fin), 0);
-      w = __all_sync(0xffffffffu, w);
-      if (!w) {
-        have = false;
-        ok = false;
-        if (lane == 0) {
-          record_error(a.err, kErrTimeout);
-          atomicExch(&s_failed, 1);
-        }
-      } else {
-        tc::fence_after();
-      }
-    }
-    if (ok) l = exchange(l, false);  // the row sum over both column halves
-    const bool write = ok && qrow != nullptr;
-    const float inv = l > 0.f ? 1.f / l : 0.f;
-    size_t wrow = 0;
-    if (PARTIAL)
-      wrow = ((size_t)rseq * a.ws_splits + a.ws_split0 + split) * (a.q_len * a.num_q_heads) +
-             (size_t)ru * a.num_q_heads + rh;
-    const size_t orow = (size_t)(rseq * a.q_len + ru) * a.num_q_heads + rh;
-#pragma unroll
-    for (int qq = 0; qq < kOCols / 32; ++qq) {
-      const int col = hc * kOCols + 32 * qq;
-      float o[32];
-      if (have) {
-        tc::ld32(trow + col, o);
-      } else {
-#pragma unroll
-        for (int i = 0; i < 32; ++i) o[i] = 0.f;
-      }
-      if (!write) continue;
-      if constexpr (PARTIAL) {
-        float4 *dst = reinterpret_cast<float4 *>(a.ws_acc + wrow * D + col);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) dst[i] = make_float4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
-      } else {
-        uint4 *dst = reinterpret_cast<uint4 *>(static_cast<T *>(a.out) + orow * D + col);
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-          dst[i] = make_uint4(Elt<T>::from_f2(o[8 * i] * inv, o[8 * i + 1] * inv),
-                              Elt<T>::from_f2(o[8 * i + 2] * inv, o[8 * i + 3] * inv),
-                              Elt<T>::from_f2(o[8 * i + 4] * inv, o[8 * i + 5] * inv),
-                              Elt<T>::from_f2(o[8 * i + 6] * inv, o[8 * i + 7] * inv));
-      }
-    }
-    if (PARTIAL && write && hc == 0) {
-      a.ws_m[wrow] = have ? m_run : -INFINITY;
-      a.ws_l[wrow] = have ? l : 0.f;
     }
   }
 

@@ -261,3 +261,39 @@ def test_cascade_without_append_any_lengths(pa, orc):
     torch.cuda.synchronize()
     assert pa.pa_device_error() == 0
     _tol.check(_f64(out), ref, w.cfg.dtype, "cascade, short sequences")
+
+
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+@pytest.mark.parametrize("scale", [-0.0884, 0.0], ids=["negative", "zero"])
+def test_prefill_nonpositive_scale(pa, orc, dtype, scale):
+    """The many-row kernel folds the scale into exp2's argument, which wants a positive
+    scale: a negative one negates the score MMA instead, and zero makes every visible
+    weight equal (the output is the mean of the visible V rows)."""
+    lens = [40, 300, 700]
+    q, K, V = _logical_case(24, lens, 8, 2, 128, dtype, q_len=40)
+    pc = Paged(orc, K, V, 16, dtype, perm_seed=16)
+    ref = pc.decode(orc, q, scale, q_len=40)
+    _tol.check(_gpu_decode(pa, pc, q, scale, 40), ref, dtype, f"scale {scale}")
+    _tol.check(_gpu_decode(pa, pc, q, scale, 40, num_splits=3), ref, dtype, f"scale {scale}, split 3")
+
+
+@pytest.mark.parametrize("scale", [-0.0884, 0.0], ids=["negative", "zero"])
+def test_cascade_nonpositive_scale(pa, orc, scale):
+    """The shared-prefix pass (many-row kernel) and the tail pass (decode kernel) take
+    the same non-positive scale."""
+    w = workloads.make("prefix_verify", num_seqs=4, q_len=8)
+    d = _dev(w)
+    kc, vc = w.bits("k_cache").copy(), w.bits("v_cache").copy()
+    slots = orc.slot_mapping(w.block_tables.numpy(), w.context_lens.numpy(), 16, w.cfg.q_len)
+    orc.append_kv(kc, vc, w.bits("k_new"), w.bits("v_new"), slots)
+    ref = orc.decode(w.bits("q"), kc, vc, w.block_tables.numpy(), w.context_lens.numpy(), scale,
+                     w.cfg.dtype, q_len=w.cfg.q_len)
+    kt = torch.from_numpy(kc.view(np.int16)).view(torch.float16).to(DEV)
+    vt = torch.from_numpy(vc.view(np.int16)).view(torch.float16).to(DEV)
+    for tail_splits in (1, 2):
+        out = torch.empty_like(d["q"])
+        pa.pa_decode_cascade(out, d["q"], kt, vt, d["block_tables"], d["context_lens"], scale,
+                             w.cfg.shared_prefix // 16, q_len=w.cfg.q_len, tail_splits=tail_splits)
+        torch.cuda.synchronize()
+        assert pa.pa_device_error() == 0
+        _tol.check(_f64(out), ref, w.cfg.dtype, f"cascade scale {scale}, tail splits {tail_splits}")
