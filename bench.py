@@ -357,6 +357,35 @@ def time_device(runner: Runner, steps: int, warmup: int, world: int):
     return step_ms, kern_ms, wall
 
 
+def time_graph(runner: Runner, steps: int, warmup: int):
+    """The fused step captured once in a CUDA graph, then replayed: the launches'
+    host cost leaves the step (each replay is one graph launch)."""
+    for _ in range(warmup):
+        runner.step()
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        runner.step()  # first use of every buffer on the capturing stream
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        runner.step()
+    for _ in range(warmup):
+        graph.replay()
+    torch.cuda.synchronize()
+    E = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    evs = [(E(), E()) for _ in range(steps)]
+    torch.cuda._sleep(int(2e7))
+    for a, b in evs:
+        a.record()
+        graph.replay()
+        b.record()
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in evs]
+
+
 def time_e2e(runner: Runner, steps: int, warmup: int):
     """Same step through the public API with the inputs in pinned host memory:
     H2D of q, new K/V rows, block tables and context lengths, then the step, then
@@ -485,6 +514,16 @@ def measure_config(pa, name, seed, device, steps, warmup, world, peaks, e2e=Fals
                                   "fused append, combine: 3 launches)"}
         runner.mode = "fused"
     if e2e:
+        # the same step as one CUDA graph replay (reported beside the stream timing)
+        try:
+            g_ms = time_graph(runner, steps, max(3, warmup))
+            assert pa.pa_device_error() == 0, "device error during the graph replays"
+            g_step = max_over_ranks(sum(g_ms), world, device) / steps
+            res["graph"] = {"ms_per_step": g_step, "value": tokens / (g_step * 1e-3),
+                            "unit": UNIT,
+                            "path": "the fused step captured in a CUDA graph, replayed"}
+        except RuntimeError as exc:  # capture refused: report it, keep the bench line
+            res["graph"] = {"error": str(exc).splitlines()[0][:200]}
         ms, h2d, d2h = time_e2e(runner, steps, max(3, warmup))
         e_ms = max_over_ranks(sum(ms), world, device) / steps
         res["e2e"] = {"value": tokens / (e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
@@ -554,7 +593,7 @@ def run_ours(args):
         "other_configs": others,
         "kernel_src_sha": {k: kernel_source_sha(k) for k in KERNEL_SOURCES},
     }
-    for extra in ("cascade", "tensor_roofline"):
+    for extra in ("cascade", "tensor_roofline", "graph"):
         if extra in r:
             line[extra] = r[extra]
     print(json.dumps(line))
@@ -563,7 +602,7 @@ def run_ours(args):
 def _path(w):
     if w.cfg.q_len > DECODE_MAX_QLEN:
         return ("pa_append_decode with q_len > 16: append launch, then the prefill kernel "
-                "(64 query rows per CTA share each K/V tile)")
+                "(persistent CTAs; 128 query rows of a KV head share each K/V chunk)")
     if w.cfg.kv_fp8:
         return "pa_decode_fp8 with k_new/v_new (fused quantising append + attention, one launch)"
     return ("pa_append_decode (fused slot mapping + append + split-KV partial, then combine)"
