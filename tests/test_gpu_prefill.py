@@ -297,3 +297,51 @@ def test_cascade_nonpositive_scale(pa, orc, scale):
         torch.cuda.synchronize()
         assert pa.pa_device_error() == 0
         _tol.check(_f64(out), ref, w.cfg.dtype, f"cascade scale {scale}, tail splits {tail_splits}")
+
+
+# ------------------------------------------------- many units per persistent CTA
+# units = ceil(q_len * g / 128) * num_kv_heads * num_seqs (* splits), all above the
+# 152 SMs, so every persistent CTA walks several units: the rings and barrier
+# phases run on across units, the next unit's q replaces the previous one, and
+# each epilogue is deferred into the next unit's first chunk.
+MANY_UNITS = [
+    # dtype, head_dim, h_q, h_kv, q_len, num_seqs
+    ("fp16", 128, 12, 4, 200, 10),  # g = 3: q rows written by the softmax threads; 200 units
+    ("bf16", 64, 16, 4, 160, 10),   # g = 4: q by TMA; 200 units
+    ("bf16", 128, 40, 8, 70, 12),   # g = 5: q by the softmax threads; 288 units
+    ("fp16", 64, 32, 8, 48, 14),    # g = 4: q by TMA, 2 row blocks per sequence; 224 units
+]
+
+
+@pytest.mark.parametrize("splits", [1, 2])
+@pytest.mark.parametrize("case", MANY_UNITS, ids=[f"{c[0]}-d{c[1]}-g{c[2] // c[3]}" for c in MANY_UNITS])
+def test_prefill_many_units_per_cta(pa, orc, case, splits):
+    dtype, d, h_q, h_kv, q_len, n = case
+    rng = np.random.default_rng(31)
+    lens = [int(x) for x in rng.integers(q_len, 1200, size=n)]
+    lens[1] = 3       # shorter than the chunk: the first rows see nothing
+    lens[2] = q_len   # the chunk is the whole context
+    lens[3] = 0       # empty sequence: zeros
+    q, K, V = _logical_case(32, lens, h_q, h_kv, d, dtype, q_len=q_len)
+    pc = Paged(orc, K, V, 16, dtype, perm_seed=17)
+    scale = float(np.float32(1.0) / np.sqrt(np.float32(d)))
+    ref = orc.decode(q, pc.k, pc.v, pc.tables, pc.lens, scale, dtype, q_len=q_len, threads=8)
+    _tol.check(_gpu_decode(pa, pc, q, scale, q_len, num_splits=splits), ref, dtype,
+               f"{dtype} d{d} g{h_q // h_kv} q_len {q_len} split {splits}")
+
+
+def test_cascade_prefix_pass_many_units_per_cta(pa, orc):
+    """A shared-prefix pass with more units than SMs (128 sequences x 8 query
+    positions x 4 heads per KV head = 32 row blocks per KV head, 256 units), then
+    the tails: sampled rows against the oracle."""
+    w = workloads.make("prefix_verify", q_len=8)
+    out, d = gpu_cascade(pa, w, tail_splits=1)
+    n_rows = w.cfg.num_seqs * w.cfg.q_len * w.cfg.num_q_heads
+    rows = np.sort(np.random.default_rng(5).choice(n_rows, size=96, replace=False))
+    ref, kc, vc, _ = oracle_step(orc, w, rows=rows)
+    _tol.check(_f64(out).reshape(n_rows, -1)[rows], ref, w.cfg.dtype, "cascade, many prefix units")
+    assert np.array_equal(_u16(d["k_cache"]), kc)
+    assert np.array_equal(_u16(d["v_cache"]), vc)
+    # the same rows through two tail partitions and the combine
+    out2, _ = gpu_cascade(pa, workloads.make("prefix_verify", q_len=8), tail_splits=2)
+    _tol.check(_f64(out2).reshape(n_rows, -1)[rows], ref, w.cfg.dtype, "cascade, tail split 2")
