@@ -44,7 +44,8 @@
  *    (contiguous groups; [QA] Q7, [ANIM] §1 figure).
  *  - Supported now: block_size 16; head_dim 64 or 128; q_len 1..4096 with a
  *    16-bit cache (up to 16 query rows per sequence go to the decode kernel, more
- *    to a kernel that shares each K/V tile among 64 query rows: chunked prefill,
+ *    to a tensor-core kernel that shares each K/V chunk among 128 query rows of a
+ *    KV head: chunked prefill,
  *    [QA] Q14, [SB11] §11.3 "Continuous Batching"); q_len 1..16 with an FP8 cache.
  *  - Alignment: every pointer 16-byte aligned.
  *
