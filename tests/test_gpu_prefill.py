@@ -345,3 +345,29 @@ def test_cascade_prefix_pass_many_units_per_cta(pa, orc):
     # the same rows through two tail partitions and the combine
     out2, _ = gpu_cascade(pa, workloads.make("prefix_verify", q_len=8), tail_splits=2)
     _tol.check(_f64(out2).reshape(n_rows, -1)[rows], ref, w.cfg.dtype, "cascade, tail split 2")
+
+
+def test_prefill_more_sequences_than_the_ranked_order_holds(pa, orc):
+    """Above 256 sequences the kernel takes them in index order and reads the
+    context lengths from global memory: 300 short sequences, every element."""
+    rng = np.random.default_rng(41)
+    lens = [int(x) for x in rng.integers(17, 120, size=300)]
+    lens[7] = 0
+    lens[8] = 5
+    q, K, V = _logical_case(42, lens, 4, 2, 64, "fp16", q_len=17)
+    pc = Paged(orc, K, V, 16, "fp16", perm_seed=18)
+    ref = orc.decode(q, pc.k, pc.v, pc.tables, pc.lens, 0.125, "fp16", q_len=17, threads=8)
+    _tol.check(_gpu_decode(pa, pc, q, 0.125, 17), ref, "fp16", "300 sequences")
+    _tol.check(_gpu_decode(pa, pc, q, 0.125, 17, num_splits=3), ref, "fp16", "300 sequences, split 3")
+
+
+def test_cascade_more_sequences_than_the_ranked_order_holds(pa, orc):
+    """The shared-prefix pass over 300 sequences (context lengths from global
+    memory), then the tails: sampled rows."""
+    w = workloads.make("prefix_verify", num_seqs=300, q_len=2, lens=("prefix", 1024, 16, 80))
+    out, d = gpu_cascade(pa, w)
+    n_rows = w.cfg.num_seqs * w.cfg.q_len * w.cfg.num_q_heads
+    rows = np.sort(np.random.default_rng(6).choice(n_rows, size=128, replace=False))
+    ref, kc, vc, _ = oracle_step(orc, w, rows=rows)
+    _tol.check(_f64(out).reshape(n_rows, -1)[rows], ref, w.cfg.dtype, "cascade, 300 sequences")
+    assert np.array_equal(_u16(d["k_cache"]), kc)
