@@ -520,6 +520,181 @@ struct MmaPath {
   }
 };
 
+// 8x8 16-bit matrix transpose across the warp: the row-major fragment (thread t
+// holds row t/4, columns 2(t%4) and 2(t%4)+1) of M in, the same fragment of M^T out.
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t a) {
+  uint32_t d;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
+  return d;
+}
+
+// ---------------------------------------------------------------------------------
+// Tensor-core path with the operands swapped, for 3..8 rows per KV head (GQA decode):
+// the 16 tokens of a tile are the MMA's M, the rows its N = 8, so a padded row costs
+// half of what it costs with the rows as M = 16.
+//   S^T[token][row] = K[token][:] . q[row][:]   (m16n8k16: A = K by ldmatrix, B = q^T
+//                                                in registers)
+//   O^T[dim][row] += V^T[dim][token] P^T[token][row]   (A = V^T by ldmatrix.trans, B =
+//                                                        P^T from S^T's accumulator)
+// The accumulator of S^T leaves P in the row-major fragment of the 8x8 blocks
+// [token][row]; one movmatrix transpose per block gives the B fragment of P^T.
+// Thread (g, c) = (lane / 4, lane % 4) holds rows 2c and 2c+1 (P, l, O^T columns) and
+// tokens g and g+8 of each tile.
+template <typename T, int D>
+struct MmaTPath {
+  static constexpr int RPC = 8;
+  static constexpr int KS = D / 16;  // k-steps of S (16 dims each)
+  static constexpr int MT = D / 16;  // m-tiles of O^T (16 dims each)
+  static constexpr int kExtraBytes = 0;
+
+  uint32_t qb[KS][2];  // B fragments of q^T: row g, dims ks*16 + 2c (+1) and + 8 (+9)
+  float o[MT][4];      // O^T: dims mt*16 + g (+8), rows 2c, 2c+1
+  float m[2], l[2];    // rows 2c + e
+  float rs[2];
+  int lim[2];
+
+  __device__ __forceinline__ void init(const DecodeArgs &a, int seq, int kvh, int row0, int L,
+                                       float sscale, uint32_t) {
+    const int lane = threadIdx.x & 31;
+    const int g = lane >> 2, c = lane & 3;
+    const T *qb_ptr = static_cast<const T *>(a.q);
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const RowInfo ri = row_info(a, kvh, row0 + 2 * c + e);
+      lim[e] = ri.valid ? (L - a.q_len + ri.u + 1) : 0;
+      m[e] = -INFINITY;
+      l[e] = 0.f;
+      rs[e] = sscale;
+    }
+    const RowInfo rq = row_info(a, kvh, row0 + g);
+    const T *qrow = rq.valid ? qb_ptr + ((size_t)(seq * a.q_len + rq.u) * a.num_q_heads + rq.h) * D
+                             : nullptr;
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+      qb[ks][0] = qrow ? __ldg(reinterpret_cast<const uint32_t *>(qrow + ks * 16 + 2 * c)) : 0u;
+      qb[ks][1] = qrow ? __ldg(reinterpret_cast<const uint32_t *>(qrow + ks * 16 + 2 * c + 8)) : 0u;
+    }
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) o[mt][i] = 0.f;
+  }
+
+  template <bool MASKED>
+  __device__ __forceinline__ void tile(uint32_t kt, uint32_t vt, int tile_idx, float) {
+    const int lane = threadIdx.x & 31;
+    const int mi = lane >> 3, ri = lane & 7;
+    // S^T: two independent chains (even and odd k-steps), then added.  A fragment
+    // of K: matrices (tokens 0-7 | 8-15) x (dims 0-7 | 8-15) of the k-step
+    float sc[4] = {0.f, 0.f, 0.f, 0.f}, sd[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+      uint32_t ka[4];
+      const int tok = ri + ((mi & 1) << 3), ch = 2 * ks + (mi >> 1);
+      ldmatrix_x4(kt + sw128_offset<kTileTokens>(tok, ch), ka[0], ka[1], ka[2], ka[3]);
+      Elt<T>::mma16816((ks & 1) ? sd : sc, ka, qb[ks][0], qb[ks][1]);
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) sc[i] += sd[i];
+    softmax_pv<MASKED>(sc, vt, tile_idx);
+  }
+
+  // Online-softmax update from this tile's raw S^T (sc[i]: token g + 8 (i >> 1), row
+  // 2c + (i & 1)) and O^T += V^T P^T with V^T fragments from the 16-bit tile at vt.
+  template <bool MASKED>
+  __device__ __forceinline__ void softmax_pv(float (&sc)[4], uint32_t vt, int tile_idx) {
+    const int lane = threadIdx.x & 31;
+    const int mi = lane >> 3, ri = lane & 7;
+    const int g = lane >> 2;
+    // scale, mask
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      float v = sc[i] * rs[i & 1];
+      if (MASKED) {
+        const int tg = tile_idx * kTileTokens + g + 8 * (i >> 1);
+        if (tg >= lim[i & 1]) v = -INFINITY;
+      }
+      sc[i] = v;
+    }
+    // online softmax per row (the 8 threads of a row differ in g: lanes c + 4g)
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      float mx = fmaxf(sc[e], sc[2 + e]);
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+      if (mx > m[e]) {
+        const float f = fast_exp2(m[e] - mx);  // m = -inf -> 0
+        l[e] *= f;
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+          o[mt][e] *= f;
+          o[mt][2 + e] *= f;
+        }
+        m[e] = mx;
+      }
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const float v = sc[2 * h + e];
+        float p;
+        if (MASKED)
+          p = (v == -INFINITY) ? 0.f : fast_exp2(v - m[e]);
+        else
+          p = fast_exp2(v - m[e]);
+        sc[2 * h + e] = p;
+        l[e] += p;
+      }
+    }
+    // P^T B fragments: (tokens 0-7) and (tokens 8-15) blocks, transposed.  bf16 P is
+    // split into hi + lo parts as in MmaPath (8 significant bits are too coarse for
+    // peaked rows); fp16 P is used directly.
+    constexpr bool kSplitP = Elt<T>::kMantBits < 10;
+    uint32_t bh[2], bl[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const float p0 = sc[2 * h], p1 = sc[2 * h + 1];
+      const uint32_t hi = Elt<T>::from_f2(p0, p1);
+      bh[h] = movmatrix_trans(hi);
+      if (kSplitP) {
+        const float2 hf = Elt<T>::to_f2(hi);
+        bl[h] = movmatrix_trans(Elt<T>::from_f2(p0 - hf.x, p1 - hf.y));
+      }
+    }
+    // O^T += V^T P^T: A fragment of V^T by ldmatrix.trans, matrices (dims 0-7 | 8-15)
+    // x (tokens 0-7 | 8-15) of the m-tile
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) {
+      uint32_t va[4];
+      const int tok = ri + ((mi >> 1) << 3), ch = 2 * mt + (mi & 1);
+      ldmatrix_x4_trans(vt + sw128_offset<kTileTokens>(tok, ch), va[0], va[1], va[2], va[3]);
+      Elt<T>::mma16816(o[mt], va, bh[0], bh[1]);
+      if (kSplitP) Elt<T>::mma16816(o[mt], va, bl[0], bl[1]);
+    }
+  }
+
+  template <int STRIDE>
+  __device__ __forceinline__ void publish(float *mrg_m, float *mrg_l, float *mrg_acc) {
+    const int lane = threadIdx.x & 31;
+    const int g = lane >> 2, c = lane & 3;
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      l[e] += __shfl_xor_sync(0xffffffffu, l[e], 4);
+      l[e] += __shfl_xor_sync(0xffffffffu, l[e], 8);
+      l[e] += __shfl_xor_sync(0xffffffffu, l[e], 16);
+      const int r = 2 * c + e;
+      if (g == 0) {
+        mrg_m[r] = m[e];
+        mrg_l[r] = l[e];
+      }
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) {
+        mrg_acc[r * STRIDE + mt * 16 + g] = o[mt][e];
+        mrg_acc[r * STRIDE + mt * 16 + g + 8] = o[mt][2 + e];
+      }
+    }
+  }
+};
+
 // Eight 16-bit values -> eight e4m3 codes of value / scale (fp32 division, nearest
 // even, saturating): the quantising append of an FP8 cache.
 template <typename T>
@@ -533,6 +708,120 @@ __device__ __forceinline__ uint2 quantize8(const uint4 v, float scale) {
   }
   return make_uint2((uint32_t)c[0] | ((uint32_t)c[1] << 16), (uint32_t)c[2] | ((uint32_t)c[3] << 16));
 }
+
+// ---------------------------------------------------------------------------------
+// FP8 (e4m3) cache, tensor-core path with swapped operands for 3..8 rows per KV
+// head: MmaTPath's layout (tokens as the MMA's M, rows as N = 8) over fp16 MMAs.
+// K's A fragments are widened from the codes in registers, V is widened into this
+// warp's shared scratch, as in Mma8Path.  Inside each 16-dim k-step the contraction
+// is permuted so that a lane's k slots {2c, 2c+1, 2c+8, 2c+9} (c = lane % 4) are
+// dims 4c..4c+3: four consecutive codes, one 32-bit shared load; q^T's B fragments
+// use the same permutation, so S is unchanged.  Each q row is scaled by a power of
+// two into fp16's range and the score scale of the row's S^T column takes it back.
+template <typename T>
+struct Mma8TPath {
+  static constexpr int D = 128;
+  static constexpr int RPC = 8;
+  static constexpr int kTile16 = kTileTokens * D * 2;  // one widened tile
+  static constexpr int kExtraBytes = kTile16;          // widened V
+  MmaTPath<__half, D> inner;
+  uint32_t wv;  // widened V tile (this warp's scratch)
+
+  __device__ __forceinline__ void init(const DecodeArgs &a, int seq, int kvh, int row0, int L,
+                                       float sscale, uint32_t scratch) {
+    const int lane = threadIdx.x & 31;
+    const int g = lane >> 2, c = lane & 3;
+    inner.init(a, seq, kvh, row0, L, sscale, scratch);  // rows, limits, O^T; q below
+    // q row g, dims ks*16 + 4c .. 4c+3 of every k-step
+    const RowInfo rq = row_info(a, kvh, row0 + g);
+    const T *qrow = rq.valid ? static_cast<const T *>(a.q) +
+                                   ((size_t)(seq * a.q_len + rq.u) * a.num_q_heads + rq.h) * D
+                             : nullptr;
+    float2 qf[MmaTPath<__half, D>::KS][2];
+    float mx = 0.f;
+#pragma unroll
+    for (int ks = 0; ks < MmaTPath<__half, D>::KS; ++ks) {
+      uint2 v = make_uint2(0u, 0u);
+      if (qrow) v = __ldg(reinterpret_cast<const uint2 *>(qrow + ks * 16 + 4 * c));
+      qf[ks][0] = Elt<T>::to_f2(v.x);
+      qf[ks][1] = Elt<T>::to_f2(v.y);
+      mx = fmaxf(mx, fmaxf(fmaxf(fabsf(qf[ks][0].x), fabsf(qf[ks][0].y)),
+                           fmaxf(fabsf(qf[ks][1].x), fabsf(qf[ks][1].y))));
+    }
+    // the 4 lanes holding row g agree on its maximum
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+    const int e_row = (mx > 0.f && isfinite(mx)) ? ilogbf(mx) : 0;
+    const float down = ldexpf(1.f, -e_row);  // |q| * down < 2: well inside fp16
+#pragma unroll
+    for (int ks = 0; ks < MmaTPath<__half, D>::KS; ++ks) {
+      inner.qb[ks][0] = Elt<__half>::from_f2(qf[ks][0].x * down, qf[ks][0].y * down);
+      inner.qb[ks][1] = Elt<__half>::from_f2(qf[ks][1].x * down, qf[ks][1].y * down);
+    }
+    // S^T column 2c + e is row 2c + e: its exponent comes from the lanes of that row
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int er = __shfl_sync(0xffffffffu, e_row, 4 * (2 * c + e));
+      inner.rs[e] = sscale * ldexpf(1.f, er);
+    }
+    wv = scratch;
+  }
+
+  __device__ __forceinline__ void widen(uint32_t src8, uint32_t dst16) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int i = 0; i < (kTileTokens * 8) / 32; ++i) {  // 128 chunks of 16 codes
+      const int idx = lane + 32 * i;
+      const int row = idx >> 3, c8 = idx & 7;
+      const uint4 v = lds128(src8 + sw128_offset_row128(row, c8));
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+      uint32_t o[8];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        o[2 * k] = e4m3x2_to_f16x2(static_cast<uint16_t>(w[k] & 0xffffu));
+        o[2 * k + 1] = e4m3x2_to_f16x2(static_cast<uint16_t>(w[k] >> 16));
+      }
+      asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
+                       dst16 + sw128_offset<kTileTokens>(row, 2 * c8)),
+                   "r"(o[0]), "r"(o[1]), "r"(o[2]), "r"(o[3])
+                   : "memory");
+      asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
+                       dst16 + sw128_offset<kTileTokens>(row, 2 * c8 + 1)),
+                   "r"(o[4]), "r"(o[5]), "r"(o[6]), "r"(o[7])
+                   : "memory");
+    }
+  }
+
+  template <bool MASKED>
+  __device__ __forceinline__ void tile(uint32_t kt, uint32_t vt, int tile_idx, float) {
+    const int lane = threadIdx.x & 31;
+    const int g = lane >> 2, c = lane & 3;
+    widen(vt, wv);
+    // S^T: A fragment of K widened in registers (tokens g and g + 8, permuted dims)
+    float sc[4] = {0.f, 0.f, 0.f, 0.f}, sd[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int ks = 0; ks < MmaTPath<__half, D>::KS; ++ks) {
+      uint32_t w0, w1;
+      asm volatile("ld.shared.b32 %0, [%1];" : "=r"(w0) : "r"(kt + sw128_offset_row128(g, ks) + 4 * c));
+      asm volatile("ld.shared.b32 %0, [%1];" : "=r"(w1) : "r"(kt + sw128_offset_row128(g + 8, ks) + 4 * c));
+      const uint32_t ka[4] = {e4m3x2_to_f16x2(static_cast<uint16_t>(w0 & 0xffffu)),
+                              e4m3x2_to_f16x2(static_cast<uint16_t>(w1 & 0xffffu)),
+                              e4m3x2_to_f16x2(static_cast<uint16_t>(w0 >> 16)),
+                              e4m3x2_to_f16x2(static_cast<uint16_t>(w1 >> 16))};
+      Elt<__half>::mma16816((ks & 1) ? sd : sc, ka, inner.qb[ks][0], inner.qb[ks][1]);
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) sc[i] += sd[i];
+    __syncwarp();  // widened V visible to every lane
+    inner.template softmax_pv<MASKED>(sc, wv, tile_idx);
+    __syncwarp();  // the scratch is rewritten by the next tile
+  }
+
+  template <int STRIDE>
+  __device__ __forceinline__ void publish(float *mrg_m, float *mrg_l, float *mrg_acc) {
+    inner.template publish<STRIDE>(mrg_m, mrg_l, mrg_acc);
+  }
+};
 
 // ---------------------------------------------------------------------------------
 // FP8 (e4m3) cache, CUDA-core path: head_dim 128, one 128-byte row per token,

@@ -20,10 +20,10 @@ constexpr int kWarps = 4;
 template <bool PARTIAL>
 constexpr int stages_for() { return PARTIAL ? 3 : 2; }
 // An FP8 stage carries half the bytes, so FP8 keeps more stages per warp in flight:
-// 4 on the CUDA-core path, 3 on the tensor-core path (which also holds a 4 KiB
+// 4 on the CUDA-core paths, 3 on the tensor-core paths (which also hold a 4 KiB
 // widened V tile per warp), both measured best and both still 3 CTAs per SM.
 template <class Path, bool PARTIAL, bool KV8>
-constexpr int stages_of() { return KV8 ? (Path::RPC == 16 ? 3 : 4) : stages_for<PARTIAL>(); }
+constexpr int stages_of() { return KV8 ? (Path::kExtraBytes > 0 ? 3 : 4) : stages_for<PARTIAL>(); }
 constexpr int kMaxCluster = 8;  // portable cluster size limit
 
 // Per device: SM count and resident CTAs per SM of one kernel (cached).
@@ -91,6 +91,7 @@ static cudaError_t launch_paths(const CUtensorMap &kmap, const CUtensorMap &vmap
                                 const DecodeArgs &a, int units, cudaStream_t st) {
   if (a.rows == 1) return launch_one<T, D, FmaPath<T, D, 4, 1>, PARTIAL>(kmap, vmap, a, units, 1, st);
   if (a.rows == 2) return launch_one<T, D, FmaPath<T, D, 8, 2>, PARTIAL>(kmap, vmap, a, units, 1, st);
+  if (a.rows <= 8) return launch_one<T, D, MmaTPath<T, D>, PARTIAL>(kmap, vmap, a, units, 1, st);
   const int groups = (a.rows + 15) / 16;
   return launch_one<T, D, MmaPath<T, D>, PARTIAL>(kmap, vmap, a, units, groups, st);
 }
@@ -100,6 +101,7 @@ static cudaError_t launch_paths8(const CUtensorMap &kmap, const CUtensorMap &vma
                                  const DecodeArgs &a, int units, cudaStream_t st) {
   if (a.rows == 1) return launch_one<T, 128, Fma8Path<T, 1>, PARTIAL, true>(kmap, vmap, a, units, 1, st);
   if (a.rows == 2) return launch_one<T, 128, Fma8Path<T, 2>, PARTIAL, true>(kmap, vmap, a, units, 1, st);
+  if (a.rows <= 8) return launch_one<T, 128, Mma8TPath<T>, PARTIAL, true>(kmap, vmap, a, units, 1, st);
   const int groups = (a.rows + 15) / 16;
   return launch_one<T, 128, Mma8Path<T>, PARTIAL, true>(kmap, vmap, a, units, groups, st);
 }

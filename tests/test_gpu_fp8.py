@@ -86,7 +86,9 @@ SMALL = [("llama7b_mha_fp8", {"num_seqs": 3}), ("gqa_fp8", {"num_seqs": 5}),
          ("gqa_fp8", {"num_seqs": 4, "num_q_heads": 8, "num_kv_heads": 4}),      # 2 rows
          ("gqa_fp8", {"num_seqs": 4, "q_len": 4}),                               # 16 rows
          ("llama7b_mha_fp8", {"num_seqs": 2, "num_q_heads": 32, "num_kv_heads": 1,
-                              "dtype": "bf16"})]                                 # 32 rows
+                              "dtype": "bf16"}),                                 # 32 rows
+         ("gqa_fp8", {"num_seqs": 4, "q_len": 2, "dtype": "fp16"}),             # 8 rows, causal
+         ("gqa_fp8", {"num_seqs": 5, "num_q_heads": 12, "num_kv_heads": 4})]    # 3 rows
 
 
 @pytest.mark.parametrize("fused", [False, True], ids=["separate", "fused"])

@@ -143,7 +143,10 @@ EDGE_LENS = [0, 1, 2, 15, 16, 17, 31, 32, 33, 100, 257]
 @pytest.mark.parametrize("dtype", ["fp16", "bf16"])
 @pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("h_q,h_kv,q_len", [(4, 4, 1), (8, 4, 1), (12, 4, 1), (16, 4, 1),
-                                            (8, 8, 2), (8, 2, 4), (32, 4, 4), (6, 2, 3)])
+                                            (8, 8, 2), (8, 2, 4), (32, 4, 4), (6, 2, 3),
+                                            # 5..8 rows per KV head, causal ones included
+                                            (8, 4, 3), (16, 2, 1), (10, 2, 1), (4, 2, 4),
+                                            (7, 1, 1)])
 def test_edge_lengths_groups_and_query_counts(pa, orc, dtype, d, h_q, h_kv, q_len):
     lens = EDGE_LENS
     q, K, V = _logical_case(3, lens, h_q, h_kv, d, dtype, q_len=q_len, qscale=2.0)
