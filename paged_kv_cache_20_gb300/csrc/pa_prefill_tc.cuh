@@ -32,8 +32,10 @@
 //               (16-bit) over the S_j columns it came from, rescale its half of O in
 //               TMEM when the row max has grown by more than 2^8 since the last
 //               rescale (until then P is taken against the older max, at most 2^8,
-//               and the final O / l is the same quotient); at the end O / l (or
-//               the partial statistics) for its half of the columns.
+//               and the final O / l is the same quotient).  A unit's results,
+//               O / l (or the partial statistics) for the warp's half of the
+//               columns, are written during the next unit's first chunk, through a
+//               shared-memory transpose into whole 64-byte row pieces.
 // S_{j+1} and S_{j+2} are computed while the softmax works on S_j.  S_{j+3} is issued
 // only after the commit of P_j V_j (the last reader of buffer j % 3) has fired.  A
 // unit's Q replaces the previous one once that unit's last S MMA has completed
