@@ -32,6 +32,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 import numpy as np
@@ -180,7 +181,9 @@ class ClockSampler:
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+        # raw samples (the JSON line carries their summary); PA_BENCH_OUT overrides
+        out_dir = os.environ.get("PA_BENCH_OUT", tempfile.gettempdir())
+        self.path = os.path.join(out_dir, f"pagedattn_clocks_rank{gpu_index}.csv")
 
     def __enter__(self):
         try:
