@@ -502,35 +502,44 @@ def time_e2e(runner: Runner, steps: int, warmup: int):
 def cpu_baseline(w: workloads.Workload, budget_s: float = 5.0) -> dict:
     """The oracle as it stands, on the host cores, over the same workload: slot
     mapping, append and attention sequence by sequence, repeated until the time
-    budget is spent.  Value in KV tokens/s."""
+    budget is spent.  Value in KV tokens/s, with all cores working on each
+    sequence's rows; a shorter run on one thread is reported beside it."""
     import oracle
     orc = oracle.get()
-    threads = os.cpu_count() or 1
     c = w.cfg
     kc, vc = w.bits("k_cache"), w.bits("v_cache")        # append is idempotent: in place
     bt, cl = w.block_tables.numpy(), w.context_lens.numpy()
     slots = orc.slot_mapping(bt, cl, c.block_size, c.q_len)
     qb = w.bits("q")
     rows_per_seq = c.q_len * c.num_q_heads
-    done_tokens, done_seqs, passes = 0, 0, 0
-    t0 = time.perf_counter()
-    while time.perf_counter() - t0 < budget_s and passes < 100:
-        for i in range(c.num_seqs):
-            sl = slice(i * c.q_len, (i + 1) * c.q_len)
-            orc.append_kv(kc, vc, w.bits("k_new")[sl], w.bits("v_new")[sl], slots[sl])
-            rows = np.arange(i * rows_per_seq, (i + 1) * rows_per_seq)
-            orc.decode(qb, kc, vc, bt, cl, w.scale, c.dtype, q_len=c.q_len, rows=rows,
-                       threads=threads)
-            done_tokens += int(cl[i])
-            done_seqs += 1
-            if time.perf_counter() - t0 > budget_s:
-                break
-        passes += 1
-    dt = time.perf_counter() - t0
+
+    def run(threads, budget):
+        done_tokens, done_seqs, passes = 0, 0, 0
+        t0 = time.perf_counter()
+        while time.perf_counter() - t0 < budget and passes < 100:
+            for i in range(c.num_seqs):
+                sl = slice(i * c.q_len, (i + 1) * c.q_len)
+                orc.append_kv(kc, vc, w.bits("k_new")[sl], w.bits("v_new")[sl], slots[sl])
+                rows = np.arange(i * rows_per_seq, (i + 1) * rows_per_seq)
+                orc.decode(qb, kc, vc, bt, cl, w.scale, c.dtype, q_len=c.q_len, rows=rows,
+                           threads=threads)
+                done_tokens += int(cl[i])
+                done_seqs += 1
+                if time.perf_counter() - t0 > budget:
+                    break
+            passes += 1
+        return done_tokens, done_seqs, passes, time.perf_counter() - t0
+
+    threads = os.cpu_count() or 1
+    done_tokens, done_seqs, passes, dt = run(threads, budget_s)
+    one_tokens, one_seqs, _, one_dt = run(1, budget_s / 2)
     return {"value": done_tokens / dt, "unit": UNIT, "cores": threads, "kind": "oracle",
             "sample": f"{c.name}: {done_seqs} sequence-steps ({passes} pass(es) over the "
                       f"{c.num_seqs} sequences, {done_tokens} KV tokens), fp64 C oracle, "
-                      f"{threads} threads, {dt:.1f} s wall"}
+                      f"{threads} threads, {dt:.1f} s wall",
+            "single_thread": {"value": one_tokens / one_dt, "unit": UNIT, "cores": 1,
+                              "sample": f"{one_seqs} sequence-steps ({one_tokens} KV tokens), "
+                                        f"{one_dt:.1f} s wall"}}
 
 
 def measure_config(pa, name, seed, device, steps, warmup, world, peaks, e2e=False,
