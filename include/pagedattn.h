@@ -229,7 +229,8 @@ PA_API pa_status pa_append_decode(void *out, const void *q, const void *k_new, c
  *                    step's append when k_new/v_new are given), cut into
  *                    tail_splits equal parts;
  * then the combine.  With tail_splits == 1 and q_len <= 16 the tail pass is a
- * single pass that merges partition 0 into its result (no combine launch).  The
+ * single pass that merges partition 0 into its result (no combine launch).  It
+ * runs alongside the prefix pass and waits for it only before that merge.  The
  * causal limit applies in both passes.
  * Caller's contract: for every sequence, table entries [0, prefix_blocks) equal
  * those of row 0, and this step's new tokens lie at or past position

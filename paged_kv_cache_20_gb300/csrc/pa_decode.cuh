@@ -353,31 +353,6 @@ struct MmaPath {
       for (int e = 0; e < 4; ++e) o[nt][e] = 0.f;
   }
 
-  // Rows given directly: this lane's two q rows (nullptr = padding) and how many
-  // leading positions each may see.
-  __device__ __forceinline__ void init_explicit(const T *(&qrow)[2], const int (&limit)[2],
-                                                float sscale) {
-    const int c2 = (threadIdx.x & 3) * 2;
-#pragma unroll
-    for (int hr = 0; hr < 2; ++hr) {
-      lim[hr] = limit[hr];
-      m[hr] = -INFINITY;
-      l[hr] = 0.f;
-      rs[hr] = sscale;
-    }
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) o[nt][e] = 0.f;
-#pragma unroll
-    for (int ks = 0; ks < KS; ++ks)
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int hr = i & 1, col = ks * 16 + c2 + (i >> 1) * 8;
-        qa[ks][i] = qrow[hr] ? __ldg(reinterpret_cast<const uint32_t *>(qrow[hr] + col)) : 0u;
-      }
-  }
-
   __device__ __forceinline__ void init(const DecodeArgs &a, int seq, int kvh, int row0, int L,
                                        float sscale, uint32_t) {
     const int c2 = (threadIdx.x & 3) * 2;
@@ -1148,7 +1123,18 @@ __global__ void __launch_bounds__(NW * 32)
   // example the KV append): setup above this point overlaps that kernel's tail.
   // Wait for it to complete before the first read of global memory: any input
   // (cache, q, tables, lengths) may have been written by it.
-  griddep_wait();
+  //
+  // The one exception is the tail pass of a cascade, which merges a prior
+  // partition (prior_m != nullptr) and waits only before its epilogue.
+  // - The kernel before it is the cascade's shared-prefix pass.  That pass writes
+  //   nothing but the prior partition, read here only after the wait, L2-only.
+  // - The prefix pass reads only the shared blocks, and this kernel's append never
+  //   writes those (the caller's contract).
+  // - Every other input was written by kernels that completed before the prefix
+  //   pass passed its own wait and allowed this launch.
+  // So the prefix pass runs while this kernel walks its own blocks.
+  const bool late_wait = a.prior_m != nullptr;
+  if (!late_wait) griddep_wait();
   griddep_launch_dependents();  // the next kernel may start its own setup
 
   const int csize = static_cast<int>(cluster_nctarank());  // 1 without a cluster launch
@@ -1342,6 +1328,7 @@ __global__ void __launch_bounds__(NW * 32)
                                                    mrg_acc + warp * RPC * kStride);
   __syncthreads();
 
+  if (late_wait) griddep_wait();  // the prior partition is complete and visible
   auto emit = [&](int r, int d8, float M, float den, const float (&num)[8]) {
     const RowInfo ri = row_info(a, kvh, row0 + r);
     if (!ri.valid) return;
@@ -1366,14 +1353,14 @@ __global__ void __launch_bounds__(NW * 32)
         // softmax, once more
         const size_t prow = (size_t)seq * a.prior_splits * (a.q_len * a.num_q_heads) +
                             (size_t)ri.u * a.num_q_heads + ri.h;
-        const float m0 = __ldg(a.prior_m + prow), l0 = __ldg(a.prior_l + prow);
+        const float m0 = __ldcg(a.prior_m + prow), l0 = __ldcg(a.prior_l + prow);
         const float Mx = fmaxf(M, m0);
         const float w1 = (M == -INFINITY) ? 0.f : fast_exp2(M - Mx);
         const float w0 = (m0 == -INFINITY) ? 0.f : fast_exp2(m0 - Mx);
         const float dd = w1 * den + w0 * l0;
         inv = dd > 0.f ? 1.f / dd : 0.f;
         const float4 *src = reinterpret_cast<const float4 *>(a.prior_acc + prow * D + d8 * 8);
-        const float4 p0 = __ldg(src), p1 = __ldg(src + 1);
+        const float4 p0 = __ldcg(src), p1 = __ldcg(src + 1);
         const float pv[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
 #pragma unroll
         for (int i = 0; i < 8; ++i) o[i] = (w1 * num[i] * vscale + w0 * pv[i]) * inv;
