@@ -46,7 +46,10 @@
  *    16-bit cache (up to 16 query rows per sequence go to the decode kernel, more
  *    to a tensor-core kernel that shares each K/V chunk among 128 query rows of a
  *    KV head: chunked prefill,
- *    [QA] Q14, [SB11] §11.3 "Continuous Batching"); q_len 1..16 with an FP8 cache.
+ *    [QA] Q14, [SB11] §11.3 "Continuous Batching"); q_len 1..4096 with an FP8
+ *    cache too, where every q_len runs on the decode kernel in groups of 16
+ *    query rows per KV head (each group reads the sequence's blocks: meant for
+ *    decode and short chunks).
  *  - Alignment: every pointer 16-byte aligned.
  *
  * Errors: argument checks run on the host before any launch and return

@@ -328,9 +328,10 @@ pa_status decode_common(void *out, float *ws, const WsLayout *lay, const void *q
   const int64_t units = (int64_t)num_seqs * num_kv_heads * num_splits;
   if (units >= (int64_t)1 << 31) return PA_ERR_INVALID_ARG;
   const bool fp8 = k_scale != nullptr;
-  // many query rows (or the shared-prefix pass): the CTA-shared pipeline kernel
-  const bool prefill = place.shared_prefix > 0 || q_len > kMaxDecodeQLen;
-  if (prefill && fp8) return PA_ERR_UNSUPPORTED;
+  // many query rows (or the shared-prefix pass): the CTA-shared pipeline kernel.
+  // Over an FP8 cache every q_len goes to the decode kernel, in row groups of 16.
+  if (fp8 && place.shared_prefix > 0) return PA_ERR_UNSUPPORTED;
+  const bool prefill = place.shared_prefix > 0 || (q_len > kMaxDecodeQLen && !fp8);
   CUtensorMap kmap, vmap;
   pa_status st = make_map(&kmap, k_cache, dtype, head_dim, num_blocks, num_kv_heads, fp8);
   if (st != PA_OK) return st;
@@ -680,7 +681,7 @@ PA_API pa_status pa_decode_fp8(void *out, const void *q, const void *k_new, cons
                               num_q_heads, num_kv_heads, head_dim, block_size, scale,
                               max_blocks_per_seq, num_blocks, q_len, dtype);
   if (st != PA_OK) return st;
-  if (head_dim != 128 || q_len > kMaxDecodeQLen) return PA_ERR_UNSUPPORTED;
+  if (head_dim != 128) return PA_ERR_UNSUPPORTED;
   if (num_splits == 1)
     return decode_common(out, nullptr, nullptr, q, k_cache, v_cache, block_tables, context_lens,
                          num_seqs, num_q_heads, num_kv_heads, head_dim, scale, 1,

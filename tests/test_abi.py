@@ -175,8 +175,9 @@ def test_cascade_rejects_bad_arguments(lib):
     assert call(d96, 2, 2, FAKE, ws_ok) == -2
 
 
-def test_fp8_keeps_the_decode_row_limit(lib):
-    # an FP8 cache goes only through the decode kernel: q_len <= 16
+def test_fp8_query_length_limit(lib):
+    # an FP8 cache takes the same q_len range as a 16-bit one, 1..4096
     args = [FAKE, FAKE, None, None, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 2, 8, 2, 128, 16, 0.1, 4,
             8]
-    assert lib.pa_decode_fp8(*args, 17, 0, 1, None, 0, None) == -2
+    assert lib.pa_decode_fp8(*args, 4097, 0, 1, None, 0, None) == -2
+    assert lib.pa_decode_fp8(*args, 0, 0, 1, None, 0, None) == -1

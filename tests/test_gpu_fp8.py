@@ -88,7 +88,11 @@ SMALL = [("llama7b_mha_fp8", {"num_seqs": 3}), ("gqa_fp8", {"num_seqs": 5}),
          ("llama7b_mha_fp8", {"num_seqs": 2, "num_q_heads": 32, "num_kv_heads": 1,
                               "dtype": "bf16"}),                                 # 32 rows
          ("gqa_fp8", {"num_seqs": 4, "q_len": 2, "dtype": "fp16"}),             # 8 rows, causal
-         ("gqa_fp8", {"num_seqs": 5, "num_q_heads": 12, "num_kv_heads": 4})]    # 3 rows
+         ("gqa_fp8", {"num_seqs": 5, "num_q_heads": 12, "num_kv_heads": 4}),    # 3 rows
+         # more than 16 rows per KV head: row groups of 16 on the decode kernel
+         ("gqa_fp8", {"num_seqs": 3, "q_len": 40, "lens": ("fixed", (40, 300, 1000))}),
+         ("llama7b_mha_fp8", {"num_seqs": 2, "q_len": 24, "num_q_heads": 8,
+                              "num_kv_heads": 8, "lens": ("fixed", (30, 700))})]
 
 
 @pytest.mark.parametrize("fused", [False, True], ids=["separate", "fused"])
