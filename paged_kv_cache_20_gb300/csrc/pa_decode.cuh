@@ -395,13 +395,20 @@ struct MmaPath {
     softmax_pv<MASKED>(sc, vt, tile_idx);
   }
 
+  // P has to be rounded to the 16-bit operand type.  fp16 keeps 11 significant bits
+  // (output error <= 2^-12 max|v|); bf16 keeps 8, too coarse for peaked rows, so
+  // bf16 P is split into hi + lo bf16 parts and both are multiplied by V (residual
+  // relative error ~2^-17).
+  static constexpr bool kSplitP = Elt<T>::kMantBits < 10;
+
   // Online-softmax update of this tile's scores S (C fragments: rows lane/4 and
-  // lane/4 + 8, tokens nt*8 + (lane%4)*2 + {0,1}) and O += P V with V^T fragments
-  // from the 16-bit tile at vt.
+  // lane/4 + 8, tokens nt*8 + (lane%4)*2 + {0,1}), rescaling O and l when a row's
+  // maximum grows.  Returns P as the A operand (rows x 16 tokens): pa, and pl for
+  // the split.
   template <bool MASKED>
-  __device__ __forceinline__ void softmax_pv(float (&sc)[2][4], uint32_t vt, int tile_idx) {
+  __device__ __forceinline__ void softmax_p(float (&sc)[2][4], int tile_idx, uint32_t (&pa)[4],
+                                            uint32_t (&pl)[4]) {
     const int lane = threadIdx.x & 31;
-    const int mi = lane >> 3, ri = lane & 7;
     // scale to base-2 units, mask, row max over the 16 tokens (4 lanes per row)
     float mx[2];
 #pragma unroll
@@ -444,22 +451,26 @@ struct MmaPath {
           l[hr] += p;
         }
     }
-    // P as the A operand (rows x 16 tokens), straight from the S fragments.  P has
-    // to be rounded to the 16-bit operand type.  fp16 keeps 11 significant bits
-    // (output error <= 2^-12 max|v|); bf16 keeps 8, too coarse for peaked rows, so
-    // bf16 P is split into hi + lo bf16 parts and both are multiplied by V
-    // (residual relative error ~2^-17).
-    constexpr bool kSplitP = Elt<T>::kMantBits < 10;
-    uint32_t pa[4], pl[4];
+    // P as the A operand, straight from the S fragments
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const float p0 = sc[i >> 1][2 * (i & 1)], p1 = sc[i >> 1][2 * (i & 1) + 1];
       pa[i] = Elt<T>::from_f2(p0, p1);
+      pl[i] = 0u;
       if (kSplitP) {
         const float2 hi = Elt<T>::to_f2(pa[i]);
         pl[i] = Elt<T>::from_f2(p0 - hi.x, p1 - hi.y);
       }
     }
+  }
+
+  // softmax_p, then O += P V with V^T fragments from the 16-bit tile at vt.
+  template <bool MASKED>
+  __device__ __forceinline__ void softmax_pv(float (&sc)[2][4], uint32_t vt, int tile_idx) {
+    const int lane = threadIdx.x & 31;
+    const int mi = lane >> 3, ri = lane & 7;
+    uint32_t pa[4], pl[4];
+    softmax_p<MASKED>(sc, tile_idx, pa, pl);
     // O += P V: B fragments (V^T) by ldmatrix.trans, two 8-dim n-tiles per load
 #pragma unroll
     for (int dp = 0; dp < NT / 2; ++dp) {
@@ -528,11 +539,10 @@ struct MmaTPath {
   float rs[2];
   int lim[2];
 
-  __device__ __forceinline__ void init(const DecodeArgs &a, int seq, int kvh, int row0, int L,
-                                       float sscale, uint32_t) {
-    const int lane = threadIdx.x & 31;
-    const int g = lane >> 2, c = lane & 3;
-    const T *qb_ptr = static_cast<const T *>(a.q);
+  // Rows 2c, 2c + 1 of this lane: causal limits, softmax state, O^T = 0.
+  __device__ __forceinline__ void init_rows(const DecodeArgs &a, int kvh, int row0, int L,
+                                            float sscale) {
+    const int c = threadIdx.x & 3;
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
       const RowInfo ri = row_info(a, kvh, row0 + 2 * c + e);
@@ -541,6 +551,18 @@ struct MmaTPath {
       l[e] = 0.f;
       rs[e] = sscale;
     }
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) o[mt][i] = 0.f;
+  }
+
+  __device__ __forceinline__ void init(const DecodeArgs &a, int seq, int kvh, int row0, int L,
+                                       float sscale, uint32_t) {
+    const int lane = threadIdx.x & 31;
+    const int g = lane >> 2, c = lane & 3;
+    const T *qb_ptr = static_cast<const T *>(a.q);
+    init_rows(a, kvh, row0, L, sscale);
     const RowInfo rq = row_info(a, kvh, row0 + g);
     const T *qrow = rq.valid ? qb_ptr + ((size_t)(seq * a.q_len + rq.u) * a.num_q_heads + rq.h) * D
                              : nullptr;
@@ -549,10 +571,6 @@ struct MmaTPath {
       qb[ks][0] = qrow ? __ldg(reinterpret_cast<const uint32_t *>(qrow + ks * 16 + 2 * c)) : 0u;
       qb[ks][1] = qrow ? __ldg(reinterpret_cast<const uint32_t *>(qrow + ks * 16 + 2 * c + 8)) : 0u;
     }
-#pragma unroll
-    for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-      for (int i = 0; i < 4; ++i) o[mt][i] = 0.f;
   }
 
   template <bool MASKED>
@@ -574,13 +592,17 @@ struct MmaTPath {
     softmax_pv<MASKED>(sc, vt, tile_idx);
   }
 
+  // bf16 P is split into hi + lo parts as in MmaPath (8 significant bits are too
+  // coarse for peaked rows); fp16 P is used directly.
+  static constexpr bool kSplitP = Elt<T>::kMantBits < 10;
+
   // Online-softmax update from this tile's raw S^T (sc[i]: token g + 8 (i >> 1), row
-  // 2c + (i & 1)) and O^T += V^T P^T with V^T fragments from the 16-bit tile at vt.
+  // 2c + (i & 1)), rescaling O^T and l when a row's maximum grows.  Returns P^T's B
+  // fragments (tokens 0-7 and 8-15, transposed): bh, and bl for the split.
   template <bool MASKED>
-  __device__ __forceinline__ void softmax_pv(float (&sc)[4], uint32_t vt, int tile_idx) {
-    const int lane = threadIdx.x & 31;
-    const int mi = lane >> 3, ri = lane & 7;
-    const int g = lane >> 2;
+  __device__ __forceinline__ void softmax_p(float (&sc)[4], int tile_idx, uint32_t (&bh)[2],
+                                            uint32_t (&bl)[2]) {
+    const int g = (threadIdx.x & 31) >> 2;
     // scale, mask
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -620,21 +642,27 @@ struct MmaTPath {
         l[e] += p;
       }
     }
-    // P^T B fragments: (tokens 0-7) and (tokens 8-15) blocks, transposed.  bf16 P is
-    // split into hi + lo parts as in MmaPath (8 significant bits are too coarse for
-    // peaked rows); fp16 P is used directly.
-    constexpr bool kSplitP = Elt<T>::kMantBits < 10;
-    uint32_t bh[2], bl[2];
+    // P^T B fragments: (tokens 0-7) and (tokens 8-15) blocks, transposed
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const float p0 = sc[2 * h], p1 = sc[2 * h + 1];
       const uint32_t hi = Elt<T>::from_f2(p0, p1);
       bh[h] = movmatrix_trans(hi);
+      bl[h] = 0u;
       if (kSplitP) {
         const float2 hf = Elt<T>::to_f2(hi);
         bl[h] = movmatrix_trans(Elt<T>::from_f2(p0 - hf.x, p1 - hf.y));
       }
     }
+  }
+
+  // softmax_p, then O^T += V^T P^T with V^T fragments from the 16-bit tile at vt.
+  template <bool MASKED>
+  __device__ __forceinline__ void softmax_pv(float (&sc)[4], uint32_t vt, int tile_idx) {
+    const int lane = threadIdx.x & 31;
+    const int mi = lane >> 3, ri = lane & 7;
+    uint32_t bh[2], bl[2];
+    softmax_p<MASKED>(sc, tile_idx, bh, bl);
     // O^T += V^T P^T: A fragment of V^T by ldmatrix.trans, matrices (dims 0-7 | 8-15)
     // x (tokens 0-7 | 8-15) of the m-tile
 #pragma unroll
@@ -684,40 +712,59 @@ __device__ __forceinline__ uint2 quantize8(const uint4 v, float scale) {
   return make_uint2((uint32_t)c[0] | ((uint32_t)c[1] << 16), (uint32_t)c[2] | ((uint32_t)c[3] << 16));
 }
 
+// Word i (compile-time after unrolling) of a 16-byte load.
+__device__ __forceinline__ uint32_t word_of(const uint4 &v, int i) {
+  return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
+}
+// Codes 0, 1 (lo) or 2, 3 (hi) of a word of four e4m3 codes -> f16x2.
+__device__ __forceinline__ uint32_t e4m3_lo_f16x2(uint32_t w) {
+  return e4m3x2_to_f16x2(static_cast<uint16_t>(w & 0xffffu));
+}
+__device__ __forceinline__ uint32_t e4m3_hi_f16x2(uint32_t w) {
+  return e4m3x2_to_f16x2(static_cast<uint16_t>(w >> 16));
+}
+
 // ---------------------------------------------------------------------------------
 // FP8 (e4m3) cache, tensor-core path with swapped operands for 3..8 rows per KV
-// head: MmaTPath's layout (tokens as the MMA's M, rows as N = 8) over fp16 MMAs.
-// K's A fragments are widened from the codes in registers, V is widened into this
-// warp's shared scratch, as in Mma8Path.  Inside each 16-dim k-step the contraction
-// is permuted so that a lane's k slots {2c, 2c+1, 2c+8, 2c+9} (c = lane % 4) are
-// dims 4c..4c+3: four consecutive codes, one 32-bit shared load; q^T's B fragments
-// use the same permutation, so S is unchanged.  Each q row is scaled by a power of
-// two into fp16's range and the score scale of the row's S^T column takes it back.
+// head: MmaTPath's layout (tokens as the MMA's M, rows as N = 8) over fp16 MMAs,
+// with both operands widened from the codes in registers (no shared-memory copy).
+// - S^T = K q^T: the contraction over head dims is permuted so that lane c's k
+//   slots {2c, 2c+1, 2c+8, 2c+9} of k-step ks are dims 32c + 4ks .. +3.  A lane
+//   reads its 32 dims of tokens g and g + 8 with two 16-byte loads each; q^T's B
+//   fragments use the same permutation, so S is unchanged.
+// - O^T += V^T P^T: the m-rows of O^T are permuted so that row g of m-tile b is
+//   dim 16g + 2b and row g + 8 is dim 16g + 2b + 1.  A lane then needs dims
+//   16g .. 16g + 15 of tokens 2c, 2c + 1, 2c + 8, 2c + 9 (the k slots of P^T), one
+//   16-byte load each; byte permutes pair the two tokens of each dim for the
+//   e4m3x2 -> f16x2 conversion.
+// Every load above is conflict-free under the 128-byte swizzle: the 8 lanes of a
+// shared-memory phase hit 8 distinct 16-byte bank groups.  Each q row is scaled by a
+// power of two into fp16's range and the score scale of its S^T column undoes it.
 template <typename T>
 struct Mma8TPath {
   static constexpr int D = 128;
   static constexpr int RPC = 8;
-  static constexpr int kTile16 = kTileTokens * D * 2;  // one widened tile
-  static constexpr int kExtraBytes = kTile16;          // widened V
-  MmaTPath<__half, D> inner;
-  uint32_t wv;  // widened V tile (this warp's scratch)
+  static constexpr int kExtraBytes = 0;
+  using Inner = MmaTPath<__half, D>;
+  static constexpr int KS = Inner::KS;
+  Inner inner;  // inner.o[b][i]: O^T dim 16g + 2b + (i >> 1), row 2c + (i & 1)
 
   __device__ __forceinline__ void init(const DecodeArgs &a, int seq, int kvh, int row0, int L,
-                                       float sscale, uint32_t scratch) {
+                                       float sscale, uint32_t) {
     const int lane = threadIdx.x & 31;
     const int g = lane >> 2, c = lane & 3;
-    inner.init(a, seq, kvh, row0, L, sscale, scratch);  // rows, limits, O^T; q below
-    // q row g, dims ks*16 + 4c .. 4c+3 of every k-step
+    inner.init_rows(a, kvh, row0, L, sscale);
+    // q row g, dims 32c + 4ks .. +3 of k-step ks
     const RowInfo rq = row_info(a, kvh, row0 + g);
     const T *qrow = rq.valid ? static_cast<const T *>(a.q) +
                                    ((size_t)(seq * a.q_len + rq.u) * a.num_q_heads + rq.h) * D
                              : nullptr;
-    float2 qf[MmaTPath<__half, D>::KS][2];
+    float2 qf[KS][2];
     float mx = 0.f;
 #pragma unroll
-    for (int ks = 0; ks < MmaTPath<__half, D>::KS; ++ks) {
+    for (int ks = 0; ks < KS; ++ks) {
       uint2 v = make_uint2(0u, 0u);
-      if (qrow) v = __ldg(reinterpret_cast<const uint2 *>(qrow + ks * 16 + 4 * c));
+      if (qrow) v = __ldg(reinterpret_cast<const uint2 *>(qrow + 32 * c + 4 * ks));
       qf[ks][0] = Elt<T>::to_f2(v.x);
       qf[ks][1] = Elt<T>::to_f2(v.y);
       mx = fmaxf(mx, fmaxf(fmaxf(fabsf(qf[ks][0].x), fabsf(qf[ks][0].y)),
@@ -729,7 +776,7 @@ struct Mma8TPath {
     const int e_row = (mx > 0.f && isfinite(mx)) ? ilogbf(mx) : 0;
     const float down = ldexpf(1.f, -e_row);  // |q| * down < 2: well inside fp16
 #pragma unroll
-    for (int ks = 0; ks < MmaTPath<__half, D>::KS; ++ks) {
+    for (int ks = 0; ks < KS; ++ks) {
       inner.qb[ks][0] = Elt<__half>::from_f2(qf[ks][0].x * down, qf[ks][0].y * down);
       inner.qb[ks][1] = Elt<__half>::from_f2(qf[ks][1].x * down, qf[ks][1].y * down);
     }
@@ -739,62 +786,72 @@ struct Mma8TPath {
       const int er = __shfl_sync(0xffffffffu, e_row, 4 * (2 * c + e));
       inner.rs[e] = sscale * ldexpf(1.f, er);
     }
-    wv = scratch;
-  }
-
-  __device__ __forceinline__ void widen(uint32_t src8, uint32_t dst16) {
-    const int lane = threadIdx.x & 31;
-#pragma unroll
-    for (int i = 0; i < (kTileTokens * 8) / 32; ++i) {  // 128 chunks of 16 codes
-      const int idx = lane + 32 * i;
-      const int row = idx >> 3, c8 = idx & 7;
-      const uint4 v = lds128(src8 + sw128_offset_row128(row, c8));
-      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-      uint32_t o[8];
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        o[2 * k] = e4m3x2_to_f16x2(static_cast<uint16_t>(w[k] & 0xffffu));
-        o[2 * k + 1] = e4m3x2_to_f16x2(static_cast<uint16_t>(w[k] >> 16));
-      }
-      asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
-                       dst16 + sw128_offset<kTileTokens>(row, 2 * c8)),
-                   "r"(o[0]), "r"(o[1]), "r"(o[2]), "r"(o[3])
-                   : "memory");
-      asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
-                       dst16 + sw128_offset<kTileTokens>(row, 2 * c8 + 1)),
-                   "r"(o[4]), "r"(o[5]), "r"(o[6]), "r"(o[7])
-                   : "memory");
-    }
   }
 
   template <bool MASKED>
   __device__ __forceinline__ void tile(uint32_t kt, uint32_t vt, int tile_idx, float) {
     const int lane = threadIdx.x & 31;
     const int g = lane >> 2, c = lane & 3;
-    widen(vt, wv);
-    // S^T: A fragment of K widened in registers (tokens g and g + 8, permuted dims)
+    const uint4 k0a = lds128(kt + sw128_offset_row128(g, 2 * c));
+    const uint4 k0b = lds128(kt + sw128_offset_row128(g, 2 * c + 1));
+    const uint4 k8a = lds128(kt + sw128_offset_row128(g + 8, 2 * c));
+    const uint4 k8b = lds128(kt + sw128_offset_row128(g + 8, 2 * c + 1));
+    const uint4 v0 = lds128(vt + sw128_offset_row128(2 * c, g));
+    const uint4 v1 = lds128(vt + sw128_offset_row128(2 * c + 1, g));
+    const uint4 v8 = lds128(vt + sw128_offset_row128(2 * c + 8, g));
+    const uint4 v9 = lds128(vt + sw128_offset_row128(2 * c + 9, g));
+    // S^T: two independent chains (even and odd k-steps), then added
     float sc[4] = {0.f, 0.f, 0.f, 0.f}, sd[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int ks = 0; ks < MmaTPath<__half, D>::KS; ++ks) {
-      uint32_t w0, w1;
-      asm volatile("ld.shared.b32 %0, [%1];" : "=r"(w0) : "r"(kt + sw128_offset_row128(g, ks) + 4 * c));
-      asm volatile("ld.shared.b32 %0, [%1];" : "=r"(w1) : "r"(kt + sw128_offset_row128(g + 8, ks) + 4 * c));
-      const uint32_t ka[4] = {e4m3x2_to_f16x2(static_cast<uint16_t>(w0 & 0xffffu)),
-                              e4m3x2_to_f16x2(static_cast<uint16_t>(w1 & 0xffffu)),
-                              e4m3x2_to_f16x2(static_cast<uint16_t>(w0 >> 16)),
-                              e4m3x2_to_f16x2(static_cast<uint16_t>(w1 >> 16))};
+    for (int ks = 0; ks < KS; ++ks) {
+      const uint32_t w0 = word_of(ks < 4 ? k0a : k0b, ks & 3);
+      const uint32_t w8 = word_of(ks < 4 ? k8a : k8b, ks & 3);
+      const uint32_t ka[4] = {e4m3_lo_f16x2(w0), e4m3_lo_f16x2(w8), e4m3_hi_f16x2(w0),
+                              e4m3_hi_f16x2(w8)};
       Elt<__half>::mma16816((ks & 1) ? sd : sc, ka, inner.qb[ks][0], inner.qb[ks][1]);
     }
 #pragma unroll
     for (int i = 0; i < 4; ++i) sc[i] += sd[i];
-    __syncwarp();  // widened V visible to every lane
-    inner.template softmax_pv<MASKED>(sc, wv, tile_idx);
-    __syncwarp();  // the scratch is rewritten by the next tile
+    uint32_t bh[2], bl[2];
+    inner.template softmax_p<MASKED>(sc, tile_idx, bh, bl);  // fp16 P: no split
+    // O^T += V^T P^T.  Word j of a lane's V chunk holds dims 16g + 4j .. +3: m-tile
+    // 2j takes dims 4j, 4j + 1 (rows g, g + 8), m-tile 2j + 1 dims 4j + 2, 4j + 3.
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint32_t x0 = word_of(v0, j), x1 = word_of(v1, j);
+      const uint32_t x8 = word_of(v8, j), x9 = word_of(v9, j);
+      const uint32_t p01 = __byte_perm(x0, x1, 0x5140), q01 = __byte_perm(x0, x1, 0x7362);
+      const uint32_t p89 = __byte_perm(x8, x9, 0x5140), q89 = __byte_perm(x8, x9, 0x7362);
+      const uint32_t va[4] = {e4m3_lo_f16x2(p01), e4m3_hi_f16x2(p01), e4m3_lo_f16x2(p89),
+                              e4m3_hi_f16x2(p89)};
+      const uint32_t vb[4] = {e4m3_lo_f16x2(q01), e4m3_hi_f16x2(q01), e4m3_lo_f16x2(q89),
+                              e4m3_hi_f16x2(q89)};
+      Elt<__half>::mma16816(inner.o[2 * j], va, bh[0], bh[1]);
+      Elt<__half>::mma16816(inner.o[2 * j + 1], vb, bh[0], bh[1]);
+    }
   }
 
   template <int STRIDE>
   __device__ __forceinline__ void publish(float *mrg_m, float *mrg_l, float *mrg_acc) {
-    inner.template publish<STRIDE>(mrg_m, mrg_l, mrg_acc);
+    const int lane = threadIdx.x & 31;
+    const int g = lane >> 2, c = lane & 3;
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      float l = inner.l[e];
+      l += __shfl_xor_sync(0xffffffffu, l, 4);
+      l += __shfl_xor_sync(0xffffffffu, l, 8);
+      l += __shfl_xor_sync(0xffffffffu, l, 16);
+      const int r = 2 * c + e;
+      if (g == 0) {
+        mrg_m[r] = inner.m[e];
+        mrg_l[r] = l;
+      }
+#pragma unroll
+      for (int b = 0; b < Inner::MT; ++b) {
+        mrg_acc[r * STRIDE + 16 * g + 2 * b] = inner.o[b][e];
+        mrg_acc[r * STRIDE + 16 * g + 2 * b + 1] = inner.o[b][2 + e];
+      }
+    }
   }
 };
 
@@ -966,37 +1023,41 @@ struct Fma8Path {
   }
 };
 
-// FP8 (e4m3) cache, tensor-core path: each warp widens its FP8 K and V tiles into
-// fp16 tiles in its own shared scratch (same 128-byte swizzled layout as a 16-bit
-// cache tile; every e4m3 value is exact in fp16), then runs the fp16 tensor-core
-// tile whatever q's type.  A bf16 q row is brought into fp16 range by an exact
-// power-of-two factor 2^-e (e: exponent of the row's largest |q|), and 2^e goes
-// into that row's score scale.  P is then fp16 too: no hi/lo split is needed.
+// FP8 (e4m3) cache, tensor-core path for 9..16 rows per KV head: MmaPath's layout
+// over fp16 MMAs (every e4m3 value is exact in fp16), with both operands widened
+// from the codes in registers, as in Mma8TPath.
+// - S = Q K^T: inside the contraction over head dims, lane c's k slots {2c, 2c+1,
+//   2c+8, 2c+9} of k-step ks are dims 32c + 4ks .. +3; each lane reads its 32 dims
+//   of tokens g and g + 8 with two 16-byte loads each, and Q's A fragments use the
+//   same permutation.
+// - O += P V: column n of n-tile nt is dim 16n + nt.  A lane's B fragments are then
+//   dims 16g .. 16g + 15 of tokens 2c, 2c + 1, 2c + 8, 2c + 9 (one 16-byte load
+//   each), paired per dim by byte permutes; its accumulators hold dims 32c + nt and
+//   32c + 16 + nt of rows g and g + 8.
+// A bf16 q row is brought into fp16 range by an exact power-of-two factor 2^-e (e:
+// exponent of the row's largest |q|), and 2^e goes into that row's score scale.  P
+// is then fp16 too: no hi/lo split is needed.
 template <typename T>
 struct Mma8Path {
   static constexpr int D = 128;
   static constexpr int RPC = 16;
-  static constexpr int kTile16 = kTileTokens * D * 2;  // one widened tile
-  static constexpr int kExtraBytes = kTile16;          // widened V
-  MmaPath<__half, D> inner;
-  uint32_t wv;  // widened V tile (this warp's scratch)
+  static constexpr int kExtraBytes = 0;
+  using Inner = MmaPath<__half, D>;
+  static constexpr int KS = Inner::KS;
+  Inner inner;
 
-  // The contraction over head dims is permuted inside each 16-dim k-step so that a
-  // lane's four k slots {2c, 2c+1, 2c+8, 2c+9} (c = lane % 4) are dims 4c..4c+3:
-  // four consecutive e4m3 codes, one 32-bit shared load.  Q's A fragments use the
-  // same permutation, so S is unchanged.
   __device__ __forceinline__ void init(const DecodeArgs &a, int seq, int kvh, int row0, int L,
-                                       float sscale, uint32_t scratch) {
-    const int c4 = (threadIdx.x & 3) * 4;
+                                       float sscale, uint32_t) {
+    const int c = threadIdx.x & 3;
     const T *qrow[2];
     inner.template init_rows<T>(a, seq, kvh, row0, L, sscale, qrow);
-    float2 qf[MmaPath<__half, D>::KS][4];
+    float2 qf[KS][4];
     float mx[2] = {0.f, 0.f};
 #pragma unroll
-    for (int ks = 0; ks < MmaPath<__half, D>::KS; ++ks)
+    for (int ks = 0; ks < KS; ++ks)
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        const int hr = i & 1, col = ks * 16 + c4 + (i >> 1) * 2;
+        const int hr = i & 1, col = 32 * c + 4 * ks + (i >> 1) * 2;
         const uint32_t v = qrow[hr] ? __ldg(reinterpret_cast<const uint32_t *>(qrow[hr] + col)) : 0u;
         qf[ks][i] = Elt<T>::to_f2(v);
         mx[hr] = fmaxf(mx[hr], fmaxf(fabsf(qf[ks][i].x), fabsf(qf[ks][i].y)));
@@ -1014,76 +1075,83 @@ struct Mma8Path {
       inner.rs[hr] = sscale * ldexpf(1.f, e);
     }
 #pragma unroll
-    for (int ks = 0; ks < MmaPath<__half, D>::KS; ++ks)
+    for (int ks = 0; ks < KS; ++ks)
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const float d = down[i & 1];
         inner.qa[ks][i] = Elt<__half>::from_f2(qf[ks][i].x * d, qf[ks][i].y * d);
       }
-    wv = scratch;
-  }
-
-  __device__ __forceinline__ void widen(uint32_t src8, uint32_t dst16) {
-    const int lane = threadIdx.x & 31;
-#pragma unroll
-    for (int i = 0; i < (kTileTokens * 8) / 32; ++i) {  // 128 chunks of 16 codes
-      const int idx = lane + 32 * i;
-      const int row = idx >> 3, c8 = idx & 7;
-      const uint4 v = lds128(src8 + sw128_offset_row128(row, c8));
-      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-      uint32_t o[8];
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        o[2 * k] = e4m3x2_to_f16x2(static_cast<uint16_t>(w[k] & 0xffffu));
-        o[2 * k + 1] = e4m3x2_to_f16x2(static_cast<uint16_t>(w[k] >> 16));
-      }
-      asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
-                       dst16 + sw128_offset<kTileTokens>(row, 2 * c8)),
-                   "r"(o[0]), "r"(o[1]), "r"(o[2]), "r"(o[3])
-                   : "memory");
-      asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
-                       dst16 + sw128_offset<kTileTokens>(row, 2 * c8 + 1)),
-                   "r"(o[4]), "r"(o[5]), "r"(o[6]), "r"(o[7])
-                   : "memory");
-    }
   }
 
   template <bool MASKED>
   __device__ __forceinline__ void tile(uint32_t kt, uint32_t vt, int tile_idx, float) {
     const int lane = threadIdx.x & 31;
-    widen(vt, wv);
-    // S = Q K^T with K's B fragments widened in registers from the FP8 tile
+    const int g = lane >> 2, c = lane & 3;
+    uint4 kw[2][2];  // [token g, g + 8][dims 32c .. +15, 32c + 16 .. +31]
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int h = 0; h < 2; ++h) kw[nt][h] = lds128(kt + sw128_offset_row128(nt * 8 + g, 2 * c + h));
+    const uint4 v0 = lds128(vt + sw128_offset_row128(2 * c, g));
+    const uint4 v1 = lds128(vt + sw128_offset_row128(2 * c + 1, g));
+    const uint4 v8 = lds128(vt + sw128_offset_row128(2 * c + 8, g));
+    const uint4 v9 = lds128(vt + sw128_offset_row128(2 * c + 9, g));
+    // S = Q K^T; even and odd k-steps accumulate separately, then add
     float sc[2][4], sd[2][4];
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
       for (int e = 0; e < 4; ++e) sc[nt][e] = sd[nt][e] = 0.f;
 #pragma unroll
-    for (int ks = 0; ks < MmaPath<__half, D>::KS; ++ks) {
+    for (int ks = 0; ks < KS; ++ks) {
       float (&acc)[2][4] = (ks & 1) ? sd : sc;
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt) {
-        uint32_t w;
-        asm volatile("ld.shared.b32 %0, [%1];"
-                     : "=r"(w)
-                     : "r"(kt + sw128_offset_row128(nt * 8 + (lane >> 2), ks) + 4 * (lane & 3)));
-        const uint32_t b0 = e4m3x2_to_f16x2(static_cast<uint16_t>(w & 0xffffu));
-        const uint32_t b1 = e4m3x2_to_f16x2(static_cast<uint16_t>(w >> 16));
-        Elt<__half>::mma16816(acc[nt], inner.qa[ks], b0, b1);
+        const uint32_t w = word_of(kw[nt][ks >> 2], ks & 3);
+        Elt<__half>::mma16816(acc[nt], inner.qa[ks], e4m3_lo_f16x2(w), e4m3_hi_f16x2(w));
       }
     }
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
       for (int e = 0; e < 4; ++e) sc[nt][e] += sd[nt][e];
-    __syncwarp();  // widened V visible to every lane
-    inner.template softmax_pv<MASKED>(sc, wv, tile_idx);
-    __syncwarp();  // the scratch is rewritten by the next tile
+    uint32_t pa[4], pl[4];
+    inner.template softmax_p<MASKED>(sc, tile_idx, pa, pl);  // fp16 P: no split
+    // O += P V.  Word j of a lane's V chunk holds dims 16g + 4j .. +3: the B columns
+    // g of n-tiles 4j .. 4j + 3.
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint32_t x0 = word_of(v0, j), x1 = word_of(v1, j);
+      const uint32_t x8 = word_of(v8, j), x9 = word_of(v9, j);
+      const uint32_t p01 = __byte_perm(x0, x1, 0x5140), q01 = __byte_perm(x0, x1, 0x7362);
+      const uint32_t p89 = __byte_perm(x8, x9, 0x5140), q89 = __byte_perm(x8, x9, 0x7362);
+      Elt<__half>::mma16816(inner.o[4 * j], pa, e4m3_lo_f16x2(p01), e4m3_lo_f16x2(p89));
+      Elt<__half>::mma16816(inner.o[4 * j + 1], pa, e4m3_hi_f16x2(p01), e4m3_hi_f16x2(p89));
+      Elt<__half>::mma16816(inner.o[4 * j + 2], pa, e4m3_lo_f16x2(q01), e4m3_lo_f16x2(q89));
+      Elt<__half>::mma16816(inner.o[4 * j + 3], pa, e4m3_hi_f16x2(q01), e4m3_hi_f16x2(q89));
+    }
   }
 
   template <int STRIDE>
   __device__ __forceinline__ void publish(float *mrg_m, float *mrg_l, float *mrg_acc) {
-    inner.template publish<STRIDE>(mrg_m, mrg_l, mrg_acc);
+    const int lane = threadIdx.x & 31;
+    const int g = lane >> 2, c = lane & 3;
+#pragma unroll
+    for (int hr = 0; hr < 2; ++hr) {
+      float l = inner.l[hr];
+      l += __shfl_xor_sync(0xffffffffu, l, 1);
+      l += __shfl_xor_sync(0xffffffffu, l, 2);
+      const int r = g + 8 * hr;
+      if (c == 0) {
+        mrg_m[r] = inner.m[hr];
+        mrg_l[r] = l;
+      }
+#pragma unroll
+      for (int nt = 0; nt < Inner::NT; ++nt) {
+        mrg_acc[r * STRIDE + 32 * c + nt] = inner.o[nt][2 * hr];
+        mrg_acc[r * STRIDE + 32 * c + 16 + nt] = inner.o[nt][2 * hr + 1];
+      }
+    }
   }
 };
 

@@ -19,11 +19,11 @@ constexpr int kMaxDevices = 64;
 constexpr int kWarps = 4;
 template <bool PARTIAL>
 constexpr int stages_for() { return PARTIAL ? 3 : 2; }
-// An FP8 stage carries half the bytes, so FP8 keeps more stages per warp in flight:
-// 4 on the CUDA-core paths, 3 on the tensor-core paths (which also hold a 4 KiB
-// widened V tile per warp), both measured best and both still 3 CTAs per SM.
+// An FP8 stage carries half the bytes, so FP8 keeps 4 stages per warp in flight
+// (still 3 CTAs per SM).  On the swapped-operand FP8 path this measured faster than
+// 3 stages with 4 CTAs per SM or 2 stages.
 template <class Path, bool PARTIAL, bool KV8>
-constexpr int stages_of() { return KV8 ? (Path::kExtraBytes > 0 ? 3 : 4) : stages_for<PARTIAL>(); }
+constexpr int stages_of() { return KV8 ? 4 : stages_for<PARTIAL>(); }
 constexpr int kMaxCluster = 8;  // portable cluster size limit
 
 // Per device: SM count and resident CTAs per SM of one kernel (cached).
