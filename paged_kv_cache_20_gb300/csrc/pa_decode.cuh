@@ -1212,14 +1212,17 @@ __global__ void __launch_bounds__(NW * 32)
   const int rest = unit / a.num_kv_heads;
   const int split = rest % a.num_splits;
   int seq = rest / a.num_splits;
+  int L;
   if (a.lpt) {
     __shared__ __align__(16) int s_lens[kLptMaxSeqs];
     __shared__ int s_pick;
     seq = lpt_sequence(a.context_lens, a.num_seqs, seq, s_lens, &s_pick);
+    L = s_lens[seq];  // already loaded (and clamped at 0) for the ranking
+  } else {
+    L = max(0, __ldg(a.context_lens + seq));
   }
   const int row0 = blockIdx.y * RPC;
 
-  const int L = max(0, __ldg(a.context_lens + seq));
   int nb = (L + kTileTokens - 1) / kTileTokens;
   if (nb > a.max_blocks_per_seq) {  // context longer than its block table
     if (threadIdx.x == 0 && split == 0 && kvh == 0 && blockIdx.y == 0 && crank == 0)

@@ -12,8 +12,9 @@ namespace pa {
 constexpr int kMaxDevices = 64;
 
 // Pipeline shape: warps per CTA, stages per warp (measured on GB300).  The single
-// pass uses 2 stages per warp, which fits 3 CTAs per SM (12 warps) and helps the
-// skewed-length workloads.  The split-KV partial pass gets the caller's
+// pass uses 4 warps of 2 stages, which fits 3 CTAs per SM (12 warps) and helps the
+// skewed-length workloads; the FP8 swapped-operand path may use 3 warps instead
+// (launch_paths8).  The split-KV partial pass gets the caller's
 // equal-size partitions; with 3 stages (2 CTAs per SM) its CTAs are deeper and
 // fewer, which measured faster there.
 constexpr int kWarps = 4;
@@ -32,13 +33,14 @@ struct DeviceFit {
   std::atomic<int> ctas_per_sm{0};
 };
 
-template <typename T, int D, class Path, bool PARTIAL, bool KV8 = false>
-static cudaError_t launch_one(const CUtensorMap &kmap, const CUtensorMap &vmap,
-                              const DecodeArgs &a, int units, int row_groups, cudaStream_t st) {
+// Resident slots (SMs x CTAs per SM) of one kernel instance on the current device,
+// cached per device; the first call also sets the kernel's shared-memory opt-in.
+template <typename T, int D, class Path, bool PARTIAL, bool KV8, int NW>
+static cudaError_t resident_slots(long long &slots) {
   constexpr int kStages = stages_of<Path, PARTIAL, KV8>();
   constexpr int kStageBytes = 2 * kTileTokens * D * (KV8 ? 1 : 2);
-  constexpr int kSmem = kWarps * (kStages * kStageBytes + Path::kExtraBytes) + 1024;
-  auto kern = paged_decode_kernel<T, D, kWarps, kStages, Path, PARTIAL, KV8>;
+  constexpr int kSmem = NW * (kStages * kStageBytes + Path::kExtraBytes) + 1024;
+  auto kern = paged_decode_kernel<T, D, NW, kStages, Path, PARTIAL, KV8>;
   static DeviceFit fit[kMaxDevices];
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -52,24 +54,39 @@ static cudaError_t launch_one(const CUtensorMap &kmap, const CUtensorMap &vmap,
     int sms = 0, per_sm = 0;
     e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kWarps * 32, kSmem);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, NW * 32, kSmem);
     if (e != cudaSuccess) return e;
     f.sms.store(sms, std::memory_order_relaxed);
     f.ctas_per_sm.store(per_sm > 0 ? per_sm : 1, std::memory_order_release);
   }
-  // Single pass: when the units would fill fewer than two waves of resident CTAs,
-  // give each unit a cluster of 2, 4 or 8 CTAs so long sequences spread over
-  // several SMs.  The partial pass already has the caller's partitions (clusters
-  // measured slower there: each CTA's fixed cost outweighs the shorter tail).
+  slots = (long long)f.sms.load(std::memory_order_relaxed) * f.ctas_per_sm.load();
+  return cudaSuccess;
+}
+
+// Launch one kernel instance with NW warps per CTA.  Single pass: while the units
+// would fill fewer than wave_num / wave_den waves of resident CTAs, double the
+// cluster size (up to kMaxCluster) so long sequences spread over several SMs.
+template <typename T, int D, class Path, bool PARTIAL, bool KV8 = false, int NW = kWarps>
+static cudaError_t launch_one(const CUtensorMap &kmap, const CUtensorMap &vmap,
+                              const DecodeArgs &a, int units, int row_groups, cudaStream_t st,
+                              int wave_num = 2, int wave_den = 1) {
+  constexpr int kStages = stages_of<Path, PARTIAL, KV8>();
+  constexpr int kStageBytes = 2 * kTileTokens * D * (KV8 ? 1 : 2);
+  constexpr int kSmem = NW * (kStages * kStageBytes + Path::kExtraBytes) + 1024;
+  auto kern = paged_decode_kernel<T, D, NW, kStages, Path, PARTIAL, KV8>;
+  long long slots = 0;
+  cudaError_t e = resident_slots<T, D, Path, PARTIAL, KV8, NW>(slots);
+  if (e != cudaSuccess) return e;
+  // The partial pass already has the caller's partitions (clusters measured slower
+  // there: each CTA's fixed cost outweighs the shorter tail).
   int cluster = 1;
   if (!PARTIAL) {
-    const long long slots = (long long)f.sms.load() * f.ctas_per_sm.load();
     const long long work = (long long)units * row_groups;
-    while (cluster < kMaxCluster && work * cluster < 2 * slots) cluster *= 2;
+    while (cluster < kMaxCluster && work * cluster * wave_den < wave_num * slots) cluster *= 2;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)units * cluster, (unsigned)row_groups, 1);
-  cfg.blockDim = dim3(kWarps * 32, 1, 1);
+  cfg.blockDim = dim3(NW * 32, 1, 1);
   cfg.dynamicSmemBytes = kSmem;
   cfg.stream = st;
   // attribute 0: programmatic dependent launch (the kernel waits on griddepcontrol
@@ -101,7 +118,20 @@ static cudaError_t launch_paths8(const CUtensorMap &kmap, const CUtensorMap &vma
                                  const DecodeArgs &a, int units, cudaStream_t st) {
   if (a.rows == 1) return launch_one<T, 128, Fma8Path<T, 1>, PARTIAL, true>(kmap, vmap, a, units, 1, st);
   if (a.rows == 2) return launch_one<T, 128, Fma8Path<T, 2>, PARTIAL, true>(kmap, vmap, a, units, 1, st);
-  if (a.rows <= 8) return launch_one<T, 128, Mma8TPath<T>, PARTIAL, true>(kmap, vmap, a, units, 1, st);
+  if (a.rows <= 8) {
+    // Single pass, measured over batch sizes (GQA and MHA shapes over FP8): when the
+    // units fit in one wave of 3-warp CTAs (4 per SM), those beat 4-warp CTAs (3 per
+    // SM) by 5-20 %; either way clusters stop growing at 1.5 waves.
+    if constexpr (!PARTIAL) {
+      long long slots3 = 0;
+      const cudaError_t e = resident_slots<T, 128, Mma8TPath<T>, false, true, 3>(slots3);
+      if (e != cudaSuccess) return e;
+      if (units < slots3)
+        return launch_one<T, 128, Mma8TPath<T>, PARTIAL, true, 3>(kmap, vmap, a, units, 1, st, 3, 2);
+      return launch_one<T, 128, Mma8TPath<T>, PARTIAL, true>(kmap, vmap, a, units, 1, st, 3, 2);
+    }
+    return launch_one<T, 128, Mma8TPath<T>, PARTIAL, true>(kmap, vmap, a, units, 1, st);
+  }
   const int groups = (a.rows + 15) / 16;
   return launch_one<T, 128, Mma8Path<T>, PARTIAL, true>(kmap, vmap, a, units, groups, st);
 }

@@ -107,14 +107,22 @@ def test_fp8_small_every_element(pa, orc, name, over, splits, fused):
     _tol.check(_f64(out), ref, w.cfg.dtype, f"{name} {over} splits {splits}")
 
 
-@pytest.mark.parametrize("name", ["llama7b_mha_fp8", "gqa_fp8"])
-def test_fp8_full_size_sampled_rows(pa, orc, name):
-    w = workloads.make(name)
+# The swapped-operand path launches 3-warp CTAs while the units fit in one wave of
+# them and 4-warp CTAs above: 7B over FP8 with q_len 4 (1024 units of 4 rows) and
+# 96 GQA sequences (768 units) take the 4-warp form.
+FULL = [("llama7b_mha_fp8", {}), ("gqa_fp8", {}),
+        ("llama7b_mha_fp8", {"q_len": 4, "pool_blocks": None}),
+        ("gqa_fp8", {"num_seqs": 96, "pool_blocks": None})]
+
+
+@pytest.mark.parametrize("name,over", FULL, ids=["7b", "gqa", "7b-q4", "gqa-96"])
+def test_fp8_full_size_sampled_rows(pa, orc, name, over):
+    w = workloads.make(name, **over)
     out, d = gpu_step(pa, w)
     n_rows = w.cfg.num_seqs * w.cfg.q_len * w.cfg.num_q_heads
     rows = np.sort(np.random.default_rng(2).choice(n_rows, size=48, replace=False))
     ref, kc, vc = oracle_step(orc, w, rows=rows)
-    _tol.check(_f64(out).reshape(n_rows, -1)[rows], ref, w.cfg.dtype, name)
+    _tol.check(_f64(out).reshape(n_rows, -1)[rows], ref, w.cfg.dtype, f"{name} {over}")
     assert np.array_equal(d["k_cache"].cpu().numpy(), kc)
     assert np.array_equal(d["v_cache"].cpu().numpy(), vc)
 
