@@ -13,8 +13,8 @@ constexpr int kMaxDevices = 64;
 
 // Pipeline shape: warps per CTA, stages per warp (measured on GB300).  The single
 // pass uses 4 warps of 2 stages, which fits 3 CTAs per SM (12 warps) and helps the
-// skewed-length workloads; the FP8 swapped-operand path may use 3 warps instead
-// (launch_paths8).  The split-KV partial pass gets the caller's
+// skewed-length workloads; the swapped-operand paths may use 3 warps instead
+// (launch_swapped).  The split-KV partial pass gets the caller's
 // equal-size partitions; with 3 stages (2 CTAs per SM) its CTAs are deeper and
 // fewer, which measured faster there.
 constexpr int kWarps = 4;
@@ -103,12 +103,31 @@ static cudaError_t launch_one(const CUtensorMap &kmap, const CUtensorMap &vmap,
   return cudaLaunchKernelEx(&cfg, kern, kmap, vmap, a);
 }
 
+// Single pass of a swapped-operand path (3..8 rows per KV head), head_dim 128.
+// Measured over batch sizes (GQA and MHA shapes, 16-bit and FP8 caches): while the
+// units fit in one wave of 3-warp CTAs (4 per SM), those beat 4-warp CTAs (3 per
+// SM) by 5-20 %, with clusters growing up to 1.5 waves.  Above that, 4-warp CTAs;
+// their clusters grow up to 1.5 waves over an FP8 cache and up to 2 waves over a
+// 16-bit one.
+template <typename T, class Path, bool KV8>
+static cudaError_t launch_swapped(const CUtensorMap &kmap, const CUtensorMap &vmap,
+                                  const DecodeArgs &a, int units, cudaStream_t st) {
+  long long slots3 = 0;
+  const cudaError_t e = resident_slots<T, 128, Path, false, KV8, 3>(slots3);
+  if (e != cudaSuccess) return e;
+  if (units < slots3) return launch_one<T, 128, Path, false, KV8, 3>(kmap, vmap, a, units, 1, st, 3, 2);
+  return launch_one<T, 128, Path, false, KV8>(kmap, vmap, a, units, 1, st, KV8 ? 3 : 2, KV8 ? 2 : 1);
+}
+
 template <typename T, int D, bool PARTIAL>
 static cudaError_t launch_paths(const CUtensorMap &kmap, const CUtensorMap &vmap,
                                 const DecodeArgs &a, int units, cudaStream_t st) {
   if (a.rows == 1) return launch_one<T, D, FmaPath<T, D, 4, 1>, PARTIAL>(kmap, vmap, a, units, 1, st);
   if (a.rows == 2) return launch_one<T, D, FmaPath<T, D, 8, 2>, PARTIAL>(kmap, vmap, a, units, 1, st);
-  if (a.rows <= 8) return launch_one<T, D, MmaTPath<T, D>, PARTIAL>(kmap, vmap, a, units, 1, st);
+  if (a.rows <= 8) {
+    if constexpr (!PARTIAL && D == 128) return launch_swapped<T, MmaTPath<T, D>, false>(kmap, vmap, a, units, st);
+    return launch_one<T, D, MmaTPath<T, D>, PARTIAL>(kmap, vmap, a, units, 1, st);
+  }
   const int groups = (a.rows + 15) / 16;
   return launch_one<T, D, MmaPath<T, D>, PARTIAL>(kmap, vmap, a, units, groups, st);
 }
@@ -119,17 +138,7 @@ static cudaError_t launch_paths8(const CUtensorMap &kmap, const CUtensorMap &vma
   if (a.rows == 1) return launch_one<T, 128, Fma8Path<T, 1>, PARTIAL, true>(kmap, vmap, a, units, 1, st);
   if (a.rows == 2) return launch_one<T, 128, Fma8Path<T, 2>, PARTIAL, true>(kmap, vmap, a, units, 1, st);
   if (a.rows <= 8) {
-    // Single pass, measured over batch sizes (GQA and MHA shapes over FP8): when the
-    // units fit in one wave of 3-warp CTAs (4 per SM), those beat 4-warp CTAs (3 per
-    // SM) by 5-20 %; either way clusters stop growing at 1.5 waves.
-    if constexpr (!PARTIAL) {
-      long long slots3 = 0;
-      const cudaError_t e = resident_slots<T, 128, Mma8TPath<T>, false, true, 3>(slots3);
-      if (e != cudaSuccess) return e;
-      if (units < slots3)
-        return launch_one<T, 128, Mma8TPath<T>, PARTIAL, true, 3>(kmap, vmap, a, units, 1, st, 3, 2);
-      return launch_one<T, 128, Mma8TPath<T>, PARTIAL, true>(kmap, vmap, a, units, 1, st, 3, 2);
-    }
+    if constexpr (!PARTIAL) return launch_swapped<T, Mma8TPath<T>, true>(kmap, vmap, a, units, st);
     return launch_one<T, 128, Mma8TPath<T>, PARTIAL, true>(kmap, vmap, a, units, 1, st);
   }
   const int groups = (a.rows + 15) / 16;

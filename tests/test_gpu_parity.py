@@ -84,21 +84,26 @@ def test_small_configs_every_element(pa, orc, name, over, fused):
     _tol.check(_f64(out), ref, w.cfg.dtype, name)
 
 
-FULL = ["llama7b_mha", "gqa", "long_split", "prefix_verify"]
+# gqa-96: 768 units of 4 rows, more than one wave of 3-warp CTAs, so the
+# swapped-operand path launches its 4-warp form (the 64-sequence gqa takes the
+# 3-warp form).
+FULL = [("llama7b_mha", {}), ("gqa", {}), ("long_split", {}), ("prefix_verify", {}),
+        ("gqa", {"num_seqs": 96, "pool_blocks": None})]
 
 
 @pytest.mark.parametrize("fused", [False, True], ids=["separate", "fused"])
-@pytest.mark.parametrize("name", FULL)
-def test_full_size_sampled_rows(pa, orc, name, fused):
+@pytest.mark.parametrize("name,over", FULL, ids=["llama7b_mha", "gqa", "long_split",
+                                                 "prefix_verify", "gqa-96"])
+def test_full_size_sampled_rows(pa, orc, name, over, fused):
     """Full-size workloads in the launch configuration bench.py times (fused)."""
-    w = workloads.make(name)
+    w = workloads.make(name, **over)
     out, d = gpu_step(pa, w, fused=fused)
     n_rows = w.cfg.num_seqs * w.cfg.q_len * w.cfg.num_q_heads
     rng = np.random.default_rng(1)
     rows = np.sort(rng.choice(n_rows, size=min(n_rows, 48), replace=False))
     ref, kc, vc, slots = oracle_step(orc, w, rows=rows)
     got = _f64(out).reshape(n_rows, -1)[rows]
-    _tol.check(got, ref, w.cfg.dtype, name)
+    _tol.check(got, ref, w.cfg.dtype, f"{name} {over}")
     # slot mapping and the appended rows, bit for bit
     gslots = pa.pa_slot_mapping(d["block_tables"], d["context_lens"], 16, w.cfg.q_len)
     assert np.array_equal(gslots.cpu().numpy(), slots)
