@@ -162,10 +162,9 @@ struct FmaPath {
     return part * CH + (kRotate ? ((jj + rot) % CH) : jj);
   }
 
-  static constexpr int kExtraBytes = 0;  // per-warp shared scratch beyond the stages
 
   __device__ __forceinline__ void init(const DecodeArgs &a, int seq, int kvh, int row0, int L,
-                                       float sscale, uint32_t) {
+                                       float sscale) {
     const int lane = threadIdx.x & 31;
     part = lane % K;
     tip = lane / K;
@@ -329,7 +328,6 @@ struct MmaPath {
   float rs[2];         // base-2 score scale of each of this lane's two rows
   int lim[2];
 
-  static constexpr int kExtraBytes = 0;
 
   // Row bookkeeping; returns this lane's two q rows (nullptr for padding rows).
   template <typename TQ>
@@ -354,7 +352,7 @@ struct MmaPath {
   }
 
   __device__ __forceinline__ void init(const DecodeArgs &a, int seq, int kvh, int row0, int L,
-                                       float sscale, uint32_t) {
+                                       float sscale) {
     const int c2 = (threadIdx.x & 3) * 2;
     const T *qrow[2];
     init_rows<T>(a, seq, kvh, row0, L, sscale, qrow);
@@ -531,7 +529,6 @@ struct MmaTPath {
   static constexpr int RPC = 8;
   static constexpr int KS = D / 16;  // k-steps of S (16 dims each)
   static constexpr int MT = D / 16;  // m-tiles of O^T (16 dims each)
-  static constexpr int kExtraBytes = 0;
 
   uint32_t qb[KS][2];  // B fragments of q^T: row g, dims ks*16 + 2c (+1) and + 8 (+9)
   float o[MT][4];      // O^T: dims mt*16 + g (+8), rows 2c, 2c+1
@@ -558,7 +555,7 @@ struct MmaTPath {
   }
 
   __device__ __forceinline__ void init(const DecodeArgs &a, int seq, int kvh, int row0, int L,
-                                       float sscale, uint32_t) {
+                                       float sscale) {
     const int lane = threadIdx.x & 31;
     const int g = lane >> 2, c = lane & 3;
     const T *qb_ptr = static_cast<const T *>(a.q);
@@ -744,13 +741,12 @@ template <typename T>
 struct Mma8TPath {
   static constexpr int D = 128;
   static constexpr int RPC = 8;
-  static constexpr int kExtraBytes = 0;
   using Inner = MmaTPath<__half, D>;
   static constexpr int KS = Inner::KS;
   Inner inner;  // inner.o[b][i]: O^T dim 16g + 2b + (i >> 1), row 2c + (i & 1)
 
   __device__ __forceinline__ void init(const DecodeArgs &a, int seq, int kvh, int row0, int L,
-                                       float sscale, uint32_t) {
+                                       float sscale) {
     const int lane = threadIdx.x & 31;
     const int g = lane >> 2, c = lane & 3;
     inner.init_rows(a, kvh, row0, L, sscale);
@@ -867,7 +863,6 @@ struct Fma8Path {
   static constexpr int TPP = 32 / K;                 // tokens per pass
   static constexpr int PASSES = kTileTokens / TPP;
   static constexpr int CH = D / 16 / K;              // 16-code chunks per lane per token
-  static constexpr int kExtraBytes = 0;
   // Under the 128-byte swizzle the 8 lanes of a shared-memory phase (2 tokens x 4
   // parts) already land on 8 distinct bank groups: no rotation needed.
 
@@ -880,7 +875,7 @@ struct Fma8Path {
   __device__ __forceinline__ int chunk(int jj) const { return part * CH + jj; }
 
   __device__ __forceinline__ void init(const DecodeArgs &a, int seq, int kvh, int row0, int L,
-                                       float sscale, uint32_t) {
+                                       float sscale) {
     const int lane = threadIdx.x & 31;
     part = lane % K;
     tip = lane / K;
@@ -1041,13 +1036,12 @@ template <typename T>
 struct Mma8Path {
   static constexpr int D = 128;
   static constexpr int RPC = 16;
-  static constexpr int kExtraBytes = 0;
   using Inner = MmaPath<__half, D>;
   static constexpr int KS = Inner::KS;
   Inner inner;
 
   __device__ __forceinline__ void init(const DecodeArgs &a, int seq, int kvh, int row0, int L,
-                                       float sscale, uint32_t) {
+                                       float sscale) {
     const int c = threadIdx.x & 3;
     const T *qrow[2];
     inner.template init_rows<T>(a, seq, kvh, row0, L, sscale, qrow);
@@ -1175,7 +1169,7 @@ __global__ void __launch_bounds__(NW * 32)
   constexpr int kStride = D + 8;  // merge-area row stride (floats): padded against bank conflicts
   static_assert(!KV8 || D == 128, "FP8 cache: head_dim 128");
   static_assert((NW + 1) * RPC * (kStride + 2) * 4 + 64 <=
-                    NW * NSTAGE * kStageBytes + NW * Path::kExtraBytes,
+                    NW * NSTAGE * kStageBytes,
                 "merge area");
 
   extern __shared__ uint8_t smem_raw[];
@@ -1337,8 +1331,7 @@ __global__ void __launch_bounds__(NW * 32)
   // the first block-table window and the q rows load concurrently
   if (n_my > 0) tbl = (lane < n_my) ? __ldg(table + tile_of(lane)) : 0;
   Path path;
-  path.init(a, seq, kvh, row0, L, sscale,
-            smem_base + NW * NSTAGE * kStageBytes + warp * Path::kExtraBytes);
+  path.init(a, seq, kvh, row0, L, sscale);
 
   const int prologue = min(NSTAGE, n_my);
   for (int n = 0; n < prologue; ++n) issue(n);

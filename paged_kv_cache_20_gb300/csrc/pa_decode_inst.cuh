@@ -13,8 +13,8 @@ constexpr int kMaxDevices = 64;
 
 // Pipeline shape: warps per CTA, stages per warp (measured on GB300).  The single
 // pass uses 4 warps of 2 stages, which fits 3 CTAs per SM (12 warps) and helps the
-// skewed-length workloads; the swapped-operand paths may use 3 warps instead
-// (launch_swapped).  The split-KV partial pass gets the caller's
+// skewed-length workloads; the tensor-core paths may use 3 warps instead
+// (launch_few_units).  The split-KV partial pass gets the caller's
 // equal-size partitions; with 3 stages (2 CTAs per SM) its CTAs are deeper and
 // fewer, which measured faster there.
 constexpr int kWarps = 4;
@@ -39,7 +39,7 @@ template <typename T, int D, class Path, bool PARTIAL, bool KV8, int NW>
 static cudaError_t resident_slots(long long &slots) {
   constexpr int kStages = stages_of<Path, PARTIAL, KV8>();
   constexpr int kStageBytes = 2 * kTileTokens * D * (KV8 ? 1 : 2);
-  constexpr int kSmem = NW * (kStages * kStageBytes + Path::kExtraBytes) + 1024;
+  constexpr int kSmem = NW * kStages * kStageBytes + 1024;
   auto kern = paged_decode_kernel<T, D, NW, kStages, Path, PARTIAL, KV8>;
   static DeviceFit fit[kMaxDevices];
   int dev = 0;
@@ -72,7 +72,7 @@ static cudaError_t launch_one(const CUtensorMap &kmap, const CUtensorMap &vmap,
                               int wave_num = 2, int wave_den = 1) {
   constexpr int kStages = stages_of<Path, PARTIAL, KV8>();
   constexpr int kStageBytes = 2 * kTileTokens * D * (KV8 ? 1 : 2);
-  constexpr int kSmem = NW * (kStages * kStageBytes + Path::kExtraBytes) + 1024;
+  constexpr int kSmem = NW * kStages * kStageBytes + 1024;
   auto kern = paged_decode_kernel<T, D, NW, kStages, Path, PARTIAL, KV8>;
   long long slots = 0;
   cudaError_t e = resident_slots<T, D, Path, PARTIAL, KV8, NW>(slots);
@@ -103,20 +103,20 @@ static cudaError_t launch_one(const CUtensorMap &kmap, const CUtensorMap &vmap,
   return cudaLaunchKernelEx(&cfg, kern, kmap, vmap, a);
 }
 
-// Single pass of a swapped-operand path (3..8 rows per KV head), head_dim 128.
-// Measured over batch sizes (GQA and MHA shapes, 16-bit and FP8 caches): while the
+// Single pass of a tensor-core path with one row group, head_dim 128.  Measured
+// over batch sizes (GQA, MHA and verify shapes, 16-bit and FP8 caches): while the
 // units fit in one wave of 3-warp CTAs (4 per SM), those beat 4-warp CTAs (3 per
-// SM) by 5-20 %, with clusters growing up to 1.5 waves.  Above that, 4-warp CTAs;
-// their clusters grow up to 1.5 waves over an FP8 cache and up to 2 waves over a
-// 16-bit one.
-template <typename T, class Path, bool KV8>
-static cudaError_t launch_swapped(const CUtensorMap &kmap, const CUtensorMap &vmap,
-                                  const DecodeArgs &a, int units, cudaStream_t st) {
+// SM) by 4-20 %, with clusters growing up to 1.5 waves.  Above that, 4-warp CTAs
+// with the caller's cluster threshold: 1.5 waves on the FP8 swapped-operand path,
+// 2 elsewhere.
+template <typename T, class Path, bool KV8, int WAVE4_NUM, int WAVE4_DEN>
+static cudaError_t launch_few_units(const CUtensorMap &kmap, const CUtensorMap &vmap,
+                                    const DecodeArgs &a, int units, cudaStream_t st) {
   long long slots3 = 0;
   const cudaError_t e = resident_slots<T, 128, Path, false, KV8, 3>(slots3);
   if (e != cudaSuccess) return e;
   if (units < slots3) return launch_one<T, 128, Path, false, KV8, 3>(kmap, vmap, a, units, 1, st, 3, 2);
-  return launch_one<T, 128, Path, false, KV8>(kmap, vmap, a, units, 1, st, KV8 ? 3 : 2, KV8 ? 2 : 1);
+  return launch_one<T, 128, Path, false, KV8>(kmap, vmap, a, units, 1, st, WAVE4_NUM, WAVE4_DEN);
 }
 
 template <typename T, int D, bool PARTIAL>
@@ -125,10 +125,13 @@ static cudaError_t launch_paths(const CUtensorMap &kmap, const CUtensorMap &vmap
   if (a.rows == 1) return launch_one<T, D, FmaPath<T, D, 4, 1>, PARTIAL>(kmap, vmap, a, units, 1, st);
   if (a.rows == 2) return launch_one<T, D, FmaPath<T, D, 8, 2>, PARTIAL>(kmap, vmap, a, units, 1, st);
   if (a.rows <= 8) {
-    if constexpr (!PARTIAL && D == 128) return launch_swapped<T, MmaTPath<T, D>, false>(kmap, vmap, a, units, st);
+    if constexpr (!PARTIAL && D == 128)
+      return launch_few_units<T, MmaTPath<T, D>, false, 2, 1>(kmap, vmap, a, units, st);
     return launch_one<T, D, MmaTPath<T, D>, PARTIAL>(kmap, vmap, a, units, 1, st);
   }
   const int groups = (a.rows + 15) / 16;
+  if constexpr (!PARTIAL && D == 128)
+    if (groups == 1) return launch_few_units<T, MmaPath<T, D>, false, 2, 1>(kmap, vmap, a, units, st);
   return launch_one<T, D, MmaPath<T, D>, PARTIAL>(kmap, vmap, a, units, groups, st);
 }
 
@@ -138,10 +141,12 @@ static cudaError_t launch_paths8(const CUtensorMap &kmap, const CUtensorMap &vma
   if (a.rows == 1) return launch_one<T, 128, Fma8Path<T, 1>, PARTIAL, true>(kmap, vmap, a, units, 1, st);
   if (a.rows == 2) return launch_one<T, 128, Fma8Path<T, 2>, PARTIAL, true>(kmap, vmap, a, units, 1, st);
   if (a.rows <= 8) {
-    if constexpr (!PARTIAL) return launch_swapped<T, Mma8TPath<T>, true>(kmap, vmap, a, units, st);
+    if constexpr (!PARTIAL) return launch_few_units<T, Mma8TPath<T>, true, 3, 2>(kmap, vmap, a, units, st);
     return launch_one<T, 128, Mma8TPath<T>, PARTIAL, true>(kmap, vmap, a, units, 1, st);
   }
   const int groups = (a.rows + 15) / 16;
+  if constexpr (!PARTIAL)
+    if (groups == 1) return launch_few_units<T, Mma8Path<T>, true, 2, 1>(kmap, vmap, a, units, st);
   return launch_one<T, 128, Mma8Path<T>, PARTIAL, true>(kmap, vmap, a, units, groups, st);
 }
 
