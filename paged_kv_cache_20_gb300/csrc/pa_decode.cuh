@@ -1168,6 +1168,7 @@ __global__ void __launch_bounds__(NW * 32)
   constexpr int RPC = Path::RPC;
   constexpr int kStride = D + 8;  // merge-area row stride (floats): padded against bank conflicts
   static_assert(!KV8 || D == 128, "FP8 cache: head_dim 128");
+  static_assert(kStride % 4 == 0, "merge rows stay 16-byte aligned");
   static_assert((NW + 1) * RPC * (kStride + 2) * 4 + 64 <=
                     NW * NSTAGE * kStageBytes,
                 "merge area");
@@ -1382,9 +1383,10 @@ __global__ void __launch_bounds__(NW * 32)
 
   // merge area: per warp m[RPC], l[RPC], acc[RPC][kStride]; then the CTA's merged
   // state cm[RPC], cl[RPC], cacc[RPC][kStride] (read by the cluster peers)
+  constexpr int kMl = (NW * RPC + 3) & ~3;  // m and l blocks padded to 16 bytes
   float *mrg_m = reinterpret_cast<float *>(smem_gen);
-  float *mrg_l = mrg_m + NW * RPC;
-  float *mrg_acc = mrg_l + NW * RPC;  // 16-byte aligned: NW*RPC*8 bytes before (NW even)
+  float *mrg_l = mrg_m + kMl;
+  float *mrg_acc = mrg_l + kMl;  // 16-byte aligned for its float4 accesses
   float *cta_acc = mrg_acc + NW * RPC * kStride;
   float *cta_m = cta_acc + RPC * kStride;
   float *cta_l = cta_m + RPC;

@@ -13,7 +13,7 @@ constexpr int kMaxDevices = 64;
 
 // Pipeline shape: warps per CTA, stages per warp (measured on GB300).  The single
 // pass uses 4 warps of 2 stages, which fits 3 CTAs per SM (12 warps) and helps the
-// skewed-length workloads; the tensor-core paths may use 3 warps instead
+// skewed-length workloads; with few units the single pass uses 3 warps instead
 // (launch_few_units).  The split-KV partial pass gets the caller's
 // equal-size partitions; with 3 stages (2 CTAs per SM) its CTAs are deeper and
 // fewer, which measured faster there.
@@ -103,12 +103,13 @@ static cudaError_t launch_one(const CUtensorMap &kmap, const CUtensorMap &vmap,
   return cudaLaunchKernelEx(&cfg, kern, kmap, vmap, a);
 }
 
-// Single pass of a tensor-core path with one row group, head_dim 128.  Measured
-// over batch sizes (GQA, MHA and verify shapes, 16-bit and FP8 caches): while the
-// units fit in one wave of 3-warp CTAs (4 per SM), those beat 4-warp CTAs (3 per
-// SM) by 4-20 %, with clusters growing up to 1.5 waves.  Above that, 4-warp CTAs
-// with the caller's cluster threshold: 1.5 waves on the FP8 swapped-operand path,
-// 2 elsewhere.
+// Single pass with one row group, head_dim 128.  Measured over batch sizes (MHA,
+// GQA and verify shapes, every path, 16-bit and FP8 caches): while the units fit
+// in one wave of 3-warp CTAs (4 per SM where registers allow), those beat 4-warp
+// CTAs (3 per SM) by 4-23 %, with clusters growing up to 1.5 waves; a CTA's fixed
+// start and end-of-unit merge then overlap a fourth CTA's loads.  Above that,
+// 4-warp CTAs with the caller's cluster threshold: 1.5 waves on the FP8
+// swapped-operand path, 2 elsewhere.
 template <typename T, class Path, bool KV8, int WAVE4_NUM, int WAVE4_DEN>
 static cudaError_t launch_few_units(const CUtensorMap &kmap, const CUtensorMap &vmap,
                                     const DecodeArgs &a, int units, cudaStream_t st) {
@@ -122,6 +123,10 @@ static cudaError_t launch_few_units(const CUtensorMap &kmap, const CUtensorMap &
 template <typename T, int D, bool PARTIAL>
 static cudaError_t launch_paths(const CUtensorMap &kmap, const CUtensorMap &vmap,
                                 const DecodeArgs &a, int units, cudaStream_t st) {
+  if constexpr (!PARTIAL && D == 128) {
+    if (a.rows == 1) return launch_few_units<T, FmaPath<T, D, 4, 1>, false, 2, 1>(kmap, vmap, a, units, st);
+    if (a.rows == 2) return launch_few_units<T, FmaPath<T, D, 8, 2>, false, 2, 1>(kmap, vmap, a, units, st);
+  }
   if (a.rows == 1) return launch_one<T, D, FmaPath<T, D, 4, 1>, PARTIAL>(kmap, vmap, a, units, 1, st);
   if (a.rows == 2) return launch_one<T, D, FmaPath<T, D, 8, 2>, PARTIAL>(kmap, vmap, a, units, 1, st);
   if (a.rows <= 8) {
@@ -138,6 +143,10 @@ static cudaError_t launch_paths(const CUtensorMap &kmap, const CUtensorMap &vmap
 template <typename T, bool PARTIAL>
 static cudaError_t launch_paths8(const CUtensorMap &kmap, const CUtensorMap &vmap,
                                  const DecodeArgs &a, int units, cudaStream_t st) {
+  if constexpr (!PARTIAL) {
+    if (a.rows == 1) return launch_few_units<T, Fma8Path<T, 1>, true, 2, 1>(kmap, vmap, a, units, st);
+    if (a.rows == 2) return launch_few_units<T, Fma8Path<T, 2>, true, 2, 1>(kmap, vmap, a, units, st);
+  }
   if (a.rows == 1) return launch_one<T, 128, Fma8Path<T, 1>, PARTIAL, true>(kmap, vmap, a, units, 1, st);
   if (a.rows == 2) return launch_one<T, 128, Fma8Path<T, 2>, PARTIAL, true>(kmap, vmap, a, units, 1, st);
   if (a.rows <= 8) {
