@@ -162,12 +162,39 @@ def traffic_record(kernel_name: str, config: str):
     return None
 
 
+def code_tokens(text: str) -> str:
+    """C/C++/CUDA source with its comments removed and whitespace runs collapsed
+    (string and character literals kept as written): what the compiler sees, so
+    that a change of wording in a comment does not void a measurement."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c in "\"'":                                  # literal: copy through its close
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
 def kernel_source_sha(kernel: str = "decode") -> str:
+    """Hash of the code (comments and layout aside) a timed kernel is built from."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "paged_kv_cache_20_gb300", "csrc")
     for name in sorted(KERNEL_SOURCES[kernel]):
-        with open(os.path.join(csrc, name), "rb") as f:
-            h.update(name.encode() + f.read())
+        with open(os.path.join(csrc, name), encoding="utf-8") as f:
+            h.update(name.encode() + code_tokens(f.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -31,10 +31,19 @@
 //     hold head_dim/K dimensions of q in registers; partial dot products are
 //     summed with a K-lane butterfly.  Lanes that hold different tokens keep
 //     separate softmax states, so no warp-wide reduction is needed per block.
-//   * Rows per unit 3..16: warp-level tensor cores (mma.sync m16n8k16, fp32
-//     accumulate).  S = Q K^T with Q (16 rows, padded) as the A operand from
+//   * Rows per unit 3..8: warp-level tensor cores (mma.sync m16n8k16, fp32
+//     accumulate) with the operands swapped: the 16 tokens of a tile are the M
+//     dimension and the rows N = 8, S^T = K q^T and O^T += V^T P^T, P^T's B
+//     fragments by movmatrix.trans from S^T's accumulator.
+//   * Rows per unit 9..16: S = Q K^T with Q (16 rows, padded) as the A operand from
 //     registers and K^T from ldmatrix; P = 2^(S - m) re-packed in registers as the
 //     A operand of O += P V, V^T fragments from ldmatrix.trans.
+//   * FP8 (e4m3) cache: the same three layouts over fp16 arithmetic, the codes
+//     widened in registers (K and V fragments straight from 16-byte shared loads
+//     and byte permutes), the per-KV-head scales folded into q and the output.
+//   * Few units (at most one wave of 3-warp CTAs): 3-warp CTAs, 4 per SM; units
+//     that fill under about two waves are shared by a 2/4/8-CTA cluster that merges
+//     through distributed shared memory.
 //   * Slots past the context (and NaN-poisoned padding) never reach the
 //     arithmetic: scores are replaced by -inf with a select and V rows past the
 //     context are zeroed in shared memory before P.V (0 * NaN would be NaN).

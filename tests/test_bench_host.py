@@ -94,9 +94,20 @@ def test_traffic_record_void_once_a_source_changes(tmp_path, monkeypatch):
     assert bench.traffic_record("paged_decode_kernel(append+attention)", "gqa") == 123.0
     assert bench.traffic_record("paged_decode_kernel(append+attention)", "llama7b_mha") is None
     p = root / "paged_kv_cache_20_gb300" / "csrc" / "pa_decode_inst.cuh"
-    p.write_text(p.read_text() + "\n// changed\n")
+    text = p.read_text()
+    # comments and layout do not change what was measured
+    p.write_text("/* reworded */\n" + text.replace("\n", "\n  ") + "\n// a note\n")
+    assert bench.kernel_source_sha("decode") == sha
+    # code does
+    p.write_text(text + "\nstatic const int kChanged = 1;\n")
     assert bench.kernel_source_sha("decode") != sha
     assert bench.traffic_record("paged_decode_kernel(append+attention)", "gqa") is None
+
+
+def test_code_tokens_keep_literals_and_drop_comments():
+    src = 'int a = 1; // one\n/* two\nlines */ const char *s = "x // y /* z */"; char c = \'"\';'
+    assert bench.code_tokens(src) == 'int a = 1; const char *s = "x // y /* z */"; char c = \'"\';'
+    assert bench.code_tokens('s = "q \\" // in"; // out\nt') == 's = "q \\" // in"; t'
 
 
 def test_workload_recipes_as_documented():
