@@ -1,0 +1,198 @@
+"""Shared-memory and fragment layouts of the decode kernels, checked on the CPU.
+
+TMA writes every K/V tile with the 128-byte swizzle: 16-byte chunk c of row t of a
+128-byte-wide sub-tile sits at chunk position c ^ (t % 8).  A warp's 16-byte
+shared load is served in 4 phases of 8 lanes and is conflict-free when the 8 lanes
+of a phase hit 8 distinct 16-byte bank groups; an ldmatrix reads each 8-row
+matrix in one phase.  Each load pattern below restates the index arithmetic of one
+path.  The FP8 paths' register-widened fragments are emulated lane by lane on the
+operand layouts of mma.sync m16n8k16 and compared with the dense products.
+"""
+import numpy as np
+import pytest
+
+
+def sw128(rows: int, row: int, chunk: int) -> int:
+    """Byte offset of 16-byte chunk `chunk` of token row `row` in a 16-bit tile of
+    `rows` rows: 128-column heads are two 64-column sub-tiles."""
+    return (chunk >> 3) * (rows * 128) + row * 128 + (((chunk & 7) ^ (row & 7)) << 4)
+
+
+def sw128_row128(row: int, chunk: int) -> int:
+    """The same for an FP8 tile: one 128-byte row per token."""
+    return row * 128 + ((chunk ^ (row & 7)) << 4)
+
+
+def conflict_free(addr_of_lane) -> bool:
+    for ph in range(4):
+        groups = {(addr_of_lane(l) >> 4) & 7 for l in range(8 * ph, 8 * ph + 8)}
+        if len(groups) != 8:
+            return False
+    return True
+
+
+@pytest.mark.parametrize("D,K", [(128, 4), (128, 8), (64, 4), (64, 8)])
+def test_cuda_core_path_loads(D, K):
+    # K lanes share a token, each holding CH chunks; D = 128 rotates a lane's chunk
+    # loop by (lane >> shift) % CH
+    CH, TPP = D // 8 // K, 32 // K
+    rotate, shift = (D == 128 and K in (4, 8)), (2 if K == 8 else 0)
+    for p in range(16 // TPP):
+        for jj in range(CH):
+            def addr(l):
+                part, tip = l % K, l // K
+                rot = (l >> shift) % CH
+                chunk = part * CH + (((jj + rot) % CH) if rotate else jj)
+                return sw128(16, p * TPP + tip, chunk)
+            assert conflict_free(addr), (D, K, p, jj)
+
+
+def test_cuda_core_path_needs_its_rotation():
+    # without the rotation, D = 128 with 4 lanes per token would conflict
+    D, K = 128, 4
+    CH = D // 8 // K
+    assert not all(conflict_free(lambda l, jj=jj: sw128(16, l // K, (l % K) * CH + jj))
+                   for jj in range(CH))
+
+
+def test_fp8_cuda_core_path_loads():
+    K, CH, TPP = 4, 2, 8
+    for p in range(2):
+        for jj in range(CH):
+            assert conflict_free(lambda l: sw128_row128(p * TPP + l // K, (l % K) * CH + jj))
+
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_tensor_core_ldmatrix_rows(D):
+    # swapped-operand path: matrix mi of an ldmatrix.x4 takes rows (tokens)
+    # ri + 8 (mi & 1) of chunk 2 ks + (mi >> 1) (K) or tokens ri + 8 (mi >> 1) of
+    # chunk 2 mt + (mi & 1) (V, transposed); each matrix is one phase
+    for ks in range(D // 16):
+        k_rows = lambda l: sw128(16, (l & 7) + (((l >> 3) & 1) << 3), 2 * ks + (l >> 4))
+        v_rows = lambda l: sw128(16, (l & 7) + ((l >> 4) << 3), 2 * ks + ((l >> 3) & 1))
+        assert conflict_free(k_rows) and conflict_free(v_rows)
+
+
+def test_fp8_tensor_core_path_loads():
+    g = lambda l: l >> 2
+    c = lambda l: l & 3
+    for h in range(2):       # K: tokens g and g + 8, chunks 2c and 2c + 1
+        for t8 in (0, 8):
+            assert conflict_free(lambda l: sw128_row128(g(l) + t8, 2 * c(l) + h))
+    for dt in (0, 1, 8, 9):  # V: tokens 2c, 2c + 1, 2c + 8, 2c + 9, chunk g
+        assert conflict_free(lambda l: sw128_row128(2 * c(l) + dt, g(l)))
+
+
+# ------------------------------------------------------------------ m16n8k16 emulation
+def mma(afr, bfr):
+    """D = A B from the per-lane fragments: lane (g, c) holds A[g][2c..2c+1],
+    A[g+8][2c..], A[g][2c+8..], A[g+8][2c+8..] and B[2c..2c+1][g], B[2c+8..][g]."""
+    A, B = np.full((16, 16), np.nan), np.full((16, 8), np.nan)
+    for lane in range(32):
+        g, c = lane >> 2, lane & 3
+        a, b = afr[lane], bfr[lane]
+        A[g, 2 * c:2 * c + 2], A[g + 8, 2 * c:2 * c + 2] = a[0], a[1]
+        A[g, 2 * c + 8:2 * c + 10], A[g + 8, 2 * c + 8:2 * c + 10] = a[2], a[3]
+        B[2 * c:2 * c + 2, g], B[2 * c + 8:2 * c + 10, g] = b[0], b[1]
+    assert not np.isnan(A).any() and not np.isnan(B).any()
+    return A @ B
+
+
+def accum(D):
+    """Accumulator fragment: lane (g, c) holds D[g][2c], D[g][2c+1], D[g+8][2c],
+    D[g+8][2c+1]."""
+    return [[D[l >> 2, 2 * (l & 3)], D[l >> 2, 2 * (l & 3) + 1],
+             D[(l >> 2) + 8, 2 * (l & 3)], D[(l >> 2) + 8, 2 * (l & 3) + 1]] for l in range(32)]
+
+
+def byte_perm(a, b, sel):
+    """prmt.b32 / __byte_perm: result byte i is byte sel[i] of (b:a)."""
+    src = list(a) + list(b)
+    return [src[(sel >> (4 * i)) & 0xF] for i in range(4)]
+
+
+@pytest.fixture
+def tile():
+    rng = np.random.default_rng(0)
+    return (rng.standard_normal((16, 128)), rng.standard_normal((16, 128)),
+            rng.standard_normal((8, 128)), rng.random((16, 8)), rng.standard_normal((16, 128)),
+            rng.random((16, 16)))
+
+
+def test_fp8_swapped_path_fragments(tile):
+    K, V, q, Pt, _, _ = tile   # K, V [token][dim], q [row][dim], P^T [token][row]
+    # S^T = K q^T: lane c's k slots of k-step ks are dims 32c + 4ks .. +3
+    ST = np.zeros((16, 8))
+    for ks in range(8):
+        afr, bfr = [], []
+        for lane in range(32):
+            g, c = lane >> 2, lane & 3
+            d0 = 32 * c + 4 * ks
+            w0, w8 = K[g, d0:d0 + 4], K[g + 8, d0:d0 + 4]
+            afr.append([w0[0:2], w8[0:2], w0[2:4], w8[2:4]])
+            bfr.append([q[g, d0:d0 + 2], q[g, d0 + 2:d0 + 4]])
+        ST += mma(afr, bfr)
+    np.testing.assert_allclose(ST, K @ q.T, rtol=1e-12, atol=1e-12)
+    # O^T += V^T P^T: row g of m-tile b is dim 16g + 2b, row g + 8 is dim 16g + 2b + 1
+    OT = np.zeros((128, 8))
+    for j in range(4):
+        for b, sel in ((2 * j, 0x5140), (2 * j + 1, 0x7362)):
+            afr, bfr = [], []
+            for lane in range(32):
+                g, c = lane >> 2, lane & 3
+                s = slice(16 * g + 4 * j, 16 * g + 4 * j + 4)
+                p01 = byte_perm(V[2 * c, s], V[2 * c + 1, s], sel)
+                p89 = byte_perm(V[2 * c + 8, s], V[2 * c + 9, s], sel)
+                afr.append([p01[0:2], p01[2:4], p89[0:2], p89[2:4]])
+                bfr.append([Pt[2 * c:2 * c + 2, g], Pt[2 * c + 8:2 * c + 10, g]])
+            frag = accum(mma(afr, bfr))
+            for lane in range(32):
+                g, c = lane >> 2, lane & 3
+                for e in range(2):
+                    OT[16 * g + 2 * b, 2 * c + e] += frag[lane][e]
+                    OT[16 * g + 2 * b + 1, 2 * c + e] += frag[lane][2 + e]
+    np.testing.assert_allclose(OT, V.T @ Pt, rtol=1e-12, atol=1e-12)
+
+
+def test_fp8_sixteen_row_path_fragments(tile):
+    K, V, _, _, Q, P = tile    # Q [row][dim], P [row][token]
+    for nt in range(2):        # S = Q K^T, tokens nt*8 .. nt*8 + 7 as the n-tile
+        S = np.zeros((16, 8))
+        for ks in range(8):
+            afr, bfr = [], []
+            for lane in range(32):
+                g, c = lane >> 2, lane & 3
+                d0 = 32 * c + 4 * ks
+                afr.append([Q[g, d0:d0 + 2], Q[g + 8, d0:d0 + 2],
+                            Q[g, d0 + 2:d0 + 4], Q[g + 8, d0 + 2:d0 + 4]])
+                k = K[nt * 8 + g, d0:d0 + 4]
+                bfr.append([k[0:2], k[2:4]])
+            S += mma(afr, bfr)
+        np.testing.assert_allclose(S, Q @ K[nt * 8:nt * 8 + 8].T, rtol=1e-12, atol=1e-12)
+    # O += P V: column n of n-tile nt is dim 16n + nt
+    O = np.zeros((16, 128))
+    for j in range(4):
+        for t in range(4):
+            nt, sel, h = 4 * j + t, (0x5140 if t < 2 else 0x7362), 2 * (t & 1)
+            afr, bfr = [], []
+            for lane in range(32):
+                g, c = lane >> 2, lane & 3
+                afr.append([P[g, 2 * c:2 * c + 2], P[g + 8, 2 * c:2 * c + 2],
+                            P[g, 2 * c + 8:2 * c + 10], P[g + 8, 2 * c + 8:2 * c + 10]])
+                s = slice(16 * g + 4 * j, 16 * g + 4 * j + 4)
+                p01 = byte_perm(V[2 * c, s], V[2 * c + 1, s], sel)
+                p89 = byte_perm(V[2 * c + 8, s], V[2 * c + 9, s], sel)
+                bfr.append([p01[h:h + 2], p89[h:h + 2]])
+            frag = accum(mma(afr, bfr))
+            for lane in range(32):
+                g, c = lane >> 2, lane & 3
+                for hr in range(2):
+                    O[g + 8 * hr, 32 * c + nt] += frag[lane][2 * hr]
+                    O[g + 8 * hr, 32 * c + 16 + nt] += frag[lane][2 * hr + 1]
+    np.testing.assert_allclose(O, P @ V, rtol=1e-12, atol=1e-12)
+
+
+def test_byte_perm_pairs_tokens_per_dim():
+    a, b = [10, 11, 12, 13], [20, 21, 22, 23]   # dims 0..3 of two tokens
+    assert byte_perm(a, b, 0x5140) == [10, 20, 11, 21]
+    assert byte_perm(a, b, 0x7362) == [12, 22, 13, 23]
