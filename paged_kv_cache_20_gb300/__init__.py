@@ -278,6 +278,7 @@ def pa_decode(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor, v_cache
 
 def pa_decode_workspace_size(num_seqs: int, num_q_heads: int, q_len: int, head_dim: int,
                              num_splits: int) -> int:
+    """Bytes of the split-KV workspace for these sizes (0 for invalid ones)."""
     return int(load().pa_decode_workspace_size(num_seqs, num_q_heads, q_len, head_dim, num_splits))
 
 
@@ -299,6 +300,8 @@ def pa_decode_partial(workspace: torch.Tensor, q: torch.Tensor, k_cache: torch.T
                       v_cache: torch.Tensor, block_tables: torch.Tensor,
                       context_lens: torch.Tensor, scale: float, num_splits: int,
                       q_len: int = 1, stream=None) -> torch.Tensor:
+    """Split-KV pass: each of num_splits partitions of every sequence's blocks writes
+    its (m, l, unnormalised acc) into the workspace; returns the workspace."""
     num_blocks, h_kv, block_size, head_dim, num_seqs, h_q, maxb = _decode_dims(
         q, k_cache, block_tables, context_lens, q_len)
     nbytes = workspace.numel() * workspace.element_size()
