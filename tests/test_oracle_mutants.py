@@ -57,6 +57,10 @@ MUTANTS = [
      "v = ldexp((double)(1024 + f), e - 24);"),
     ("bf16_subnormal_scale", "v = ldexp((double)f, -133);", "v = ldexp((double)f, -126);"),
     ("softmax_not_normalised", "double p = s[t] / den;", "double p = s[t];"),
+    ("slot_position_off_by_one", "int64_t pos = (int64_t)context_lens[i] - q_len + u;",
+     "int64_t pos = (int64_t)context_lens[i] - q_len + u + 1;"),
+    ("slot_negative_position_not_skipped", "if (pos < 0) {\n                out = -1;",
+     "if (pos < -block_size) {\n                out = -1;"),
     ("copy_blocks_wrong_direction",
      "k_cache[(int64_t)dst[i] * block_elems + e] = k_cache[(int64_t)src[i] * block_elems + e];",
      "k_cache[(int64_t)src[i] * block_elems + e] = k_cache[(int64_t)dst[i] * block_elems + e];"),
