@@ -40,6 +40,16 @@ def _ptr(a: np.ndarray, ctype):
     return a.ctypes.data_as(ctype)
 
 
+def _run_rows(run, n: int, threads: int) -> list:
+    """run(lo, hi) over [0, n), in slices over a thread pool when threads > 1 (the
+    C calls release the interpreter lock); returns the status codes."""
+    if threads <= 1 or n < 2:
+        return [run(0, n)]
+    bounds = np.linspace(0, n, min(n, threads * 4) + 1).astype(int)
+    with ThreadPoolExecutor(max_workers=threads) as ex:
+        return list(ex.map(lambda ab: run(*ab), zip(bounds[:-1], bounds[1:])))
+
+
 def _u16(a: np.ndarray) -> np.ndarray:
     a = np.ascontiguousarray(a)
     if a.dtype == np.uint16:
@@ -173,8 +183,10 @@ class Oracle:
                                    _ptr(vs, self._f32p))
 
     def decode_fp8(self, q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens,
-                   scale: float, dtype, q_len: int = 1, rows=None) -> np.ndarray:
-        """fp64 attention over e4m3 caches (value = code * per-KV-head scale)."""
+                   scale: float, dtype, q_len: int = 1, rows=None, threads: int = 1) -> np.ndarray:
+        """fp64 attention over e4m3 caches (value = code * per-KV-head scale).
+        ``threads`` > 1 splits the rows over a thread pool (each row is computed on
+        its own, so the result does not depend on the split)."""
         qb = _u16(q)
         kc = np.ascontiguousarray(k_cache, dtype=np.uint8)
         vc = np.ascontiguousarray(v_cache, dtype=np.uint8)
@@ -188,14 +200,20 @@ class Oracle:
         rows_arr = (np.arange(num_seqs * q_len * h_q, dtype=np.int64) if rows is None
                     else np.ascontiguousarray(rows, dtype=np.int64))
         out = np.empty((rows_arr.shape[0], head_dim), dtype=np.float64)
-        rc = self.lib.orc_decode_fp8(_ptr(out, _c_f64p), _ptr(rows_arr, _c_i64p),
-                                     rows_arr.shape[0], _ptr(qb, _c_u16p), _ptr(kc, self._u8p),
-                                     _ptr(vc, self._u8p), _ptr(ks, self._f32p),
-                                     _ptr(vs, self._f32p), _ptr(bt, _c_i32p), _ptr(cl, _c_i32p),
-                                     num_seqs, h_q, h_kv, head_dim, block_size, float(scale),
-                                     bt.shape[1], q_len, _dtype_code(dtype))
-        if rc != 0:
-            raise ValueError(f"oracle fp8 decode failed: {rc}")
+
+        def run(lo: int, hi: int) -> int:
+            sub = rows_arr[lo:hi]
+            return self.lib.orc_decode_fp8(_ptr(out[lo:hi], _c_f64p), _ptr(sub, _c_i64p), hi - lo,
+                                           _ptr(qb, _c_u16p), _ptr(kc, self._u8p),
+                                           _ptr(vc, self._u8p), _ptr(ks, self._f32p),
+                                           _ptr(vs, self._f32p), _ptr(bt, _c_i32p),
+                                           _ptr(cl, _c_i32p), num_seqs, h_q, h_kv, head_dim,
+                                           block_size, float(scale), bt.shape[1], q_len,
+                                           _dtype_code(dtype))
+
+        rcs = _run_rows(run, rows_arr.shape[0], threads)
+        if any(rc != 0 for rc in rcs):
+            raise ValueError(f"oracle fp8 decode failed: {rcs}")
         return out.reshape(qb.shape) if rows is None else out
 
     # -- copy-on-write block copy (in place) ------------------------------------
@@ -240,13 +258,7 @@ class Oracle:
                                        head_dim, block_size, float(scale), bt.shape[1], q_len,
                                        _dtype_code(dtype))
 
-        n = rows_arr.shape[0]
-        if threads <= 1 or n < 2:
-            rcs = [run(0, n)]
-        else:
-            bounds = np.linspace(0, n, min(n, threads * 4) + 1).astype(int)
-            with ThreadPoolExecutor(max_workers=threads) as ex:
-                rcs = list(ex.map(lambda ab: run(*ab), zip(bounds[:-1], bounds[1:])))
+        rcs = _run_rows(run, rows_arr.shape[0], threads)
         if any(rc != 0 for rc in rcs):
             raise ValueError(f"oracle decode failed: {rcs}")
         if rows is None:

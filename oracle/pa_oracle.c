@@ -116,27 +116,43 @@ uint8_t orc_e4m3_from_float(float x)
     return (uint8_t)(sign | best);
 }
 
-void orc_decode_e4m3(double *out, const uint8_t *bits, int64_t n)
-{
-    for (int64_t i = 0; i < n; i++)
-        out[i] = orc_e4m3_to_double(bits[i]);
-}
-
 void orc_encode_e4m3(uint8_t *out, const float *x, int64_t n)
 {
     for (int64_t i = 0; i < n; i++)
         out[i] = orc_e4m3_from_float(x[i]);
 }
 
+/* Every 16-bit and 8-bit pattern decoded once, by the functions above, when the
+ * library is loaded.  Decoding is exact, so looking a value up gives the same
+ * double as calling the decoder; it only spares the attention loops a call to
+ * ldexp per element. */
+static double fp16_value[65536], bf16_value[65536], e4m3_value[256];
+
+__attribute__((constructor)) static void fill_decode_tables(void)
+{
+    for (int b = 0; b < 65536; b++) {
+        fp16_value[b] = orc_fp16_to_double((uint16_t)b);
+        bf16_value[b] = orc_bf16_to_double((uint16_t)b);
+    }
+    for (int b = 0; b < 256; b++)
+        e4m3_value[b] = orc_e4m3_to_double((uint8_t)b);
+}
+
 static double elt(const uint16_t *base, size_t idx, int dtype)
 {
-    return dtype == ORC_BF16 ? orc_bf16_to_double(base[idx]) : orc_fp16_to_double(base[idx]);
+    return dtype == ORC_BF16 ? bf16_value[base[idx]] : fp16_value[base[idx]];
 }
 
 void orc_decode_bits(double *out, const uint16_t *bits, int64_t n, int dtype)
 {
     for (int64_t i = 0; i < n; i++)
         out[i] = elt(bits, (size_t)i, dtype);
+}
+
+void orc_decode_e4m3(double *out, const uint8_t *bits, int64_t n)
+{
+    for (int64_t i = 0; i < n; i++)
+        out[i] = e4m3_value[bits[i]];
 }
 
 /* ---- slot mapping ([PANO] §2.3 write_kv) ----
@@ -270,7 +286,7 @@ static double cache_at(const orc_call *c, const void *cache, const float *scales
                        int kvh)
 {
     if (c->kv_fp8)
-        return orc_e4m3_to_double(((const uint8_t *)cache)[idx]) * (double)scales[kvh];
+        return e4m3_value[((const uint8_t *)cache)[idx]] * (double)scales[kvh];
     return elt((const uint16_t *)cache, idx, c->dtype);
 }
 

@@ -61,6 +61,11 @@ MUTANTS = [
      "int64_t pos = (int64_t)context_lens[i] - q_len + u + 1;"),
     ("slot_negative_position_not_skipped", "if (pos < 0) {\n                out = -1;",
      "if (pos < -block_size) {\n                out = -1;"),
+    ("bf16_table_filled_by_fp16_decoder",
+     "bf16_value[b] = orc_bf16_to_double((uint16_t)b);",
+     "bf16_value[b] = orc_fp16_to_double((uint16_t)b);"),
+    ("e4m3_table_shifted_by_one", "e4m3_value[b] = orc_e4m3_to_double((uint8_t)b);",
+     "e4m3_value[b] = orc_e4m3_to_double((uint8_t)(b + 1));"),
     ("copy_blocks_wrong_direction",
      "k_cache[(int64_t)dst[i] * block_elems + e] = k_cache[(int64_t)src[i] * block_elems + e];",
      "k_cache[(int64_t)src[i] * block_elems + e] = k_cache[(int64_t)dst[i] * block_elems + e];"),
