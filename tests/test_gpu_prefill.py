@@ -3,8 +3,8 @@ CUDA library vs the fp64 oracle through the C ABI (needs a GPU).
 
 Both reach the same attention as pa_decode -- softmax(scale q K^T) V over each
 row's causal window -- so each is compared with the oracle's plain definition:
-every element at small sizes, sampled rows at full size, and the appended cache
-bit for bit.
+every element, at small sizes and at the full workload sizes, and the appended
+cache bit for bit.
 """
 import numpy as np
 import pytest
@@ -13,8 +13,8 @@ import torch
 import workloads
 from tests import _tol
 from tests.oracle_pins import Paged
-from tests.test_gpu_parity import (DEV, _dev, _f64, _gpu_decode, _logical_case, _to_dev, _u16,
-                                   gpu_step, oracle_step)
+from tests.test_gpu_parity import (DEV, THREADS, _dev, _f64, _gpu_decode, _logical_case,
+                                   _to_dev, _u16, full_oracle, gpu_step, oracle_step)
 
 pytestmark = pytest.mark.gpu
 
@@ -51,15 +51,13 @@ def test_chunked_prefill_every_element(pa, orc, name, over, fused, splits):
 
 
 @pytest.mark.parametrize("fused", [False, True], ids=["separate", "fused"])
-def test_chunked_prefill_full_size_sampled_rows(pa, orc, fused):
-    """The full chunked-prefill workload in the launch configuration bench.py times."""
+def test_chunked_prefill_full_size_every_element(pa, orc, fused):
+    """The full chunked-prefill workload in the launch configuration bench.py times,
+    every output element (the oracle runs once for both launch forms)."""
     w = workloads.make("chunked_prefill")
     out, d = gpu_step(pa, w, fused=fused)
-    n_rows = w.cfg.num_seqs * w.cfg.q_len * w.cfg.num_q_heads
-    rng = np.random.default_rng(2)
-    rows = np.sort(rng.choice(n_rows, size=64, replace=False))
-    ref, kc, vc, _ = oracle_step(orc, w, rows=rows)
-    _tol.check(_f64(out).reshape(n_rows, -1)[rows], ref, w.cfg.dtype, "chunked_prefill")
+    ref, kc, vc, _ = full_oracle(orc, ("chunked_prefill", ""), w)
+    _tol.check(_f64(out), ref, w.cfg.dtype, "chunked_prefill")
     assert np.array_equal(_u16(d["k_cache"]), kc)
     assert np.array_equal(_u16(d["v_cache"]), vc)
 
@@ -140,14 +138,12 @@ def test_cascade_every_element(pa, orc, case, fused, tail_splits):
     _tol.check(_f64(out), ref, w.cfg.dtype, f"cascade {case}")
 
 
-def test_cascade_full_size_sampled_rows(pa, orc):
+def test_cascade_full_size_every_element(pa, orc):
     """prefix_verify at full size, in the launch configuration bench.py times."""
     w = workloads.make("prefix_verify")
     out, d = gpu_cascade(pa, w)
-    n_rows = w.cfg.num_seqs * w.cfg.q_len * w.cfg.num_q_heads
-    rows = np.sort(np.random.default_rng(3).choice(n_rows, size=64, replace=False))
-    ref, kc, vc, _ = oracle_step(orc, w, rows=rows)
-    _tol.check(_f64(out).reshape(n_rows, -1)[rows], ref, w.cfg.dtype, "cascade full")
+    ref, kc, vc, _ = oracle_step(orc, w)
+    _tol.check(_f64(out), ref, w.cfg.dtype, "cascade full")
     assert np.array_equal(_u16(d["k_cache"]), kc)
     assert np.array_equal(_u16(d["v_cache"]), vc)
 
@@ -190,15 +186,12 @@ def test_prefill_partial_statistics_match_oracle_partitions(pa, orc):
     assert np.abs(lse_g - (m[ok] + np.log(l[ok]))).max() < 1e-4
 
 
-def test_prefill_longest_chunk_sampled_rows(pa, orc):
-    """q_len at the library's limit (4096): one sequence, GQA, sampled rows."""
+def test_prefill_longest_chunk_every_element(pa, orc):
+    """q_len at the library's limit (4096): one sequence, GQA, every element."""
     w = workloads.make("chunked_prefill", num_seqs=1, q_len=4096, lens=("fixed", (4400,)))
     out, d = gpu_step(pa, w, fused=True)
-    n_rows = w.cfg.q_len * w.cfg.num_q_heads
-    rows = np.sort(np.random.default_rng(4).choice(n_rows, size=48, replace=False))
-    rows = np.unique(np.concatenate([rows, [0, n_rows - 1]]))   # first and last query rows
-    ref, kc, vc, _ = oracle_step(orc, w, rows=rows)
-    _tol.check(_f64(out).reshape(n_rows, -1)[rows], ref, w.cfg.dtype, "q_len 4096")
+    ref, kc, vc, _ = oracle_step(orc, w)
+    _tol.check(_f64(out), ref, w.cfg.dtype, "q_len 4096")
     assert np.array_equal(_u16(d["k_cache"]), kc)
 
 
@@ -325,7 +318,7 @@ def test_prefill_many_units_per_cta(pa, orc, case, splits):
     q, K, V = _logical_case(32, lens, h_q, h_kv, d, dtype, q_len=q_len)
     pc = Paged(orc, K, V, 16, dtype, perm_seed=17)
     scale = float(np.float32(1.0) / np.sqrt(np.float32(d)))
-    ref = orc.decode(q, pc.k, pc.v, pc.tables, pc.lens, scale, dtype, q_len=q_len, threads=8)
+    ref = orc.decode(q, pc.k, pc.v, pc.tables, pc.lens, scale, dtype, q_len=q_len, threads=THREADS)
     _tol.check(_gpu_decode(pa, pc, q, scale, q_len, num_splits=splits), ref, dtype,
                f"{dtype} d{d} g{h_q // h_kv} q_len {q_len} split {splits}")
 
@@ -333,18 +326,16 @@ def test_prefill_many_units_per_cta(pa, orc, case, splits):
 def test_cascade_prefix_pass_many_units_per_cta(pa, orc):
     """A shared-prefix pass with more units than SMs (128 sequences x 8 query
     positions x 4 heads per KV head = 32 row blocks per KV head, 256 units), then
-    the tails: sampled rows against the oracle."""
+    the tails: every element against the oracle."""
     w = workloads.make("prefix_verify", q_len=8)
     out, d = gpu_cascade(pa, w, tail_splits=1)
-    n_rows = w.cfg.num_seqs * w.cfg.q_len * w.cfg.num_q_heads
-    rows = np.sort(np.random.default_rng(5).choice(n_rows, size=96, replace=False))
-    ref, kc, vc, _ = oracle_step(orc, w, rows=rows)
-    _tol.check(_f64(out).reshape(n_rows, -1)[rows], ref, w.cfg.dtype, "cascade, many prefix units")
+    ref, kc, vc, _ = oracle_step(orc, w)
+    _tol.check(_f64(out), ref, w.cfg.dtype, "cascade, many prefix units")
     assert np.array_equal(_u16(d["k_cache"]), kc)
     assert np.array_equal(_u16(d["v_cache"]), vc)
-    # the same rows through two tail partitions and the combine
+    # the same through two tail partitions and the combine
     out2, _ = gpu_cascade(pa, workloads.make("prefix_verify", q_len=8), tail_splits=2)
-    _tol.check(_f64(out2).reshape(n_rows, -1)[rows], ref, w.cfg.dtype, "cascade, tail split 2")
+    _tol.check(_f64(out2), ref, w.cfg.dtype, "cascade, tail split 2")
 
 
 def test_prefill_more_sequences_than_the_ranked_order_holds(pa, orc):
@@ -356,18 +347,16 @@ def test_prefill_more_sequences_than_the_ranked_order_holds(pa, orc):
     lens[8] = 5
     q, K, V = _logical_case(42, lens, 4, 2, 64, "fp16", q_len=17)
     pc = Paged(orc, K, V, 16, "fp16", perm_seed=18)
-    ref = orc.decode(q, pc.k, pc.v, pc.tables, pc.lens, 0.125, "fp16", q_len=17, threads=8)
+    ref = orc.decode(q, pc.k, pc.v, pc.tables, pc.lens, 0.125, "fp16", q_len=17, threads=THREADS)
     _tol.check(_gpu_decode(pa, pc, q, 0.125, 17), ref, "fp16", "300 sequences")
     _tol.check(_gpu_decode(pa, pc, q, 0.125, 17, num_splits=3), ref, "fp16", "300 sequences, split 3")
 
 
 def test_cascade_more_sequences_than_the_ranked_order_holds(pa, orc):
     """The shared-prefix pass over 300 sequences (context lengths from global
-    memory), then the tails: sampled rows."""
+    memory), then the tails: every element."""
     w = workloads.make("prefix_verify", num_seqs=300, q_len=2, lens=("prefix", 1024, 16, 80))
     out, d = gpu_cascade(pa, w)
-    n_rows = w.cfg.num_seqs * w.cfg.q_len * w.cfg.num_q_heads
-    rows = np.sort(np.random.default_rng(6).choice(n_rows, size=128, replace=False))
-    ref, kc, vc, _ = oracle_step(orc, w, rows=rows)
-    _tol.check(_f64(out).reshape(n_rows, -1)[rows], ref, w.cfg.dtype, "cascade, 300 sequences")
+    ref, kc, vc, _ = oracle_step(orc, w)
+    _tol.check(_f64(out), ref, w.cfg.dtype, "cascade, 300 sequences")
     assert np.array_equal(_u16(d["k_cache"]), kc)
