@@ -47,8 +47,10 @@ import workloads  # noqa: E402
 METRIC = "paged decode attention: KV tokens/s and achieved HBM GB/s (% of GB300 peak)"
 UNIT = "KV tokens/s"
 DEFAULT_CONFIG = "llama7b_mha"
-OTHER_CONFIGS = ["gqa", "long_split", "prefix_verify", "llama7b_mha_fp8", "gqa_fp8",
-                 "chunked_prefill"]
+# gqa last: the end of the printed line carries it in full even where only the
+# line's tail is kept
+OTHER_CONFIGS = ["long_split", "prefix_verify", "llama7b_mha_fp8", "gqa_fp8", "chunked_prefill",
+                 "gqa"]
 DECODE_MAX_QLEN = 16              # more query rows per sequence go to the prefill kernel
 L2_BYTES = 129 << 20             # GB300 L2; every workload's KV cache is several times larger
 NOMINAL_HBM_GBS = 8000.0
@@ -363,13 +365,24 @@ class Runner:
                 ev_pair[1].record()
 
 
-def time_device(runner: Runner, steps: int, warmup: int, world: int):
+def l2_read_through(buf: torch.Tensor) -> None:
+    """Read every byte of a buffer of at least twice the L2 (a reduction whose
+    result is discarded): the next kernel finds none of the previous step's lines
+    in L2, and no dirty lines are left for it to write back."""
+    torch.sum(buf)
+
+
+def time_device(runner: Runner, steps: int, warmup: int, world: int, evict=None):
     """Time exactly `steps` steps twice, after `warmup` untimed ones.
     - Back to back, with one event pair around all of them: the headline.
       Launches follow each other on the stream as in a serving loop.
     - With events around every step and around its attention launch: per-step
       percentiles and per-launch kernel times.  Those events sit between the
       launches, so this pass is slower.
+    - With `evict` (a buffer >= 2x L2): a third pass like the second with an
+      untimed read-through of that buffer before every step, so no step finds
+      the previous one's data in L2; its per-launch kernel times are returned
+      as a fifth value.
     Each pass is bracketed by a barrier and a device synchronisation on both
     sides."""
     for _ in range(warmup):
@@ -405,7 +418,17 @@ def time_device(runner: Runner, steps: int, warmup: int, world: int):
     barrier(world)
     step_ms = [x.elapsed_time(y) for x, y, _, _ in evs]
     kern_ms = [x.elapsed_time(y) for _, _, x, y in evs]
-    return loop_ms, step_ms, kern_ms, wall
+    if evict is None:
+        return loop_ms, step_ms, kern_ms, wall
+    ev2 = [(E(), E()) for _ in range(steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    for k0, k1 in ev2:
+        l2_read_through(evict)
+        runner.step((k0, k1))
+    torch.cuda.synchronize()
+    barrier(world)
+    return loop_ms, step_ms, kern_ms, wall, [x.elapsed_time(y) for x, y in ev2]
 
 
 def time_graph(runner: Runner, steps: int, warmup: int):
@@ -578,7 +601,9 @@ def measure_config(pa, name, seed, device, steps, warmup, world, peaks, e2e=Fals
     runner.fused = False
     sep_loop, _, sep_kern_ms, _ = time_device(runner, steps, warmup, world)
     runner.fused = True
-    loop_ms, step_ms, kern_ms, wall = time_device(runner, steps, warmup, world)
+    evict = torch.empty(2 * L2_BYTES // 4 + 1024, dtype=torch.float32, device=device).fill_(1.0)
+    loop_ms, step_ms, kern_ms, wall, ev_ms = time_device(runner, steps, warmup, world, evict)
+    del evict
     assert pa.pa_device_error() == 0, "device error during the timed run"
     ab = algorithmic_bytes(w)
     total_ms = max_over_ranks(loop_ms, world, device)
@@ -602,6 +627,9 @@ def measure_config(pa, name, seed, device, steps, warmup, world, peaks, e2e=Fals
                      "frac_of_8tbs": achieved / NOMINAL_HBM_GBS,
                      "traffic": traffic_record(kern_name, name), "kernel": kern_name,
                      "kernel_us": kern_avg * 1e3,
+                     "kernel_us_l2_evicted": statistics.mean(ev_ms) * 1e3,
+                     "frac_l2_evicted": ab["fused_launch"] / (statistics.mean(ev_ms) * 1e-3)
+                     / 1e9 / peak,
                      "bytes_per_launch": ab["fused_launch"],
                      "bytes_per_kv_token": ab["per_token"],
                      "attention_only_kernel_us": statistics.mean(sep_kern_ms) * 1e3},
@@ -657,10 +685,16 @@ def config_obj(w: workloads.Workload, path: str) -> dict:
             "kv_dtype": "e4m3 (per-KV-head scales)" if c.kv_fp8 else c.dtype,
             "q_dtype": c.dtype, "q_len": c.q_len, "num_splits": c.num_splits,
             "context_tokens": w.total_tokens, "unique_kv_tokens": w.info["unique_tokens"],
-            "pool_blocks": w.num_blocks, "path": path,
-            "l2": ("not flushed: the KV cache read each step is "
-                   f"{w.info['unique_tokens'] * 2 * c.num_kv_heads * c.head_dim * (1 if c.kv_fp8 else ELT) / 2**20:.0f} MiB,"
-                   f" larger than the {L2_BYTES >> 20} MiB L2")}
+            "pool_blocks": w.num_blocks, "path": path}
+
+
+def config_l2(w: workloads.Workload) -> str:
+    c = w.cfg
+    mib = w.info["unique_tokens"] * 2 * c.num_kv_heads * c.head_dim * (1 if c.kv_fp8 else ELT) / 2**20
+    return (f"not flushed between the back-to-back steps: the KV cache read each step is "
+            f"{mib:.0f} MiB, larger than the {L2_BYTES >> 20} MiB L2; the roofline's "
+            f"kernel_us_l2_evicted repeats the kernel timing with a read-through of "
+            f"{2 * L2_BYTES >> 20} MiB before every step")
 
 
 def run_ours(args):
@@ -683,17 +717,9 @@ def run_ours(args):
             if name == main:
                 continue
             o = measure_config(pa, name, rank, device, args.steps, args.warmup, world, peaks)
-            others[name] = {"value": o["value"], "unit": UNIT, "ms_per_step": o["ms_per_step"],
-                            "separate_launches_ms_per_step": o["separate_launches_ms_per_step"],
-                            "roofline_frac": o["roofline"]["frac"],
-                            "achieved_gbs": o["roofline"]["achieved"],
-                            "kernel_us": o["roofline"]["kernel_us"],
-                            "frac_of_8tbs": o["roofline"]["frac_of_8tbs"],
-                            "config": config_obj(o["w"], _path(o["w"]))}
-            for extra in ("cascade", "tensor_roofline"):
-                if extra in o:
-                    others[name][extra] = o[extra]
+            others[name] = other_entry(o)
             del o
+    copy = None if args.only else measure_copy_blocks(pa, device, peaks)
     cpu = cpu_baseline(r["w"]) if (rank == 0 and not args.no_cpu) else None
     if rank != 0:
         return
@@ -703,7 +729,7 @@ def run_ours(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": r["ms_per_step"],
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": f"{w.cfg.dtype} in, fp32 accumulate", "data": "synthetic",
-        "config": config_obj(w, _path(w)),
+        "config": {**config_obj(w, _path(w)), "l2": config_l2(w)},
         "roofline": r["roofline"], "cpu_baseline": cpu, "e2e": r.get("e2e"),
         "gpu_launches": args.steps * r["runner"].launches_per_step,
         "clocks": clocks, "step_p10_p50_p90_ms": r["step_ms_p10_p50_p90"],
@@ -713,13 +739,69 @@ def run_ours(args):
                    "with events around every step and launch"),
         "step_algorithmic_gbs": r["step_gbs"],
         "separate_launches_ms_per_step": r["separate_launches_ms_per_step"],
-        "other_configs": others,
         "kernel_src_sha": {k: kernel_source_sha(k) for k in KERNEL_SOURCES},
     }
     for extra in ("cascade", "tensor_roofline", "graph"):
         if extra in r:
             line[extra] = r[extra]
+    if copy is not None:
+        line["copy_blocks"] = copy
+    line["other_configs"] = others      # last, gqa last within it
     print(json.dumps(line))
+
+
+def _sig(x, digits=4):
+    """x rounded to `digits` significant digits (keeps the printed line short)."""
+    return float(f"{x:.{digits}g}") if isinstance(x, float) else x
+
+
+def other_entry(o: dict) -> dict:
+    """The compact record of one further workload in the JSON line."""
+    r, c = o["roofline"], o["w"].cfg
+    e = {"value": _sig(o["value"]), "ms_per_step": _sig(o["ms_per_step"]),
+         "separate_launches_ms_per_step": _sig(o["separate_launches_ms_per_step"]),
+         "kernel_us": _sig(r["kernel_us"]), "kernel_us_l2_evicted": _sig(r["kernel_us_l2_evicted"]),
+         "roofline_frac": _sig(r["frac"]), "frac_l2_evicted": _sig(r["frac_l2_evicted"]),
+         "frac_of_8tbs": _sig(r["frac_of_8tbs"]), "achieved_gbs": _sig(r["achieved"]),
+         "config": {"workload": c.name, "num_seqs": c.num_seqs,
+                    "kv_dtype": "e4m3" if c.kv_fp8 else c.dtype}}
+    if "cascade" in o:
+        e["cascade"] = {"ms_per_step": _sig(o["cascade"]["ms_per_step"]),
+                        "kernel_us": _sig(o["cascade"]["kernel_us"])}
+    if "tensor_roofline" in o:
+        t = o["tensor_roofline"]
+        e["tensor_roofline"] = {"achieved_tflops": _sig(t["achieved"]), "frac": _sig(t["frac"]),
+                                "peak": t["peak"]}
+    return e
+
+
+def measure_copy_blocks(pa, device, peaks, n_pairs=512, steps=20, warmup=5) -> dict:
+    """pa_copy_blocks on a pool of the 7B shape (32 KV heads, 16 x 128 fp16 per
+    block and head): n_pairs random source blocks to distinct destinations, K and
+    V.  Bytes per launch: each block read once and written once."""
+    h_kv, bs, d = 32, 16, 128
+    num_blocks = 4 * n_pairs
+    k = torch.randn(num_blocks, h_kv, bs, d, device=device, dtype=torch.float16)
+    v = torch.randn_like(k)
+    perm = torch.randperm(num_blocks, generator=torch.Generator().manual_seed(0))
+    src = perm[:n_pairs].to(torch.int32).to(device)
+    dst = perm[n_pairs:2 * n_pairs].to(torch.int32).to(device)
+    for _ in range(warmup):
+        pa.pa_copy_blocks(k, v, src, dst)
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(steps):
+        pa.pa_copy_blocks(k, v, src, dst)
+    b.record()
+    torch.cuda.synchronize()
+    assert pa.pa_device_error() == 0, "device error during the block copies"
+    us = a.elapsed_time(b) * 1e3 / steps
+    nbytes = 2 * 2 * n_pairs * h_kv * bs * d * ELT
+    gbs = nbytes / (us * 1e-6) / 1e9
+    peak = peaks.get("hbm_gbs") or FALLBACK_HBM_GBS
+    return {"pairs": n_pairs, "bytes_per_launch": nbytes, "us": _sig(us), "gbs": _sig(gbs),
+            "frac": _sig(gbs / peak), "pool": "7B shape, fp16, 32 KV heads"}
 
 
 def _path(w):
