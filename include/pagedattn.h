@@ -319,7 +319,9 @@ PA_API pa_status pa_selftest_wait_timeout(void *stream);
  * device memory is allocated or freed.  All calls on a device share the array:
  * calls that can overlap on the GPU (unordered streams) race.  The first call on
  * a device looks up the array's device address with that device current; make
- * it before any stream capture.
+ * it before any stream capture.  The address is kept for the life of the
+ * process: do not use the library across a cudaDeviceReset of that device (the
+ * same holds for the error word of pa_device_error).
  */
 #define PA_NOALLOC_SCRATCH_BYTES ((size_t)8 << 20)
 PA_API pa_status pa_decode_split_noalloc(void *out, const void *q, const void *k_cache,

@@ -19,7 +19,10 @@
 //     zero because the partial pass writes every entry the combine pass reads;
 //   * the first call on a device looks up the array's device address
 //     (cudaGetSymbolAddress) with that device current; make that first call
-//     before any stream capture.
+//     before any stream capture;
+//   * that address is kept for the life of the process, so the library must not
+//     outlive a reset of the device's primary context (cudaDeviceReset): after a
+//     reset the kept address no longer names the array.
 #include <cuda_runtime.h>
 
 #include <mutex>

@@ -79,6 +79,12 @@ def test_noalloc_matches_workspace_pair_two_calls_in_a_row(pa):
             got = out.cpu().double().numpy()
             _tol.check(got, want.cpu().double().numpy(), c.dtype, f"{name} call {call}")
             assert torch.equal(out, want)
+        # the Python binding of the same entry point
+        out = torch.full_like(d["q"], float("nan"))
+        pa.pa_decode_split_noalloc(out, d["q"], d["k_cache"], d["v_cache"], d["block_tables"],
+                                   d["context_lens"], w.scale, splits, q_len=c.q_len)
+        torch.cuda.synchronize()
+        assert torch.equal(out, want)
     assert pa.pa_device_error() == pa.PA_OK
 
 
@@ -91,3 +97,10 @@ def test_noalloc_refuses_sizes_beyond_its_array(pa):
     assert _noalloc_via_abi(pa, w, d, out, 64) == pa.PA_ERR_INVALID_ARG
     torch.cuda.synchronize()
     assert int(out.abs().sum()) == 0          # nothing was launched
+    # the binding raises the library's status and leaves out untouched
+    with pytest.raises(pa.PagedAttnError) as exc:
+        pa.pa_decode_split_noalloc(out, d["q"], d["k_cache"], d["v_cache"], d["block_tables"],
+                                   d["context_lens"], w.scale, 64, q_len=c.q_len)
+    assert exc.value.status == pa.PA_ERR_INVALID_ARG
+    torch.cuda.synchronize()
+    assert int(out.abs().sum()) == 0
