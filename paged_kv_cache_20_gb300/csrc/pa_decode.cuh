@@ -86,6 +86,9 @@ struct DecodeArgs {
   // Prefill kernel, shared-prefix mode (> 0): the query rows of every sequence
   // attend to the first `shared_prefix` blocks of block-table row 0.
   int shared_prefix;
+  // Prefill kernel: most persistent CTAs to launch (0: one per SM).  A cascade's
+  // shared-prefix pass leaves the other SMs to the tail pass that overlaps it.
+  int max_ctas;
   // Prefill kernel: q rows arrive by TMA through the kernel's q tensor map (the KV
   // group size divides 128); otherwise each thread loads its own row
   int q_tma;

@@ -45,7 +45,9 @@ cudaError_t launch_prefill_t(const CUtensorMap &kmap, const CUtensorMap &vmap, c
     if (e != cudaSuccess) return e;
     sm_count[dev].store(sms, std::memory_order_relaxed);
   }
-  const long long gx = std::min<long long>(units, std::max(1, sms));
+  long long cap = std::max(1, sms);
+  if (a.max_ctas > 0) cap = std::min<long long>(cap, a.max_ctas);
+  const long long gx = std::min<long long>(units, cap);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)gx, 1, 1);
   cfg.blockDim = dim3(kTcThreads, 1, 1);

@@ -196,3 +196,61 @@ def test_byte_perm_pairs_tokens_per_dim():
     a, b = [10, 11, 12, 13], [20, 21, 22, 23]   # dims 0..3 of two tokens
     assert byte_perm(a, b, 0x5140) == [10, 20, 11, 21]
     assert byte_perm(a, b, 0x7362) == [12, 22, 13, 23]
+
+
+# ------------------------------------------------------------ many-row (prefill) kernel
+@pytest.mark.parametrize("PB", [64])
+def test_prefill_epilogue_scratch(PB):
+    """The epilogue's transpose: lane l writes its row's CPR chunks at
+    l*PB + 16*(c ^ swz(l)); lane l then reads chunk c = l % CPR of row
+    RPI*j + l // CPR.  Both directions conflict-free, and every (row, chunk) read
+    back is the one written."""
+    CPR = PB // 16
+    RPI = 32 // CPR
+
+    def swz(r):
+        return (r // (8 // CPR)) % CPR
+
+    def waddr(l, c):
+        return l * PB + ((c ^ swz(l)) << 4)
+
+    for c in range(CPR):
+        assert conflict_free(lambda l: waddr(l, c))
+    stored = {waddr(l, c): (l, c) for l in range(32) for c in range(CPR)}
+    assert len(stored) == 32 * CPR and max(stored) < 32 * PB
+    for j in range(CPR):
+        def raddr(l):
+            r = RPI * j + l // CPR
+            return r * PB + (((l % CPR) ^ swz(r)) << 4)
+        assert conflict_free(raddr)
+        for l in range(32):
+            assert stored[raddr(l)] == (RPI * j + l // CPR, l % CPR)
+
+
+@pytest.mark.parametrize("CG", [2])
+def test_prefill_p_columns_match_the_pv_operand(CG):
+    """P_j in tensor memory (CG column groups, one softmax warp each per 32 rows):
+    the softmax warp of column group g writes positions
+    g*kCols + 2e, +1 of a 128-position chunk into word column g*kCols + e (hi) and
+    g*kCols + kCols/2 + e (lo); the P V MMA's K step kk reads positions 16kk..16kk+15
+    from 8 word columns at pc = (kk // kSteps)*kCols + (kk % kSteps)*8 (lo at
+    + kCols/2).  Every position lands where the MMA reads it, and hi and lo never
+    overlap another group's columns."""
+    chunk = 128
+    kCols = chunk // CG
+    kSteps = kCols // 16
+    written_hi, written_lo = {}, {}
+    for g in range(CG):
+        for e in range(kCols // 2):
+            for p in (0, 1):
+                pos = g * kCols + 2 * e + p
+                written_hi[pos] = (g * kCols + e, p)
+                written_lo[pos] = (g * kCols + kCols // 2 + e, p)
+    cols = [c for c, _ in written_hi.values()] + [c for c, _ in written_lo.values()]
+    assert sorted(set(cols)) == list(range(chunk))        # the chunk's 128 columns, each used
+    for kk in range(chunk // 16):
+        pc = (kk // kSteps) * kCols + (kk % kSteps) * 8
+        for i in range(16):                                 # k index inside the step
+            pos = 16 * kk + i
+            assert written_hi[pos] == (pc + i // 2, i % 2)  # lower k in the low half
+            assert written_lo[pos] == (pc + kCols // 2 + i // 2, i % 2)
