@@ -50,7 +50,7 @@ DEFAULT_CONFIG = "llama7b_mha"
 # gqa last: the end of the printed line carries it in full even where only the
 # line's tail is kept
 OTHER_CONFIGS = ["long_split", "prefix_verify", "llama7b_mha_fp8", "gqa_fp8", "chunked_prefill",
-                 "gqa"]
+                 "chunked_prefill_fp8", "gqa"]
 DECODE_MAX_QLEN = 16              # more query rows per sequence go to the prefill kernel
 L2_BYTES = 129 << 20             # GB300 L2; every workload's KV cache is several times larger
 NOMINAL_HBM_GBS = 8000.0
@@ -647,8 +647,11 @@ def measure_config(pa, name, seed, device, steps, warmup, world, peaks, e2e=Fals
             "peak": tpeak or 1900.0, "unit": "TFLOP/s",
             "frac": fl / (kern_avg * 1e-3) / 1e12 / (tpeak or 1900.0),
             "peak_source": "measured bf16 dense (burst)" if tpeak else "fallback",
-            "kernel": "append_step_kernel+paged_prefill_tc_kernel (tcgen05.mma, M = 128)"}
-        res["roofline"]["kernel"] = "append_step_kernel+paged_prefill_kernel"
+            "kernel": ("append_step_fp8_kernel+paged_prefill_tc_kernel (tcgen05.mma, M = 128, "
+                       "e4m3 codes widened to fp16 in shared memory)" if w.cfg.kv_fp8 else
+                       "append_step_kernel+paged_prefill_tc_kernel (tcgen05.mma, M = 128)")}
+        res["roofline"]["kernel"] = ("append_step_fp8_kernel+paged_prefill_tc_kernel" if w.cfg.kv_fp8
+                                     else "append_step_kernel+paged_prefill_kernel")
         res["roofline"]["traffic"] = traffic_record("paged_prefill_tc_kernel", name)
     if w.cfg.shared_prefix:
         runner.mode = "cascade"

@@ -42,14 +42,15 @@
  *    AttentionWithKVCache.forward updates the cache before computing scores).
  *  - GQA: query head h reads KV head h / (num_q_heads / num_kv_heads)
  *    (contiguous groups; [QA] Q7, [ANIM] §1 figure).
- *  - Supported now: block_size 16; head_dim 64 or 128; q_len 1..4096 with a
+ *  - Supported now: block_size 8, 16 or 32 (the kernels walk 16-token tiles: a
+ *    32-token block is two tiles, a tile of an 8-token pool spans two blocks);
+ *    head_dim 64 or 128; q_len 1..4096 with a
  *    16-bit cache (up to 16 query rows per sequence go to the decode kernel, more
  *    to a tensor-core kernel that shares each K/V chunk among 128 query rows of a
  *    KV head: chunked prefill,
  *    [QA] Q14, [SB11] §11.3 "Continuous Batching"); q_len 1..4096 with an FP8
- *    cache too, where every q_len runs on the decode kernel in groups of 16
- *    query rows per KV head (each group reads the sequence's blocks: meant for
- *    decode and short chunks).
+ *    cache too, split between the same two kernels (the many-row kernel widens
+ *    each chunk of codes to fp16 in shared memory).
  *  - Alignment: every pointer 16-byte aligned.
  *
  * Errors: argument checks run on the host before any launch and return
@@ -170,7 +171,8 @@ PA_API pa_status pa_decode(void *out, const void *q, const void *k_cache, const 
  * byte offset align256(sizeof acc), section l at align256 after m.
  * Partition p of sequence i covers blocks [p*C, (p+1)*C) with
  * C = ceil(ceil(context_lens[i] / block_size) / num_splits); partitions past
- * the end are empty.
+ * the end are empty.  With 8-token blocks the partitions are counted in 16-token
+ * tiles instead (C = ceil(ceil(context_lens[i] / 16) / num_splits) tiles).
  */
 PA_API size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int q_len, int head_dim,
                                        int num_splits);
@@ -238,6 +240,8 @@ PA_API pa_status pa_append_decode(void *out, const void *q, const void *k_new, c
  * Caller's contract: for every sequence, table entries [0, prefix_blocks) equal
  * those of row 0, and this step's new tokens lie at or past position
  * prefix_blocks * block_size (so the append never writes a shared block).
+ * prefix_blocks * block_size must be a multiple of 16 (PA_ERR_UNSUPPORTED
+ * otherwise: the two passes split at a 16-token tile).
  * k_new and v_new are both NULL (no append) or both given.  16-bit caches only.
  */
 PA_API pa_status pa_decode_cascade(void *out, const void *q, const void *k_new, const void *v_new,
@@ -272,7 +276,9 @@ PA_API pa_status pa_append_kv_fp8(void *k_cache, void *v_cache, const void *k_ne
  * new rows are first quantised into the cache as pa_append_kv_fp8 would (slots of
  * the last q_len positions, as pa_slot_mapping), in the same launch.  num_splits == 1:
  * single pass, workspace may be NULL; num_splits > 1: split-KV partial pass into the
- * workspace (layout of pa_decode_partial) and the combine.
+ * workspace (layout of pa_decode_partial) and the combine.  With more than 16
+ * query rows per sequence (chunked prefill over an FP8 cache, [QA] Q4 and Q14) the
+ * fused append is a launch of its own before the attention, as in pa_append_decode.
  */
 PA_API pa_status pa_decode_fp8(void *out, const void *q, const void *k_new, const void *v_new,
                                void *k_cache, void *v_cache, const float *k_scale,

@@ -22,7 +22,9 @@
 
 namespace {
 
-constexpr int kBlockSize = 16;
+// Block sizes the kernels take: a block of 32 tokens is read as two 16-token tiles,
+// a 16-token tile spans two blocks of 8
+bool supported_block(int b) { return b == 8 || b == 16 || b == 32; }
 constexpr int kMaxDevices = 64;
 constexpr int kMaxQLen = 4096;       // query rows per sequence accepted by the ABI
 constexpr int kMaxDecodeQLen = 16;   // at most this many go to the decode kernel
@@ -64,7 +66,7 @@ __global__ void slot_mapping_kernel(int64_t *out, const int32_t *block_tables,
 template <int D>
 __global__ void append_kv_kernel(uint16_t *k_cache, uint16_t *v_cache, const uint16_t *k_new,
                                  const uint16_t *v_new, const int64_t *slot_mapping, int n_tokens,
-                                 int num_kv_heads, int64_t num_slots, unsigned *err) {
+                                 int num_kv_heads, int block_size, int64_t num_slots, unsigned *err) {
   pa::griddep_wait();  // the slot mapping may come from the previous kernel
   pa::griddep_launch_dependents();
   constexpr int kChunks = D / 8;
@@ -81,8 +83,8 @@ __global__ void append_kv_kernel(uint16_t *k_cache, uint16_t *v_cache, const uin
       if (c == 0 && h == 0) pa::record_error(err, pa::kErrCheck);
       continue;
     }
-    const int64_t block = slot / kBlockSize, offset = slot % kBlockSize;
-    const int64_t dst = ((block * num_kv_heads + h) * kBlockSize + offset) * D + c * 8;
+    const int64_t block = slot / block_size, offset = slot % block_size;
+    const int64_t dst = ((block * num_kv_heads + h) * block_size + offset) * D + c * 8;
     const int64_t src = (t * num_kv_heads + h) * D + c * 8;
     const uint4 kv = __ldg(reinterpret_cast<const uint4 *>(k_new + src));
     const uint4 vv = __ldg(reinterpret_cast<const uint4 *>(v_new + src));
@@ -98,8 +100,8 @@ template <int D>
 __global__ void append_step_kernel(uint16_t *k_cache, uint16_t *v_cache, const uint16_t *k_new,
                                    const uint16_t *v_new, const int32_t *block_tables,
                                    const int32_t *context_lens, int num_seqs, int q_len,
-                                   int num_kv_heads, int max_blocks_per_seq, int64_t num_slots,
-                                   unsigned *err) {
+                                   int num_kv_heads, int block_size, int max_blocks_per_seq,
+                                   int64_t num_slots, unsigned *err) {
   pa::griddep_wait();
   pa::griddep_launch_dependents();
   constexpr int kChunks = D / 8;
@@ -113,21 +115,63 @@ __global__ void append_step_kernel(uint16_t *k_cache, uint16_t *v_cache, const u
     const int i = (int)(t / q_len), u = (int)(t % q_len);
     const int64_t pos = (int64_t)context_lens[i] - q_len + u;
     if (pos < 0) continue;
-    const int64_t lb = pos / kBlockSize;
+    const int64_t lb = pos / block_size;
     if (lb >= max_blocks_per_seq) {
       if (c == 0) pa::record_error(err, pa::kErrCheck);
       continue;
     }
     const int64_t slot =
-        (int64_t)block_tables[(int64_t)i * max_blocks_per_seq + lb] * kBlockSize + pos % kBlockSize;
+        (int64_t)block_tables[(int64_t)i * max_blocks_per_seq + lb] * block_size + pos % block_size;
     if (slot < 0 || slot >= num_slots) {
       if (c == 0) pa::record_error(err, pa::kErrCheck);
       continue;
     }
-    const int64_t dst = (((slot / kBlockSize) * num_kv_heads + h) * kBlockSize + slot % kBlockSize) * D + c * 8;
+    const int64_t dst = (((slot / block_size) * num_kv_heads + h) * block_size + slot % block_size) * D + c * 8;
     const int64_t src = (t * num_kv_heads + h) * D + c * 8;
     *reinterpret_cast<uint4 *>(k_cache + dst) = __ldg(reinterpret_cast<const uint4 *>(k_new + src));
     *reinterpret_cast<uint4 *>(v_cache + dst) = __ldg(reinterpret_cast<const uint4 *>(v_new + src));
+  }
+}
+
+// The same append into an FP8 cache, quantising: code = e4m3(x / scale[head]).  One
+// thread per 8 values of a (token, head) row.
+template <typename T, int D>
+__global__ void append_step_fp8_kernel(uint8_t *k_cache, uint8_t *v_cache, const uint16_t *k_new,
+                                       const uint16_t *v_new, const int32_t *block_tables,
+                                       const int32_t *context_lens, int num_seqs, int q_len,
+                                       int num_kv_heads, int block_size, int max_blocks_per_seq,
+                                       int64_t num_slots, const float *k_scale,
+                                       const float *v_scale, unsigned *err) {
+  pa::griddep_wait();
+  pa::griddep_launch_dependents();
+  constexpr int kChunks = D / 8;
+  const int64_t total = (int64_t)num_seqs * q_len * num_kv_heads * kChunks;
+  for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
+       idx += (int64_t)gridDim.x * blockDim.x) {
+    const int c = (int)(idx % kChunks);
+    const int64_t th = idx / kChunks;
+    const int h = (int)(th % num_kv_heads);
+    const int64_t t = th / num_kv_heads;  // token row of k_new: seq * q_len + u
+    const int i = (int)(t / q_len), u = (int)(t % q_len);
+    const int64_t pos = (int64_t)context_lens[i] - q_len + u;
+    if (pos < 0) continue;
+    const int64_t lb = pos / block_size;
+    if (lb >= max_blocks_per_seq) {
+      if (c == 0) pa::record_error(err, pa::kErrCheck);
+      continue;
+    }
+    const int64_t slot =
+        (int64_t)block_tables[(int64_t)i * max_blocks_per_seq + lb] * block_size + pos % block_size;
+    if (slot < 0 || slot >= num_slots) {
+      if (c == 0) pa::record_error(err, pa::kErrCheck);
+      continue;
+    }
+    const int64_t dst = (((slot / block_size) * num_kv_heads + h) * block_size + slot % block_size) * D + c * 8;
+    const int64_t src = (t * num_kv_heads + h) * D + c * 8;
+    const uint4 kv = __ldg(reinterpret_cast<const uint4 *>(k_new + src));
+    const uint4 vv = __ldg(reinterpret_cast<const uint4 *>(v_new + src));
+    *reinterpret_cast<uint2 *>(k_cache + dst) = pa::quantize8<T>(kv, __ldg(k_scale + h));
+    *reinterpret_cast<uint2 *>(v_cache + dst) = pa::quantize8<T>(vv, __ldg(v_scale + h));
   }
 }
 
@@ -136,8 +180,9 @@ __global__ void append_step_kernel(uint16_t *k_cache, uint16_t *v_cache, const u
 template <typename T, int D>
 __global__ void append_kv_fp8_kernel(uint8_t *k_cache, uint8_t *v_cache, const uint16_t *k_new,
                                      const uint16_t *v_new, const int64_t *slot_mapping,
-                                     int n_tokens, int num_kv_heads, int64_t num_slots,
-                                     const float *k_scale, const float *v_scale, unsigned *err) {
+                                     int n_tokens, int num_kv_heads, int block_size,
+                                     int64_t num_slots, const float *k_scale,
+                                     const float *v_scale, unsigned *err) {
   pa::griddep_wait();
   pa::griddep_launch_dependents();
   constexpr int kChunks = D / 8;
@@ -154,8 +199,8 @@ __global__ void append_kv_fp8_kernel(uint8_t *k_cache, uint8_t *v_cache, const u
       if (c == 0 && h == 0) pa::record_error(err, pa::kErrCheck);
       continue;
     }
-    const int64_t block = slot / kBlockSize, offset = slot % kBlockSize;
-    const int64_t dst = ((block * num_kv_heads + h) * kBlockSize + offset) * D + c * 8;
+    const int64_t block = slot / block_size, offset = slot % block_size;
+    const int64_t dst = ((block * num_kv_heads + h) * block_size + offset) * D + c * 8;
     const int64_t src = (t * num_kv_heads + h) * D + c * 8;
     const uint4 kv = __ldg(reinterpret_cast<const uint4 *>(k_new + src));
     const uint4 vv = __ldg(reinterpret_cast<const uint4 *>(v_new + src));
@@ -230,15 +275,20 @@ bool supported_dtype(pa_dtype d) { return d == PA_FP16 || d == PA_BF16; }
 
 // Tensor map over one cache: [num_blocks * num_kv_heads tiles][16 rows][head_dim],
 // box = 16 rows x 64 columns, 128-byte swizzle, zero fill outside.
+// Tensor map over a cache [num_blocks][num_kv_heads][block_size][head_dim] as
+// [head_dim, R, num_blocks * num_kv_heads * block_size / R] with R = min(block_size,
+// 16) rows per box: a (block, head) pair of a 32-token block is two consecutive
+// 16-row boxes; an 8-token block is one 8-row box.  128-byte rows, 128-byte swizzle.
 pa_status make_map(CUtensorMap *map, const void *cache, pa_dtype dtype, int head_dim,
-                   int num_blocks, int num_kv_heads, bool fp8 = false) {
+                   int num_blocks, int num_kv_heads, int block_size, bool fp8 = false) {
   std::call_once(g_encode_once, load_encode);
   if (g_encode == nullptr) return PA_ERR_CUDA;
   const int elt = fp8 ? 1 : 2;
-  cuuint64_t dims[3] = {(cuuint64_t)head_dim, (cuuint64_t)kBlockSize,
-                        (cuuint64_t)num_blocks * (cuuint64_t)num_kv_heads};
-  cuuint64_t strides[2] = {(cuuint64_t)head_dim * elt, (cuuint64_t)kBlockSize * head_dim * elt};
-  cuuint32_t box[3] = {(cuuint32_t)(128 / elt), (cuuint32_t)kBlockSize, 1};  // 128-byte rows
+  const int rows = block_size < 16 ? block_size : 16;
+  cuuint64_t dims[3] = {(cuuint64_t)head_dim, (cuuint64_t)rows,
+                        (cuuint64_t)num_blocks * (cuuint64_t)num_kv_heads * (block_size / rows)};
+  cuuint64_t strides[2] = {(cuuint64_t)head_dim * elt, (cuuint64_t)rows * head_dim * elt};
+  cuuint32_t box[3] = {(cuuint32_t)(128 / elt), (cuuint32_t)rows, 1};  // 128-byte rows
   cuuint32_t elem_strides[3] = {1, 1, 1};
   const CUtensorMapDataType ty = fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
                                      : (dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
@@ -298,11 +348,12 @@ pa_status check_decode(const void *q, const void *k_cache, const void *v_cache,
   if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache)) return PA_ERR_INVALID_ARG;
   if (!supported_dtype(dtype)) return PA_ERR_UNSUPPORTED;
   if (head_dim != 64 && head_dim != 128) return PA_ERR_UNSUPPORTED;
-  if (block_size != kBlockSize) return PA_ERR_UNSUPPORTED;
+  if (!supported_block(block_size)) return PA_ERR_UNSUPPORTED;
   if (q_len > kMaxQLen) return PA_ERR_UNSUPPORTED;
   // 32-bit index limits used by the kernels
-  if ((int64_t)num_blocks * num_kv_heads >= (int64_t)1 << 31) return PA_ERR_INVALID_ARG;
-  if ((int64_t)num_seqs * max_blocks_per_seq >= (int64_t)1 << 31) return PA_ERR_INVALID_ARG;
+  if ((int64_t)num_blocks * num_kv_heads * 2 >= (int64_t)1 << 31) return PA_ERR_INVALID_ARG;
+  if ((int64_t)num_seqs * max_blocks_per_seq * 2 >= (int64_t)1 << 31) return PA_ERR_INVALID_ARG;
+  if ((int64_t)max_blocks_per_seq * block_size >= (int64_t)1 << 31) return PA_ERR_INVALID_ARG;
   if ((int64_t)num_seqs * q_len * num_q_heads >= (int64_t)1 << 31) return PA_ERR_INVALID_ARG;
   return PA_OK;
 }
@@ -337,7 +388,7 @@ int cascade_prefix_ctas() {
 pa_status decode_common(void *out, float *ws, const WsLayout *lay, const void *q,
                         const void *k_cache, const void *v_cache, const int32_t *block_tables,
                         const int32_t *context_lens, int num_seqs, int num_q_heads,
-                        int num_kv_heads, int head_dim, float scale, int num_splits,
+                        int num_kv_heads, int head_dim, int block_size, float scale, int num_splits,
                         int max_blocks_per_seq, int num_blocks, int q_len, pa_dtype dtype,
                         void *stream, const void *k_new = nullptr, const void *v_new = nullptr,
                         const float *k_scale = nullptr, const float *v_scale = nullptr,
@@ -345,14 +396,14 @@ pa_status decode_common(void *out, float *ws, const WsLayout *lay, const void *q
   const int64_t units = (int64_t)num_seqs * num_kv_heads * num_splits;
   if (units >= (int64_t)1 << 31) return PA_ERR_INVALID_ARG;
   const bool fp8 = k_scale != nullptr;
-  // many query rows (or the shared-prefix pass): the CTA-shared pipeline kernel.
-  // Over an FP8 cache every q_len goes to the decode kernel, in row groups of 16.
+  // many query rows (or the shared-prefix pass): the CTA-shared pipeline kernel,
+  // over a 16-bit or an FP8 cache
   if (fp8 && place.shared_prefix > 0) return PA_ERR_UNSUPPORTED;
-  const bool prefill = place.shared_prefix > 0 || (q_len > kMaxDecodeQLen && !fp8);
+  const bool prefill = place.shared_prefix > 0 || q_len > kMaxDecodeQLen;
   CUtensorMap kmap, vmap;
-  pa_status st = make_map(&kmap, k_cache, dtype, head_dim, num_blocks, num_kv_heads, fp8);
+  pa_status st = make_map(&kmap, k_cache, dtype, head_dim, num_blocks, num_kv_heads, block_size, fp8);
   if (st != PA_OK) return st;
-  st = make_map(&vmap, v_cache, dtype, head_dim, num_blocks, num_kv_heads, fp8);
+  st = make_map(&vmap, v_cache, dtype, head_dim, num_blocks, num_kv_heads, block_size, fp8);
   if (st != PA_OK) return st;
   pa::DecodeArgs a;
   a.q = q;
@@ -371,6 +422,9 @@ pa_status decode_common(void *out, float *ws, const WsLayout *lay, const void *q
   a.group = num_q_heads / num_kv_heads;
   a.rows = a.group * q_len;
   a.max_blocks_per_seq = max_blocks_per_seq;
+  a.block_size = block_size;
+  a.max_tiles = (int)(((int64_t)max_blocks_per_seq * block_size + pa::kTileTokens - 1) /
+                      pa::kTileTokens);
   a.num_blocks = num_blocks;
   a.num_splits = num_splits;
   a.lpt = num_seqs <= pa::kLptMaxSeqs ? 1 : 0;
@@ -380,10 +434,11 @@ pa_status decode_common(void *out, float *ws, const WsLayout *lay, const void *q
   a.v_cache = static_cast<uint16_t *>(const_cast<void *>(v_cache));
   a.k_scale = k_scale;
   a.v_scale = v_scale;
-  a.first_block = place.first_block;
+  // (the callers' block counts cover whole 16-token tiles)
+  a.first_block = place.first_block * block_size / pa::kTileTokens;
   a.ws_splits = place.ws_splits > 0 ? place.ws_splits : num_splits;
   a.ws_split0 = place.ws_split0;
-  a.shared_prefix = place.shared_prefix;
+  a.shared_prefix = place.shared_prefix * block_size / pa::kTileTokens;
   a.max_ctas = place.max_ctas;
   a.q_tma = 0;
   a.s_negate = 0;
@@ -406,18 +461,32 @@ pa_status decode_common(void *out, float *ws, const WsLayout *lay, const void *q
       // append runs as its own launch first (ordered by the stream).
       const int64_t total = (int64_t)num_seqs * q_len * num_kv_heads * (head_dim / 8);
       const unsigned blocks = (unsigned)std::min<int64_t>((total + 255) / 256, 1 << 20);
-      const int64_t num_slots = (int64_t)num_blocks * kBlockSize;
-      auto kc = static_cast<uint16_t *>(const_cast<void *>(k_cache));
-      auto vc = static_cast<uint16_t *>(const_cast<void *>(v_cache));
+      const int64_t num_slots = (int64_t)num_blocks * block_size;
       auto kn = static_cast<const uint16_t *>(k_new);
       auto vn = static_cast<const uint16_t *>(v_new);
-      e = head_dim == 128
-              ? pa::launch_dependent(append_step_kernel<128>, blocks, 256, s, kc, vc, kn, vn,
-                                     block_tables, context_lens, num_seqs, q_len, num_kv_heads,
-                                     max_blocks_per_seq, num_slots, a.err)
-              : pa::launch_dependent(append_step_kernel<64>, blocks, 256, s, kc, vc, kn, vn,
-                                     block_tables, context_lens, num_seqs, q_len, num_kv_heads,
-                                     max_blocks_per_seq, num_slots, a.err);
+      if (fp8) {  // quantising (head_dim 128)
+        auto kc8 = static_cast<uint8_t *>(const_cast<void *>(k_cache));
+        auto vc8 = static_cast<uint8_t *>(const_cast<void *>(v_cache));
+        e = dtype == PA_FP16
+                ? pa::launch_dependent(append_step_fp8_kernel<__half, 128>, blocks, 256, s, kc8, vc8,
+                                       kn, vn, block_tables, context_lens, num_seqs, q_len,
+                                       num_kv_heads, block_size, max_blocks_per_seq, num_slots,
+                                       k_scale, v_scale, a.err)
+                : pa::launch_dependent(append_step_fp8_kernel<__nv_bfloat16, 128>, blocks, 256, s,
+                                       kc8, vc8, kn, vn, block_tables, context_lens, num_seqs,
+                                       q_len, num_kv_heads, block_size, max_blocks_per_seq,
+                                       num_slots, k_scale, v_scale, a.err);
+      } else {
+        auto kc = static_cast<uint16_t *>(const_cast<void *>(k_cache));
+        auto vc = static_cast<uint16_t *>(const_cast<void *>(v_cache));
+        e = head_dim == 128
+                ? pa::launch_dependent(append_step_kernel<128>, blocks, 256, s, kc, vc, kn, vn,
+                                       block_tables, context_lens, num_seqs, q_len, num_kv_heads,
+                                       block_size, max_blocks_per_seq, num_slots, a.err)
+                : pa::launch_dependent(append_step_kernel<64>, blocks, 256, s, kc, vc, kn, vn,
+                                       block_tables, context_lens, num_seqs, q_len, num_kv_heads,
+                                       block_size, max_blocks_per_seq, num_slots, a.err);
+      }
       if (e != cudaSuccess) return PA_ERR_CUDA;
       a.k_new = a.v_new = nullptr;
     }
@@ -431,14 +500,15 @@ pa_status decode_common(void *out, float *ws, const WsLayout *lay, const void *q
     }
     if (a.scale_log2 == 0.f) a.scale_log2 = 1e-30f;
     CUtensorMap qmap;
-    a.q_tma = (128 % a.group == 0) ? 1 : 0;
+    // (over an FP8 cache a bf16 q is converted to fp16 by the softmax threads)
+    a.q_tma = (128 % a.group == 0 && !(fp8 && dtype == PA_BF16)) ? 1 : 0;
     if (a.q_tma) {
       st = make_q_map(&qmap, q, dtype, head_dim, num_q_heads, (int64_t)num_seqs * q_len, a.group);
       if (st != PA_OK) return st;
     } else {
       qmap = kmap;  // unused
     }
-    e = pa::launch_prefill(kmap, vmap, qmap, a, head_dim, dtype == PA_FP16, partial, s);
+    e = pa::launch_prefill(kmap, vmap, qmap, a, head_dim, dtype == PA_FP16, partial, fp8, s);
   } else if (fp8)
     e = dtype == PA_FP16 ? pa::launch_decode8_fp16(kmap, vmap, a, partial, (int)units, s)
                          : pa::launch_decode8_bf16(kmap, vmap, a, partial, (int)units, s);
@@ -473,7 +543,7 @@ PA_API pa_status pa_slot_mapping(int64_t *slot_mapping, const int32_t *block_tab
   if (!slot_mapping || !block_tables || !context_lens) return PA_ERR_INVALID_ARG;
   if (num_seqs <= 0 || max_blocks_per_seq <= 0 || block_size <= 0 || q_len <= 0)
     return PA_ERR_INVALID_ARG;
-  if (block_size != kBlockSize) return PA_ERR_UNSUPPORTED;
+  if (!supported_block(block_size)) return PA_ERR_UNSUPPORTED;
   if ((int64_t)num_seqs * q_len >= (int64_t)1 << 31 ||
       (int64_t)num_seqs * max_blocks_per_seq >= (int64_t)1 << 31)
     return PA_ERR_INVALID_ARG;
@@ -498,14 +568,14 @@ PA_API pa_status pa_append_kv(void *k_cache, void *v_cache, const void *k_new, c
     return PA_ERR_INVALID_ARG;
   if (!supported_dtype(dtype)) return PA_ERR_UNSUPPORTED;
   if (head_dim != 64 && head_dim != 128) return PA_ERR_UNSUPPORTED;
-  if (block_size != kBlockSize) return PA_ERR_UNSUPPORTED;
+  if (!supported_block(block_size)) return PA_ERR_UNSUPPORTED;
   if (n_tokens == 0) return PA_OK;
   unsigned *err = error_word();
   if (err == nullptr) return PA_ERR_CUDA;
   const int64_t total = (int64_t)n_tokens * num_kv_heads * (head_dim / 8);
   const int threads = 256;
   const int blocks = (int)std::min<int64_t>((total + threads - 1) / threads, 1 << 20);
-  const int64_t num_slots = (int64_t)num_blocks * kBlockSize;
+  const int64_t num_slots = (int64_t)num_blocks * block_size;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   auto kc = static_cast<uint16_t *>(k_cache);
   auto vc = static_cast<uint16_t *>(v_cache);
@@ -513,11 +583,11 @@ PA_API pa_status pa_append_kv(void *k_cache, void *v_cache, const void *k_new, c
   auto vn = static_cast<const uint16_t *>(v_new);
   cudaError_t e = head_dim == 128
                       ? pa::launch_dependent(append_kv_kernel<128>, blocks, threads, s, kc, vc, kn,
-                                             vn, slot_mapping, n_tokens, num_kv_heads, num_slots,
-                                             err)
+                                             vn, slot_mapping, n_tokens, num_kv_heads, block_size,
+                                             num_slots, err)
                       : pa::launch_dependent(append_kv_kernel<64>, blocks, threads, s, kc, vc, kn,
-                                             vn, slot_mapping, n_tokens, num_kv_heads, num_slots,
-                                             err);
+                                             vn, slot_mapping, n_tokens, num_kv_heads, block_size,
+                                             num_slots, err);
   return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
@@ -531,11 +601,11 @@ PA_API pa_status pa_copy_blocks(void *k_cache, void *v_cache, const int32_t *src
   if (!aligned16(k_cache) || !aligned16(v_cache)) return PA_ERR_INVALID_ARG;
   if (!supported_dtype(dtype)) return PA_ERR_UNSUPPORTED;
   if (head_dim != 64 && head_dim != 128) return PA_ERR_UNSUPPORTED;
-  if (block_size != kBlockSize) return PA_ERR_UNSUPPORTED;
+  if (!supported_block(block_size)) return PA_ERR_UNSUPPORTED;
   if (n_pairs == 0) return PA_OK;
   unsigned *err = error_word();
   if (err == nullptr) return PA_ERR_CUDA;
-  const int64_t chunks = (int64_t)num_kv_heads * kBlockSize * head_dim * 2 / 16;
+  const int64_t chunks = (int64_t)num_kv_heads * block_size * head_dim * 2 / 16;
   const int64_t total = (int64_t)n_pairs * chunks;
   const int threads = 256;
   const unsigned blocks = (unsigned)std::min<int64_t>((total + threads - 1) / threads, 1 << 20);
@@ -557,7 +627,7 @@ PA_API pa_status pa_decode(void *out, const void *q, const void *k_cache, const 
                               max_blocks_per_seq, num_blocks, q_len, dtype);
   if (st != PA_OK) return st;
   return decode_common(out, nullptr, nullptr, q, k_cache, v_cache, block_tables, context_lens,
-                       num_seqs, num_q_heads, num_kv_heads, head_dim, scale, 1,
+                       num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, scale, 1,
                        max_blocks_per_seq, num_blocks, q_len, dtype, stream);
 }
 
@@ -577,14 +647,14 @@ PA_API pa_status pa_append_decode(void *out, const void *q, const void *k_new, c
   if (st != PA_OK) return st;
   if (num_splits == 1)
     return decode_common(out, nullptr, nullptr, q, k_cache, v_cache, block_tables, context_lens,
-                         num_seqs, num_q_heads, num_kv_heads, head_dim, scale, 1,
+                         num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, scale, 1,
                          max_blocks_per_seq, num_blocks, q_len, dtype, stream, k_new, v_new);
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return PA_ERR_INVALID_ARG;
   const WsLayout lay = ws_layout(num_seqs, num_q_heads, q_len, head_dim, num_splits);
   if (workspace_bytes < lay.total) return PA_ERR_INVALID_ARG;
   st = decode_common(nullptr, static_cast<float *>(workspace), &lay, q, k_cache, v_cache,
                      block_tables, context_lens, num_seqs, num_q_heads, num_kv_heads, head_dim,
-                     scale, num_splits, max_blocks_per_seq, num_blocks, q_len, dtype, stream,
+                     block_size, scale, num_splits, max_blocks_per_seq, num_blocks, q_len, dtype, stream,
                      k_new, v_new);
   if (st != PA_OK) return st;
   return pa_decode_combine(out, workspace, workspace_bytes, num_seqs, num_q_heads, head_dim,
@@ -607,6 +677,8 @@ PA_API pa_status pa_decode_cascade(void *out, const void *q, const void *k_new, 
                               max_blocks_per_seq, num_blocks, q_len, dtype);
   if (st != PA_OK) return st;
   if (prefix_blocks > max_blocks_per_seq) return PA_ERR_INVALID_ARG;
+  // the two passes split each row's positions at a 16-token tile boundary
+  if ((int64_t)prefix_blocks * block_size % pa::kTileTokens != 0) return PA_ERR_UNSUPPORTED;
   if (tail_splits >= (1 << 20)) return PA_ERR_INVALID_ARG;
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return PA_ERR_INVALID_ARG;
   const int parts = 1 + tail_splits;
@@ -620,7 +692,7 @@ PA_API pa_status pa_decode_cascade(void *out, const void *q, const void *k_new, 
   head.shared_prefix = prefix_blocks;
   head.max_ctas = cascade_prefix_ctas();
   st = decode_common(nullptr, ws, &lay, q, k_cache, v_cache, block_tables, context_lens, num_seqs,
-                     num_q_heads, num_kv_heads, head_dim, scale, 1, max_blocks_per_seq,
+                     num_q_heads, num_kv_heads, head_dim, block_size, scale, 1, max_blocks_per_seq,
                      num_blocks, q_len, dtype, stream, nullptr, nullptr, nullptr, nullptr, head);
   if (st != PA_OK) return st;
   // 2. each sequence's own blocks past the prefix (with this step's append, if
@@ -634,14 +706,14 @@ PA_API pa_status pa_decode_cascade(void *out, const void *q, const void *k_new, 
     tail.prior_lay = &lay;
     tail.prior_splits = parts;
     return decode_common(out, nullptr, nullptr, q, k_cache, v_cache, block_tables, context_lens,
-                         num_seqs, num_q_heads, num_kv_heads, head_dim, scale, 1,
+                         num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, scale, 1,
                          max_blocks_per_seq, num_blocks, q_len, dtype, stream, k_new, v_new,
                          nullptr, nullptr, tail);
   }
   tail.ws_splits = parts;
   tail.ws_split0 = 1;
   st = decode_common(nullptr, ws, &lay, q, k_cache, v_cache, block_tables, context_lens, num_seqs,
-                     num_q_heads, num_kv_heads, head_dim, scale, tail_splits, max_blocks_per_seq,
+                     num_q_heads, num_kv_heads, head_dim, block_size, scale, tail_splits, max_blocks_per_seq,
                      num_blocks, q_len, dtype, stream, k_new, v_new, nullptr, nullptr, tail);
   if (st != PA_OK) return st;
   // 3. merge the partitions
@@ -661,14 +733,14 @@ PA_API pa_status pa_append_kv_fp8(void *k_cache, void *v_cache, const void *k_ne
   if (!aligned16(k_cache) || !aligned16(v_cache) || !aligned16(k_new) || !aligned16(v_new))
     return PA_ERR_INVALID_ARG;
   if (!supported_dtype(new_dtype)) return PA_ERR_UNSUPPORTED;
-  if (head_dim != 128 || block_size != kBlockSize) return PA_ERR_UNSUPPORTED;
+  if (head_dim != 128 || !supported_block(block_size)) return PA_ERR_UNSUPPORTED;
   if (n_tokens == 0) return PA_OK;
   unsigned *err = error_word();
   if (err == nullptr) return PA_ERR_CUDA;
   const int64_t total = (int64_t)n_tokens * num_kv_heads * (head_dim / 8);
   const int threads = 256;
   const unsigned blocks = (unsigned)std::min<int64_t>((total + threads - 1) / threads, 1 << 20);
-  const int64_t num_slots = (int64_t)num_blocks * kBlockSize;
+  const int64_t num_slots = (int64_t)num_blocks * block_size;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   auto kc = static_cast<uint8_t *>(k_cache);
   auto vc = static_cast<uint8_t *>(v_cache);
@@ -677,10 +749,11 @@ PA_API pa_status pa_append_kv_fp8(void *k_cache, void *v_cache, const void *k_ne
   cudaError_t e = new_dtype == PA_FP16
                       ? pa::launch_dependent(append_kv_fp8_kernel<__half, 128>, blocks, threads, s,
                                              kc, vc, kn, vn, slot_mapping, n_tokens, num_kv_heads,
-                                             num_slots, k_scale, v_scale, err)
+                                             block_size, num_slots, k_scale, v_scale, err)
                       : pa::launch_dependent(append_kv_fp8_kernel<__nv_bfloat16, 128>, blocks,
                                              threads, s, kc, vc, kn, vn, slot_mapping, n_tokens,
-                                             num_kv_heads, num_slots, k_scale, v_scale, err);
+                                             num_kv_heads, block_size, num_slots, k_scale, v_scale,
+                                             err);
   return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
@@ -703,7 +776,7 @@ PA_API pa_status pa_decode_fp8(void *out, const void *q, const void *k_new, cons
   if (head_dim != 128) return PA_ERR_UNSUPPORTED;
   if (num_splits == 1)
     return decode_common(out, nullptr, nullptr, q, k_cache, v_cache, block_tables, context_lens,
-                         num_seqs, num_q_heads, num_kv_heads, head_dim, scale, 1,
+                         num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, scale, 1,
                          max_blocks_per_seq, num_blocks, q_len, dtype, stream, k_new, v_new,
                          k_scale, v_scale);
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return PA_ERR_INVALID_ARG;
@@ -711,7 +784,7 @@ PA_API pa_status pa_decode_fp8(void *out, const void *q, const void *k_new, cons
   if (workspace_bytes < lay.total) return PA_ERR_INVALID_ARG;
   st = decode_common(nullptr, static_cast<float *>(workspace), &lay, q, k_cache, v_cache,
                      block_tables, context_lens, num_seqs, num_q_heads, num_kv_heads, head_dim,
-                     scale, num_splits, max_blocks_per_seq, num_blocks, q_len, dtype, stream,
+                     block_size, scale, num_splits, max_blocks_per_seq, num_blocks, q_len, dtype, stream,
                      k_new, v_new, k_scale, v_scale);
   if (st != PA_OK) return st;
   return pa_decode_combine(out, workspace, workspace_bytes, num_seqs, num_q_heads, head_dim,
@@ -742,7 +815,7 @@ PA_API pa_status pa_decode_partial(void *workspace, size_t workspace_bytes, cons
   if (workspace_bytes < lay.total) return PA_ERR_INVALID_ARG;
   return decode_common(nullptr, static_cast<float *>(workspace), &lay, q, k_cache, v_cache,
                        block_tables, context_lens, num_seqs, num_q_heads, num_kv_heads, head_dim,
-                       scale, num_splits, max_blocks_per_seq, num_blocks, q_len, dtype, stream);
+                       block_size, scale, num_splits, max_blocks_per_seq, num_blocks, q_len, dtype, stream);
 }
 
 PA_API pa_status pa_decode_combine(void *out, const void *workspace, size_t workspace_bytes,

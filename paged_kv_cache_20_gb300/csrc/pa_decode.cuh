@@ -53,7 +53,9 @@
 
 namespace pa {
 
-constexpr int kTileTokens = 16;  // block_size: tokens per physical block / TMA tile
+// Tokens per tile: the kernels walk a sequence in 16-token tiles.  A cache block of
+// 16 tokens is one tile, one of 32 tokens two tiles, one of 8 tokens half a tile.
+constexpr int kTileTokens = 16;
 
 struct DecodeArgs {
   const void *q;                 // [num_seqs][q_len][num_q_heads][D]
@@ -66,6 +68,8 @@ struct DecodeArgs {
   unsigned *err;                 // device error word
   int num_seqs, num_q_heads, num_kv_heads, q_len, group, rows;  // rows = group * q_len
   int max_blocks_per_seq, num_blocks, num_splits;
+  int block_size;                // tokens per cache block: 8, 16 or 32
+  int max_tiles;                 // 16-token tiles a block-table row covers (rounded up)
   int lpt;                       // 1: take sequences longest first (num_seqs <= kLptMaxSeqs)
   float scale_log2;              // scale * log2(e): scores in base-2 units
   // fused append (k_new == nullptr: none).  The unit writes its own KV head's rows
@@ -78,13 +82,13 @@ struct DecodeArgs {
   // FP8 (e4m3) cache: value = code * scale of its KV head ([num_kv_heads] each)
   const float *k_scale;
   const float *v_scale;
-  // Partitioning of each sequence's blocks: blocks before first_block are skipped
+  // Partitioning of each sequence's tiles: tiles before first_block are skipped
   // (a shared prefix handled elsewhere); the partial pass writes partitions
   // ws_split0 .. ws_split0 + num_splits - 1 of a workspace laid out for ws_splits.
   int first_block;
   int ws_splits, ws_split0;
   // Prefill kernel, shared-prefix mode (> 0): the query rows of every sequence
-  // attend to the first `shared_prefix` blocks of block-table row 0.
+  // attend to the first `shared_prefix` tiles of block-table row 0.
   int shared_prefix;
   // Prefill kernel: most persistent CTAs to launch (0: one per SM).  A cascade's
   // shared-prefix pass leaves the other SMs to the tail pass that overlaps it.
@@ -104,6 +108,58 @@ struct DecodeArgs {
 };
 
 constexpr int kLptMaxSeqs = 256;
+
+// A table entry that is not read: no block, the tile rows it would hold are
+// zero-filled and nothing is reported
+constexpr int kNoBlock = -2147483647 - 1;
+
+// The tile range [tb, te) of partition `split` of a walk over tiles [fb, nb): the
+// partitions cover whole cache blocks where a block spans whole tiles (16 or 32
+// tokens: the split counts blocks), whole tiles where it is smaller (8 tokens).
+struct TileRange {
+  int tb, te;
+};
+__device__ __forceinline__ TileRange partition_tiles(int nb, int fb, int num_splits, int split,
+                                                     int block_size) {
+  const int upb = block_size > kTileTokens ? block_size / kTileTokens : 1;  // tiles per unit
+  const int units = (nb - fb + upb - 1) / upb;
+  const int per = (units + num_splits - 1) / num_splits * upb;
+  TileRange r;
+  r.tb = min(nb, fb + split * per);
+  r.te = min(nb, r.tb + per);
+  return r;
+}
+
+// Block-table entries behind tile j of a sequence's walk (row `table`, context
+// length L): e0 holds the tile's rows (16-token block j; first block j / 2 of a
+// 32-token pair of tiles; 8-token block 2j), e1 the second 8-token block 2j + 1
+// while it lies inside the row and holds a position < L (else kNoBlock).
+__device__ __forceinline__ void tile_entries(const int32_t *table, int j, int block_size,
+                                             int max_blocks, int L, int &e0, int &e1) {
+  e1 = kNoBlock;
+  if (block_size == 16) {
+    e0 = __ldg(table + j);
+  } else if (block_size == 32) {
+    e0 = __ldg(table + (j >> 1));
+  } else {
+    e0 = __ldg(table + 2 * j);
+    if (2 * j + 1 < max_blocks && j * kTileTokens + 8 < L) e1 = __ldg(table + 2 * j + 1);
+  }
+}
+
+// TMA box index (z of the cache's tensor map) of block `id` for KV head kvh;
+// sub = which 16-row half of a 32-token block.  -1 (outside the map: zero fill)
+// for kNoBlock, and for an id outside the pool, which is also reported.
+__device__ __forceinline__ int tile_box(int id, int sub, int kvh, int num_kv_heads, int num_blocks,
+                                        int block_size, unsigned *err) {
+  if (id == kNoBlock) return -1;
+  if (id < 0 || id >= num_blocks) {
+    record_error(err, kErrCheck);
+    return -1;
+  }
+  const int z = id * num_kv_heads + kvh;
+  return block_size == 32 ? 2 * z + sub : z;
+}
 
 // Longest-processing-time order: the sequence of rank `rank` when sequences are
 // sorted by context length, longest first (ties by index).  Every CTA computes
@@ -1230,16 +1286,15 @@ __global__ void __launch_bounds__(NW * 32)
   }
   const int row0 = blockIdx.y * RPC;
 
-  int nb = (L + kTileTokens - 1) / kTileTokens;
-  if (nb > a.max_blocks_per_seq) {  // context longer than its block table
+  const int bsz = a.block_size;
+  int nb = (L + kTileTokens - 1) / kTileTokens;  // tiles
+  if ((int64_t)L > (int64_t)a.max_blocks_per_seq * bsz) {  // context longer than its table
     if (threadIdx.x == 0 && split == 0 && kvh == 0 && blockIdx.y == 0 && crank == 0)
       record_error(a.err, kErrCheck);
-    nb = a.max_blocks_per_seq;
+    nb = min(nb, a.max_tiles);
   }
-  const int fb = min(nb, a.first_block);
-  const int per = (nb - fb + a.num_splits - 1) / a.num_splits;
-  const int tb = min(nb, fb + split * per);
-  const int te = min(nb, tb + per);
+  const TileRange part = partition_tiles(nb, min(nb, a.first_block), a.num_splits, split, bsz);
+  const int tb = part.tb, te = part.te;
   const int first_masked = (L - a.q_len + 1) / kTileTokens;  // tiles >= this need masking
   // base-2 score scale (times the K scale of an FP8 cache) and the V scale
   const float sscale = a.scale_log2 * (KV8 ? __ldg(a.k_scale + kvh) : 1.f);
@@ -1250,24 +1305,24 @@ __global__ void __launch_bounds__(NW * 32)
   // write identical bytes), then orders those generic-proxy stores before its own
   // TMA reads of the cache.
   if (a.k_new != nullptr && te > tb && te * kTileTokens > L - a.q_len) {
-    const int64_t num_slots = (int64_t)a.num_blocks * kTileTokens;
+    const int64_t num_slots = (int64_t)a.num_blocks * bsz;
     for (int idx = threadIdx.x; idx < a.q_len * (D / 8); idx += NW * 32) {
       const int u = idx / (D / 8), c = idx % (D / 8);
       const int pos = L - a.q_len + u;
       if (pos < 0) continue;
-      const int lb = pos / kTileTokens;
+      const int lb = pos / bsz;
       if (lb >= a.max_blocks_per_seq) {
         record_error(a.err, kErrCheck);
         continue;
       }
       const int64_t slot = (int64_t)__ldg(a.block_tables + (size_t)seq * a.max_blocks_per_seq + lb) *
-                               kTileTokens + pos % kTileTokens;
+                               bsz + pos % bsz;
       if (slot < 0 || slot >= num_slots) {
         record_error(a.err, kErrCheck);
         continue;
       }
-      const int64_t blk = slot / kTileTokens, off = slot % kTileTokens;
-      const size_t dst = (size_t)(((blk * a.num_kv_heads + kvh) * kTileTokens + off) * D + c * 8);
+      const int64_t blk = slot / bsz, off = slot % bsz;
+      const size_t dst = (size_t)(((blk * a.num_kv_heads + kvh) * bsz + off) * D + c * 8);
       const size_t src = ((size_t)(seq * a.q_len + u) * a.num_kv_heads + kvh) * D + c * 8;
       const uint4 kv = __ldg(reinterpret_cast<const uint4 *>(a.k_new + src));
       const uint4 vv = __ldg(reinterpret_cast<const uint4 *>(a.v_new + src));
@@ -1314,35 +1369,46 @@ __global__ void __launch_bounds__(NW * 32)
   };
   const int32_t *table = a.block_tables + (size_t)seq * a.max_blocks_per_seq;
   const uint32_t my_stages = smem_base + warp * NSTAGE * kStageBytes;
-  int tbl = 0;  // lane i holds the block id of tile n = window + i
+  // lane i holds the block-table entries of tile n = window + i
+  int tbl = 0, tbl2 = kNoBlock;
+  auto load_window = [&](int n0) {
+    if (n0 + lane < n_my)
+      tile_entries(table, tile_of(n0 + lane), bsz, a.max_blocks_per_seq, L, tbl, tbl2);
+  };
 
   auto issue = [&](int n) {
-    if ((n & 31) == 0 && n > 0) {
-      tbl = (n + lane < n_my) ? __ldg(table + tile_of(n + lane)) : 0;
-    }
-    const int phys = __shfl_sync(0xffffffffu, tbl, n & 31);
+    if ((n & 31) == 0 && n > 0) load_window(n);
+    const int e0 = __shfl_sync(0xffffffffu, tbl, n & 31);
+    const int e1 = __shfl_sync(0xffffffffu, tbl2, n & 31);
     if (lane == 0) {
       const int s = n % NSTAGE;
       const uint32_t bar = smem_u32(&bars[warp * NSTAGE + s]);
       const uint32_t kdst = my_stages + s * kStageBytes;
-      int z;
-      if (phys >= 0 && phys < a.num_blocks) {
-        z = phys * a.num_kv_heads + kvh;
-      } else {
-        record_error(a.err, kErrCheck);
-        z = -1;  // entirely outside the tensor map: TMA fills the tile with zeros
-      }
+      // boxes outside the tensor map (bad or missing blocks) arrive zero-filled
+      const int z0 = tile_box(e0, tile_of(n) & 1, kvh, a.num_kv_heads, a.num_blocks, bsz, a.err);
       mbar_arrive_expect_tx(bar, kStageBytes);
+      if (bsz == 8) {  // two 8-row boxes per tile: blocks 2j (rows 0-7) and 2j + 1
+        const int z1 = tile_box(e1, 0, kvh, a.num_kv_heads, a.num_blocks, bsz, a.err);
 #pragma unroll
-      for (int hh = 0; hh < kTileBytes / (kTileTokens * 128); ++hh) {
-        tma_load_3d(kdst + hh * (kTileTokens * 128), &kmap, hh * kBoxCols, 0, z, bar);
-        tma_load_3d(kdst + kTileBytes + hh * (kTileTokens * 128), &vmap, hh * kBoxCols, 0, z, bar);
+        for (int hh = 0; hh < kTileBytes / (kTileTokens * 128); ++hh) {
+          const uint32_t o = hh * (kTileTokens * 128);
+          tma_load_3d(kdst + o, &kmap, hh * kBoxCols, 0, z0, bar);
+          tma_load_3d(kdst + o + 8 * 128, &kmap, hh * kBoxCols, 0, z1, bar);
+          tma_load_3d(kdst + kTileBytes + o, &vmap, hh * kBoxCols, 0, z0, bar);
+          tma_load_3d(kdst + kTileBytes + o + 8 * 128, &vmap, hh * kBoxCols, 0, z1, bar);
+        }
+      } else {
+#pragma unroll
+        for (int hh = 0; hh < kTileBytes / (kTileTokens * 128); ++hh) {
+          tma_load_3d(kdst + hh * (kTileTokens * 128), &kmap, hh * kBoxCols, 0, z0, bar);
+          tma_load_3d(kdst + kTileBytes + hh * (kTileTokens * 128), &vmap, hh * kBoxCols, 0, z0, bar);
+        }
       }
     }
   };
 
   // the first block-table window and the q rows load concurrently
-  if (n_my > 0) tbl = (lane < n_my) ? __ldg(table + tile_of(lane)) : 0;
+  if (n_my > 0) load_window(0);
   Path path;
   path.init(a, seq, kvh, row0, L, sscale);
 

@@ -45,11 +45,13 @@ cudaError_t launch_decode8_bf16(const CUtensorMap &kmap, const CUtensorMap &vmap
                                 const DecodeArgs &args, bool partial, int units,
                                 cudaStream_t stream);
 // Many query rows per KV head (q_len above the decode kernel's limit, or the
-// shared-prefix pass of a cascade when args.shared_prefix > 0): 64 rows per CTA,
-// grid ([num_seqs x] num_splits x row blocks, num_kv_heads).
+// shared-prefix pass of a cascade when args.shared_prefix > 0): units of 128 query
+// rows of one KV head, walked by persistent CTAs (one per SM, at most
+// args.max_ctas when that is positive).  kv8: the cache holds e4m3 codes
+// (head_dim 128; fp16 names the type of q and out).
 cudaError_t launch_prefill(const CUtensorMap &kmap, const CUtensorMap &vmap, const CUtensorMap &qmap,
                            const DecodeArgs &args, int head_dim, bool fp16, bool partial,
-                           cudaStream_t stream);
+                           bool kv8, cudaStream_t stream);
 cudaError_t launch_combine_fp16(const CombineArgs &args, int head_dim, cudaStream_t stream);
 cudaError_t launch_combine_bf16(const CombineArgs &args, int head_dim, cudaStream_t stream);
 

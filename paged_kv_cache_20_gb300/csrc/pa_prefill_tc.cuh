@@ -44,6 +44,13 @@
 // read out before they announce that unit's first P.  bf16 P is split into hi + lo
 // bf16 parts, both multiplied by V, so that P keeps ~16 significant bits as the
 // fp16 path does.  Every wait is bounded.
+//
+// FP8 (e4m3) cache (KV8): the producers load each chunk's codes (128 positions x
+// 128 bytes) into the first half of a ring stage, then widen them in place to fp16
+// in the layout the 16-bit path loads (e4m3 is exact in fp16), and only then
+// release the stage to the MMA issuers; the MMAs run on fp16 operands.  Each KV
+// head's K scale goes into the score scale and its V scale into the output; a
+// bf16 q row is scaled into fp16 by a power of two that its score scale undoes.
 #pragma once
 
 #include "pa_decode.cuh"
@@ -57,6 +64,19 @@ constexpr int kTcBlocks = kTcChunk / kTileTokens;  // cache blocks per chunk
 constexpr int kTcCtl = 4;                          // K, V producers; P V and S issuers
 constexpr int kTcSoft = 8;                         // softmax warps
 constexpr int kTcThreads = 32 * (kTcCtl + kTcSoft);
+// Over an FP8 cache four more warps widen the codes (one per scheduler), and the
+// softmax warps come after them
+constexpr int kTcConv = 4;
+constexpr int kTcThreads8 = 32 * (kTcCtl + kTcConv + kTcSoft);
+// FP8 register split (setmaxnreg): the control and widening warpgroups give up
+// registers to the two softmax warpgroups.  2 x 128 x 112 + 2 x 128 x 144 =
+// 65 536 = 512 threads x 128, the registers the block is launched with (the
+// smallest split at which no region of the kernel spills).
+constexpr int kTcRegsLow8 = 112;
+constexpr int kTcRegsSoft8 = 144;
+constexpr int kTcRegsLaunch8 = 128;
+static_assert(2 * 128 * kTcRegsLow8 + 2 * 128 * kTcRegsSoft8 == kTcThreads8 * kTcRegsLaunch8,
+              "register split");
 constexpr float kTcRescale = 8.f;                  // base-2 growth that forces a rescale
 constexpr int kTcScrBytes = 32 * 64;               // epilogue scratch per softmax warp
 
@@ -146,7 +166,8 @@ struct TcGeo {
 struct TcUnit {
   int valid;
   int kvh, zseq, split, row_base, tseq;
-  int tb, te;      // the partition: blocks [tb, te) of the walked table row
+  int tb, te;      // the partition: 16-token tiles [tb, te) of the walked table row
+  int lwalk;       // positions of the walked row that hold tokens
   int t_end, nch;  // blocks any row of the unit sees, and the chunks covering them
   int vis_end;     // no row of the unit uses a position at or past it
   // the caller's row of the unit (row >= 0)
@@ -184,23 +205,24 @@ __device__ __forceinline__ TcUnit tc_unit(const DecodeArgs &a, const TcGeo &geo,
   t.row_base = (geo.nrb_n - 1 - rbi) * kTcRows;
   t.tseq = t.zseq;  // block-table row that is walked (row 0 for a shared prefix)
 
-  int nb;
+  int nb;  // tiles
   const int Lt = max(0, lens[t.tseq]);
   if (shared) {
-    nb = min(a.shared_prefix, a.max_blocks_per_seq);
+    nb = min(a.shared_prefix, a.max_tiles);
   } else {
     nb = (Lt + kTileTokens - 1) / kTileTokens;
-    if (nb > a.max_blocks_per_seq) {
+    if ((int64_t)Lt > (int64_t)a.max_blocks_per_seq * a.block_size) {
       if (rec && t.kvh == 0 && t.split == 0) record_error(a.err, kErrCheck);
-      nb = a.max_blocks_per_seq;
+      nb = min(nb, a.max_tiles);
     }
   }
-  // blocks before first_block belong to another pass (a cascade's shared prefix);
-  // the rest is cut into num_splits equal partitions
-  const int fb = shared ? 0 : min(nb, a.first_block);
-  const int per = (nb - fb + a.num_splits - 1) / a.num_splits;
-  t.tb = min(nb, fb + t.split * per);
-  t.te = min(nb, t.tb + per);
+  t.lwalk = shared ? nb * kTileTokens : Lt;
+  // tiles before first_block belong to another pass (a cascade's shared prefix);
+  // the rest is cut into num_splits partitions of whole blocks (or tiles)
+  const TileRange part = partition_tiles(nb, shared ? 0 : min(nb, a.first_block), a.num_splits,
+                                         t.split, a.block_size);
+  t.tb = part.tb;
+  t.te = part.te;
 
   // the largest causal limit of the unit's rows: its last row's (one sequence), or
   // the largest over the sequences whose rows it holds (shared prefix)
@@ -244,14 +266,68 @@ __device__ __forceinline__ TcUnit tc_unit(const DecodeArgs &a, const TcGeo &geo,
   return t;
 }
 
-template <typename T, int D, int NK, int NV, bool PARTIAL>
-__global__ void __launch_bounds__(kTcThreads, 1)
+template <bool B, class X, class Y> struct TcPick { using type = X; };
+template <class X, class Y> struct TcPick<false, X, Y> { using type = Y; };
+
+__device__ __forceinline__ void sts128(uint32_t addr, const uint4 v) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z),
+               "r"(v.w)
+               : "memory");
+}
+
+// Widen the e4m3 codes of `rows` positions of a chunk in place, from position r0
+// (one warp).  The codes of position r
+// sit in bytes [128 r, 128 r + 128) of the stage, 16-byte chunk c (dims 16c ..
+// 16c + 15) at chunk position c ^ (r % 8), as TMA writes them with the 128-byte
+// swizzle.  The fp16 result takes the 16-bit tile layout: dims 64h .. 64h + 63 of
+// position r in bytes [h * 16384 + 128 r, +128), 16-byte chunk c' at c' ^ (r % 8).
+// Lane l widens positions r0 + l, r0 + l + 32, ...: it reads a position's eight
+// chunks before it writes over them, and no other lane touches that position, so
+// no synchronisation is needed inside the loop.  Every 8 lanes of a shared-memory
+// phase hit 8 distinct 16-byte bank groups (r % 8 differs between them).
+__device__ __forceinline__ void tc_widen_e4m3_rows(uint32_t st, int r0, int rows, int lane) {
+#pragma unroll 1
+  for (int k = 0; k < rows / 32; ++k) {
+    const int r = r0 + 32 * k + lane;
+    const uint32_t src = st + r * 128;
+    // dims 64 .. 127 first: they go to the second half, which holds no codes; then
+    // dims 0 .. 63, all four chunks read before the first write over the codes row
+#pragma unroll
+    for (int h = 1; h >= 0; --h) {
+      uint4 v[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) v[i] = lds128(src + (((4 * h + i) ^ (r & 7)) << 4));
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        uint4 lo, hi;
+        lo.x = e4m3_lo_f16x2(v[i].x);
+        lo.y = e4m3_hi_f16x2(v[i].x);
+        lo.z = e4m3_lo_f16x2(v[i].y);
+        lo.w = e4m3_hi_f16x2(v[i].y);
+        hi.x = e4m3_lo_f16x2(v[i].z);
+        hi.y = e4m3_hi_f16x2(v[i].z);
+        hi.z = e4m3_lo_f16x2(v[i].w);
+        hi.w = e4m3_hi_f16x2(v[i].w);
+        const uint32_t row = st + h * (kTcChunk * 128) + r * 128;
+        sts128(row + (((2 * i) ^ (r & 7)) << 4), lo);
+        sts128(row + (((2 * i + 1) ^ (r & 7)) << 4), hi);
+      }
+    }
+  }
+}
+
+template <typename T, int D, int NK, int NV, bool PARTIAL, bool KV8 = false>
+__global__ void __launch_bounds__(KV8 ? kTcThreads8 : kTcThreads, 1)
     paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
                             const __grid_constant__ CUtensorMap vmap,
                             const __grid_constant__ CUtensorMap qmap, const DecodeArgs a) {
-  using Lay = TcLayout<T, D>;
+  // MMA operand type: fp16 over an FP8 cache (codes widened; q converted), else T
+  using TM = typename TcPick<KV8, __half, T>::type;
+  using Lay = TcLayout<TM, D>;
   constexpr int H = Lay::kHalves;
-  constexpr bool kBf16 = Elt<T>::kMantBits < 10;
+  constexpr bool kBf16 = Elt<TM>::kMantBits < 10;
+  static_assert(!KV8 || D == 128, "FP8 cache: head_dim 128");
+  constexpr int kSoft0 = KV8 ? kTcCtl + kTcConv : kTcCtl;  // first softmax warp
   constexpr int kOCols = D / 2;  // O columns per softmax warp
   static_assert(NK >= 2 && NV >= 2, "ring depth");
   static_assert(D == 64 || D == 128, "head_dim");
@@ -261,6 +337,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   __shared__ __align__(8) uint64_t k_empty[NK];
   __shared__ __align__(8) uint64_t v_full[NV];
   __shared__ __align__(8) uint64_t v_empty[NV];
+  __shared__ __align__(8) uint64_t k_land[NK];   // FP8: the codes have landed (TMA)
+  __shared__ __align__(8) uint64_t v_land[NV];
   __shared__ __align__(8) uint64_t s_full[3];
   __shared__ __align__(8) uint64_t p_full;
   __shared__ __align__(8) uint64_t p_ack;        // the MMA thread has taken P_j
@@ -312,13 +390,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   }
   if (threadIdx.x == 0) {
     s_failed = 0;
+    // over an FP8 cache a stage is full once both of its widening warps are done
     for (int s = 0; s < NK; ++s) {
-      mbar_init(smem_u32(&k_full[s]), 1);
+      mbar_init(smem_u32(&k_full[s]), KV8 ? 2 : 1);
       mbar_init(smem_u32(&k_empty[s]), 1);
+      mbar_init(smem_u32(&k_land[s]), 1);
     }
     for (int s = 0; s < NV; ++s) {
-      mbar_init(smem_u32(&v_full[s]), 1);
+      mbar_init(smem_u32(&v_full[s]), KV8 ? 2 : 1);
       mbar_init(smem_u32(&v_empty[s]), 1);
+      mbar_init(smem_u32(&v_land[s]), 1);
     }
     for (int b = 0; b < 3; ++b) mbar_init(smem_u32(&s_full[b]), 1);
     mbar_init(smem_u32(&p_full), kTcSoft);
@@ -347,6 +428,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   volatile int *failed = &s_failed;
   TcGeo geo;
   geo.init(a);
+  if constexpr (KV8) {
+    // warpgroups 0 (producers, issuers) and 1 (widening) give registers to 2 and 3
+    // (softmax); every warp of a warpgroup executes the same instruction
+    if (warp < kSoft0)
+      asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kTcRegsLow8));
+    else
+      asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kTcRegsSoft8));
+  }
 
   if (warp < 2) {
     // ------------------------------------------------------------ TMA producers
@@ -355,6 +444,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const uint32_t ring = is_k ? sK : sV;
     uint64_t *full = is_k ? k_full : v_full;
     uint64_t *empty = is_k ? k_empty : v_empty;
+    // the barrier the loads complete on: over an FP8 cache the codes land first and
+    // the widening warps announce the stage (full)
+    uint64_t *land = KV8 ? (is_k ? k_land : v_land) : full;
     const int NS = is_k ? NK : NV;
     int g = 0, issued = 0;  // chunks of this CTA so far (all units), loads issued
     bool ok = true;
@@ -362,12 +454,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const TcUnit t = tc_unit(a, geo, k, s_order, lens, lane, -1, is_k && lane == 0);
       if (!t.valid) break;
       const int32_t *table = a.block_tables + (size_t)t.tseq * a.max_blocks_per_seq;
-      // block-table window: lane l holds entry tb + 32w + l of window w (4 chunks);
-      // the next window is loaded a whole window ahead, so no TMA issue waits on a
-      // table load
+      // block-table window (16-token blocks: a block is a tile): lane l holds entry
+      // tb + 32w + l of window w (4 chunks); the next window is loaded a whole window
+      // ahead, so no TMA issue waits on a table load.  Other block sizes read their
+      // entries per chunk.
       auto table_at = [&](int w) -> int {
         const int blk = t.tb + 32 * w + lane;
-        return blk < t.t_end ? __ldg(table + blk) : -1;
+        return (a.block_size == 16 && blk < t.t_end) ? __ldg(table + blk) : -1;
       };
       int win_cur = 0, win_nxt = 0;
       if (t.nch > 0) {
@@ -392,22 +485,35 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
           break;
         }
-        const int blk = t.tb + ch * kTcBlocks + lane;
+        // lane l loads tile tb + 8 ch + l of the chunk (16-token blocks: the window's
+        // entry; 32-token blocks: half l % 2 of a block), or with 8-token blocks the
+        // 8-row box of block 2 (tb + 8 ch) + l.  z stays -1 (zero fill) past the walk.
+        const int bsz = a.block_size;
+        const int tile = t.tb + ch * kTcBlocks + (bsz == 8 ? (lane >> 1) : lane);
         const int phys = __shfl_sync(0xffffffffu, win_cur, ((ch & 3) * kTcBlocks + lane) & 31);
         int z = -1;  // outside the tensor map: zero fill
-        if (lane < kTcBlocks && blk < t.t_end) {
-          if (phys >= 0 && phys < a.num_blocks)
-            z = phys * a.num_kv_heads + t.kvh;
-          else if (is_k)
-            record_error(a.err, kErrCheck);
+        if (lane < (bsz == 8 ? 2 * kTcBlocks : kTcBlocks) && tile < t.t_end) {
+          int id = phys;
+          if (bsz == 32) {
+            id = __ldg(table + (tile >> 1));
+          } else if (bsz == 8) {
+            const int blk = 2 * tile + (lane & 1);
+            id = (blk < a.max_blocks_per_seq && blk * 8 < t.lwalk) ? __ldg(table + blk) : kNoBlock;
+          }
+          z = tile_box(id, tile & 1, t.kvh, a.num_kv_heads, a.num_blocks, bsz, a.err);
         }
-        const uint32_t bar = smem_u32(&full[s]);
-        if (lane == 0) mbar_arrive_expect_tx(bar, Lay::kKVBytes);
+        const uint32_t bar = smem_u32(&land[s]);
+        if (lane == 0) mbar_arrive_expect_tx(bar, KV8 ? Lay::kKVBytes / 2 : Lay::kKVBytes);
         __syncwarp();
-        if (lane < kTcBlocks) {
-          const uint32_t dst = ring + s * Lay::kKVBytes + lane * (kTileTokens * 128);
+        const int box_rows = bsz == 8 ? 8 : kTileTokens;
+        if (lane < kTcChunk / box_rows) {
+          const uint32_t dst = ring + s * Lay::kKVBytes + lane * (box_rows * 128);
+          if constexpr (KV8) {
+            tma_load_3d(dst, map, 0, 0, z, bar);  // box_rows positions x 128 codes
+          } else {
 #pragma unroll
-          for (int hh = 0; hh < H; ++hh) tma_load_3d(dst + hh * (kTcChunk * 128), map, hh * 64, 0, z, bar);
+            for (int hh = 0; hh < H; ++hh) tma_load_3d(dst + hh * (kTcChunk * 128), map, hh * 64, 0, z, bar);
+          }
         }
         issued = gg + 1;
       }
@@ -416,7 +522,42 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // the last loads have landed before the CTA may exit (bounded; at once unless a
     // consumer gave up)
     for (int k = max(0, issued - NS); k < issued; ++k)
-      (void)mbar_wait_bounded(smem_u32(&full[k % NS]), (k / NS) & 1);
+      (void)mbar_wait_bounded(smem_u32(&land[k % NS]), (k / NS) & 1);
+  } else if (KV8 && warp >= kTcCtl && warp < kSoft0) {
+    // ------------------------------------------------------------ FP8 widening
+    // warps 4, 5: K positions [0, 64) and [64, 128) of every chunk; 6, 7: V
+    const int cw = warp - kTcCtl;
+    const bool is_k = cw < 2;
+    const int r0 = (cw & 1) * (kTcChunk / 2);
+    const uint32_t ring = is_k ? sK : sV;
+    uint64_t *land = is_k ? k_land : v_land;
+    uint64_t *full = is_k ? k_full : v_full;
+    const int NS = is_k ? NK : NV;
+    int g = 0;
+    bool ok = true;
+    for (int k = 0; ok; ++k) {
+      const TcUnit t = tc_unit(a, geo, k, s_order, lens, lane, -1, false);
+      if (!t.valid) break;
+      for (int ch = 0; ch < t.nch; ++ch) {
+        const int gg = g + ch;
+        const int s = gg % NS;
+        bool w = mbar_wait_bounded(smem_u32(&land[s]), (gg / NS) & 1);
+        w = __all_sync(0xffffffffu, w);
+        if (!w || *failed) {
+          ok = false;
+          if (!w && lane == 0) {
+            record_error(a.err, kErrTimeout);
+            atomicExch(&s_failed, 1);
+          }
+          break;
+        }
+        tc_widen_e4m3_rows(ring + s * Lay::kKVBytes, r0, kTcChunk / 2, lane);
+        fence_proxy_async_smem();  // the fp16 rows visible to the tensor core
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&full[s]));
+      }
+      g += t.nch;
+    }
   } else if (warp == 2 || warp == 3) {
     // ------------------------------------------------------------ MMA issue
     // bit 13 of the instruction descriptor negates A (Q): S = -Q K^T for a negative scale
@@ -466,6 +607,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           ok = wait_all(&q_ready, qn & 1);
           if (!ok) break;
         }
+        // over an FP8 cache the scores carry the unit's K scale; a negative one
+        // negates Q K^T as a negative softmax scale does
+        uint32_t idS = kIdS;
+        if (KV8 && __ldg(a.k_scale + t.kvh) < 0.f) idS ^= 1u << 13;
         for (int j = 0; ok && j < t.nch; ++j) {
           const int gg = g + j;
           ok = wait_all(&k_full[gg % NK], (gg / NK) & 1);
@@ -482,7 +627,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
               // a K step of 16 columns: +32 bytes inside the 128-byte row, +one
               // column-group block every 4 steps (descriptor addresses count 16 bytes)
               tc::mma_f16(dst, dQ + (uint64_t)(((kk >> 2) * (kTcRows * 128) + (kk & 3) * 32) >> 4),
-                          kd + (uint64_t)(((kk >> 2) * (kTcChunk * 128) + (kk & 3) * 32) >> 4), kIdS,
+                          kd + (uint64_t)(((kk >> 2) * (kTcChunk * 128) + (kk & 3) * 32) >> 4), idS,
                           kk > 0 ? 1u : 0u);
             }
             tc::commit(smem_u32(&s_full[gg % 3]));
@@ -540,13 +685,24 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     (void)mbar_wait_bounded(smem_u32(&mma_fin), 0);
   } else {
     // ------------------------------------------------------------ softmax rows
-    const int hc = (warp - kTcCtl) >> 2;  // column half of this warp
+    const int hc = (warp - kSoft0) >> 2;  // column half of this warp
     const int q4 = warp & 3;              // lane group (TMEM access rule)
     const int row = 32 * q4 + lane;       // = TMEM lane
     const uint32_t trow = tmem + ((uint32_t)(32 * q4) << 16);
-    const int tid = (warp - kTcCtl) * 32 + lane;  // 0..255
-    const float rs = a.scale_log2;
-    const uint64_t rs2 = tc::f2pack(rs, rs);
+    const int tid = (warp - kSoft0) * 32 + lane;  // 0..255
+    // base-2 score scale of this thread's row (positive; see the host), per unit
+    // over an FP8 cache: |K scale| and the row's q exponent folded in
+    float rs = a.scale_log2;
+    uint64_t rs2 = tc::f2pack(rs, rs);
+    float vs_u = 1.f;  // the unit's V scale (FP8 cache)
+    auto unit_scales = [&](const TcUnit &t, int e_row) {
+      if constexpr (KV8) {
+        const float r = a.scale_log2 * fabsf(__ldg(a.k_scale + t.kvh)) * ldexpf(1.f, e_row);
+        rs = r > 0.f ? r : 1e-30f;
+        rs2 = tc::f2pack(rs, rs);
+        vs_u = __ldg(a.v_scale + t.kvh);
+      }
+    };
     bool ok = true;
     int xph = 0;  // exchanges done (phase of xbar[q4])
     // max (or, at the end, sum) of this warp's value and the partner warp's
@@ -567,14 +723,45 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                       : nullptr;
     };
     // Q row -> shared memory in the swizzled K-major layout of the MMA's A operand
-    // (each warp of the pair writes half of the row's 16-byte chunks)
-    auto write_q = [&](const TcUnit &t) {
+    // (each warp of the pair writes half of the row's 16-byte chunks).  Over an FP8
+    // cache a bf16 row goes in as fp16 scaled by 2^-e, e the exponent of its largest
+    // magnitude (both warps of the row find the same e); returns e.
+    auto write_q = [&](const TcUnit &t) -> int {
       const T *qrow = q_ptr(t);
+      constexpr bool kConv = KV8 && Elt<T>::kMantBits < 10;
+      int e_row = 0;
+      float down = 1.f;
+      if constexpr (kConv) {
+        float mx = 0.f;
+        if (qrow) {
+#pragma unroll 4
+          for (int c = 0; c < D / 8; ++c) {
+            const uint4 v = __ldg(reinterpret_cast<const uint4 *>(qrow) + c);
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const float2 f = Elt<T>::to_f2(w[i]);
+              mx = fmaxf(mx, fmaxf(fabsf(f.x), fabsf(f.y)));
+            }
+          }
+        }
+        e_row = (mx > 0.f && isfinite(mx)) ? ilogbf(mx) : 0;
+        down = ldexpf(1.f, -e_row);  // |q| * down < 2: well inside fp16
+      }
 #pragma unroll
       for (int ci = 0; ci < D / 16; ++ci) {
         const int c = hc * (D / 16) + ci;
         uint4 v = make_uint4(0u, 0u, 0u, 0u);
         if (qrow) v = __ldg(reinterpret_cast<const uint4 *>(qrow) + c);
+        if constexpr (kConv) {
+          uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float2 f = Elt<T>::to_f2(w[i]);
+            w[i] = Elt<__half>::from_f2(f.x * down, f.y * down);
+          }
+          v = make_uint4(w[0], w[1], w[2], w[3]);
+        }
         const int hh = c >> 3, cc = c & 7;
         const uint32_t addr = base + hh * (kTcRows * 128) + row * 128 + ((cc ^ (row & 7)) << 4);
         asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y),
@@ -584,6 +771,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&q_ready));
+      return e_row;
     };
 
     // ---- epilogue of a finished unit: O / l (or the unnormalised partial and its
@@ -591,8 +779,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // through its shared-memory scratch, so that a store instruction writes 64-byte
     // pieces of 8 rows instead of 16 bytes of 32 rows (32 lines an instruction).
     // roff: the row's output (or workspace) row, -1 for padding rows.
-    const uint32_t scr = sScr + (uint32_t)(warp - kTcCtl) * kTcScrBytes;
-    auto epilogue = [&](bool have, int gl, float sc, float m_fin, long long roff) -> bool {
+    const uint32_t scr = sScr + (uint32_t)(warp - kSoft0) * kTcScrBytes;
+    // sc multiplies O on the way out (1 / l, with the V scale of an FP8 cache); a
+    // partial's O is multiplied by ovs (the V scale) and sc is its l
+    auto epilogue = [&](bool have, int gl, float sc, float m_fin, long long roff, float ovs) -> bool {
       if (have) {
         // the unit's last P V (and with it every earlier one) has completed; the next
         // P V to commit to that barrier needs a P this warp has not announced yet
@@ -620,7 +810,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           uint32_t wv[16];
           if constexpr (PARTIAL) {
 #pragma unroll
-            for (int i = 0; i < 16; ++i) wv[i] = __float_as_uint(o[16 * h2 + i]);
+            for (int i = 0; i < 16; ++i) wv[i] = __float_as_uint(o[16 * h2 + i] * ovs);
           } else {
 #pragma unroll
             for (int i = 0; i < 16; ++i) wv[i] = Elt<T>::from_f2(o[2 * i] * sc, o[2 * i + 1] * sc);
@@ -659,17 +849,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // a finished unit whose epilogue waits for the next unit's first chunk
     bool pend = false;
     int pend_gl = 0;
-    float pend_sc = 0.f, pend_m = 0.f;
+    float pend_sc = 0.f, pend_m = 0.f, pend_vs = 1.f;
     long long pend_roff = -1;
 
     int g = 0;   // chunks of this CTA so far (all units)
     int qn = 0;  // Q buffers written (without TMA)
+    int e_cur = 0, e_next = 0;  // the row's q exponent (FP8 cache, bf16 q), this unit and next
     TcUnit cu = tc_unit(a, geo, 0, s_order, lens, lane, row, false);
     if (!a.q_tma && cu.valid && cu.nch > 0) {
-      write_q(cu);
+      e_cur = write_q(cu);
       qn = 1;
     }
     for (int k = 0; ok && cu.valid; ++k) {
+      unit_scales(cu, e_cur);
       const int lim_row = cu.rvalid ? min(cu.vis, cu.te * kTileTokens) : 0;  // padding rows: 0
       float m_run = -INFINITY, l = 0.f;
       for (int j = 0; j < cu.nch; ++j) {
@@ -735,18 +927,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
               tc::f2unpack(tc::ffma2(hh, tc::f2pack(-1.f, -1.f), pp), sv[2 * e], sv[2 * e + 1]);
               ps2[e & 1] = tc::fadd2(ps2[e & 1], pp);
             } else {
-              hw[e] = Elt<T>::from_f2(p0, p1);
+              hw[e] = Elt<TM>::from_f2(p0, p1);
               // the sum of the rounded weights P V is taken with: the quotient O / l
               // is then an exact convex combination of V rows (a dominant weight's
               // rounding cancels)
-              const float2 hf = Elt<T>::to_f2(hw[e]);
+              const float2 hf = Elt<TM>::to_f2(hw[e]);
               ps2[e & 1] = tc::fadd2(ps2[e & 1], tc::f2pack(hf.x, hf.y));
             }
           }
           tc::st32u(ts, hw);
           if constexpr (Lay::kSplitP) {
 #pragma unroll
-            for (int e = 0; e < 32; ++e) hw[e] = Elt<T>::from_f2(sv[2 * e], sv[2 * e + 1]);
+            for (int e = 0; e < 32; ++e) hw[e] = Elt<TM>::from_f2(sv[2 * e], sv[2 * e + 1]);
             tc::st32u(ts + 32, hw);
           }
         }
@@ -788,7 +980,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           // the previous unit's epilogue: its last P V has been completing under this
           // chunk's softmax.  This unit's first P V overwrites O, and is announced
           // only below.
-          if (!epilogue(true, pend_gl, pend_sc, pend_m, pend_roff)) {
+          if (!epilogue(true, pend_gl, pend_sc, pend_m, pend_roff, pend_vs)) {
             ok = false;
             break;
           }
@@ -833,6 +1025,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       // the next unit's Q (without TMA) goes in while this unit's P V drains: its
       // buffer is free once this unit's last S MMA has completed
       const TcUnit nu = tc_unit(a, geo, k + 1, s_order, lens, lane, row, false);
+      e_next = 0;
       if (!a.q_tma && nu.valid && nu.nch > 0) {
         if (qn > 0) {
           bool w = mbar_wait_bounded(smem_u32(&q_free), (qn - 1) & 1);
@@ -842,7 +1035,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             break;
           }
         }
-        write_q(nu);
+        e_next = write_q(nu);
         ++qn;
       }
 
@@ -858,27 +1051,29 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (!ok) break;
         pend = true;
         pend_gl = g + cu.nch - 1;
-        pend_sc = PARTIAL ? l : (l > 0.f ? 1.f / l : 0.f);
+        pend_sc = PARTIAL ? l : (l > 0.f ? vs_u / l : 0.f);
         pend_m = m_run;
+        pend_vs = vs_u;
         pend_roff = roff;
       } else {
         // no position in this unit's partition: zeros (empty statistics)
         if (pend) {
-          if (!epilogue(true, pend_gl, pend_sc, pend_m, pend_roff)) {
+          if (!epilogue(true, pend_gl, pend_sc, pend_m, pend_roff, pend_vs)) {
             ok = false;
             break;
           }
           pend = false;
         }
-        if (!epilogue(false, 0, 0.f, 0.f, roff)) {
+        if (!epilogue(false, 0, 0.f, 0.f, roff, 1.f)) {
           ok = false;
           break;
         }
       }
       g += cu.nch;
       cu = nu;
+      e_cur = e_next;
     }
-    if (ok && pend) ok = epilogue(true, pend_gl, pend_sc, pend_m, pend_roff);
+    if (ok && pend) ok = epilogue(true, pend_gl, pend_sc, pend_m, pend_roff, pend_vs);
     if (!ok && lane == 0) {
       record_error(a.err, kErrTimeout);
       atomicExch(&s_failed, 1);

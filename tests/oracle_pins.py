@@ -231,6 +231,22 @@ def pin_paging_invariance(o):
         assert np.array_equal(got, ref)
 
 
+def pin_block_size_invariance(o):
+    """The same logical sequences in pools of 8-, 16- and 32-token blocks (random
+    physical order) attend to bit-identical results, and equal torch SDPA: the
+    block size only changes where the rows live ([PANO] §2.3: block_size is a
+    parameter of the pool)."""
+    lens = [1, 7, 8, 9, 31, 33, 64, 70]
+    q, K, V = _rand_case(61, len(lens), 6, 2, 32, BF16, lens, q_len=1)
+    scale = float(np.float32(0.19))   # the oracle takes the scale as a float
+    ref = Paged(o, K, V, 16, BF16, perm_seed=3).decode(o, q, scale)
+    for bs in (8, 32):
+        got = Paged(o, K, V, bs, BF16, perm_seed=4).decode(o, q, scale)
+        assert np.array_equal(got, ref), bs
+    for i in range(len(lens)):
+        assert np.abs(ref[i] - _sdpa(q[i], K[i], V[i], scale, BF16, 1)).max() < 1e-12, i
+
+
 def pin_context_one_returns_v(o):
     for dtype in (FP16, BF16):
         q, K, V = _rand_case(7, 2, 4, 4, 64, dtype, [1, 1], qscale=3.0)

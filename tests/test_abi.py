@@ -87,7 +87,7 @@ def _decode(lib, **kw):
     ({"out": None}, -1), ({"q": None}, -1), ({"k": None}, -1), ({"bt": None}, -1),
     ({"n": 0}, -1), ({"hq": 6, "hkv": 4}, -1), ({"hkv": 0}, -1), ({"qlen": 0}, -1),
     ({"maxb": 0}, -1), ({"nblocks": -1}, -1), ({"q": FAKE + 2}, -1), ({"out": FAKE + 8}, -1),
-    ({"scale": float("nan")}, -1), ({"d": 96}, -2), ({"d": 256}, -2), ({"bs": 32}, -2),
+    ({"scale": float("nan")}, -1), ({"d": 96}, -2), ({"d": 256}, -2), ({"bs": 24}, -2), ({"bs": 4}, -2),
     ({"qlen": 4097}, -2), ({"dtype": 5}, -2), ({"nblocks": 1 << 30, "hkv": 4, "hq": 4}, -1),
 ])
 def test_decode_rejects_bad_arguments(lib, kw, status):
@@ -112,13 +112,15 @@ def test_append_and_slot_mapping_reject_bad_arguments(lib):
     assert lib.pa_append_kv(FAKE, FAKE, FAKE, FAKE, FAKE, -1, 2, 128, 16, 8, 0, None) == -1
     assert lib.pa_append_kv(FAKE, FAKE, FAKE + 4, FAKE, FAKE, 4, 2, 128, 16, 8, 0, None) == -1
     assert lib.pa_append_kv(FAKE, FAKE, FAKE, FAKE, FAKE, 4, 2, 80, 16, 8, 0, None) == -2
-    assert lib.pa_append_kv(FAKE, FAKE, FAKE, FAKE, FAKE, 4, 2, 128, 8, 8, 0, None) == -2
+    assert lib.pa_append_kv(FAKE, FAKE, FAKE, FAKE, FAKE, 4, 2, 128, 24, 8, 0, None) == -2
+    for bs in (8, 16, 32):  # the block sizes the kernels take (nothing to append: no launch)
+        assert lib.pa_append_kv(FAKE, FAKE, FAKE, FAKE, FAKE, 0, 2, 128, bs, 8, 0, None) == 0
     assert lib.pa_append_kv(FAKE, FAKE, FAKE, FAKE, FAKE, 4, 2, 128, 16, 8, 3, None) == -2
     assert lib.pa_append_kv(FAKE, FAKE, FAKE, FAKE, FAKE, 0, 2, 128, 16, 8, 0, None) == 0
     assert lib.pa_slot_mapping(None, FAKE, FAKE, 2, 4, 16, 1, None) == -1
     assert lib.pa_slot_mapping(FAKE, FAKE, FAKE, 0, 4, 16, 1, None) == -1
     assert lib.pa_slot_mapping(FAKE, FAKE, FAKE, 2, 4, 16, 0, None) == -1
-    assert lib.pa_slot_mapping(FAKE, FAKE, FAKE, 2, 4, 32, 1, None) == -2
+    assert lib.pa_slot_mapping(FAKE, FAKE, FAKE, 2, 4, 24, 1, None) == -2
 
 
 def test_product_and_oracle_share_nothing():

@@ -44,7 +44,7 @@ def gpu_step(pa, w, num_splits=1, fused=True):
                          d["block_tables"], d["context_lens"], w.scale, c.q_len, num_splits,
                          k_new=d["k_new"], v_new=d["v_new"])
     else:
-        slots = pa.pa_slot_mapping(d["block_tables"], d["context_lens"], 16, c.q_len)
+        slots = pa.pa_slot_mapping(d["block_tables"], d["context_lens"], c.block_size, c.q_len)
         pa.pa_append_kv_fp8(d["k_cache"], d["v_cache"], d["k_new"], d["v_new"], slots,
                             d["k_scale"], d["v_scale"])
         pa.pa_decode_fp8(out, d["q"], d["k_cache"], d["v_cache"], d["k_scale"], d["v_scale"],
@@ -57,7 +57,7 @@ def gpu_step(pa, w, num_splits=1, fused=True):
 def oracle_step(orc, w, rows=None, threads=os.cpu_count() or 1):
     c = w.cfg
     kc, vc = w.bits("k_cache").copy(), w.bits("v_cache").copy()
-    slots = orc.slot_mapping(w.block_tables.numpy(), w.context_lens.numpy(), 16, c.q_len)
+    slots = orc.slot_mapping(w.block_tables.numpy(), w.context_lens.numpy(), c.block_size, c.q_len)
     orc.append_kv_fp8(kc, vc, w.bits("k_new"), w.bits("v_new"), slots, c.dtype,
                       w.k_scale.numpy(), w.v_scale.numpy())
     out = orc.decode_fp8(w.bits("q"), kc, vc, w.k_scale.numpy(), w.v_scale.numpy(),
@@ -91,10 +91,17 @@ SMALL = [("llama7b_mha_fp8", {"num_seqs": 3}), ("gqa_fp8", {"num_seqs": 5}),
                               "dtype": "bf16"}),                                 # 32 rows
          ("gqa_fp8", {"num_seqs": 4, "q_len": 2, "dtype": "fp16"}),             # 8 rows, causal
          ("gqa_fp8", {"num_seqs": 5, "num_q_heads": 12, "num_kv_heads": 4}),    # 3 rows
-         # more than 16 rows per KV head: row groups of 16 on the decode kernel
+         # more than 16 rows per KV head: the tensor-core many-row kernel, the codes
+         # widened to fp16 in shared memory; a bf16 q is converted (row-scaled) by
+         # the softmax threads, an fp16 one arrives by TMA when the group divides 128
          ("gqa_fp8", {"num_seqs": 3, "q_len": 40, "lens": ("fixed", (40, 300, 1000))}),
          ("llama7b_mha_fp8", {"num_seqs": 2, "q_len": 24, "num_q_heads": 8,
-                              "num_kv_heads": 8, "lens": ("fixed", (30, 700))})]
+                              "num_kv_heads": 8, "lens": ("fixed", (30, 700))}),
+         ("gqa_fp8", {"num_seqs": 3, "q_len": 100, "dtype": "fp16",
+                      "lens": ("fixed", (100, 357, 1500))}),                  # q by TMA
+         ("gqa_fp8", {"num_seqs": 2, "q_len": 64, "num_q_heads": 10, "num_kv_heads": 2,
+                      "lens": ("fixed", (64, 900))}),                          # g = 5
+         ("chunked_prefill_fp8", {"num_seqs": 2, "q_len": 130, "lens": ("fixed", (130, 2000))})]
 
 
 @pytest.mark.parametrize("fused", [False, True], ids=["separate", "fused"])
@@ -114,10 +121,11 @@ def test_fp8_small_every_element(pa, orc, name, over, splits, fused):
 # 96 GQA sequences (768 units) take the 4-warp form.
 FULL = [("llama7b_mha_fp8", {}), ("gqa_fp8", {}),
         ("llama7b_mha_fp8", {"q_len": 4, "pool_blocks": None}),
-        ("gqa_fp8", {"num_seqs": 96, "pool_blocks": None})]
+        ("gqa_fp8", {"num_seqs": 96, "pool_blocks": None}),
+        ("chunked_prefill_fp8", {})]
 
 
-@pytest.mark.parametrize("name,over", FULL, ids=["7b", "gqa", "7b-q4", "gqa-96"])
+@pytest.mark.parametrize("name,over", FULL, ids=["7b", "gqa", "7b-q4", "gqa-96", "chunked"])
 def test_fp8_full_size_every_element(pa, orc, name, over):
     w = workloads.make(name, **over)
     out, d = gpu_step(pa, w)
@@ -135,3 +143,40 @@ def test_fp8_edge_lengths(pa, orc):
         out, d = gpu_step(pa, w, splits)
         ref, kc, vc = oracle_step(orc, w)
         _tol.check(_f64(out), ref, "bf16", f"edges splits {splits}")
+
+
+@pytest.mark.parametrize("splits", [1, 3])
+def test_fp8_many_rows_edge_lengths(pa, orc, splits):
+    """33 query rows per sequence (132 per KV head: the many-row kernel) over contexts
+    shorter than, equal to and longer than q_len, empty ones included."""
+    cfg = workloads.config("gqa_fp8", num_seqs=9, q_len=33,
+                           lens=("fixed", (0, 1, 3, 15, 16, 17, 33, 100, 257)), spare_blocks=3)
+    w = workloads.make(cfg)
+    out, d = gpu_step(pa, w, splits)
+    ref, kc, vc = oracle_step(orc, w)
+    assert np.array_equal(d["k_cache"].cpu().numpy(), kc)
+    _tol.check(_f64(out), ref, "bf16", f"many-row edges splits {splits}")
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+def test_fp8_many_rows_scales_and_q_magnitudes(pa, orc, dtype):
+    """The many-row kernel folds each KV head's K scale into the score scale (a
+    negative one negates the scores) and its V scale into the output, and scales
+    each q row into fp16 by a power of two: negative, tiny and zero scales, and q
+    rows of very different magnitudes."""
+    w = workloads.make("gqa_fp8", num_seqs=3, q_len=40, dtype=dtype,
+                       lens=("fixed", (40, 333, 1200)))
+    ks, vs = w.k_scale.clone(), w.v_scale.clone()
+    ks[0], ks[1], ks[2] = -ks[0], 1e-7, 0.0
+    vs[3], vs[4] = -vs[3], 0.0
+    w.k_scale.copy_(ks)
+    w.v_scale.copy_(vs)
+    q = w.q.float()
+    q[0] *= 300.0 if dtype == "bf16" else 30.0      # large rows (bf16: scaled into fp16)
+    q[1, :, :4] *= 1e-3                              # small rows
+    w.q.copy_(q.to(w.q.dtype))
+    out, d = gpu_step(pa, w)
+    ref, kc, vc = oracle_step(orc, w)
+    assert np.array_equal(d["k_cache"].cpu().numpy(), kc)
+    assert np.array_equal(d["v_cache"].cpu().numpy(), vc)
+    _tol.check(_f64(out), ref, dtype, f"scales and magnitudes {dtype}")

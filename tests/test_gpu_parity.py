@@ -120,7 +120,8 @@ def test_full_size_every_element(pa, orc, name, over, fused):
     ref, kc, vc, slots = full_oracle(orc, (name, repr(over)), w)
     _tol.check(_f64(out), ref, w.cfg.dtype, f"{name} {over}")
     # slot mapping and the appended rows, bit for bit
-    gslots = pa.pa_slot_mapping(d["block_tables"], d["context_lens"], 16, w.cfg.q_len)
+    gslots = pa.pa_slot_mapping(d["block_tables"], d["context_lens"], w.cfg.block_size,
+                               w.cfg.q_len)
     assert np.array_equal(gslots.cpu().numpy(), slots)
     assert np.array_equal(_u16(d["k_cache"]), kc)
     assert np.array_equal(_u16(d["v_cache"]), vc)

@@ -106,7 +106,7 @@ def gpu_cascade(pa, w, tail_splits=1, fused=True):
                              d["context_lens"], w.scale, P, q_len=w.cfg.q_len,
                              tail_splits=tail_splits, k_new=d["k_new"], v_new=d["v_new"])
     else:
-        slots = pa.pa_slot_mapping(d["block_tables"], d["context_lens"], 16, w.cfg.q_len)
+        slots = pa.pa_slot_mapping(d["block_tables"], d["context_lens"], w.cfg.block_size, w.cfg.q_len)
         pa.pa_append_kv(d["k_cache"], d["v_cache"], d["k_new"], d["v_new"], slots)
         pa.pa_decode_cascade(out, d["q"], d["k_cache"], d["v_cache"], d["block_tables"],
                              d["context_lens"], w.scale, P, q_len=w.cfg.q_len,

@@ -1,7 +1,8 @@
 """Seeded random configurations, CUDA path vs the fp64 oracle, every element (needs a
 GPU).
 
-Each case draws a dtype, head_dim, KV head count, group size, q_len, context
+Each case draws a dtype, head_dim, block size (8, 16 or 32 tokens), KV head count,
+group size, q_len, context
 lengths (empty, shorter than q_len and longer), a split count and fused or separate
 launches, so that combinations the hand-written cases do not list still meet the
 oracle.  The pool is NaN-poisoned outside the written slots.
@@ -31,8 +32,7 @@ def _case(seed: int, fp8: bool):
     rng = np.random.default_rng(1000 + seed)
     h_kv = int(rng.choice([1, 2, 4, 8]))
     g = int(rng.choice([1, 2, 3, 4, 5, 8]))
-    q_len = int(rng.choice([1, 2, 3, 4, 7, 16, 17, 33] if fp8 else
-                           [1, 2, 3, 4, 7, 16, 17, 33, 100, 300]))
+    q_len = int(rng.choice([1, 2, 3, 4, 7, 16, 17, 33, 100, 300]))
     n = int(rng.integers(1, 6))
     lens = [int(x) for x in rng.integers(q_len, 1500, size=n)]
     if n > 1 and rng.random() < 0.5:
@@ -44,6 +44,7 @@ def _case(seed: int, fp8: bool):
             "head_dim": 128 if fp8 else int(rng.choice([64, 128]))}
     splits = int(rng.choice([1, 2, 5]))
     fused = bool(rng.random() < 0.5)
+    over["block_size"] = int(rng.choice([8, 16, 32]))
     return over, splits, fused
 
 
@@ -72,7 +73,7 @@ def test_random_fp8_cache(pa, orc, seed):
                          d["block_tables"], d["context_lens"], w.scale, c.q_len, splits,
                          k_new=d["k_new"], v_new=d["v_new"])
     else:
-        slots = pa.pa_slot_mapping(d["block_tables"], d["context_lens"], 16, c.q_len)
+        slots = pa.pa_slot_mapping(d["block_tables"], d["context_lens"], c.block_size, c.q_len)
         pa.pa_append_kv_fp8(d["k_cache"], d["v_cache"], d["k_new"], d["v_new"], slots,
                             d["k_scale"], d["v_scale"])
         pa.pa_decode_fp8(out, d["q"], d["k_cache"], d["v_cache"], d["k_scale"], d["v_scale"],
@@ -80,7 +81,7 @@ def test_random_fp8_cache(pa, orc, seed):
     torch.cuda.synchronize()
     assert pa.pa_device_error() == 0
     kc, vc = w.bits("k_cache").copy(), w.bits("v_cache").copy()
-    slots = orc.slot_mapping(w.block_tables.numpy(), w.context_lens.numpy(), 16, c.q_len)
+    slots = orc.slot_mapping(w.block_tables.numpy(), w.context_lens.numpy(), c.block_size, c.q_len)
     orc.append_kv_fp8(kc, vc, w.bits("k_new"), w.bits("v_new"), slots, c.dtype,
                       w.k_scale.numpy(), w.v_scale.numpy())
     ref = orc.decode_fp8(w.bits("q"), kc, vc, w.k_scale.numpy(), w.v_scale.numpy(),

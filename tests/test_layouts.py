@@ -254,3 +254,52 @@ def test_prefill_p_columns_match_the_pv_operand(CG):
             pos = 16 * kk + i
             assert written_hi[pos] == (pc + i // 2, i % 2)  # lower k in the low half
             assert written_lo[pos] == (pc + kCols // 2 + i // 2, i % 2)
+
+
+def test_prefill_fp8_widening_in_place():
+    """The many-row kernel over an FP8 cache widens a chunk's codes in place.  Lane l
+    of a widening warp handles position r = r0 + 32k + l: it reads the swizzled
+    16-byte code chunks 4..7 (dims 64..127) and writes them, widened, to the second
+    half of the 16-bit tile layout ([half][128 positions][128 B], chunk c' of a row
+    at c' ^ (r % 8)), then reads chunks 0..3 and writes the first half, which lies
+    over the codes row.  Simulated byte for byte: every code is read before it is
+    overwritten, every fp16 dim lands where the MMA reads it, and each phase's
+    loads and stores are conflict-free."""
+    chunk = 128
+    mem = {}
+    for r in range(chunk):
+        for c in range(8):
+            for b in range(16):
+                mem[r * 128 + ((c ^ (r & 7)) << 4) + b] = ("code", r, 16 * c + b)
+    for k in range(chunk // 32):
+        for h in (1, 0):
+            for i in range(4):
+                c = 4 * h + i
+                assert conflict_free(lambda l: (32 * k + l) * 128 + ((c ^ ((32 * k + l) & 7)) << 4))
+            got = {}
+            for l in range(32):                          # all loads of the phase first
+                r = 32 * k + l
+                for i in range(4):
+                    c = 4 * h + i
+                    a = r * 128 + ((c ^ (r & 7)) << 4)
+                    got[(l, i)] = [mem[a + b] for b in range(16)]
+                    assert got[(l, i)] == [("code", r, 16 * c + b) for b in range(16)]
+            for i in range(4):
+                for f in (2 * i, 2 * i + 1):
+                    def waddr(l):
+                        r = 32 * k + l
+                        return h * chunk * 128 + r * 128 + ((f ^ (r & 7)) << 4)
+                    assert conflict_free(waddr)
+                    for l in range(32):
+                        r = 32 * k + l
+                        for b in range(8):              # 8 fp16 values = 16 bytes
+                            dim = 16 * (4 * h + i) + 8 * (f - 2 * i) + b
+                            mem[waddr(l) + 2 * b] = ("fp16", r, dim)
+                            mem[waddr(l) + 2 * b + 1] = ("fp16", r, dim)
+    # the 16-bit layout: dims 64h + 8f' .. +7 of position r at h*16384 + 128r + ((f' ^ r%8) << 4)
+    for r in range(chunk):
+        for h in range(2):
+            for fp in range(8):
+                a = h * chunk * 128 + r * 128 + ((fp ^ (r & 7)) << 4)
+                for b in range(8):
+                    assert mem[a + 2 * b] == ("fp16", r, 64 * h + 8 * fp + b)

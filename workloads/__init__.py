@@ -22,7 +22,7 @@ Workloads (shapes from the configurations the library is measured on):
   chunked_prefill 16 seqs, each appending a chunk of 512 new tokens (8192 tokens a
                   step) at the end of a context uniform in [512, 8192], causal;
                   32 q / 8 KV heads, head_dim 128, bf16
-  llama7b_mha_fp8, gqa_fp8
+  llama7b_mha_fp8, gqa_fp8, chunked_prefill_fp8
                   the same shapes over an FP8 (e4m3) cache with one scale per KV
                   head (K and V separately, drawn in [0.02, 0.05]); q and the new
                   rows stay in the 16-bit type
@@ -95,6 +95,8 @@ CONFIGS: dict[str, Config] = {
                               lens=("uniform", 512, 4096), kv_fp8=True),
     "gqa_fp8": Config("gqa_fp8", 64, 32, 8, 128, 16, "bf16",
                       lens=("lognormal", 1500.0, 0.5, 8192), kv_fp8=True),
+    "chunked_prefill_fp8": Config("chunked_prefill_fp8", 16, 32, 8, 128, 16, "bf16", q_len=512,
+                                  lens=("uniform", 512, 8192), kv_fp8=True),
 }
 
 
