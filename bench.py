@@ -142,7 +142,8 @@ def attention_flops(w: workloads.Workload) -> float:
 _COMMON_SRC = ("pa_device.cuh", "pa_launch.h", "pa_api.cu", "pa_decode.cuh")
 KERNEL_SOURCES = {
     "decode": _COMMON_SRC + ("pa_decode_inst.cuh", "pa_decode_fp16.cu", "pa_decode_bf16.cu"),
-    "prefill": _COMMON_SRC + ("pa_prefill_tc.cuh", "pa_tc.cuh", "pa_prefill.cu"),
+    "prefill": _COMMON_SRC + ("pa_prefill_tc.cuh", "pa_tc.cuh", "pa_prefill_inst.cuh",
+                              "pa_prefill.cu"),
 }
 
 

@@ -508,13 +508,21 @@ pa_status decode_common(void *out, float *ws, const WsLayout *lay, const void *q
     } else {
       qmap = kmap;  // unused
     }
-    e = pa::launch_prefill(kmap, vmap, qmap, a, head_dim, dtype == PA_FP16, partial, fp8, s);
-  } else if (fp8)
+    e = block_size == 16
+            ? pa::launch_prefill(kmap, vmap, qmap, a, head_dim, dtype == PA_FP16, partial, fp8, s)
+            : pa::launch_prefill_bx(kmap, vmap, qmap, a, head_dim, dtype == PA_FP16, partial, fp8, s);
+  } else if (fp8 && block_size == 16)
     e = dtype == PA_FP16 ? pa::launch_decode8_fp16(kmap, vmap, a, partial, (int)units, s)
                          : pa::launch_decode8_bf16(kmap, vmap, a, partial, (int)units, s);
-  else
+  else if (fp8)
+    e = dtype == PA_FP16 ? pa::launch_decode8_fp16_bx(kmap, vmap, a, partial, (int)units, s)
+                         : pa::launch_decode8_bf16_bx(kmap, vmap, a, partial, (int)units, s);
+  else if (block_size == 16)
     e = dtype == PA_FP16 ? pa::launch_decode_fp16(kmap, vmap, a, head_dim, partial, (int)units, s)
                          : pa::launch_decode_bf16(kmap, vmap, a, head_dim, partial, (int)units, s);
+  else
+    e = dtype == PA_FP16 ? pa::launch_decode_fp16_bx(kmap, vmap, a, head_dim, partial, (int)units, s)
+                         : pa::launch_decode_bf16_bx(kmap, vmap, a, head_dim, partial, (int)units, s);
   return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 

@@ -1223,7 +1223,9 @@ struct Mma8Path {
 // C > 1 along x): the C*NW warps take the unit's blocks round-robin, each CTA
 // merges its warps, then the CTAs merge through distributed shared memory.  This
 // splits one long sequence over several SMs without any global workspace.
-template <typename T, int D, int NW, int NSTAGE, class Path, bool PARTIAL, bool KV8>
+// BS: the cache's block size when it is fixed at compile time (16), or 0 to read it
+// from the arguments (8 or 32 tokens).
+template <typename T, int D, int NW, int NSTAGE, class Path, bool PARTIAL, bool KV8, int BS>
 __global__ void __launch_bounds__(NW * 32)
     paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
                         const __grid_constant__ CUtensorMap vmap, const DecodeArgs a) {
@@ -1286,7 +1288,7 @@ __global__ void __launch_bounds__(NW * 32)
   }
   const int row0 = blockIdx.y * RPC;
 
-  const int bsz = a.block_size;
+  const int bsz = BS ? BS : a.block_size;
   int nb = (L + kTileTokens - 1) / kTileTokens;  // tiles
   if ((int64_t)L > (int64_t)a.max_blocks_per_seq * bsz) {  // context longer than its table
     if (threadIdx.x == 0 && split == 0 && kvh == 0 && blockIdx.y == 0 && crank == 0)

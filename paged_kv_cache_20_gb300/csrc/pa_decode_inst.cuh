@@ -35,12 +35,12 @@ struct DeviceFit {
 
 // Resident slots (SMs x CTAs per SM) of one kernel instance on the current device,
 // cached per device; the first call also sets the kernel's shared-memory opt-in.
-template <typename T, int D, class Path, bool PARTIAL, bool KV8, int NW>
+template <int BS, typename T, int D, class Path, bool PARTIAL, bool KV8, int NW>
 static cudaError_t resident_slots(long long &slots) {
   constexpr int kStages = stages_of<Path, PARTIAL, KV8>();
   constexpr int kStageBytes = 2 * kTileTokens * D * (KV8 ? 1 : 2);
   constexpr int kSmem = NW * kStages * kStageBytes + 1024;
-  auto kern = paged_decode_kernel<T, D, NW, kStages, Path, PARTIAL, KV8>;
+  auto kern = paged_decode_kernel<T, D, NW, kStages, Path, PARTIAL, KV8, BS>;
   static DeviceFit fit[kMaxDevices];
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -66,16 +66,16 @@ static cudaError_t resident_slots(long long &slots) {
 // Launch one kernel instance with NW warps per CTA.  Single pass: while the units
 // would fill fewer than wave_num / wave_den waves of resident CTAs, double the
 // cluster size (up to kMaxCluster) so long sequences spread over several SMs.
-template <typename T, int D, class Path, bool PARTIAL, bool KV8 = false, int NW = kWarps>
+template <int BS, typename T, int D, class Path, bool PARTIAL, bool KV8 = false, int NW = kWarps>
 static cudaError_t launch_one(const CUtensorMap &kmap, const CUtensorMap &vmap,
                               const DecodeArgs &a, int units, int row_groups, cudaStream_t st,
                               int wave_num = 2, int wave_den = 1) {
   constexpr int kStages = stages_of<Path, PARTIAL, KV8>();
   constexpr int kStageBytes = 2 * kTileTokens * D * (KV8 ? 1 : 2);
   constexpr int kSmem = NW * kStages * kStageBytes + 1024;
-  auto kern = paged_decode_kernel<T, D, NW, kStages, Path, PARTIAL, KV8>;
+  auto kern = paged_decode_kernel<T, D, NW, kStages, Path, PARTIAL, KV8, BS>;
   long long slots = 0;
-  cudaError_t e = resident_slots<T, D, Path, PARTIAL, KV8, NW>(slots);
+  cudaError_t e = resident_slots<BS, T, D, Path, PARTIAL, KV8, NW>(slots);
   if (e != cudaSuccess) return e;
   // The partial pass already has the caller's partitions (clusters measured slower
   // there: each CTA's fixed cost outweighs the shorter tail).
@@ -110,73 +110,75 @@ static cudaError_t launch_one(const CUtensorMap &kmap, const CUtensorMap &vmap,
 // start and end-of-unit merge then overlap a fourth CTA's loads.  Above that,
 // 4-warp CTAs with the caller's cluster threshold: 1.5 waves on the FP8
 // swapped-operand path, 2 elsewhere.
-template <typename T, class Path, bool KV8, int WAVE4_NUM, int WAVE4_DEN>
+template <int BS, typename T, class Path, bool KV8, int WAVE4_NUM, int WAVE4_DEN>
 static cudaError_t launch_few_units(const CUtensorMap &kmap, const CUtensorMap &vmap,
                                     const DecodeArgs &a, int units, cudaStream_t st) {
   long long slots3 = 0;
-  const cudaError_t e = resident_slots<T, 128, Path, false, KV8, 3>(slots3);
+  const cudaError_t e = resident_slots<BS, T, 128, Path, false, KV8, 3>(slots3);
   if (e != cudaSuccess) return e;
-  if (units < slots3) return launch_one<T, 128, Path, false, KV8, 3>(kmap, vmap, a, units, 1, st, 3, 2);
-  return launch_one<T, 128, Path, false, KV8>(kmap, vmap, a, units, 1, st, WAVE4_NUM, WAVE4_DEN);
+  if (units < slots3) return launch_one<BS, T, 128, Path, false, KV8, 3>(kmap, vmap, a, units, 1, st, 3, 2);
+  return launch_one<BS, T, 128, Path, false, KV8>(kmap, vmap, a, units, 1, st, WAVE4_NUM, WAVE4_DEN);
 }
 
-template <typename T, int D, bool PARTIAL>
+template <int BS, typename T, int D, bool PARTIAL>
 static cudaError_t launch_paths(const CUtensorMap &kmap, const CUtensorMap &vmap,
                                 const DecodeArgs &a, int units, cudaStream_t st) {
   if constexpr (!PARTIAL && D == 128) {
-    if (a.rows == 1) return launch_few_units<T, FmaPath<T, D, 4, 1>, false, 2, 1>(kmap, vmap, a, units, st);
-    if (a.rows == 2) return launch_few_units<T, FmaPath<T, D, 8, 2>, false, 2, 1>(kmap, vmap, a, units, st);
+    if (a.rows == 1) return launch_few_units<BS, T, FmaPath<T, D, 4, 1>, false, 2, 1>(kmap, vmap, a, units, st);
+    if (a.rows == 2) return launch_few_units<BS, T, FmaPath<T, D, 8, 2>, false, 2, 1>(kmap, vmap, a, units, st);
   }
-  if (a.rows == 1) return launch_one<T, D, FmaPath<T, D, 4, 1>, PARTIAL>(kmap, vmap, a, units, 1, st);
-  if (a.rows == 2) return launch_one<T, D, FmaPath<T, D, 8, 2>, PARTIAL>(kmap, vmap, a, units, 1, st);
+  if (a.rows == 1) return launch_one<BS, T, D, FmaPath<T, D, 4, 1>, PARTIAL>(kmap, vmap, a, units, 1, st);
+  if (a.rows == 2) return launch_one<BS, T, D, FmaPath<T, D, 8, 2>, PARTIAL>(kmap, vmap, a, units, 1, st);
   if (a.rows <= 8) {
     if constexpr (!PARTIAL && D == 128)
-      return launch_few_units<T, MmaTPath<T, D>, false, 2, 1>(kmap, vmap, a, units, st);
-    return launch_one<T, D, MmaTPath<T, D>, PARTIAL>(kmap, vmap, a, units, 1, st);
+      return launch_few_units<BS, T, MmaTPath<T, D>, false, 2, 1>(kmap, vmap, a, units, st);
+    return launch_one<BS, T, D, MmaTPath<T, D>, PARTIAL>(kmap, vmap, a, units, 1, st);
   }
   const int groups = (a.rows + 15) / 16;
   if constexpr (!PARTIAL && D == 128)
-    if (groups == 1) return launch_few_units<T, MmaPath<T, D>, false, 2, 1>(kmap, vmap, a, units, st);
-  return launch_one<T, D, MmaPath<T, D>, PARTIAL>(kmap, vmap, a, units, groups, st);
+    if (groups == 1) return launch_few_units<BS, T, MmaPath<T, D>, false, 2, 1>(kmap, vmap, a, units, st);
+  return launch_one<BS, T, D, MmaPath<T, D>, PARTIAL>(kmap, vmap, a, units, groups, st);
 }
 
-template <typename T, bool PARTIAL>
+template <int BS, typename T, bool PARTIAL>
 static cudaError_t launch_paths8(const CUtensorMap &kmap, const CUtensorMap &vmap,
                                  const DecodeArgs &a, int units, cudaStream_t st) {
   if constexpr (!PARTIAL) {
-    if (a.rows == 1) return launch_few_units<T, Fma8Path<T, 1>, true, 2, 1>(kmap, vmap, a, units, st);
-    if (a.rows == 2) return launch_few_units<T, Fma8Path<T, 2>, true, 2, 1>(kmap, vmap, a, units, st);
+    if (a.rows == 1) return launch_few_units<BS, T, Fma8Path<T, 1>, true, 2, 1>(kmap, vmap, a, units, st);
+    if (a.rows == 2) return launch_few_units<BS, T, Fma8Path<T, 2>, true, 2, 1>(kmap, vmap, a, units, st);
   }
-  if (a.rows == 1) return launch_one<T, 128, Fma8Path<T, 1>, PARTIAL, true>(kmap, vmap, a, units, 1, st);
-  if (a.rows == 2) return launch_one<T, 128, Fma8Path<T, 2>, PARTIAL, true>(kmap, vmap, a, units, 1, st);
+  if (a.rows == 1) return launch_one<BS, T, 128, Fma8Path<T, 1>, PARTIAL, true>(kmap, vmap, a, units, 1, st);
+  if (a.rows == 2) return launch_one<BS, T, 128, Fma8Path<T, 2>, PARTIAL, true>(kmap, vmap, a, units, 1, st);
   if (a.rows <= 8) {
-    if constexpr (!PARTIAL) return launch_few_units<T, Mma8TPath<T>, true, 3, 2>(kmap, vmap, a, units, st);
-    return launch_one<T, 128, Mma8TPath<T>, PARTIAL, true>(kmap, vmap, a, units, 1, st);
+    if constexpr (!PARTIAL) return launch_few_units<BS, T, Mma8TPath<T>, true, 3, 2>(kmap, vmap, a, units, st);
+    return launch_one<BS, T, 128, Mma8TPath<T>, PARTIAL, true>(kmap, vmap, a, units, 1, st);
   }
   const int groups = (a.rows + 15) / 16;
   if constexpr (!PARTIAL)
-    if (groups == 1) return launch_few_units<T, Mma8Path<T>, true, 2, 1>(kmap, vmap, a, units, st);
-  return launch_one<T, 128, Mma8Path<T>, PARTIAL, true>(kmap, vmap, a, units, groups, st);
+    if (groups == 1) return launch_few_units<BS, T, Mma8Path<T>, true, 2, 1>(kmap, vmap, a, units, st);
+  return launch_one<BS, T, 128, Mma8Path<T>, PARTIAL, true>(kmap, vmap, a, units, groups, st);
 }
 
 // FP8 (e4m3) cache, head_dim 128; T is the type of q and out.
-template <typename T>
+// BS = 16: kernels built for 16-token blocks; BS = 0: kernels that read the block
+// size (8 or 32) from the arguments.
+template <int BS, typename T>
 static cudaError_t launch_decode8_t(const CUtensorMap &kmap, const CUtensorMap &vmap,
                                     const DecodeArgs &a, bool partial, int units, cudaStream_t st) {
-  return partial ? launch_paths8<T, true>(kmap, vmap, a, units, st)
-                 : launch_paths8<T, false>(kmap, vmap, a, units, st);
+  return partial ? launch_paths8<BS, T, true>(kmap, vmap, a, units, st)
+                 : launch_paths8<BS, T, false>(kmap, vmap, a, units, st);
 }
 
-template <typename T>
+template <int BS, typename T>
 static cudaError_t launch_decode_t(const CUtensorMap &kmap, const CUtensorMap &vmap,
                                    const DecodeArgs &a, int head_dim, bool partial, int units,
                                    cudaStream_t st) {
   if (head_dim == 128)
-    return partial ? launch_paths<T, 128, true>(kmap, vmap, a, units, st)
-                   : launch_paths<T, 128, false>(kmap, vmap, a, units, st);
+    return partial ? launch_paths<BS, T, 128, true>(kmap, vmap, a, units, st)
+                   : launch_paths<BS, T, 128, false>(kmap, vmap, a, units, st);
   if (head_dim == 64)
-    return partial ? launch_paths<T, 64, true>(kmap, vmap, a, units, st)
-                   : launch_paths<T, 64, false>(kmap, vmap, a, units, st);
+    return partial ? launch_paths<BS, T, 64, true>(kmap, vmap, a, units, st)
+                   : launch_paths<BS, T, 64, false>(kmap, vmap, a, units, st);
   return cudaErrorInvalidValue;
 }
 

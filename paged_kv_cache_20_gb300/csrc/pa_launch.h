@@ -31,6 +31,7 @@ struct CombineArgs;
 
 // rows_per_unit = (num_q_heads / num_kv_heads) * q_len selects the path;
 // grid.x = num_seqs * num_kv_heads * num_splits is set by the caller in `units`.
+// These take a cache of 16-token blocks.
 cudaError_t launch_decode_fp16(const CUtensorMap &kmap, const CUtensorMap &vmap,
                                const DecodeArgs &args, int head_dim, bool partial, int units,
                                cudaStream_t stream);
@@ -44,6 +45,19 @@ cudaError_t launch_decode8_fp16(const CUtensorMap &kmap, const CUtensorMap &vmap
 cudaError_t launch_decode8_bf16(const CUtensorMap &kmap, const CUtensorMap &vmap,
                                 const DecodeArgs &args, bool partial, int units,
                                 cudaStream_t stream);
+// The same for a cache of 8- or 32-token blocks (the block size read at run time).
+cudaError_t launch_decode_fp16_bx(const CUtensorMap &kmap, const CUtensorMap &vmap,
+                                  const DecodeArgs &args, int head_dim, bool partial, int units,
+                                  cudaStream_t stream);
+cudaError_t launch_decode_bf16_bx(const CUtensorMap &kmap, const CUtensorMap &vmap,
+                                  const DecodeArgs &args, int head_dim, bool partial, int units,
+                                  cudaStream_t stream);
+cudaError_t launch_decode8_fp16_bx(const CUtensorMap &kmap, const CUtensorMap &vmap,
+                                   const DecodeArgs &args, bool partial, int units,
+                                   cudaStream_t stream);
+cudaError_t launch_decode8_bf16_bx(const CUtensorMap &kmap, const CUtensorMap &vmap,
+                                   const DecodeArgs &args, bool partial, int units,
+                                   cudaStream_t stream);
 // Many query rows per KV head (q_len above the decode kernel's limit, or the
 // shared-prefix pass of a cascade when args.shared_prefix > 0): units of 128 query
 // rows of one KV head, walked by persistent CTAs (one per SM, at most
@@ -52,6 +66,10 @@ cudaError_t launch_decode8_bf16(const CUtensorMap &kmap, const CUtensorMap &vmap
 cudaError_t launch_prefill(const CUtensorMap &kmap, const CUtensorMap &vmap, const CUtensorMap &qmap,
                            const DecodeArgs &args, int head_dim, bool fp16, bool partial,
                            bool kv8, cudaStream_t stream);
+// The same for a cache of 8- or 32-token blocks.
+cudaError_t launch_prefill_bx(const CUtensorMap &kmap, const CUtensorMap &vmap,
+                              const CUtensorMap &qmap, const DecodeArgs &args, int head_dim,
+                              bool fp16, bool partial, bool kv8, cudaStream_t stream);
 cudaError_t launch_combine_fp16(const CombineArgs &args, int head_dim, cudaStream_t stream);
 cudaError_t launch_combine_bf16(const CombineArgs &args, int head_dim, cudaStream_t stream);
 

@@ -182,7 +182,7 @@ struct TcUnit {
 // call it (the shared-prefix limit is a warp maximum).
 __device__ __forceinline__ TcUnit tc_unit(const DecodeArgs &a, const TcGeo &geo, int k,
                                           const int *s_order, const int *lens, int lane, int row,
-                                          bool rec) {
+                                          bool rec, int bsz) {
   TcUnit t;
   const int G = gridDim.x;
   const bool shared = a.shared_prefix > 0;
@@ -211,7 +211,7 @@ __device__ __forceinline__ TcUnit tc_unit(const DecodeArgs &a, const TcGeo &geo,
     nb = min(a.shared_prefix, a.max_tiles);
   } else {
     nb = (Lt + kTileTokens - 1) / kTileTokens;
-    if ((int64_t)Lt > (int64_t)a.max_blocks_per_seq * a.block_size) {
+    if ((int64_t)Lt > (int64_t)a.max_blocks_per_seq * bsz) {
       if (rec && t.kvh == 0 && t.split == 0) record_error(a.err, kErrCheck);
       nb = min(nb, a.max_tiles);
     }
@@ -220,7 +220,7 @@ __device__ __forceinline__ TcUnit tc_unit(const DecodeArgs &a, const TcGeo &geo,
   // tiles before first_block belong to another pass (a cascade's shared prefix);
   // the rest is cut into num_splits partitions of whole blocks (or tiles)
   const TileRange part = partition_tiles(nb, shared ? 0 : min(nb, a.first_block), a.num_splits,
-                                         t.split, a.block_size);
+                                         t.split, bsz);
   t.tb = part.tb;
   t.te = part.te;
 
@@ -316,7 +316,9 @@ __device__ __forceinline__ void tc_widen_e4m3_rows(uint32_t st, int r0, int rows
   }
 }
 
-template <typename T, int D, int NK, int NV, bool PARTIAL, bool KV8 = false>
+// BS16: the cache's blocks are 16 tokens (fixed at compile time); otherwise the
+// block size (8 or 32) is read from the arguments.
+template <typename T, int D, int NK, int NV, bool PARTIAL, bool KV8, bool BS16>
 __global__ void __launch_bounds__(KV8 ? kTcThreads8 : kTcThreads, 1)
     paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
                             const __grid_constant__ CUtensorMap vmap,
@@ -328,6 +330,7 @@ __global__ void __launch_bounds__(KV8 ? kTcThreads8 : kTcThreads, 1)
   constexpr bool kBf16 = Elt<TM>::kMantBits < 10;
   static_assert(!KV8 || D == 128, "FP8 cache: head_dim 128");
   constexpr int kSoft0 = KV8 ? kTcCtl + kTcConv : kTcCtl;  // first softmax warp
+  const int kBsz = BS16 ? 16 : a.block_size;
   constexpr int kOCols = D / 2;  // O columns per softmax warp
   static_assert(NK >= 2 && NV >= 2, "ring depth");
   static_assert(D == 64 || D == 128, "head_dim");
@@ -451,7 +454,7 @@ __global__ void __launch_bounds__(KV8 ? kTcThreads8 : kTcThreads, 1)
     int g = 0, issued = 0;  // chunks of this CTA so far (all units), loads issued
     bool ok = true;
     for (int k = 0; ok; ++k) {
-      const TcUnit t = tc_unit(a, geo, k, s_order, lens, lane, -1, is_k && lane == 0);
+      const TcUnit t = tc_unit(a, geo, k, s_order, lens, lane, -1, is_k && lane == 0, kBsz);
       if (!t.valid) break;
       const int32_t *table = a.block_tables + (size_t)t.tseq * a.max_blocks_per_seq;
       // block-table window (16-token blocks: a block is a tile): lane l holds entry
@@ -460,7 +463,7 @@ __global__ void __launch_bounds__(KV8 ? kTcThreads8 : kTcThreads, 1)
       // entries per chunk.
       auto table_at = [&](int w) -> int {
         const int blk = t.tb + 32 * w + lane;
-        return (a.block_size == 16 && blk < t.t_end) ? __ldg(table + blk) : -1;
+        return (kBsz == 16 && blk < t.t_end) ? __ldg(table + blk) : -1;
       };
       int win_cur = 0, win_nxt = 0;
       if (t.nch > 0) {
@@ -488,7 +491,7 @@ __global__ void __launch_bounds__(KV8 ? kTcThreads8 : kTcThreads, 1)
         // lane l loads tile tb + 8 ch + l of the chunk (16-token blocks: the window's
         // entry; 32-token blocks: half l % 2 of a block), or with 8-token blocks the
         // 8-row box of block 2 (tb + 8 ch) + l.  z stays -1 (zero fill) past the walk.
-        const int bsz = a.block_size;
+        const int bsz = kBsz;
         const int tile = t.tb + ch * kTcBlocks + (bsz == 8 ? (lane >> 1) : lane);
         const int phys = __shfl_sync(0xffffffffu, win_cur, ((ch & 3) * kTcBlocks + lane) & 31);
         int z = -1;  // outside the tensor map: zero fill
@@ -536,7 +539,7 @@ __global__ void __launch_bounds__(KV8 ? kTcThreads8 : kTcThreads, 1)
     int g = 0;
     bool ok = true;
     for (int k = 0; ok; ++k) {
-      const TcUnit t = tc_unit(a, geo, k, s_order, lens, lane, -1, false);
+      const TcUnit t = tc_unit(a, geo, k, s_order, lens, lane, -1, false, kBsz);
       if (!t.valid) break;
       for (int ch = 0; ch < t.nch; ++ch) {
         const int gg = g + ch;
@@ -580,7 +583,7 @@ __global__ void __launch_bounds__(KV8 ? kTcThreads8 : kTcThreads, 1)
       int qn = 0;            // units with chunks so far: the phase of q_full / q_ready / q_free
       bool q_flight = false;  // a Q load issued and not yet seen landed
       for (int k = 0; ok; ++k) {
-        const TcUnit t = tc_unit(a, geo, k, s_order, lens, lane, -1, false);
+        const TcUnit t = tc_unit(a, geo, k, s_order, lens, lane, -1, false, kBsz);
         if (!t.valid) break;
         if (t.nch == 0) continue;
         if (a.q_tma) {
@@ -643,7 +646,7 @@ __global__ void __launch_bounds__(KV8 ? kTcThreads8 : kTcThreads, 1)
     } else {
       // O += P_j V_j, P from S buffer j % 3; a unit's first chunk overwrites O
       for (int k = 0; ok; ++k) {
-        const TcUnit t = tc_unit(a, geo, k, s_order, lens, lane, -1, false);
+        const TcUnit t = tc_unit(a, geo, k, s_order, lens, lane, -1, false, kBsz);
         if (!t.valid) break;
         for (int j = 0; ok && j < t.nch; ++j) {
           const int gg = g + j;
@@ -855,7 +858,7 @@ __global__ void __launch_bounds__(KV8 ? kTcThreads8 : kTcThreads, 1)
     int g = 0;   // chunks of this CTA so far (all units)
     int qn = 0;  // Q buffers written (without TMA)
     int e_cur = 0, e_next = 0;  // the row's q exponent (FP8 cache, bf16 q), this unit and next
-    TcUnit cu = tc_unit(a, geo, 0, s_order, lens, lane, row, false);
+    TcUnit cu = tc_unit(a, geo, 0, s_order, lens, lane, row, false, kBsz);
     if (!a.q_tma && cu.valid && cu.nch > 0) {
       e_cur = write_q(cu);
       qn = 1;
@@ -1024,7 +1027,7 @@ __global__ void __launch_bounds__(KV8 ? kTcThreads8 : kTcThreads, 1)
 
       // the next unit's Q (without TMA) goes in while this unit's P V drains: its
       // buffer is free once this unit's last S MMA has completed
-      const TcUnit nu = tc_unit(a, geo, k + 1, s_order, lens, lane, row, false);
+      const TcUnit nu = tc_unit(a, geo, k + 1, s_order, lens, lane, row, false, kBsz);
       e_next = 0;
       if (!a.q_tma && nu.valid && nu.nch > 0) {
         if (qn > 0) {
