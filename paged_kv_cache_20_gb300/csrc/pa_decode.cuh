@@ -1302,45 +1302,6 @@ __global__ void __launch_bounds__(NW * 32)
   const float sscale = a.scale_log2 * (KV8 ? __ldg(a.k_scale + kvh) : 1.f);
   const float vscale = KV8 ? __ldg(a.v_scale + kvh) : 1.f;
 
-  // Fused append: every CTA whose block range holds a new token writes all of this
-  // unit's new rows itself (CTAs of one cluster, row group or neighbouring split
-  // write identical bytes), then orders those generic-proxy stores before its own
-  // TMA reads of the cache.
-  if (a.k_new != nullptr && te > tb && te * kTileTokens > L - a.q_len) {
-    const int64_t num_slots = (int64_t)a.num_blocks * bsz;
-    for (int idx = threadIdx.x; idx < a.q_len * (D / 8); idx += NW * 32) {
-      const int u = idx / (D / 8), c = idx % (D / 8);
-      const int pos = L - a.q_len + u;
-      if (pos < 0) continue;
-      const int lb = pos / bsz;
-      if (lb >= a.max_blocks_per_seq) {
-        record_error(a.err, kErrCheck);
-        continue;
-      }
-      const int64_t slot = (int64_t)__ldg(a.block_tables + (size_t)seq * a.max_blocks_per_seq + lb) *
-                               bsz + pos % bsz;
-      if (slot < 0 || slot >= num_slots) {
-        record_error(a.err, kErrCheck);
-        continue;
-      }
-      const int64_t blk = slot / bsz, off = slot % bsz;
-      const size_t dst = (size_t)(((blk * a.num_kv_heads + kvh) * bsz + off) * D + c * 8);
-      const size_t src = ((size_t)(seq * a.q_len + u) * a.num_kv_heads + kvh) * D + c * 8;
-      const uint4 kv = __ldg(reinterpret_cast<const uint4 *>(a.k_new + src));
-      const uint4 vv = __ldg(reinterpret_cast<const uint4 *>(a.v_new + src));
-      if constexpr (KV8) {  // quantise: e4m3(x / scale), 8 codes per chunk
-        uint8_t *kc = reinterpret_cast<uint8_t *>(a.k_cache), *vc = reinterpret_cast<uint8_t *>(a.v_cache);
-        *reinterpret_cast<uint2 *>(kc + dst) = quantize8<T>(kv, __ldg(a.k_scale + kvh));
-        *reinterpret_cast<uint2 *>(vc + dst) = quantize8<T>(vv, __ldg(a.v_scale + kvh));
-      } else {
-        *reinterpret_cast<uint4 *>(a.k_cache + dst) = kv;
-        *reinterpret_cast<uint4 *>(a.v_cache + dst) = vv;
-      }
-    }
-    fence_proxy_async_global();
-    __syncthreads();
-  }
-
   if (threadIdx.x == 0) {
     s_failed = 0;
     prefetch_tensormap(&kmap);
@@ -1413,6 +1374,57 @@ __global__ void __launch_bounds__(NW * 32)
   if (n_my > 0) load_window(0);
   Path path;
   path.init(a, seq, kvh, row0, L, sscale);
+
+  // Fused append: every CTA that reads a tile holding a new position writes all of
+  // this unit's new rows itself (CTAs of one row group or neighbouring split that
+  // also read one write identical bytes), then orders those generic-proxy stores
+  // before its own TMA reads of the cache.  Tile j is read by cluster warp
+  // (j - tb - rot) mod ntiles, modulo TW.  The table window and q above are already
+  // in flight: neither is written here.
+  bool reads_new = false;
+  if (a.k_new != nullptr && ntiles > 0) {
+    const int j1 = min(te, (L + kTileTokens - 1) / kTileTokens);  // past the last new tile
+    for (int j = max(tb, max(0, L - a.q_len) / kTileTokens); j < j1; ++j) {
+      int k = j - tb - rot;
+      if (k < 0) k += ntiles;
+      reads_new |= (k % TW) / NW == crank;
+    }
+  }
+  if (reads_new) {
+    const int64_t num_slots = (int64_t)a.num_blocks * bsz;
+    for (int idx = threadIdx.x; idx < a.q_len * (D / 8); idx += NW * 32) {
+      const int u = idx / (D / 8), c = idx % (D / 8);
+      const int pos = L - a.q_len + u;
+      if (pos < 0) continue;
+      const int lb = pos / bsz;
+      if (lb >= a.max_blocks_per_seq) {
+        record_error(a.err, kErrCheck);
+        continue;
+      }
+      const int64_t slot = (int64_t)__ldg(a.block_tables + (size_t)seq * a.max_blocks_per_seq + lb) *
+                               bsz + pos % bsz;
+      if (slot < 0 || slot >= num_slots) {
+        record_error(a.err, kErrCheck);
+        continue;
+      }
+      const int64_t blk = slot / bsz, off = slot % bsz;
+      const size_t dst = (size_t)(((blk * a.num_kv_heads + kvh) * bsz + off) * D + c * 8);
+      const size_t src = ((size_t)(seq * a.q_len + u) * a.num_kv_heads + kvh) * D + c * 8;
+      const uint4 kv = __ldg(reinterpret_cast<const uint4 *>(a.k_new + src));
+      const uint4 vv = __ldg(reinterpret_cast<const uint4 *>(a.v_new + src));
+      if constexpr (KV8) {  // quantise: e4m3(x / scale), 8 codes per chunk
+        uint8_t *kc = reinterpret_cast<uint8_t *>(a.k_cache), *vc = reinterpret_cast<uint8_t *>(a.v_cache);
+        *reinterpret_cast<uint2 *>(kc + dst) = quantize8<T>(kv, __ldg(a.k_scale + kvh));
+        *reinterpret_cast<uint2 *>(vc + dst) = quantize8<T>(vv, __ldg(a.v_scale + kvh));
+      } else {
+        *reinterpret_cast<uint4 *>(a.k_cache + dst) = kv;
+        *reinterpret_cast<uint4 *>(a.v_cache + dst) = vv;
+      }
+    }
+    fence_proxy_async_global();
+    __syncthreads();
+  }
+
 
   const int prologue = min(NSTAGE, n_my);
   for (int n = 0; n < prologue; ++n) issue(n);
