@@ -31,9 +31,11 @@ constexpr int kMaxDecodeQLen = 16;   // at most this many go to the decode kerne
 // Share of the SMs a cascade's shared-prefix pass runs on (num / den); the rest
 // serve the tail pass that overlaps it.  Measured on 128 sequences sharing a
 // 1024-token prefix (q_len 4, 32/8 heads): 152, 128, 96, 76, 64, 48 and 38 prefix
-// CTAs gave 112.2, 112.4, 103.2, 100.7, 104.4, 110.4 and 117.7 us per step.
-constexpr int kCascadePrefixShareNum = 1;
-constexpr int kCascadePrefixShareDen = 2;
+// CTAs gave 112.2, 112.4, 103.2, 100.7, 104.4, 110.4 and 117.7 us per step; after
+// a shorter decode prologue, 68, 72, 76, 80 and 84 gave 103.4, 101.9, 101.0, 100.4
+// and 100.5 us.
+constexpr int kCascadePrefixShareNum = 10;
+constexpr int kCascadePrefixShareDen = 19;
 
 __device__ unsigned int g_error_word;  // one per device (module global)
 
