@@ -386,6 +386,25 @@ def test_fused_append_decode_edges(pa, orc, q_len, splits):
     _tol.check(_f64(out), ref, w.cfg.dtype, f"fused q_len {q_len} splits {splits}")
 
 
+@pytest.mark.parametrize("name,q_len", [("llama7b_mha", 2), ("gqa", 4), ("prefix_verify", 4),
+                                        ("gqa", 16)])
+def test_fused_append_by_the_ctas_that_read_the_new_tiles(pa, orc, name, q_len):
+    """In the fused step only the CTAs whose warps read a tile holding a new position
+    write the new rows.  Few sequences launch as 2-8-CTA clusters, and lengths of
+    1-41 tiles with offsets inside and across tiles put those tiles on every warp
+    and CTA of a cluster (the walk's start also rotates with the KV head): the
+    whole pool must still match the oracle's append bit for bit."""
+    lens = tuple(16 * t + o for t, o in zip(range(1, 42, 4), (1, 15, 16, 3, 8, 0, 12, 5, 16, 9, 2)))
+    cfg = workloads.config(name, num_seqs=len(lens), q_len=q_len, lens=("fixed", lens),
+                           spare_blocks=3, shared_prefix=0)
+    w = workloads.make(cfg)
+    out, d = gpu_step(pa, w, num_splits=1, fused=True)
+    ref, kc, vc, _ = oracle_step(orc, w)
+    assert np.array_equal(_u16(d["k_cache"]), kc)
+    assert np.array_equal(_u16(d["v_cache"]), vc)
+    _tol.check(_f64(out), ref, w.cfg.dtype, f"{name} q_len {q_len}")
+
+
 def test_copy_blocks_bit_exact_and_cow_decode(pa, orc):
     """Copy-on-write: copies are bit-exact against the oracle on the whole pool, bad
     pairs are skipped and reported, and a sequence redirected to its private copy
