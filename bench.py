@@ -740,7 +740,11 @@ def run_ours(args):
         "instrumented_ms_per_step": r["instrumented_ms_per_step"],
         "timing": ("ms_per_step: the timed steps back to back under one event pair; "
                    "step_p10_p50_p90_ms and the roofline's kernel time: a second pass "
-                   "with events around every step and launch"),
+                   "with events around every step and launch.  Back to back, each "
+                   "launch is a programmatic dependent of the previous one, so its "
+                   "start overlaps that launch's tail and ms_per_step can be below "
+                   "the per-launch kernel time; the events of the second pass sit "
+                   "between launches and remove that overlap"),
         "step_algorithmic_gbs": r["step_gbs"],
         "separate_launches_ms_per_step": r["separate_launches_ms_per_step"],
         "kernel_src_sha": {k: kernel_source_sha(k) for k in KERNEL_SOURCES},
