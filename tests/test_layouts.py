@@ -303,3 +303,60 @@ def test_prefill_fp8_widening_in_place():
                 a = h * chunk * 128 + r * 128 + ((fp ^ (r & 7)) << 4)
                 for b in range(8):
                     assert mem[a + 2 * b] == ("fp16", r, 64 * h + 8 * fp + b)
+
+
+def _tile_walk(tb, te, kvh, num_kv_heads, gw, TW):
+    """The tiles cluster warp gw reads, in the decode kernel's order: tile number
+    k = gw + TW n, rotated by rot = kvh * ntiles / num_kv_heads."""
+    ntiles = te - tb
+    if ntiles <= 0:
+        return []
+    rot = (kvh * ntiles) // num_kv_heads
+    n_my = (ntiles - gw + TW - 1) // TW if ntiles - gw > 0 else 0
+    out = []
+    for n in range(n_my):
+        k = gw + TW * n + rot
+        if k >= ntiles:
+            k -= ntiles
+        out.append(tb + k)
+    return out
+
+
+def _reads_new(L, q_len, tb, te, kvh, num_kv_heads, crank, NW, TW):
+    """The fused append's test: does CTA crank read a tile holding a new position
+    (the inverse of the walk, as the kernel computes it)."""
+    ntiles = te - tb
+    if ntiles <= 0:
+        return False
+    rot = (kvh * ntiles) // num_kv_heads
+    j1 = min(te, (L + 15) // 16)
+    for j in range(max(tb, max(0, L - q_len) // 16), j1):
+        k = j - tb - rot
+        if k < 0:
+            k += ntiles
+        if (k % TW) // NW == crank:
+            return True
+    return False
+
+
+@pytest.mark.parametrize("NW,csize", [(4, 1), (4, 2), (3, 4), (4, 8)])
+def test_fused_append_owner_matches_the_tile_walk(NW, csize):
+    """The CTAs that append are exactly those whose warps' walks contain a tile of
+    a new position; every tile of the unit is walked by exactly one warp."""
+    TW = NW * csize
+    rng = np.random.default_rng(3)
+    for _ in range(400):
+        L = int(rng.integers(0, 700))
+        q_len = int(rng.integers(1, 17))
+        kvh, H = int(rng.integers(0, 8)), 8
+        nb = (L + 15) // 16
+        # a partition [tb, te) of the tiles, as the split pass takes them
+        tb = int(rng.integers(0, nb + 1))
+        te = int(rng.integers(tb, nb + 1))
+        walks = [_tile_walk(tb, te, kvh, H, gw, TW) for gw in range(TW)]
+        flat = sorted(t for w in walks for t in w)
+        assert flat == list(range(tb, te))
+        new_tiles = {p // 16 for p in range(max(0, L - q_len), L)}
+        for crank in range(csize):
+            mine = {t for gw in range(crank * NW, crank * NW + NW) for t in walks[gw]}
+            assert _reads_new(L, q_len, tb, te, kvh, H, crank, NW, TW) == bool(mine & new_tiles)
