@@ -211,24 +211,45 @@ __global__ void append_kv_fp8_kernel(uint8_t *k_cache, uint8_t *v_cache, const u
   }
 }
 
-// Copy-on-write block copy: one thread per 16-byte chunk of a (pair, head, row).
-__global__ void copy_blocks_kernel(uint4 *k_cache, uint4 *v_cache, const int32_t *src,
-                                   const int32_t *dst, int n_pairs, int64_t chunks_per_block,
-                                   int num_blocks, unsigned *err) {
+// Copy-on-write block copy.  Pair i = blockIdx.y (+ gridDim.y steps); each thread
+// copies kCopyUnroll 16-byte chunks of the block's K and of its V, blockDim.x
+// chunks apart, with all of its loads issued before its stores (eight 16-byte
+// loads in flight per thread).
+constexpr int kCopyUnroll = 4;
+constexpr int kCopyThreads = 256;
+__global__ void __launch_bounds__(kCopyThreads)
+    copy_blocks_kernel(uint4 *k_cache, uint4 *v_cache, const int32_t *src, const int32_t *dst,
+                       int n_pairs, int64_t chunks_per_block, int num_blocks, unsigned *err) {
   pa::griddep_wait();
   pa::griddep_launch_dependents();
-  const int64_t total = (int64_t)n_pairs * chunks_per_block;
-  for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
-       idx += (int64_t)gridDim.x * blockDim.x) {
-    const int i = (int)(idx / chunks_per_block);
-    const int64_t c = idx % chunks_per_block;
+  const int64_t c0 = (int64_t)blockIdx.x * (kCopyThreads * kCopyUnroll) + threadIdx.x;
+  for (int i = blockIdx.y; i < n_pairs; i += gridDim.y) {
     const int s = __ldg(src + i), d = __ldg(dst + i);
     if (s < 0 || s >= num_blocks || d < 0 || d >= num_blocks) {
-      if (c == 0) pa::record_error(err, pa::kErrCheck);
+      if (blockIdx.x == 0 && threadIdx.x == 0) pa::record_error(err, pa::kErrCheck);
       continue;
     }
-    k_cache[(int64_t)d * chunks_per_block + c] = k_cache[(int64_t)s * chunks_per_block + c];
-    v_cache[(int64_t)d * chunks_per_block + c] = v_cache[(int64_t)s * chunks_per_block + c];
+    const uint4 *ks = k_cache + (int64_t)s * chunks_per_block;
+    const uint4 *vs = v_cache + (int64_t)s * chunks_per_block;
+    uint4 *kd = k_cache + (int64_t)d * chunks_per_block;
+    uint4 *vd = v_cache + (int64_t)d * chunks_per_block;
+    uint4 kv[kCopyUnroll], vv[kCopyUnroll];
+#pragma unroll
+    for (int u = 0; u < kCopyUnroll; ++u) {
+      const int64_t c = c0 + u * kCopyThreads;
+      if (c < chunks_per_block) {
+        kv[u] = ks[c];
+        vv[u] = vs[c];
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kCopyUnroll; ++u) {
+      const int64_t c = c0 + u * kCopyThreads;
+      if (c < chunks_per_block) {
+        kd[c] = kv[u];
+        vd[c] = vv[u];
+      }
+    }
   }
 }
 
@@ -616,10 +637,11 @@ PA_API pa_status pa_copy_blocks(void *k_cache, void *v_cache, const int32_t *src
   unsigned *err = error_word();
   if (err == nullptr) return PA_ERR_CUDA;
   const int64_t chunks = (int64_t)num_kv_heads * block_size * head_dim * 2 / 16;
-  const int64_t total = (int64_t)n_pairs * chunks;
-  const int threads = 256;
-  const unsigned blocks = (unsigned)std::min<int64_t>((total + threads - 1) / threads, 1 << 20);
-  cudaError_t e = pa::launch_dependent(copy_blocks_kernel, blocks, threads,
+  // x: the chunks of one block; y: the pairs (further pairs loop)
+  const int64_t per_cta = (int64_t)kCopyThreads * kCopyUnroll;
+  const dim3 blocks((unsigned)((chunks + per_cta - 1) / per_cta),
+                    (unsigned)std::min(n_pairs, 65535), 1);
+  cudaError_t e = pa::launch_dependent(copy_blocks_kernel, blocks, kCopyThreads,
                                        static_cast<cudaStream_t>(stream),
                                        static_cast<uint4 *>(k_cache), static_cast<uint4 *>(v_cache),
                                        src_blocks, dst_blocks, n_pairs, chunks, num_blocks, err);

@@ -11,10 +11,10 @@ namespace pa {
 // may be scheduled before that work finishes, and must call griddepcontrol.wait
 // before touching global memory (every kernel of this library does).
 template <typename... Params, typename... Args>
-cudaError_t launch_dependent(void (*kern)(Params...), unsigned grid, unsigned block,
+cudaError_t launch_dependent(void (*kern)(Params...), dim3 grid, unsigned block,
                              cudaStream_t stream, Args &&...args) {
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid, 1, 1);
+  cfg.gridDim = grid;
   cfg.blockDim = dim3(block, 1, 1);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
