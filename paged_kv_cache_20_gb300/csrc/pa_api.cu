@@ -64,29 +64,24 @@ __global__ void slot_mapping_kernel(int64_t *out, const int32_t *block_tables,
   out[idx] = slot;
 }
 
-// One thread per 16-byte chunk of one (token, head) row; K and V together.
+// The appends: one CTA per new token row (its slot worked out once), its threads
+// over the (head, 16-byte chunk) pieces of that row, K and V together.
+inline unsigned append_threads(int num_kv_heads, int head_dim) {
+  const int pieces = num_kv_heads * (head_dim / 8);
+  return (unsigned)std::min(1024, (pieces + 31) / 32 * 32);
+}
+
+// Row t of k_new / v_new (all heads) into block blk, row off of every head.
 template <int D>
-__global__ void append_kv_kernel(uint16_t *k_cache, uint16_t *v_cache, const uint16_t *k_new,
-                                 const uint16_t *v_new, const int64_t *slot_mapping, int n_tokens,
-                                 int num_kv_heads, int block_size, int64_t num_slots, unsigned *err) {
-  pa::griddep_wait();  // the slot mapping may come from the previous kernel
-  pa::griddep_launch_dependents();
+__device__ __forceinline__ void append_row(uint16_t *__restrict__ k_cache,
+                                           uint16_t *__restrict__ v_cache,
+                                           const uint16_t *__restrict__ k_new,
+                                           const uint16_t *__restrict__ v_new, int64_t t,
+                                           int num_kv_heads, int block_size, int64_t blk, int off) {
   constexpr int kChunks = D / 8;
-  const int64_t total = (int64_t)n_tokens * num_kv_heads * kChunks;
-  for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
-       idx += (int64_t)gridDim.x * blockDim.x) {
-    const int c = (int)(idx % kChunks);
-    const int64_t th = idx / kChunks;
-    const int h = (int)(th % num_kv_heads);
-    const int64_t t = th / num_kv_heads;
-    const int64_t slot = slot_mapping[t];
-    if (slot < 0) continue;
-    if (slot >= num_slots) {
-      if (c == 0 && h == 0) pa::record_error(err, pa::kErrCheck);
-      continue;
-    }
-    const int64_t block = slot / block_size, offset = slot % block_size;
-    const int64_t dst = ((block * num_kv_heads + h) * block_size + offset) * D + c * 8;
+  for (int hc = threadIdx.x; hc < num_kv_heads * kChunks; hc += blockDim.x) {
+    const int h = hc / kChunks, c = hc % kChunks;
+    const int64_t dst = ((blk * num_kv_heads + h) * block_size + off) * D + c * 8;
     const int64_t src = (t * num_kv_heads + h) * D + c * 8;
     const uint4 kv = __ldg(reinterpret_cast<const uint4 *>(k_new + src));
     const uint4 vv = __ldg(reinterpret_cast<const uint4 *>(v_new + src));
@@ -95,9 +90,75 @@ __global__ void append_kv_kernel(uint16_t *k_cache, uint16_t *v_cache, const uin
   }
 }
 
+// The same into an FP8 cache, quantising: code = e4m3(x / scale[head]).
+template <typename T, int D>
+__device__ __forceinline__ void append_row_fp8(uint8_t *__restrict__ k_cache,
+                                               uint8_t *__restrict__ v_cache,
+                                               const uint16_t *__restrict__ k_new,
+                                               const uint16_t *__restrict__ v_new, int64_t t,
+                                               int num_kv_heads, int block_size, int64_t blk,
+                                               int off, const float *k_scale,
+                                               const float *v_scale) {
+  constexpr int kChunks = D / 8;
+  for (int hc = threadIdx.x; hc < num_kv_heads * kChunks; hc += blockDim.x) {
+    const int h = hc / kChunks, c = hc % kChunks;
+    const int64_t dst = ((blk * num_kv_heads + h) * block_size + off) * D + c * 8;
+    const int64_t src = (t * num_kv_heads + h) * D + c * 8;
+    const uint4 kv = __ldg(reinterpret_cast<const uint4 *>(k_new + src));
+    const uint4 vv = __ldg(reinterpret_cast<const uint4 *>(v_new + src));
+    *reinterpret_cast<uint2 *>(k_cache + dst) = pa::quantize8<T>(kv, __ldg(k_scale + h));
+    *reinterpret_cast<uint2 *>(v_cache + dst) = pa::quantize8<T>(vv, __ldg(v_scale + h));
+  }
+}
+
+// Append through a slot mapping: CTA t takes token row t.
+template <int D>
+__global__ void append_kv_kernel(uint16_t *k_cache, uint16_t *v_cache, const uint16_t *k_new,
+                                 const uint16_t *v_new, const int64_t *slot_mapping, int n_tokens,
+                                 int num_kv_heads, int block_size, int64_t num_slots, unsigned *err) {
+  pa::griddep_wait();  // the slot mapping may come from the previous kernel
+  pa::griddep_launch_dependents();
+  const int64_t t = blockIdx.x;
+  const int64_t slot = slot_mapping[t];
+  if (slot < 0) return;
+  if (slot >= num_slots) {
+    if (threadIdx.x == 0) pa::record_error(err, pa::kErrCheck);
+    return;
+  }
+  const int64_t blk = slot / block_size;
+  append_row<D>(k_cache, v_cache, k_new, v_new, t, num_kv_heads, block_size, blk,
+                (int)(slot - blk * block_size));
+}
+
 // Append of one step's new rows straight from the block tables: token u of
 // sequence i sits at position context_lens[i] - q_len + u (the slot of the slot
-// mapping kernel, computed in place).  One thread per 16-byte chunk.
+// mapping kernel, computed in place).  CTA t takes token row t = i * q_len + u.
+// Returns the row's block (-1: nothing to write).
+__device__ __forceinline__ int64_t step_slot_block(const int32_t *block_tables,
+                                                   const int32_t *context_lens, int q_len,
+                                                   int block_size, int max_blocks_per_seq,
+                                                   int64_t num_slots, unsigned *err, int &off) {
+  const int t = blockIdx.x;
+  const int i = t / q_len, u = t - i * q_len;
+  const int64_t pos = (int64_t)context_lens[i] - q_len + u;
+  if (pos < 0) return -1;
+  const int64_t lb = pos / block_size;
+  if (lb >= max_blocks_per_seq) {
+    if (threadIdx.x == 0) pa::record_error(err, pa::kErrCheck);
+    return -1;
+  }
+  const int64_t slot =
+      (int64_t)block_tables[(int64_t)i * max_blocks_per_seq + lb] * block_size +
+      (pos - lb * block_size);
+  if (slot < 0 || slot >= num_slots) {
+    if (threadIdx.x == 0) pa::record_error(err, pa::kErrCheck);
+    return -1;
+  }
+  const int64_t blk = slot / block_size;
+  off = (int)(slot - blk * block_size);
+  return blk;
+}
+
 template <int D>
 __global__ void append_step_kernel(uint16_t *k_cache, uint16_t *v_cache, const uint16_t *k_new,
                                    const uint16_t *v_new, const int32_t *block_tables,
@@ -106,37 +167,14 @@ __global__ void append_step_kernel(uint16_t *k_cache, uint16_t *v_cache, const u
                                    int64_t num_slots, unsigned *err) {
   pa::griddep_wait();
   pa::griddep_launch_dependents();
-  constexpr int kChunks = D / 8;
-  const int64_t total = (int64_t)num_seqs * q_len * num_kv_heads * kChunks;
-  for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
-       idx += (int64_t)gridDim.x * blockDim.x) {
-    const int c = (int)(idx % kChunks);
-    const int64_t th = idx / kChunks;
-    const int h = (int)(th % num_kv_heads);
-    const int64_t t = th / num_kv_heads;  // token row of k_new: seq * q_len + u
-    const int i = (int)(t / q_len), u = (int)(t % q_len);
-    const int64_t pos = (int64_t)context_lens[i] - q_len + u;
-    if (pos < 0) continue;
-    const int64_t lb = pos / block_size;
-    if (lb >= max_blocks_per_seq) {
-      if (c == 0) pa::record_error(err, pa::kErrCheck);
-      continue;
-    }
-    const int64_t slot =
-        (int64_t)block_tables[(int64_t)i * max_blocks_per_seq + lb] * block_size + pos % block_size;
-    if (slot < 0 || slot >= num_slots) {
-      if (c == 0) pa::record_error(err, pa::kErrCheck);
-      continue;
-    }
-    const int64_t dst = (((slot / block_size) * num_kv_heads + h) * block_size + slot % block_size) * D + c * 8;
-    const int64_t src = (t * num_kv_heads + h) * D + c * 8;
-    *reinterpret_cast<uint4 *>(k_cache + dst) = __ldg(reinterpret_cast<const uint4 *>(k_new + src));
-    *reinterpret_cast<uint4 *>(v_cache + dst) = __ldg(reinterpret_cast<const uint4 *>(v_new + src));
-  }
+  int off = 0;
+  const int64_t blk = step_slot_block(block_tables, context_lens, q_len, block_size,
+                                      max_blocks_per_seq, num_slots, err, off);
+  if (blk < 0) return;
+  append_row<D>(k_cache, v_cache, k_new, v_new, blockIdx.x, num_kv_heads, block_size, blk, off);
 }
 
-// The same append into an FP8 cache, quantising: code = e4m3(x / scale[head]).  One
-// thread per 8 values of a (token, head) row.
+// The same append into an FP8 cache, quantising: code = e4m3(x / scale[head]).
 template <typename T, int D>
 __global__ void append_step_fp8_kernel(uint8_t *k_cache, uint8_t *v_cache, const uint16_t *k_new,
                                        const uint16_t *v_new, const int32_t *block_tables,
@@ -146,39 +184,15 @@ __global__ void append_step_fp8_kernel(uint8_t *k_cache, uint8_t *v_cache, const
                                        const float *v_scale, unsigned *err) {
   pa::griddep_wait();
   pa::griddep_launch_dependents();
-  constexpr int kChunks = D / 8;
-  const int64_t total = (int64_t)num_seqs * q_len * num_kv_heads * kChunks;
-  for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
-       idx += (int64_t)gridDim.x * blockDim.x) {
-    const int c = (int)(idx % kChunks);
-    const int64_t th = idx / kChunks;
-    const int h = (int)(th % num_kv_heads);
-    const int64_t t = th / num_kv_heads;  // token row of k_new: seq * q_len + u
-    const int i = (int)(t / q_len), u = (int)(t % q_len);
-    const int64_t pos = (int64_t)context_lens[i] - q_len + u;
-    if (pos < 0) continue;
-    const int64_t lb = pos / block_size;
-    if (lb >= max_blocks_per_seq) {
-      if (c == 0) pa::record_error(err, pa::kErrCheck);
-      continue;
-    }
-    const int64_t slot =
-        (int64_t)block_tables[(int64_t)i * max_blocks_per_seq + lb] * block_size + pos % block_size;
-    if (slot < 0 || slot >= num_slots) {
-      if (c == 0) pa::record_error(err, pa::kErrCheck);
-      continue;
-    }
-    const int64_t dst = (((slot / block_size) * num_kv_heads + h) * block_size + slot % block_size) * D + c * 8;
-    const int64_t src = (t * num_kv_heads + h) * D + c * 8;
-    const uint4 kv = __ldg(reinterpret_cast<const uint4 *>(k_new + src));
-    const uint4 vv = __ldg(reinterpret_cast<const uint4 *>(v_new + src));
-    *reinterpret_cast<uint2 *>(k_cache + dst) = pa::quantize8<T>(kv, __ldg(k_scale + h));
-    *reinterpret_cast<uint2 *>(v_cache + dst) = pa::quantize8<T>(vv, __ldg(v_scale + h));
-  }
+  int off = 0;
+  const int64_t blk = step_slot_block(block_tables, context_lens, q_len, block_size,
+                                      max_blocks_per_seq, num_slots, err, off);
+  if (blk < 0) return;
+  append_row_fp8<T, D>(k_cache, v_cache, k_new, v_new, blockIdx.x, num_kv_heads, block_size, blk,
+                       off, k_scale, v_scale);
 }
 
-// Quantising append into an FP8 cache: one thread per 8 values of a (token, head)
-// row; code = e4m3(x / scale[head]).
+// Quantising append into an FP8 cache through a slot mapping: CTA t takes token row t.
 template <typename T, int D>
 __global__ void append_kv_fp8_kernel(uint8_t *k_cache, uint8_t *v_cache, const uint16_t *k_new,
                                      const uint16_t *v_new, const int64_t *slot_mapping,
@@ -187,28 +201,16 @@ __global__ void append_kv_fp8_kernel(uint8_t *k_cache, uint8_t *v_cache, const u
                                      const float *v_scale, unsigned *err) {
   pa::griddep_wait();
   pa::griddep_launch_dependents();
-  constexpr int kChunks = D / 8;
-  const int64_t total = (int64_t)n_tokens * num_kv_heads * kChunks;
-  for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
-       idx += (int64_t)gridDim.x * blockDim.x) {
-    const int c = (int)(idx % kChunks);
-    const int64_t th = idx / kChunks;
-    const int h = (int)(th % num_kv_heads);
-    const int64_t t = th / num_kv_heads;
-    const int64_t slot = slot_mapping[t];
-    if (slot < 0) continue;
-    if (slot >= num_slots) {
-      if (c == 0 && h == 0) pa::record_error(err, pa::kErrCheck);
-      continue;
-    }
-    const int64_t block = slot / block_size, offset = slot % block_size;
-    const int64_t dst = ((block * num_kv_heads + h) * block_size + offset) * D + c * 8;
-    const int64_t src = (t * num_kv_heads + h) * D + c * 8;
-    const uint4 kv = __ldg(reinterpret_cast<const uint4 *>(k_new + src));
-    const uint4 vv = __ldg(reinterpret_cast<const uint4 *>(v_new + src));
-    *reinterpret_cast<uint2 *>(k_cache + dst) = pa::quantize8<T>(kv, __ldg(k_scale + h));
-    *reinterpret_cast<uint2 *>(v_cache + dst) = pa::quantize8<T>(vv, __ldg(v_scale + h));
+  const int64_t t = blockIdx.x;
+  const int64_t slot = slot_mapping[t];
+  if (slot < 0) return;
+  if (slot >= num_slots) {
+    if (threadIdx.x == 0) pa::record_error(err, pa::kErrCheck);
+    return;
   }
+  const int64_t blk = slot / block_size;
+  append_row_fp8<T, D>(k_cache, v_cache, k_new, v_new, t, num_kv_heads, block_size, blk,
+                       (int)(slot - blk * block_size), k_scale, v_scale);
 }
 
 // Copy-on-write block copy.  Pair i = blockIdx.y (+ gridDim.y steps); each thread
@@ -482,8 +484,8 @@ pa_status decode_common(void *out, float *ws, const WsLayout *lay, const void *q
     if (k_new != nullptr) {
       // The rows of a CTA depend on new tokens that other CTAs' rows own, so the
       // append runs as its own launch first (ordered by the stream).
-      const int64_t total = (int64_t)num_seqs * q_len * num_kv_heads * (head_dim / 8);
-      const unsigned blocks = (unsigned)std::min<int64_t>((total + 255) / 256, 1 << 20);
+      const unsigned blocks = (unsigned)(num_seqs * q_len);  // one CTA per token row
+      const unsigned threads = append_threads(num_kv_heads, head_dim);
       const int64_t num_slots = (int64_t)num_blocks * block_size;
       auto kn = static_cast<const uint16_t *>(k_new);
       auto vn = static_cast<const uint16_t *>(v_new);
@@ -491,22 +493,22 @@ pa_status decode_common(void *out, float *ws, const WsLayout *lay, const void *q
         auto kc8 = static_cast<uint8_t *>(const_cast<void *>(k_cache));
         auto vc8 = static_cast<uint8_t *>(const_cast<void *>(v_cache));
         e = dtype == PA_FP16
-                ? pa::launch_dependent(append_step_fp8_kernel<__half, 128>, blocks, 256, s, kc8, vc8,
-                                       kn, vn, block_tables, context_lens, num_seqs, q_len,
+                ? pa::launch_dependent(append_step_fp8_kernel<__half, 128>, blocks, threads, s,
+                                       kc8, vc8, kn, vn, block_tables, context_lens, num_seqs, q_len,
                                        num_kv_heads, block_size, max_blocks_per_seq, num_slots,
                                        k_scale, v_scale, a.err)
-                : pa::launch_dependent(append_step_fp8_kernel<__nv_bfloat16, 128>, blocks, 256, s,
-                                       kc8, vc8, kn, vn, block_tables, context_lens, num_seqs,
+                : pa::launch_dependent(append_step_fp8_kernel<__nv_bfloat16, 128>, blocks,
+                                       threads, s, kc8, vc8, kn, vn, block_tables, context_lens, num_seqs,
                                        q_len, num_kv_heads, block_size, max_blocks_per_seq,
                                        num_slots, k_scale, v_scale, a.err);
       } else {
         auto kc = static_cast<uint16_t *>(const_cast<void *>(k_cache));
         auto vc = static_cast<uint16_t *>(const_cast<void *>(v_cache));
         e = head_dim == 128
-                ? pa::launch_dependent(append_step_kernel<128>, blocks, 256, s, kc, vc, kn, vn,
+                ? pa::launch_dependent(append_step_kernel<128>, blocks, threads, s, kc, vc, kn, vn,
                                        block_tables, context_lens, num_seqs, q_len, num_kv_heads,
                                        block_size, max_blocks_per_seq, num_slots, a.err)
-                : pa::launch_dependent(append_step_kernel<64>, blocks, 256, s, kc, vc, kn, vn,
+                : pa::launch_dependent(append_step_kernel<64>, blocks, threads, s, kc, vc, kn, vn,
                                        block_tables, context_lens, num_seqs, q_len, num_kv_heads,
                                        block_size, max_blocks_per_seq, num_slots, a.err);
       }
@@ -603,9 +605,8 @@ PA_API pa_status pa_append_kv(void *k_cache, void *v_cache, const void *k_new, c
   if (n_tokens == 0) return PA_OK;
   unsigned *err = error_word();
   if (err == nullptr) return PA_ERR_CUDA;
-  const int64_t total = (int64_t)n_tokens * num_kv_heads * (head_dim / 8);
-  const int threads = 256;
-  const int blocks = (int)std::min<int64_t>((total + threads - 1) / threads, 1 << 20);
+  const unsigned blocks = (unsigned)n_tokens;  // one CTA per token row
+  const unsigned threads = append_threads(num_kv_heads, head_dim);
   const int64_t num_slots = (int64_t)num_blocks * block_size;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   auto kc = static_cast<uint16_t *>(k_cache);
@@ -769,9 +770,8 @@ PA_API pa_status pa_append_kv_fp8(void *k_cache, void *v_cache, const void *k_ne
   if (n_tokens == 0) return PA_OK;
   unsigned *err = error_word();
   if (err == nullptr) return PA_ERR_CUDA;
-  const int64_t total = (int64_t)n_tokens * num_kv_heads * (head_dim / 8);
-  const int threads = 256;
-  const unsigned blocks = (unsigned)std::min<int64_t>((total + threads - 1) / threads, 1 << 20);
+  const unsigned blocks = (unsigned)n_tokens;  // one CTA per token row
+  const unsigned threads = append_threads(num_kv_heads, head_dim);
   const int64_t num_slots = (int64_t)num_blocks * block_size;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   auto kc = static_cast<uint8_t *>(k_cache);
