@@ -1635,7 +1635,7 @@ __global__ void __launch_bounds__(128) split_combine_kernel(const CombineArgs a)
         den += wt * lw;
       }
       const int cnt = min(32, a.num_splits - p0);
-#pragma unroll 4
+#pragma unroll 8
       for (int k = 0; k < cnt; ++k) {
         const float wk = __shfl_sync(0xffffffffu, wt, k);
         const float *acc = a.ws_acc + (base + (p0 + k) * pstride) * D + lane * PER;
