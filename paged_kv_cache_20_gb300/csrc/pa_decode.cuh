@@ -1252,6 +1252,19 @@ __global__ void __launch_bounds__(NW * 32)
   const uint32_t smem_base = (smem_u32(smem_raw) + 1023u) & ~1023u;  // 128B-swizzle tiles: 1 KiB
   uint8_t *smem_gen = smem_raw + (smem_base - smem_u32(smem_raw));
 
+  // shared-memory state and the tensor-map descriptors: nothing another kernel writes
+  if (threadIdx.x == 0) {
+    s_failed = 0;
+    prefetch_tensormap(&kmap);
+    prefetch_tensormap(&vmap);
+  }
+  if (lane == 0) {
+#pragma unroll
+    for (int s = 0; s < NSTAGE; ++s) mbar_init(smem_u32(&bars[warp * NSTAGE + s]), 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+
   // Launched as a programmatic dependent of the previous kernel on the stream (for
   // example the KV append): setup above this point overlaps that kernel's tail.
   // Wait for it to complete before the first read of global memory: any input
@@ -1301,18 +1314,6 @@ __global__ void __launch_bounds__(NW * 32)
   // base-2 score scale (times the K scale of an FP8 cache) and the V scale
   const float sscale = a.scale_log2 * (KV8 ? __ldg(a.k_scale + kvh) : 1.f);
   const float vscale = KV8 ? __ldg(a.v_scale + kvh) : 1.f;
-
-  if (threadIdx.x == 0) {
-    s_failed = 0;
-    prefetch_tensormap(&kmap);
-    prefetch_tensormap(&vmap);
-  }
-  if (lane == 0) {
-#pragma unroll
-    for (int s = 0; s < NSTAGE; ++s) mbar_init(smem_u32(&bars[warp * NSTAGE + s]), 1);
-    fence_mbar_init();
-  }
-  __syncwarp();
 
   // This warp's tiles: the unit's ntiles blocks are visited from a starting offset
   // `rot` that differs between the KV heads of a sequence, tile number
