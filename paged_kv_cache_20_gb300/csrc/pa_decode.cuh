@@ -1658,4 +1658,52 @@ __global__ void __launch_bounds__(128) split_combine_kernel(const CombineArgs a)
     *reinterpret_cast<uint32_t *>(o + k) = Elt<T>::from_f2(num[k] * inv, num[k + 1] * inv);
 }
 
+// With few rows and many partitions the warps of the form above are too few to
+// hide the partitions' load latency: this form gives each row D / 32 warps, one
+// dimension per lane, every partition's load of that dimension in flight at once.
+// The partitions are summed in the same order, so both forms give the same bits.
+template <typename T, int D>
+__global__ void __launch_bounds__(128) split_combine_spread_kernel(const CombineArgs a) {
+  constexpr int kWarpsPerRow = D / 32;
+  const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  const int row_id = gw / kWarpsPerRow, dim = (gw % kWarpsPerRow) * 32 + lane;
+  if (row_id >= a.num_seqs * a.rows_per_seq) return;
+  griddep_wait();  // the workspace comes from the partial pass just before
+  griddep_launch_dependents();
+  const int seq = row_id / a.rows_per_seq, r = row_id % a.rows_per_seq;
+  const size_t base = (size_t)seq * a.num_splits * a.rows_per_seq + r;
+  const size_t pstride = a.rows_per_seq;
+  float M = -INFINITY;
+  for (int p = lane; p < a.num_splits; p += 32) {
+    const size_t w = base + p * pstride;
+    if (a.ws_l[w] > 0.f) M = fmaxf(M, a.ws_m[w]);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  float den = 0.f, num = 0.f;
+  if (M != -INFINITY) {
+    for (int p0 = 0; p0 < a.num_splits; p0 += 32) {
+      float wt = 0.f;
+      if (p0 + lane < a.num_splits) {
+        const size_t w = base + (p0 + lane) * pstride;
+        const float lw = a.ws_l[w];
+        wt = lw > 0.f ? fast_exp2(a.ws_m[w] - M) : 0.f;
+        den += wt * lw;
+      }
+      const int cnt = min(32, a.num_splits - p0);
+#pragma unroll 16
+      for (int k = 0; k < cnt; ++k) {
+        const float wk = __shfl_sync(0xffffffffu, wt, k);
+        num += wk * a.ws_acc[(base + (p0 + k) * pstride) * D + dim];
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+  }
+  const float inv = den > 0.f ? 1.f / den : 0.f;
+  static_cast<uint16_t *>(a.out)[((size_t)seq * a.rows_per_seq + r) * D + dim] =
+      Elt<T>::from_f(num * inv);
+}
+
 }  // namespace pa

@@ -184,9 +184,21 @@ static cudaError_t launch_decode_t(const CUtensorMap &kmap, const CUtensorMap &v
 
 template <typename T>
 static cudaError_t launch_combine_t(const CombineArgs &a, int head_dim, cudaStream_t st) {
-  const long long warps = (long long)a.num_seqs * a.rows_per_seq;
-  const int blocks = (int)((warps * 32 + 127) / 128);
-  if (blocks == 0) return cudaSuccess;
+  const long long rows = (long long)a.num_seqs * a.rows_per_seq;
+  if (rows == 0) return cudaSuccess;
+  // One dimension per lane (split_combine_spread_kernel) for more than 8 partitions
+  // of at most 512 rows.  Measured on GB300: 4 x 32 rows of 16 partitions, 92.5 ->
+  // 90.5 us per step; 8 x 32 rows of 8 partitions and 64 x 32 rows of 4 partitions
+  // were slower spread.
+  if (a.num_splits > 8 && rows <= 512) {
+    const int blocks = (int)((rows * (head_dim / 32) * 32 + 127) / 128);
+    if (head_dim == 128)
+      return launch_dependent(split_combine_spread_kernel<T, 128>, blocks, 128, st, a);
+    if (head_dim == 64)
+      return launch_dependent(split_combine_spread_kernel<T, 64>, blocks, 128, st, a);
+    return cudaErrorInvalidValue;
+  }
+  const int blocks = (int)((rows * 32 + 127) / 128);
   if (head_dim == 128) return launch_dependent(split_combine_kernel<T, 128>, blocks, 128, st, a);
   if (head_dim == 64) return launch_dependent(split_combine_kernel<T, 64>, blocks, 128, st, a);
   return cudaErrorInvalidValue;
