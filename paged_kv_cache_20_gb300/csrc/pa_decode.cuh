@@ -72,9 +72,9 @@ struct DecodeArgs {
   int max_tiles;                 // 16-token tiles a block-table row covers (rounded up)
   int lpt;                       // 1: take sequences longest first (num_seqs <= kLptMaxSeqs)
   float scale_log2;              // scale * log2(e): scores in base-2 units
-  // fused append (k_new == nullptr: none).  The unit writes its own KV head's rows
-  // of this step's new tokens -- positions context_len - q_len + u -- into the
-  // cache before reading it.
+  // fused append (k_new == nullptr: none).  The CTAs of a unit that read a tile
+  // holding one of this step's new tokens -- positions context_len - q_len + u --
+  // write the unit's KV head's rows of them into the cache before reading it.
   const uint16_t *k_new;         // [num_seqs * q_len][num_kv_heads][D]
   const uint16_t *v_new;
   uint16_t *k_cache;             // the memory the tensor maps describe
@@ -1596,7 +1596,8 @@ __global__ void __launch_bounds__(NW * 32)
 }
 
 // ---------------------------------------------------------------------------------
-// Split-KV combine: one warp per (sequence, row); lanes cover head_dim.
+// Split-KV combine: one warp per (sequence, row), lanes covering head_dim (or, in
+// split_combine_spread_kernel below, head_dim / 32 warps per row).
 struct CombineArgs {
   void *out;
   const float *ws_acc, *ws_m, *ws_l;
