@@ -262,23 +262,26 @@ def test_partial_statistics_match_oracle_partitions(pa, orc):
     assert np.abs(lse_g - lse_o).max() < 1e-4
 
 
-def test_combine_alone_on_oracle_partials(pa, orc):
+# 7 partitions: one warp per row; 12 and 33 (more than 8, few rows): one dimension
+# per lane, and 33 also takes the second group of 32 partitions
+@pytest.mark.parametrize("S,D", [(7, 64), (12, 64), (12, 128), (33, 128)])
+def test_combine_alone_on_oracle_partials(pa, orc, S, D):
     lens = [3, 64, 500, 0, 17]
-    S, q_len = 7, 1
-    q, K, V = _logical_case(12, lens, 4, 4, 64, "fp16", q_len=q_len, qscale=2.0)
+    q_len = 1
+    q, K, V = _logical_case(12, lens, 4, 4, D, "fp16", q_len=q_len, qscale=2.0)
     pc = Paged(orc, K, V, 16, "fp16", perm_seed=8)
     m, l, acc = orc.decode_partitions(q, pc.k, pc.v, pc.tables, pc.lens, 0.125, "fp16", S)
-    want = orc.combine(m, l, acc).reshape(5, 1, 4, 64)
-    nbytes = pa.pa_decode_workspace_size(5, 4, 1, 64, S)
+    want = orc.combine(m, l, acc).reshape(5, 1, 4, D)
+    nbytes = pa.pa_decode_workspace_size(5, 4, 1, D, S)
     ws = torch.zeros(nbytes, dtype=torch.uint8, device=DEV)
-    g_acc, g_m, g_l = pa.workspace_views(ws, 5, 4, 1, 64, S)
+    g_acc, g_m, g_l = pa.workspace_views(ws, 5, 4, 1, D, S)
     g_acc.copy_(torch.from_numpy(acc).float())
     g_m.copy_(torch.from_numpy(m / np.log(2.0)).float())   # base-2 units
     g_l.copy_(torch.from_numpy(l).float())
-    out = torch.empty((5, 1, 4, 64), dtype=torch.float16, device=DEV)
+    out = torch.empty((5, 1, 4, D), dtype=torch.float16, device=DEV)
     pa.pa_decode_combine(out, ws, S)
     torch.cuda.synchronize()
-    _tol.check(_f64(out), want, "fp16", "combine")
+    _tol.check(_f64(out), want, "fp16", f"combine of {S} partitions")
 
 
 def test_bad_block_id_is_reported_not_faulted(pa, orc):
